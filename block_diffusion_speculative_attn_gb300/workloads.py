@@ -1,0 +1,207 @@
+"""Seeded synthetic workloads for the draft/verify step.
+
+This module only draws random inputs with the shapes, value distributions and
+paging structure of the source pages' workloads; it holds none of the step's
+arithmetic (no attention, no acceptance rule, no block layout).  Both the CUDA
+path and the CPU oracle consume what it returns.
+
+Structure (sequence lengths, page permutation, block tables) comes from numpy
+PCG64; large tensors come from a seeded torch generator on the requested device
+so that multi-GB caches are drawn where they live.  bf16 values are fp32
+N(0, 1) rounded to nearest even.
+"""
+from __future__ import annotations
+
+import dataclasses
+import math
+
+import numpy as np
+import torch
+
+DRAFT, VERIFY = 0, 1
+
+
+@dataclasses.dataclass(frozen=True)
+class StepConfig:
+    """One synthetic workload.  ctx is (lo, hi) inclusive, or a tuple of exact lengths."""
+    name: str
+    bs: int
+    Hq: int
+    Hkv: int
+    D: int
+    B: int
+    page_size: int
+    ctx: tuple
+    modes: tuple               # attention passes in step order, DRAFT=0 / VERIFY=1
+    V: int = 0                 # 0: no acceptance stage
+    accept: str = ""           # "indep2" | "perturb" | "near_uniform" | ""
+    seed: int = 1234
+
+    @property
+    def G(self) -> int:
+        return self.Hq // self.Hkv
+
+    @property
+    def mask_token_id(self) -> int:
+        return max(self.V - 1, 0)
+
+
+# The five workloads, index order fixed (seed = 1234 + index).
+CONFIGS = {
+    # Tiny case: 2 requests, GQA 2/1, D 64, contexts 200 and 256, 16-token pages
+    # shuffled in the pool, B = 8, both modes; acceptance over a 1000-token vocab.
+    "tiny": StepConfig("tiny", 2, 2, 1, 64, 8, 16, (200, 256), (DRAFT, VERIFY), 1000, "indep2",
+                       1234),
+    # Qwen3-8B-shaped DFlash verify: 32 requests, 32/8 heads, D 128, contexts U[1024, 4096],
+    # 64-token pages, B = 16 causal; acceptance over 151936 tokens, q = p with logit noise.
+    "qwen3_8b_verify": StepConfig("qwen3_8b_verify", 32, 32, 8, 128, 16, 64, ((1024, 4096),),
+                                  (VERIFY,), 151936, "perturb", 1235),
+    # LLaDA2.0-style block diffusion draft: 64 requests, 16/4 heads, B = 32 bidirectional,
+    # contexts U[512, 8192], 32-token pages, no acceptance stage.
+    "llada2_block_draft": StepConfig("llada2_block_draft", 64, 16, 4, 128, 32, 32,
+                                     ((512, 8192),), (DRAFT,), 0, "", 1236),
+    # Uno 1K/8K-shaped high-concurrency step: 256 requests, 32/8 heads, contexts
+    # U[1024, 9216], B = 16: draft pass then verify pass on the same cache, then acceptance.
+    "uno_1k8k_step": StepConfig("uno_1k8k_step", 256, 32, 8, 128, 16, 64, ((1024, 9216),),
+                                (DRAFT, VERIFY), 151936, "perturb", 1237),
+    # Long context, low batch: 4 requests of 131072 tokens, 64/8 heads, B = 16 causal,
+    # split-KV path; acceptance with near-uniform q (high rejection).
+    "long_ctx_verify": StepConfig("long_ctx_verify", 4, 64, 8, 128, 16, 64, (131072,) * 4,
+                                  (VERIFY,), 151936, "near_uniform", 1238),
+}
+CONFIG_ORDER = list(CONFIGS)
+
+
+def config(name: str) -> StepConfig:
+    return CONFIGS[name]
+
+
+# ---------------------------------------------------------------------------
+# Structure: sequence lengths, page pool permutation, block tables (numpy).
+
+def seq_lens_for(cfg: StepConfig, rng: np.random.Generator) -> np.ndarray:
+    if len(cfg.ctx) == 1 and isinstance(cfg.ctx[0], tuple):
+        lo, hi = cfg.ctx[0]
+        return rng.integers(lo, hi + 1, size=cfg.bs, dtype=np.int64).astype(np.int32)
+    assert len(cfg.ctx) == cfg.bs
+    return np.asarray(cfg.ctx, dtype=np.int32)
+
+
+def paging_for(seq_lens: np.ndarray, B: int, page_size: int, rng: np.random.Generator,
+               extra_pages: int = 0, max_pages_per_req: int | None = None):
+    """Each request owns ceil((L+B)/ps) pages drawn from a randomly permuted pool.
+
+    Returns (block_table [bs, max_pages] int32 with -1 past the owned pages, num_pages).
+    """
+    need = [(int(L) + B + page_size - 1) // page_size for L in seq_lens]
+    total = sum(need) + extra_pages
+    perm = rng.permutation(total).astype(np.int32)
+    max_pages = max(need) if max_pages_per_req is None else max_pages_per_req
+    table = np.full((len(seq_lens), max_pages), -1, dtype=np.int32)
+    at = 0
+    for r, n in enumerate(need):
+        table[r, :n] = perm[at:at + n]
+        at += n
+    return table, total
+
+
+@dataclasses.dataclass
+class AttnInputs:
+    cfg: StepConfig
+    seq_lens: np.ndarray        # [bs] int32, committed context length L_r
+    block_table: np.ndarray     # [bs, max_pages] int32
+    num_pages: int
+    q: torch.Tensor             # [bs*B, Hq, D] bf16
+    k_cache: torch.Tensor       # [num_pages*ps, Hkv, D] bf16
+    v_cache: torch.Tensor       # [num_pages*ps, Hkv, D] bf16
+    scale: float
+
+    @property
+    def max_ctx_len(self) -> int:
+        return int(self.seq_lens.max())
+
+
+def _gen(device, seed: int) -> torch.Generator:
+    g = torch.Generator(device=device)
+    g.manual_seed(seed)
+    return g
+
+
+def randn_bf16(shape, g: torch.Generator, device) -> torch.Tensor:
+    return torch.randn(shape, generator=g, device=device, dtype=torch.float32).to(torch.bfloat16)
+
+
+def make_attn_inputs(cfg: StepConfig, device="cpu", seed: int | None = None,
+                     seq_lens: np.ndarray | None = None, extra_pages: int = 0) -> AttnInputs:
+    seed = cfg.seed if seed is None else seed
+    rng = np.random.Generator(np.random.PCG64(seed))
+    if seq_lens is None:
+        seq_lens = seq_lens_for(cfg, rng)
+    seq_lens = np.asarray(seq_lens, dtype=np.int32)
+    table, num_pages = paging_for(seq_lens, cfg.B, cfg.page_size, rng, extra_pages)
+    g = _gen(device, seed)
+    slots = num_pages * cfg.page_size
+    q = randn_bf16((cfg.bs * cfg.B, cfg.Hq, cfg.D), g, device)
+    k = randn_bf16((slots, cfg.Hkv, cfg.D), g, device)
+    v = randn_bf16((slots, cfg.Hkv, cfg.D), g, device)
+    return AttnInputs(cfg, seq_lens, table, num_pages, q, k, v, 1.0 / math.sqrt(cfg.D))
+
+
+# ---------------------------------------------------------------------------
+# Acceptance inputs: verifier p, draft q, drafts sampled from q, uniforms.
+
+@dataclasses.dataclass
+class AcceptInputs:
+    block_ids: torch.Tensor     # [bs, B] int32: verified token, then drafts d_1..d_{B-1}
+    p: torch.Tensor             # [bs, B, V] fp32
+    q: torch.Tensor             # [bs, B-1, V] fp32
+    u_acc: torch.Tensor         # [bs, B-1] fp32 in [0, 1)
+    u_samp: torch.Tensor        # [bs] fp32 in [0, 1)
+    seq_lens: torch.Tensor      # [bs] int32
+
+
+def make_accept_inputs(cfg: StepConfig, device="cpu", seed: int | None = None,
+                       bs: int | None = None, seq_lens: np.ndarray | None = None) -> AcceptInputs:
+    seed = (cfg.seed if seed is None else seed) + 7919
+    bs = cfg.bs if bs is None else bs
+    B, V = cfg.B, cfg.V
+    g = _gen(device, seed)
+    f32 = torch.float32
+    if cfg.accept == "indep2":
+        p = torch.softmax(2.0 * torch.randn((bs, B, V), generator=g, device=device, dtype=f32), -1)
+        q = torch.softmax(2.0 * torch.randn((bs, B - 1, V), generator=g, device=device,
+                                            dtype=f32), -1)
+    elif cfg.accept == "perturb":
+        logits = 3.0 * torch.randn((bs, B, V), generator=g, device=device, dtype=f32)
+        p = torch.softmax(logits, -1)
+        noise = torch.randn((bs, B - 1, V), generator=g, device=device, dtype=f32)
+        q = torch.softmax(logits[:, :B - 1] + noise, -1)
+        del logits, noise
+    elif cfg.accept == "near_uniform":
+        p = torch.softmax(3.0 * torch.randn((bs, B, V), generator=g, device=device, dtype=f32), -1)
+        q = torch.softmax(0.1 * torch.randn((bs, B - 1, V), generator=g, device=device,
+                                            dtype=f32), -1)
+    else:
+        raise ValueError(f"config {cfg.name} has no acceptance stage")
+    drafts = torch.multinomial(q.reshape(-1, V), 1, generator=g).reshape(bs, B - 1)
+    verified = torch.randint(0, V, (bs, 1), generator=g, device=device)
+    block_ids = torch.cat([verified, drafts], dim=1).to(torch.int32).contiguous()
+    u_acc = torch.rand((bs, B - 1), generator=g, device=device, dtype=f32)
+    u_samp = torch.rand((bs,), generator=g, device=device, dtype=f32)
+    if seq_lens is None:
+        seq_lens = torch.randint(1, 4096, (bs,), generator=g, device=device).to(torch.int32)
+    else:
+        seq_lens = torch.as_tensor(np.asarray(seq_lens, np.int32), device=device)
+    return AcceptInputs(block_ids, p.contiguous(), q.contiguous(), u_acc, u_samp, seq_lens)
+
+
+def draft_from(q_rows: np.ndarray, u: np.ndarray) -> np.ndarray:
+    """Inverse-CDF draws from rows of q (numpy, for small host-side workloads)."""
+    c = np.cumsum(q_rows.astype(np.float64), axis=-1)
+    idx = (c < (u[..., None] * c[..., -1:])).sum(-1)
+    return np.minimum(idx, q_rows.shape[-1] - 1).astype(np.int32)
+
+
+def bf16_bits(t: torch.Tensor) -> np.ndarray:
+    """uint16 bit patterns of a bf16 tensor (host copy)."""
+    return t.detach().cpu().contiguous().view(torch.int16).numpy().view(np.uint16)

@@ -1,0 +1,170 @@
+"""fp64 CPU oracle for the block-diffusion draft/verify step (test infrastructure).
+
+This package is the checker, not the product.  Only ``tests/``, the smoke check
+in ``__graft_entry__`` and the CPU-baseline leg of ``bench.py`` import it.  The
+CUDA library never links or calls it, and it shares no code with the library:
+the arithmetic lives in ``bdsa_oracle.c`` (plain C, fp64), written from the
+source pages' definitions:
+
+* prepare block -- "From DFlash to dLLM Self-Spec (II): SGLang Spec V2",
+  section 2.2.2; "... (IV)", section 4.4.1 (block init).
+* block attention masks -- "SGLang dLLM / LLaDA 2.0", section "Attention Mask";
+  "... (IV)", section 4.4.1 (causal verify over the past KV).
+* acceptance -- "... (IV)", section 4.3.1 (min(1, p/q), correction token);
+  "Unlocking Lossless Speedups in LLMs via Discrete Diffusion", background on
+  speculative decoding and the Psi-Spec step (longest accepted prefix, residual
+  resampling, first token always accepted); "... (II)", section 2.2.5 (greedy
+  accept/bonus, commit_len = accept_len + 1).
+
+Pins (tests/test_oracle_*.py): torch CPU scaled_dot_product_attention in fp64
+(causal prefill / unmasked / decode special cases), closed forms (constant V,
+zero Q with lse = log n), page-permutation invariance, hand-worked acceptance
+fixtures under tests/golden/, numpy searchsorted for the sampling rule, and the
+lossless property by chi-square and the 1 - TV acceptance rate.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import subprocess
+
+import numpy as np
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_SRC = os.path.join(_HERE, "bdsa_oracle.c")
+_LIB = os.path.join(_HERE, "liboracle.so")
+_lib = None
+
+
+def build(force: bool = False) -> str:
+    """Compile bdsa_oracle.c into liboracle.so (gcc, -O2, OpenMP, strict fp)."""
+    if force or not os.path.exists(_LIB) or os.path.getmtime(_LIB) < os.path.getmtime(_SRC):
+        cmd = ["gcc", "-O2", "-std=c11", "-fPIC", "-shared", "-fopenmp",
+               "-ffp-contract=off", "-fno-fast-math", "-o", _LIB + ".tmp", _SRC, "-lm"]
+        subprocess.check_call(cmd)
+        os.replace(_LIB + ".tmp", _LIB)
+    return _LIB
+
+
+def _load():
+    global _lib
+    if _lib is None:
+        build()
+        lib = ctypes.CDLL(_LIB)
+        P = ctypes.c_void_p
+        i32, i64, f64 = ctypes.c_int32, ctypes.c_int64, ctypes.c_double
+        lib.oracle_prepare_block.argtypes = [P, P, P, i32, i32, i32, i32, i32, i32, P, P, P]
+        lib.oracle_prepare_block.restype = i32
+        lib.oracle_block_attn.argtypes = [P, P, P, P, i32, i32, P, i32, i32, i32, i32, i32,
+                                          i32, f64, i32, P, P, i32]
+        lib.oracle_block_attn.restype = i32
+        lib.oracle_spec_accept.argtypes = [P, P, i64, i64, P, i64, i64, P, P, P, i32, i32, i32,
+                                           P, P, P, P, P, P, i32]
+        lib.oracle_spec_accept.restype = None
+        lib.oracle_inv_cdf.argtypes = [P, i32, f64, P]
+        lib.oracle_inv_cdf.restype = i32
+        lib.oracle_max_threads.argtypes = []
+        lib.oracle_max_threads.restype = i32
+        _lib = lib
+    return _lib
+
+
+def _ptr(a: np.ndarray | None):
+    return None if a is None else a.ctypes.data_as(ctypes.c_void_p)
+
+
+def _c(a, dtype):
+    return np.ascontiguousarray(a, dtype=dtype)
+
+
+def max_threads() -> int:
+    return int(_load().oracle_max_threads())
+
+
+def prepare_block(verified_id, seq_lens, block_table, num_pages, B, page_size, mask_token_id):
+    """Returns (block_ids, positions, cache_loc, n_out_of_range), each [bs, B] int32."""
+    lib = _load()
+    verified_id = _c(verified_id, np.int32)
+    seq_lens = _c(seq_lens, np.int32)
+    block_table = _c(block_table, np.int32)
+    bs, max_pages = block_table.shape
+    block_ids = np.empty((bs, B), np.int32)
+    positions = np.empty((bs, B), np.int32)
+    cache_loc = np.empty((bs, B), np.int32)
+    bad = lib.oracle_prepare_block(_ptr(verified_id), _ptr(seq_lens), _ptr(block_table),
+                                   max_pages, num_pages, bs, B, page_size, mask_token_id,
+                                   _ptr(block_ids), _ptr(positions), _ptr(cache_loc))
+    return block_ids, positions, cache_loc, int(bad)
+
+
+def block_attn(q_bits, k_bits, v_bits, block_table, seq_lens, B, Hq, Hkv, D, page_size,
+               scale, mode, num_pages=None, nthreads=1):
+    """fp64 block attention.
+
+    q_bits: uint16 bf16 bit patterns [bs*B, Hq, D]; k_bits/v_bits: [slots, Hkv, D].
+    mode: 0 = DRAFT (bidirectional block), 1 = VERIFY (token-causal block).
+    Returns (out [bs*B, Hq, D] fp64, lse [bs*B, Hq] fp64 natural log).
+    """
+    lib = _load()
+    q_bits = _c(q_bits, np.uint16)
+    k_bits = _c(k_bits, np.uint16)
+    v_bits = _c(v_bits, np.uint16)
+    block_table = _c(block_table, np.int32)
+    seq_lens = _c(seq_lens, np.int32)
+    bs, max_pages = block_table.shape
+    if num_pages is None:
+        num_pages = k_bits.shape[0] // page_size
+    out = np.empty((bs * B, Hq, D), np.float64)
+    lse = np.empty((bs * B, Hq), np.float64)
+    bad = lib.oracle_block_attn(_ptr(q_bits), _ptr(k_bits), _ptr(v_bits), _ptr(block_table),
+                                max_pages, num_pages, _ptr(seq_lens), bs, B, Hq, Hkv, D,
+                                page_size, float(scale), int(mode), _ptr(out), _ptr(lse),
+                                int(nthreads))
+    if bad:
+        raise ValueError(f"oracle: {bad} rows referenced out-of-range pages")
+    return out, lse
+
+
+def spec_accept(block_ids, p, q, u_acc, u_samp, seq_lens, *, p_strides=None, q_strides=None,
+                V=None, nthreads=1):
+    """Speculative acceptance (stochastic if q is not None, else greedy).
+
+    p: fp32 [bs, B, V] (or any array addressed through p_strides=(stride_r, stride_i)),
+    q: fp32 [bs, B-1, V] or None.  Returns dict of int32 arrays and 'flags'.
+    """
+    lib = _load()
+    block_ids = _c(block_ids, np.int32)
+    bs, B = block_ids.shape
+    p = np.ascontiguousarray(p, dtype=np.float32)
+    if V is None:
+        V = p.shape[-1]
+    if p_strides is None:
+        p_strides = (B * V, V)
+    if q is not None:
+        q = np.ascontiguousarray(q, dtype=np.float32)
+        if q_strides is None:
+            q_strides = ((B - 1) * V, V)
+    else:
+        q_strides = (0, 0)
+    u_acc = _c(u_acc, np.float32)
+    u_samp = _c(u_samp, np.float32)
+    seq_lens = _c(seq_lens, np.int32)
+    out = {k: np.empty(bs, np.int32) for k in ("accept_len", "commit_len", "bonus_id",
+                                                "new_seq_lens", "flags")}
+    out["out_tokens"] = np.empty((bs, B), np.int32)
+    lib.oracle_spec_accept(_ptr(block_ids), _ptr(p), p_strides[0], p_strides[1], _ptr(q),
+                           q_strides[0], q_strides[1], _ptr(u_acc), _ptr(u_samp),
+                           _ptr(seq_lens), bs, B, V, _ptr(out["accept_len"]),
+                           _ptr(out["commit_len"]), _ptr(out["out_tokens"]),
+                           _ptr(out["bonus_id"]), _ptr(out["new_seq_lens"]), _ptr(out["flags"]),
+                           int(nthreads))
+    return out
+
+
+def inv_cdf(w, u):
+    """InvCDF(w, u): smallest k with C_k > u*S (fp64 sums).  Returns (k, near_flag)."""
+    lib = _load()
+    w = _c(w, np.float32)
+    flag = np.zeros(1, np.int32)
+    k = lib.oracle_inv_cdf(_ptr(w), w.shape[0], float(u), _ptr(flag))
+    return int(k), bool(flag[0])

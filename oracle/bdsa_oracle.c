@@ -1,0 +1,368 @@
+/*
+ * bdsa_oracle.c -- plain, slow, fp64 CPU oracle for one block-diffusion
+ * draft/verify step over a paged KV cache.
+ *
+ * TEST INFRASTRUCTURE ONLY.  Nothing on the product path links, loads or
+ * calls this file: only tests/, the smoke check and the CPU-baseline leg of
+ * bench.py do.  It shares no code, header, table or constant with the CUDA
+ * library; it is written directly from the definitions on the source pages:
+ *
+ *   [P1] "From DFlash to dLLM Self-Spec (IV): Self-Spec dLLM & AR Uni-Model",
+ *        sections 4.3.1 (p/q acceptance) and 4.4.1 (LinearSpec block init,
+ *        causal verify, greedy longest-prefix loop with bonus).
+ *   [P2] "Unlocking Lossless Speedups in LLMs via Discrete Diffusion",
+ *        background on speculative decoding / rejection sampling and the
+ *        Psi-Spec sampling step (first token always accepted, longest
+ *        accepted prefix, residual resampling).
+ *   [P3] "From DFlash to dLLM Self-Spec (II): SGLang Spec V2", sections 2.2.2
+ *        (prepare block: block_ids / positions / cache_loc) and 2.2.5
+ *        (greedy accept/bonus rule, commit_len = accept_len + 1).
+ *   [P4] "SGLang dLLM / LLaDA 2.0", section "Attention Mask" (context query
+ *        sees the whole cache; intra-block query is a rectangle in block
+ *        diffusion, a token-causal trapezoid in chunked prefill).
+ *
+ * Every floating-point quantity is computed in fp64 from inputs widened
+ * exactly (bf16 -> fp64, fp32 -> fp64), except the two decisions whose
+ * precision the boundary fixes in fp32: the acceptance ratio p/q and the
+ * residual weights max(0, p - q).  Loops follow the definitions literally: no
+ * blocking, no fusion, no reordering beyond an OpenMP split over independent
+ * outputs.
+ */
+#include <math.h>
+#include <stdint.h>
+#include <stdlib.h>
+#include <string.h>
+
+#ifdef _OPENMP
+#include <omp.h>
+#endif
+
+/* ------------------------------------------------------------------------ */
+/* bf16 -> fp64, exact: a bf16 value is the top 16 bits of an IEEE fp32.     */
+static double bf16_to_f64(uint16_t h) {
+    uint32_t bits = ((uint32_t)h) << 16;
+    float f;
+    memcpy(&f, &bits, sizeof f);
+    return (double)f;
+}
+
+/* ------------------------------------------------------------------------ */
+/* prepare_block  [P3 2.2.2; P1 4.4.1 block init; P3 2.3.5 planning_len]
+ *
+ * For request r and block slot i in [0, B):
+ *   block_ids[r,i] = verified_id[r] if i == 0 else mask_token_id
+ *   positions[r,i] = L_r + i                       (L_r = seq_lens[r])
+ *   cache_loc[r,i] = page * page_size + (L_r + i) % page_size,
+ *                    page = block_table[r, (L_r + i) / page_size]
+ * Returns the number of (r,i) whose page lookup was out of range (those get
+ * cache_loc = -1).
+ */
+int oracle_prepare_block(const int32_t *verified_id, const int32_t *seq_lens,
+                         const int32_t *block_table, int max_pages_per_req,
+                         int num_pages, int bs, int B, int page_size,
+                         int mask_token_id, int32_t *block_ids,
+                         int32_t *positions, int32_t *cache_loc) {
+    int bad = 0;
+    for (int r = 0; r < bs; ++r) {
+        for (int i = 0; i < B; ++i) {
+            long pos = (long)seq_lens[r] + i;
+            block_ids[r * B + i] = (i == 0) ? verified_id[r] : mask_token_id;
+            positions[r * B + i] = (int32_t)pos;
+            long page_idx = pos / page_size;
+            int32_t loc = -1;
+            if (seq_lens[r] >= 0 && page_idx < max_pages_per_req) {
+                int32_t page = block_table[(long)r * max_pages_per_req + page_idx];
+                if (page >= 0 && page < num_pages)
+                    loc = (int32_t)((long)page * page_size + pos % page_size);
+            }
+            if (loc < 0) ++bad;
+            cache_loc[r * B + i] = loc;
+        }
+    }
+    return bad;
+}
+
+/* ------------------------------------------------------------------------ */
+/* Block attention over a paged cache  [P4 "Attention Mask"; P1 4.4.1;
+ * P3 2.2.3-2.2.4]
+ *
+ * One output row: request r, block row i, query head j.  KV head h = j / G
+ * (G = Hq / Hkv, contiguous groups).  Keys t in [0, L_r + B); key t of
+ * request r lives at cache slot block_table[r, t/ps] * ps + t % ps.
+ *   allowed(i, t) = t < L_r  (context query: whole cache)
+ *                   or mode == DRAFT (0)   (rectangular intra-block mask)
+ *                   or (t - L_r) <= i      (VERIFY (1): token-causal)
+ *   s_t = scale * <q[r,i,j], k[t,h]>
+ *   o   = sum_t softmax(s)_t v[t,h],   lse = log sum_t exp(s_t)
+ * Written as a two-pass softmax: scores, max, exp-sum, weighted sum.
+ * Returns 0, or -1 if a needed page id is out of range.
+ */
+static int attn_one_row(const uint16_t *q, const uint16_t *k_cache,
+                        const uint16_t *v_cache, const int32_t *block_table,
+                        int max_pages_per_req, int num_pages,
+                        const int32_t *seq_lens, int B, int Hq, int Hkv, int D,
+                        int page_size, double scale, int mode, int r, int i,
+                        int j, double *scores, double *out_row,
+                        double *lse_out) {
+    int G = Hq / Hkv;
+    int h = j / G;
+    long L = seq_lens[r];
+    long n_keys = L + B;
+    const uint16_t *qrow = q + (((long)r * B + i) * Hq + j) * D;
+
+    double smax = -INFINITY;
+    for (long t = 0; t < n_keys; ++t) {
+        int allowed = (t < L) || (mode == 0) || (t - L <= i);
+        if (!allowed) {
+            scores[t] = -INFINITY;
+            continue;
+        }
+        long page_idx = t / page_size;
+        if (page_idx >= max_pages_per_req) return -1;
+        int32_t page = block_table[(long)r * max_pages_per_req + page_idx];
+        if (page < 0 || page >= num_pages) return -1;
+        long slot = (long)page * page_size + t % page_size;
+        const uint16_t *krow = k_cache + (slot * Hkv + h) * D;
+        double dot = 0.0;
+        for (int d = 0; d < D; ++d) dot += bf16_to_f64(qrow[d]) * bf16_to_f64(krow[d]);
+        scores[t] = scale * dot;
+        if (scores[t] > smax) smax = scores[t];
+    }
+    double denom = 0.0;
+    for (long t = 0; t < n_keys; ++t) {
+        if (scores[t] == -INFINITY) continue;
+        denom += exp(scores[t] - smax);
+    }
+    for (int d = 0; d < D; ++d) out_row[d] = 0.0;
+    for (long t = 0; t < n_keys; ++t) {
+        if (scores[t] == -INFINITY) continue;
+        double w = exp(scores[t] - smax) / denom;
+        long page_idx = t / page_size;
+        int32_t page = block_table[(long)r * max_pages_per_req + page_idx];
+        long slot = (long)page * page_size + t % page_size;
+        const uint16_t *vrow = v_cache + (slot * Hkv + h) * D;
+        for (int d = 0; d < D; ++d) out_row[d] += w * bf16_to_f64(vrow[d]);
+    }
+    if (lse_out) *lse_out = smax + log(denom);
+    return 0;
+}
+
+/* Full attention: out is [bs*B, Hq, D] fp64, lse is [bs*B, Hq] fp64 (may be
+ * NULL).  Requests are independent; OpenMP splits over (r, j) pairs when
+ * nthreads > 1.  Returns the number of rows that hit an out-of-range page. */
+int oracle_block_attn(const uint16_t *q, const uint16_t *k_cache,
+                      const uint16_t *v_cache, const int32_t *block_table,
+                      int max_pages_per_req, int num_pages,
+                      const int32_t *seq_lens, int bs, int B, int Hq, int Hkv,
+                      int D, int page_size, double scale, int mode,
+                      double *out, double *lse, int nthreads) {
+    long max_keys = 0;
+    for (int r = 0; r < bs; ++r)
+        if ((long)seq_lens[r] + B > max_keys) max_keys = (long)seq_lens[r] + B;
+    int bad = 0;
+    long units = (long)bs * Hq;
+#ifdef _OPENMP
+    if (nthreads < 1) nthreads = 1;
+#pragma omp parallel num_threads(nthreads) reduction(+ : bad)
+#endif
+    {
+        double *scores = (double *)malloc(sizeof(double) * (size_t)(max_keys > 0 ? max_keys : 1));
+#ifdef _OPENMP
+#pragma omp for schedule(dynamic, 1)
+#endif
+        for (long u = 0; u < units; ++u) {
+            int r = (int)(u / Hq), j = (int)(u % Hq);
+            for (int i = 0; i < B; ++i) {
+                long row = ((long)r * B + i) * Hq + j;
+                double l = 0.0;
+                int rc = attn_one_row(q, k_cache, v_cache, block_table, max_pages_per_req,
+                                      num_pages, seq_lens, B, Hq, Hkv, D, page_size, scale,
+                                      mode, r, i, j, scores, out + row * D, &l);
+                if (rc != 0) {
+                    ++bad;
+                    for (int d = 0; d < D; ++d) out[row * D + d] = NAN;
+                    l = NAN;
+                }
+                if (lse) lse[row] = l;
+            }
+        }
+        free(scores);
+    }
+    return bad;
+}
+
+/* ------------------------------------------------------------------------ */
+/* Speculative acceptance  [P1 4.3.1; P2 background + Psi-Spec step;
+ * P3 2.2.5; P1 4.4.1 greedy loop]
+ *
+ * Row r, draft tokens d_i = block_ids[r, i] for i = 1..B-1 (slot 0 is the
+ * already verified token and is never tested: the first token is always
+ * accepted).  p[r, i] is the verifier distribution for block slot i+1
+ * (p[r, B-1] is the bonus distribution); q[r, i-1] is the draft distribution
+ * d_i was drawn from.  Strides are in elements.
+ *
+ * Stochastic (q != NULL):
+ *   accept d_i  iff  u_acc[r, i-1] < min(1, p[i-1][d_i] / q[i-1][d_i])
+ *                (fp32 ratio, IEEE correctly rounded; q == 0 accepts iff p > 0)
+ *   a = number of leading accepted drafts
+ *   a <  B-1: token = InvCDF(max(0, p[a] - q[a]), u_samp)  (fp32 weights;
+ *             if they sum to 0, sample p[a] instead)
+ *   a == B-1: token = InvCDF(p[B-1], u_samp)              (bonus)
+ * Greedy (q == NULL):
+ *   a = number of leading i with d_i == argmax p[i-1]  (lowest index on ties)
+ *   token = argmax p[a]
+ * InvCDF(w, u) = smallest k with C_k > u * S, C_k = sum_{j<=k} w_j in index
+ * order, S = C_{V-1}, all sums in fp64.
+ * Outputs: accept_len = a, commit_len = a + 1, out_tokens[r] = d_1..d_a,
+ * token, -1 padding; bonus_id = token; new_seq_lens = seq_lens + a + 1.
+ * flags[r] (may be NULL) marks rows whose integer result is decided within
+ * the fp rounding margin and so is not unique across summation orders:
+ *   bit 0: some tested |p/q - u| < 1e-6 (fp64)
+ *   bit 1: u*S within 1e-6*S of C_{k-1} or C_k for the chosen k
+ *   bit 2: residual mass was zero, sampled from p
+ *   bit 3: a draft id was outside [0, V) (treated as rejected)
+ *   bit 4: greedy argmax had a tie at a deciding position
+ */
+static int inv_cdf_f32w(const float *w, int V, double u, int *flag_near) {
+    double S = 0.0;
+    for (int k = 0; k < V; ++k) S += (double)w[k];
+    double T = u * S;
+    double C = 0.0, Cprev = 0.0;
+    int chosen = -1;
+    for (int k = 0; k < V; ++k) {
+        Cprev = C;
+        C += (double)w[k];
+        if (C > T) {
+            chosen = k;
+            break;
+        }
+    }
+    if (chosen < 0) { /* rounding fallback: last positive-weight index */
+        for (int k = V - 1; k >= 0; --k)
+            if (w[k] > 0.0f) {
+                chosen = k;
+                break;
+            }
+        if (flag_near) *flag_near = 1;
+        return chosen;
+    }
+    if (flag_near && ((T - Cprev) < 1e-6 * S || (C - T) < 1e-6 * S)) *flag_near = 1;
+    return chosen;
+}
+
+static int argmax_lowest(const float *x, int V, int *tie) {
+    int best = 0;
+    for (int k = 1; k < V; ++k)
+        if (x[k] > x[best]) best = k;
+    if (tie) {
+        *tie = 0;
+        for (int k = 0; k < V; ++k)
+            if (k != best && x[k] == x[best]) *tie = 1;
+    }
+    return best;
+}
+
+void oracle_spec_accept(const int32_t *block_ids, const float *p, int64_t p_stride_r,
+                        int64_t p_stride_i, const float *q, int64_t q_stride_r,
+                        int64_t q_stride_i, const float *u_acc, const float *u_samp,
+                        const int32_t *seq_lens, int bs, int B, int V, int32_t *accept_len,
+                        int32_t *commit_len, int32_t *out_tokens, int32_t *bonus_id,
+                        int32_t *new_seq_lens, int32_t *flags, int nthreads) {
+#ifdef _OPENMP
+    if (nthreads < 1) nthreads = 1;
+#pragma omp parallel num_threads(nthreads)
+#endif
+    {
+        float *w = (float *)malloc(sizeof(float) * (size_t)V);
+#ifdef _OPENMP
+#pragma omp for schedule(static)
+#endif
+        for (int r = 0; r < bs; ++r) {
+            int flag = 0;
+            const int32_t *ids = block_ids + (long)r * B;
+            int a = 0, token = -1;
+            if (q != NULL) {
+                for (int i = 1; i < B; ++i) {
+                    int d = ids[i];
+                    if (d < 0 || d >= V) {
+                        flag |= 8;
+                        break;
+                    }
+                    float pv = p[(long)r * p_stride_r + (long)(i - 1) * p_stride_i + d];
+                    float qv = q[(long)r * q_stride_r + (long)(i - 1) * q_stride_i + d];
+                    float u = u_acc[(long)r * (B - 1) + (i - 1)];
+                    int acc;
+                    if (qv == 0.0f) {
+                        acc = pv > 0.0f;
+                    } else {
+                        volatile float ratio = pv / qv; /* fp32, correctly rounded */
+                        float lim = ratio < 1.0f ? ratio : 1.0f;
+                        acc = u < lim;
+                        if (fabs((double)pv / (double)qv - (double)u) < 1e-6) flag |= 1;
+                    }
+                    if (!acc) break;
+                    ++a;
+                }
+                const float *pa = p + (long)r * p_stride_r + (long)a * p_stride_i;
+                int near = 0;
+                if (a < B - 1) {
+                    const float *qa = q + (long)r * q_stride_r + (long)a * q_stride_i;
+                    int any = 0;
+                    for (int k = 0; k < V; ++k) {
+                        float diff = pa[k] - qa[k]; /* fp32 */
+                        w[k] = diff > 0.0f ? diff : 0.0f;
+                        if (w[k] > 0.0f) any = 1;
+                    }
+                    if (!any) {
+                        flag |= 4;
+                        token = inv_cdf_f32w(pa, V, (double)u_samp[r], &near);
+                    } else {
+                        token = inv_cdf_f32w(w, V, (double)u_samp[r], &near);
+                    }
+                } else {
+                    token = inv_cdf_f32w(pa, V, (double)u_samp[r], &near);
+                }
+                if (near) flag |= 2;
+            } else {
+                for (int i = 1; i < B; ++i) {
+                    int tie = 0;
+                    int tp = argmax_lowest(p + (long)r * p_stride_r + (long)(i - 1) * p_stride_i, V, &tie);
+                    if (tie) flag |= 16;
+                    if (ids[i] != tp) break;
+                    ++a;
+                }
+                int tie = 0;
+                token = argmax_lowest(p + (long)r * p_stride_r + (long)a * p_stride_i, V, &tie);
+                if (tie) flag |= 16;
+            }
+            accept_len[r] = a;
+            commit_len[r] = a + 1;
+            for (int i = 0; i < B; ++i) {
+                int32_t v = -1;
+                if (i < a) v = ids[i + 1];
+                else if (i == a) v = token;
+                out_tokens[(long)r * B + i] = v;
+            }
+            bonus_id[r] = token;
+            new_seq_lens[r] = seq_lens[r] + a + 1;
+            if (flags) flags[r] = flag;
+        }
+        free(w);
+    }
+}
+
+/* Exposed for tests of the sampling rule itself. */
+int oracle_inv_cdf(const float *w, int V, double u, int32_t *flag_near) {
+    int near = 0;
+    int k = inv_cdf_f32w(w, V, u, &near);
+    if (flag_near) *flag_near = near;
+    return k;
+}
+
+int oracle_max_threads(void) {
+#ifdef _OPENMP
+    return omp_get_max_threads();
+#else
+    return 1;
+#endif
+}
