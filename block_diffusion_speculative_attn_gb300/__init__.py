@@ -1,0 +1,210 @@
+"""Block-diffusion self-speculative draft/verify step for NVIDIA GB300 (sm_103a).
+
+Thin Python binding over the C ABI of ``libbdsa.so`` (declared in
+``include/bdsa.h``).  This module only marshals arguments: it checks tensor
+dtypes/devices, allocates outputs and workspaces with torch, and passes raw
+device pointers plus the current CUDA stream.  Every step of the computation
+runs in the library's CUDA kernels; there is no fallback of any kind, and every
+call raises if the library is not built or a call returns an error status.
+
+Calls (all asynchronous on the current stream):
+  prepare_block     block ids / positions / cache slots of each request's block
+  block_attn_paged  block attention over the paged cache, DRAFT or VERIFY mask
+  spec_accept       lossless speculative acceptance (stochastic or greedy)
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+
+import torch
+
+DRAFT, VERIFY = 0, 1
+_HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_HERE, "libbdsa.so")
+
+STATUS = {0: "BDSA_OK", 1: "BDSA_INVALID_ARG", 2: "BDSA_UNSUPPORTED", 3: "BDSA_MISALIGNED",
+          4: "BDSA_WORKSPACE_TOO_SMALL", 5: "BDSA_CUDA_ERROR", 16: "BDSA_DEVICE_OUT_OF_RANGE",
+          17: "BDSA_DEVICE_TIMEOUT"}
+
+# Every symbol include/bdsa.h declares.
+EXPORTS = ("bdsa_status_string", "bdsa_version", "bdsa_prepare_block",
+           "bdsa_block_attn_workspace_bytes", "bdsa_block_attn_paged",
+           "bdsa_spec_accept_workspace_bytes", "bdsa_spec_accept")
+
+_lib = None
+
+
+class BdsaError(RuntimeError):
+    def __init__(self, fn: str, status: int):
+        self.status = status
+        super().__init__(f"{fn} failed: {STATUS.get(status, status)}")
+
+
+def lib() -> ctypes.CDLL:
+    """Load libbdsa.so (raises if it has not been built)."""
+    global _lib
+    if _lib is not None:
+        return _lib
+    if not os.path.exists(LIB_PATH):
+        raise RuntimeError(f"libbdsa.so is not built ({LIB_PATH}); run "
+                           "`python -c 'import __graft_entry__ as g; g.build()'`")
+    L = ctypes.CDLL(LIB_PATH)
+    P, i32, i64, f32, sz = (ctypes.c_void_p, ctypes.c_int32, ctypes.c_int64, ctypes.c_float,
+                            ctypes.c_size_t)
+    L.bdsa_status_string.argtypes = [i32]
+    L.bdsa_status_string.restype = ctypes.c_char_p
+    L.bdsa_version.argtypes = []
+    L.bdsa_version.restype = ctypes.c_char_p
+    L.bdsa_prepare_block.argtypes = [P, P, P, i32, i32, i32, i32, i32, i32, P, P, P, P, P]
+    L.bdsa_prepare_block.restype = i32
+    L.bdsa_block_attn_workspace_bytes.argtypes = [i32] * 7
+    L.bdsa_block_attn_workspace_bytes.restype = sz
+    L.bdsa_block_attn_paged.argtypes = [P, P, P, P, i32, i32, P, i32, i32, i32, i32, i32, i32,
+                                        i32, f32, i32, P, P, P, sz, i32, P, P]
+    L.bdsa_block_attn_paged.restype = i32
+    L.bdsa_spec_accept_workspace_bytes.argtypes = [i32] * 4
+    L.bdsa_spec_accept_workspace_bytes.restype = sz
+    L.bdsa_spec_accept.argtypes = [P, P, i64, i64, P, i64, i64, P, P, P, i32, i32, i32, P, P, P,
+                                   P, P, P, sz, i32, P, P]
+    L.bdsa_spec_accept.restype = i32
+    _lib = L
+    return L
+
+
+def _check(fn: str, status: int):
+    if status != 0:
+        raise BdsaError(fn, status)
+
+
+def _ptr(t):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def _stream(device) -> ctypes.c_void_p:
+    return ctypes.c_void_p(torch.cuda.current_stream(device).cuda_stream)
+
+
+def _dev(t: torch.Tensor, name: str, dtype) -> torch.Tensor:
+    if not isinstance(t, torch.Tensor) or not t.is_cuda:
+        raise ValueError(f"{name} must be a CUDA tensor")
+    if t.dtype != dtype:
+        raise TypeError(f"{name} must be {dtype}, got {t.dtype}")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+    return t
+
+
+def num_sms(device=None) -> int:
+    return torch.cuda.get_device_properties(device).multi_processor_count
+
+
+# ---------------------------------------------------------------------------
+def prepare_block(verified_id, seq_lens, block_table, num_pages: int, B: int, page_size: int,
+                  mask_token_id: int, out=None, dev_status=None):
+    """bdsa_prepare_block.  Returns (block_ids, positions, cache_loc), int32 [bs, B]."""
+    _dev(verified_id, "verified_id", torch.int32)
+    _dev(seq_lens, "seq_lens", torch.int32)
+    _dev(block_table, "block_table", torch.int32)
+    bs, max_pages = block_table.shape
+    if out is None:
+        out = tuple(torch.empty((bs, B), dtype=torch.int32, device=block_table.device)
+                    for _ in range(3))
+    for name, t in zip(("block_ids", "positions", "cache_loc"), out):
+        _dev(t, name, torch.int32)
+    st = lib().bdsa_prepare_block(_ptr(verified_id), _ptr(seq_lens), _ptr(block_table),
+                                  max_pages, num_pages, bs, B, page_size, mask_token_id,
+                                  _ptr(out[0]), _ptr(out[1]), _ptr(out[2]), _ptr(dev_status),
+                                  _stream(block_table.device))
+    _check("bdsa_prepare_block", st)
+    return out
+
+
+def block_attn_workspace_bytes(bs, B, Hq, Hkv, D, max_ctx_len, sms: int = 0) -> int:
+    return int(lib().bdsa_block_attn_workspace_bytes(bs, B, Hq, Hkv, D, max_ctx_len, sms))
+
+
+def block_attn_paged(q, k_cache, v_cache, block_table, seq_lens, *, B: int, page_size: int,
+                     scale: float, mode: int, max_ctx_len: int, num_pages: int | None = None,
+                     out=None, lse=None, workspace=None, dev_status=None, sms: int = 0):
+    """bdsa_block_attn_paged.  q [bs*B, Hq, D] bf16, caches [slots, Hkv, D] bf16.
+
+    Returns out [bs*B, Hq, D] bf16 (lse is filled when given, fp32 [bs*B, Hq]).
+    """
+    _dev(q, "q", torch.bfloat16)
+    _dev(k_cache, "k_cache", torch.bfloat16)
+    _dev(v_cache, "v_cache", torch.bfloat16)
+    _dev(block_table, "block_table", torch.int32)
+    _dev(seq_lens, "seq_lens", torch.int32)
+    bs, max_pages = block_table.shape
+    Hq, D = q.shape[1], q.shape[2]
+    Hkv = k_cache.shape[1]
+    if num_pages is None:
+        num_pages = k_cache.shape[0] // page_size
+    if out is None:
+        out = torch.empty_like(q)
+    _dev(out, "out", torch.bfloat16)
+    if lse is not None:
+        _dev(lse, "lse", torch.float32)
+    need = block_attn_workspace_bytes(bs, B, Hq, Hkv, D, max_ctx_len, sms)
+    if workspace is None and need > 0:
+        workspace = torch.empty(need, dtype=torch.uint8, device=q.device)
+    ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    st = lib().bdsa_block_attn_paged(_ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(block_table),
+                                     max_pages, num_pages, _ptr(seq_lens), int(max_ctx_len), bs,
+                                     B, Hq, Hkv, D, page_size, float(scale), int(mode), _ptr(out),
+                                     _ptr(lse), _ptr(workspace), ws_bytes, sms, _ptr(dev_status),
+                                     _stream(q.device))
+    _check("bdsa_block_attn_paged", st)
+    return out
+
+
+def spec_accept_workspace_bytes(bs, B, V, sms: int = 0) -> int:
+    return int(lib().bdsa_spec_accept_workspace_bytes(bs, B, V, sms))
+
+
+def spec_accept(block_ids, p, q, u_acc, u_samp, seq_lens, *, p_strides=None, q_strides=None,
+                V: int | None = None, out=None, workspace=None, dev_status=None, sms: int = 0):
+    """bdsa_spec_accept.  q=None selects greedy mode.
+
+    Returns dict with accept_len, commit_len, bonus_id, new_seq_lens ([bs] int32) and
+    out_tokens ([bs, B] int32).
+    """
+    _dev(block_ids, "block_ids", torch.int32)
+    _dev(seq_lens, "seq_lens", torch.int32)
+    if not (p.is_cuda and p.dtype == torch.float32):
+        raise TypeError("p must be a CUDA float32 tensor")
+    bs, B = block_ids.shape
+    V = p.shape[-1] if V is None else V
+    if p_strides is None:
+        _dev(p, "p", torch.float32)
+        p_strides = (B * V, V)
+    if q is not None:
+        if not (q.is_cuda and q.dtype == torch.float32):
+            raise TypeError("q must be a CUDA float32 tensor")
+        if q_strides is None:
+            _dev(q, "q", torch.float32)
+            q_strides = ((B - 1) * V, V)
+        _dev(u_acc, "u_acc", torch.float32)
+        _dev(u_samp, "u_samp", torch.float32)
+    else:
+        q_strides = (0, 0)
+    dev = block_ids.device
+    if out is None:
+        out = {k: torch.empty(bs, dtype=torch.int32, device=dev)
+               for k in ("accept_len", "commit_len", "bonus_id", "new_seq_lens")}
+        out["out_tokens"] = torch.empty((bs, B), dtype=torch.int32, device=dev)
+    need = spec_accept_workspace_bytes(bs, B, V, sms)
+    if workspace is None:
+        workspace = torch.empty(max(need, 256), dtype=torch.uint8, device=dev)
+    ws_bytes = workspace.numel() * workspace.element_size()
+    st = lib().bdsa_spec_accept(_ptr(block_ids), _ptr(p), int(p_strides[0]), int(p_strides[1]),
+                                _ptr(q), int(q_strides[0]), int(q_strides[1]),
+                                _ptr(u_acc) if q is not None else None,
+                                _ptr(u_samp) if q is not None else None, _ptr(seq_lens), bs, B,
+                                V, _ptr(out["accept_len"]), _ptr(out["commit_len"]),
+                                _ptr(out["out_tokens"]), _ptr(out["bonus_id"]),
+                                _ptr(out["new_seq_lens"]), _ptr(workspace), ws_bytes, sms,
+                                _ptr(dev_status), _stream(dev))
+    _check("bdsa_spec_accept", st)
+    return out

@@ -1,0 +1,178 @@
+// bdsa_api.cu -- the extern "C" boundary of libbdsa.so (declared in
+// include/bdsa.h): synchronous host-side argument checks, workspace sizing and
+// dispatch to the kernel launchers.  No call allocates device memory.
+#include <cuda_runtime.h>
+#include <math.h>
+#include <stdint.h>
+
+#include "../../include/bdsa.h"
+#include "bdsa_internal.h"
+
+namespace bdsa {
+
+int device_num_sms(int requested) {
+    if (requested > 0) return requested;
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return 148;
+    static int cache[64] = {0};
+    if (dev >= 0 && dev < 64 && cache[dev] > 0) return cache[dev];
+    int n = 0;
+    if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0)
+        n = 148;
+    if (dev >= 0 && dev < 64) cache[dev] = n;
+    return n;
+}
+
+}  // namespace bdsa
+
+namespace {
+
+bool aligned(const void *p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+
+bool pow2(int x) { return x > 0 && (x & (x - 1)) == 0; }
+
+}  // namespace
+
+extern "C" {
+
+const char *bdsa_status_string(int32_t status) {
+    switch (status) {
+        case BDSA_OK: return "BDSA_OK";
+        case BDSA_INVALID_ARG: return "BDSA_INVALID_ARG: invalid argument";
+        case BDSA_UNSUPPORTED: return "BDSA_UNSUPPORTED: shape not supported by this build";
+        case BDSA_MISALIGNED: return "BDSA_MISALIGNED: pointer or stride alignment";
+        case BDSA_WORKSPACE_TOO_SMALL: return "BDSA_WORKSPACE_TOO_SMALL";
+        case BDSA_CUDA_ERROR: return "BDSA_CUDA_ERROR: CUDA call or launch failed";
+        case BDSA_DEVICE_OUT_OF_RANGE: return "BDSA_DEVICE_OUT_OF_RANGE: index out of range on device";
+        case BDSA_DEVICE_TIMEOUT: return "BDSA_DEVICE_TIMEOUT: bounded device wait expired";
+        default: return "BDSA_UNKNOWN_STATUS";
+    }
+}
+
+const char *bdsa_version(void) { return "0.1.0"; }
+
+int32_t bdsa_prepare_block(const int32_t *verified_id, const int32_t *seq_lens,
+                           const int32_t *block_table, int32_t max_pages_per_req,
+                           int32_t num_pages, int32_t bs, int32_t B, int32_t page_size,
+                           int32_t mask_token_id, int32_t *block_ids, int32_t *positions,
+                           int32_t *cache_loc, int32_t *dev_status, void *stream) {
+    if (bs < 0 || B < 1 || page_size < 1 || max_pages_per_req < 1 || num_pages < 1)
+        return BDSA_INVALID_ARG;
+    if (bs == 0) return BDSA_OK;
+    if (!verified_id || !seq_lens || !block_table || !block_ids || !positions || !cache_loc)
+        return BDSA_INVALID_ARG;
+    if ((int64_t)bs * B > INT32_MAX) return BDSA_UNSUPPORTED;
+    return bdsa::launch_prepare_block(verified_id, seq_lens, block_table, max_pages_per_req,
+                                      num_pages, bs, B, page_size, mask_token_id, block_ids,
+                                      positions, cache_loc, dev_status,
+                                      static_cast<cudaStream_t>(stream));
+}
+
+size_t bdsa_block_attn_workspace_bytes(int32_t bs, int32_t B, int32_t Hq, int32_t Hkv, int32_t D,
+                                       int32_t max_ctx_len, int32_t num_sms) {
+    if (bs <= 0 || B <= 0 || Hq <= 0 || Hkv <= 0 || D <= 0 || max_ctx_len < 0) return 0;
+    return bdsa::attn_plan(bs, B, Hq, Hkv, D, max_ctx_len, bdsa::device_num_sms(num_sms))
+        .workspace;
+}
+
+int32_t bdsa_block_attn_paged(const bdsa_bf16 *q, const bdsa_bf16 *k_cache,
+                              const bdsa_bf16 *v_cache, const int32_t *block_table,
+                              int32_t max_pages_per_req, int32_t num_pages,
+                              const int32_t *seq_lens, int32_t max_ctx_len, int32_t bs,
+                              int32_t B, int32_t Hq, int32_t Hkv, int32_t D, int32_t page_size,
+                              float softmax_scale, int32_t mode, bdsa_bf16 *out, float *lse,
+                              void *workspace, size_t workspace_bytes, int32_t num_sms,
+                              int32_t *dev_status, void *stream) {
+    if (bs < 0 || B < 1 || Hq < 1 || Hkv < 1 || max_pages_per_req < 1 || num_pages < 1 ||
+        max_ctx_len < 0 || !isfinite(softmax_scale) ||
+        (mode != BDSA_MODE_DRAFT && mode != BDSA_MODE_VERIFY))
+        return BDSA_INVALID_ARG;
+    if (bs == 0) return BDSA_OK;
+    if (!q || !k_cache || !v_cache || !block_table || !seq_lens || !out) return BDSA_INVALID_ARG;
+    if (Hq % Hkv != 0) return BDSA_INVALID_ARG;
+    if (D != 64 && D != 128) return BDSA_UNSUPPORTED;
+    if (B > 64 || (Hq / Hkv) * B > 128) return BDSA_UNSUPPORTED;
+    if (!pow2(page_size) || page_size < 8) return BDSA_UNSUPPORTED;
+    if ((int64_t)num_pages * page_size > INT32_MAX) return BDSA_UNSUPPORTED;
+    if ((int64_t)bs * B > INT32_MAX) return BDSA_UNSUPPORTED;
+    if (!aligned(q, 16) || !aligned(k_cache, 16) || !aligned(v_cache, 16) || !aligned(out, 16) ||
+        (lse && !aligned(lse, 4)) || (workspace && !aligned(workspace, 256)))
+        return BDSA_MISALIGNED;
+    bdsa::AttnArgs a;
+    a.q = reinterpret_cast<const uint16_t *>(q);
+    a.k_cache = reinterpret_cast<const uint16_t *>(k_cache);
+    a.v_cache = reinterpret_cast<const uint16_t *>(v_cache);
+    a.block_table = block_table;
+    a.seq_lens = seq_lens;
+    a.max_pages = max_pages_per_req;
+    a.num_pages = num_pages;
+    a.max_ctx_len = max_ctx_len;
+    a.bs = bs;
+    a.B = B;
+    a.Hq = Hq;
+    a.Hkv = Hkv;
+    a.D = D;
+    a.page_size = page_size;
+    a.mode = mode;
+    a.num_sms = bdsa::device_num_sms(num_sms);
+    a.scale = softmax_scale;
+    a.out = reinterpret_cast<uint16_t *>(out);
+    a.lse = lse;
+    a.workspace = workspace;
+    a.workspace_bytes = workspace_bytes;
+    a.dev_status = dev_status;
+    return bdsa::launch_block_attn(a, static_cast<cudaStream_t>(stream));
+}
+
+size_t bdsa_spec_accept_workspace_bytes(int32_t bs, int32_t B, int32_t V, int32_t num_sms) {
+    if (bs <= 0 || B <= 0 || V <= 0) return 0;
+    return bdsa::accept_plan(bs, B, V, bdsa::device_num_sms(num_sms)).workspace;
+}
+
+int32_t bdsa_spec_accept(const int32_t *block_ids, const float *p, int64_t p_stride_r,
+                         int64_t p_stride_i, const float *q, int64_t q_stride_r,
+                         int64_t q_stride_i, const float *u_acc, const float *u_samp,
+                         const int32_t *seq_lens, int32_t bs, int32_t B, int32_t V,
+                         int32_t *accept_len, int32_t *commit_len, int32_t *out_tokens,
+                         int32_t *bonus_id, int32_t *new_seq_lens, void *workspace,
+                         size_t workspace_bytes, int32_t num_sms, int32_t *dev_status,
+                         void *stream) {
+    if (bs < 0 || B < 1 || V < 1 || p_stride_r < 0 || p_stride_i < 0 || q_stride_r < 0 ||
+        q_stride_i < 0)
+        return BDSA_INVALID_ARG;
+    if (bs == 0) return BDSA_OK;
+    if (B > 64) return BDSA_UNSUPPORTED;
+    if (bs > 65535) return BDSA_UNSUPPORTED;
+    if (!block_ids || !p || !seq_lens || !accept_len || !commit_len || !out_tokens || !bonus_id ||
+        !new_seq_lens)
+        return BDSA_INVALID_ARG;
+    if (q != nullptr && (!u_samp || (B > 1 && !u_acc))) return BDSA_INVALID_ARG;
+    if (!aligned(p, 4) || (q && !aligned(q, 4)) || (workspace && !aligned(workspace, 256)))
+        return BDSA_MISALIGNED;
+    bdsa::AcceptArgs a;
+    a.block_ids = block_ids;
+    a.p = p;
+    a.q = q;
+    a.psr = p_stride_r;
+    a.psi = p_stride_i;
+    a.qsr = q_stride_r;
+    a.qsi = q_stride_i;
+    a.u_acc = u_acc;
+    a.u_samp = u_samp;
+    a.seq_lens = seq_lens;
+    a.bs = bs;
+    a.B = B;
+    a.V = V;
+    a.num_sms = bdsa::device_num_sms(num_sms);
+    a.accept_len = accept_len;
+    a.commit_len = commit_len;
+    a.out_tokens = out_tokens;
+    a.bonus_id = bonus_id;
+    a.new_seq_lens = new_seq_lens;
+    a.workspace = workspace;
+    a.workspace_bytes = workspace_bytes;
+    a.dev_status = dev_status;
+    return bdsa::launch_spec_accept(a, static_cast<cudaStream_t>(stream));
+}
+
+}  // extern "C"

@@ -1,0 +1,69 @@
+// bdsa_internal.h -- host-side launch interfaces shared between the C ABI
+// (bdsa_api.cu) and the kernel translation units.  Not installed.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stddef.h>
+#include <stdint.h>
+
+namespace bdsa {
+
+// ---------------------------------------------------------------- attention
+struct AttnPlan {
+    int nsplit;           // KV splits per (request, KV head)
+    int tiles_per_split;  // 128-key tiles per split
+    size_t workspace;     // bytes of split partials (0 when nsplit == 1)
+};
+
+AttnPlan attn_plan(int bs, int B, int Hq, int Hkv, int D, int max_ctx_len, int num_sms);
+
+struct AttnArgs {
+    const uint16_t *q, *k_cache, *v_cache;
+    const int32_t *block_table, *seq_lens;
+    int max_pages, num_pages, max_ctx_len, bs, B, Hq, Hkv, D, page_size, mode, num_sms;
+    float scale;
+    uint16_t *out;
+    float *lse;
+    void *workspace;
+    size_t workspace_bytes;
+    int32_t *dev_status;
+};
+
+// Returns a bdsa_status code.
+int launch_block_attn(const AttnArgs &a, cudaStream_t stream);
+
+// ---------------------------------------------------------------- prepare
+int launch_prepare_block(const int32_t *verified_id, const int32_t *seq_lens,
+                         const int32_t *block_table, int max_pages, int num_pages, int bs, int B,
+                         int page_size, int mask_token_id, int32_t *block_ids,
+                         int32_t *positions, int32_t *cache_loc, int32_t *dev_status,
+                         cudaStream_t stream);
+
+// ---------------------------------------------------------------- accept
+struct AcceptPlan {
+    int nchunk;       // CTAs per row
+    int nseg;         // 256-element segments per vocabulary row
+    size_t workspace; // bytes
+};
+
+AcceptPlan accept_plan(int bs, int B, int V, int num_sms);
+
+struct AcceptArgs {
+    const int32_t *block_ids;
+    const float *p, *q;
+    int64_t psr, psi, qsr, qsi;
+    const float *u_acc, *u_samp;
+    const int32_t *seq_lens;
+    int bs, B, V, num_sms;
+    int32_t *accept_len, *commit_len, *out_tokens, *bonus_id, *new_seq_lens;
+    void *workspace;
+    size_t workspace_bytes;
+    int32_t *dev_status;
+};
+
+int launch_spec_accept(const AcceptArgs &a, cudaStream_t stream);
+
+// ---------------------------------------------------------------- misc
+int device_num_sms(int requested);
+
+}  // namespace bdsa

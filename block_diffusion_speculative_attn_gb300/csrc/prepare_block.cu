@@ -1,0 +1,55 @@
+// prepare_block.cu -- per-round block layout in one launch.
+//
+// "From DFlash to dLLM Self-Spec (II): SGLang Spec V2", section 2.2.2: the
+// block starts with the last verified token, every other slot holds the mask
+// token, and positions / cache locations are prepared in the same kernel
+// instead of a chain of small eager ops.  One thread per (request, slot).
+#include <cuda_runtime.h>
+
+#include "bdsa_device.cuh"
+#include "bdsa_internal.h"
+
+namespace bdsa {
+namespace {
+
+__global__ void __launch_bounds__(256)
+    prepare_block_kernel(const int32_t *__restrict__ verified_id,
+                         const int32_t *__restrict__ seq_lens,
+                         const int32_t *__restrict__ block_table, int max_pages, int num_pages,
+                         int bs, int B, int page_size, int mask_token_id,
+                         int32_t *__restrict__ block_ids, int32_t *__restrict__ positions,
+                         int32_t *__restrict__ cache_loc, int32_t *dev_status) {
+    const long idx = (long)blockIdx.x * blockDim.x + threadIdx.x;
+    if (idx >= (long)bs * B) return;
+    const int r = (int)(idx / B), i = (int)(idx % B);
+    const int L = seq_lens[r];
+    const long pos = (long)L + i;
+    block_ids[idx] = (i == 0) ? verified_id[r] : mask_token_id;
+    positions[idx] = (int32_t)pos;
+    int32_t loc = -1;
+    const long page_idx = pos / page_size;
+    if (L >= 0 && page_idx < max_pages) {
+        const int32_t page = block_table[(long)r * max_pages + page_idx];
+        if (page >= 0 && page < num_pages) loc = (int32_t)((long)page * page_size + pos % page_size);
+    }
+    if (loc < 0) report_status(dev_status, BDSA_DEVICE_OUT_OF_RANGE);
+    cache_loc[idx] = loc;
+}
+
+}  // namespace
+
+int launch_prepare_block(const int32_t *verified_id, const int32_t *seq_lens,
+                         const int32_t *block_table, int max_pages, int num_pages, int bs, int B,
+                         int page_size, int mask_token_id, int32_t *block_ids,
+                         int32_t *positions, int32_t *cache_loc, int32_t *dev_status,
+                         cudaStream_t stream) {
+    const long n = (long)bs * B;
+    if (n == 0) return BDSA_OK;
+    const unsigned grid = (unsigned)((n + 255) / 256);
+    prepare_block_kernel<<<grid, 256, 0, stream>>>(verified_id, seq_lens, block_table, max_pages,
+                                                   num_pages, bs, B, page_size, mask_token_id,
+                                                   block_ids, positions, cache_loc, dev_status);
+    return cudaGetLastError() == cudaSuccess ? BDSA_OK : BDSA_CUDA_ERROR;
+}
+
+}  // namespace bdsa

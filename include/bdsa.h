@@ -1,0 +1,192 @@
+/*
+ * bdsa.h -- C ABI of libbdsa.so: one draft/verify step of block-diffusion
+ * self-speculative decoding over a paged KV cache, for NVIDIA GB300 (sm_103a).
+ *
+ * The step, in call order:
+ *   bdsa_prepare_block     lay out each request's block (token ids, positions,
+ *                          cache slots);
+ *   bdsa_block_attn_paged  block attention of the B block queries over the
+ *                          committed context plus the block itself, with a
+ *                          bidirectional (draft) or token-causal (verify)
+ *                          intra-block mask;
+ *   bdsa_spec_accept       lossless speculative acceptance: longest accepted
+ *                          prefix, then a residual correction or bonus token.
+ *
+ * Conventions for every call
+ *   - All tensor pointers are DEVICE pointers owned by the caller.  The library
+ *     allocates nothing: scratch comes from a caller-provided workspace sized by
+ *     the matching *_workspace_bytes query.
+ *   - Calls are asynchronous on `stream` (a cudaStream_t passed as void*; NULL
+ *     is the legacy default stream) and never synchronise the device.
+ *   - Tensors are dense row-major with the shapes given; int32 indices.
+ *   - Host-side argument checks return a status synchronously and launch
+ *     nothing.  Data errors that only the device can see (a page id outside the
+ *     pool, a draft id outside the vocabulary, ...) are reported through the
+ *     optional `dev_status` int32 device word: the first error code is stored
+ *     with an atomic compare-and-swap from 0, the affected unit of work is
+ *     skipped (its outputs are zero / -1), and the kernel never traps.  Callers
+ *     zero *dev_status before the step and read it whenever convenient.
+ *   - Bounded waits: every spin inside a kernel has a time limit; on expiry the
+ *     kernel stores BDSA_DEVICE_TIMEOUT in dev_status and returns.
+ *
+ * Notation: bs requests, block size B, Hq query heads, Hkv KV heads, G = Hq/Hkv
+ * (query head j reads KV head j / G), head dim D, page size ps, L_r = committed
+ * context length of request r (keys already in the cache before the block),
+ * V vocabulary size.
+ */
+#ifndef BDSA_H_
+#define BDSA_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum bdsa_status {
+    BDSA_OK = 0,
+    BDSA_INVALID_ARG = 1,          /* null pointer, negative size, bad mode, ... */
+    BDSA_UNSUPPORTED = 2,          /* a valid request this build does not handle (D, B, G*B) */
+    BDSA_MISALIGNED = 3,           /* a pointer or stride breaks the alignment rules below */
+    BDSA_WORKSPACE_TOO_SMALL = 4,
+    BDSA_CUDA_ERROR = 5,           /* a CUDA runtime/driver call or launch failed */
+    /* codes written to *dev_status by kernels */
+    BDSA_DEVICE_OUT_OF_RANGE = 16, /* page id / slot / position / token id out of range */
+    BDSA_DEVICE_TIMEOUT = 17       /* a bounded wait expired; outputs of that unit undefined */
+} bdsa_status;
+
+typedef struct bdsa_bf16 { uint16_t bits; } bdsa_bf16; /* IEEE bfloat16 storage */
+
+enum { BDSA_MODE_DRAFT = 0, BDSA_MODE_VERIFY = 1 };
+
+/* Human-readable name of a status code (static string, never NULL). */
+const char *bdsa_status_string(int32_t status);
+
+/* Library version as "major.minor.patch" (static string). */
+const char *bdsa_version(void);
+
+/* ------------------------------------------------------------------------ */
+/* bdsa_prepare_block
+ *
+ * "From DFlash to dLLM Self-Spec (II): SGLang Spec V2", section 2.2.2 (the
+ * block starts with the last verified token, the other slots are mask tokens;
+ * positions and cache locations are prepared in the same kernel); "... (IV)",
+ * section 4.4.1 (LinearSpec block init); section 2.3.5 of (II) (the caller has
+ * reserved pages for at least L_r + B tokens).
+ *
+ * For r in [0, bs), i in [0, B):
+ *   block_ids[r,i] = i == 0 ? verified_id[r] : mask_token_id
+ *   positions[r,i] = L_r + i
+ *   cache_loc[r,i] = block_table[r, (L_r+i)/ps] * ps + (L_r+i) % ps
+ *
+ * verified_id [bs], seq_lens [bs] (= L_r), block_table [bs, max_pages_per_req]
+ * (page ids in [0, num_pages)); outputs block_ids / positions / cache_loc
+ * [bs, B].  A lookup outside the table or the pool sets cache_loc = -1 and
+ * dev_status = BDSA_DEVICE_OUT_OF_RANGE.  One launch.
+ */
+int32_t bdsa_prepare_block(const int32_t *verified_id, const int32_t *seq_lens,
+                           const int32_t *block_table, int32_t max_pages_per_req,
+                           int32_t num_pages, int32_t bs, int32_t B, int32_t page_size,
+                           int32_t mask_token_id, int32_t *block_ids, int32_t *positions,
+                           int32_t *cache_loc, int32_t *dev_status, void *stream);
+
+/* ------------------------------------------------------------------------ */
+/* bdsa_block_attn_paged
+ *
+ * "SGLang dLLM / LLaDA 2.0", section "Attention Mask": the block's queries see
+ * the whole cached context (as in chunked prefill) and, inside the block, a
+ * rectangle (block diffusion, DRAFT) or a token-causal trapezoid (chunked
+ * prefill, VERIFY).  "From DFlash to dLLM Self-Spec (IV)", section 4.4.1: the
+ * draft pass uses the bidirectional view, the verify pass the causal view over
+ * the past KV; "... (II)", sections 2.2.3-2.2.4: both passes run a fixed block
+ * of B tokens per request.
+ *
+ * For request r, block row i, query head j (KV head h = j / G):
+ *   o[r*B+i, j] = sum_t softmax_t(scale * <q[r*B+i, j], k[t, h]>) v[t, h]
+ *   over keys t in [0, L_r + B) with
+ *   allowed(i, t) = t < L_r  or  mode == DRAFT  or  t - L_r <= i.
+ * Key t of request r is cache slot block_table[r, t/ps] * ps + t % ps; the
+ * block's own K/V (positions L_r..L_r+B-1) must already be in the cache.
+ *
+ * q        [bs*B, Hq, D] bf16 (post-RoPE)
+ * k_cache, v_cache  [num_pages*ps, Hkv, D] bf16
+ * out      [bs*B, Hq, D] bf16
+ * lse      [bs*B, Hq] fp32 natural-log sum-exp of the scaled scores, or NULL
+ * max_ctx_len  host-side upper bound on every L_r (the scheduler's planning
+ *          length); it sizes the split-KV plan.  L_r above it is still handled
+ *          correctly, only with less parallelism.
+ * Arithmetic: bf16 products, fp32 accumulation and softmax; P is rounded to
+ * bf16 for the PV product.
+ * Supported: D in {64, 128}; 1 <= B <= 64; G*B <= 128; page_size a power of two
+ * >= 8; q, k_cache, v_cache, out 16-byte aligned.
+ * Workspace: at least bdsa_block_attn_workspace_bytes(...) bytes of device
+ * memory, 256-byte aligned (may be NULL when that query returns 0).
+ */
+size_t bdsa_block_attn_workspace_bytes(int32_t bs, int32_t B, int32_t Hq, int32_t Hkv, int32_t D,
+                                       int32_t max_ctx_len, int32_t num_sms);
+
+int32_t bdsa_block_attn_paged(const bdsa_bf16 *q, const bdsa_bf16 *k_cache,
+                              const bdsa_bf16 *v_cache, const int32_t *block_table,
+                              int32_t max_pages_per_req, int32_t num_pages,
+                              const int32_t *seq_lens, int32_t max_ctx_len, int32_t bs,
+                              int32_t B, int32_t Hq, int32_t Hkv, int32_t D, int32_t page_size,
+                              float softmax_scale, int32_t mode, bdsa_bf16 *out, float *lse,
+                              void *workspace, size_t workspace_bytes, int32_t num_sms,
+                              int32_t *dev_status, void *stream);
+
+/* ------------------------------------------------------------------------ */
+/* bdsa_spec_accept
+ *
+ * "From DFlash to dLLM Self-Spec (IV)", section 4.3.1: a draft token is
+ * accepted with probability min(1, p/q), and a rejection is corrected from the
+ * verifier; "Unlocking Lossless Speedups in LLMs via Discrete Diffusion",
+ * background on speculative decoding (keep the longest accepted prefix,
+ * resample the first rejected position from the residual distribution; the
+ * output distribution equals the verifier's) and the Psi-Spec step (the first
+ * token is always accepted); "From DFlash to dLLM Self-Spec (II)", section
+ * 2.2.5 (greedy rule: accept while the draft equals the verifier argmax, bonus
+ * = verifier argmax at the first mismatch, commit_len = accept_len + 1, one
+ * kernel emits accept_len, commit_lens, bonus ids, out tokens, new seq lens).
+ *
+ * Row r: block_ids[r] = [verified, d_1, ..., d_{B-1}].  p[r,i] is the verifier
+ * distribution for block slot i+1 (p[r,B-1] is the bonus distribution); q[r,i-1]
+ * is the draft distribution d_i was drawn from.  Element (r, i, k) of p is at
+ * p[r*p_stride_r + i*p_stride_i + k] (likewise q); stride 0 broadcasts.
+ *
+ * Stochastic mode (q != NULL):
+ *   a = number of leading i in 1..B-1 with u_acc[r,i-1] < min(1, p/q), where
+ *       p/q = p[r,i-1][d_i] / q[r,i-1][d_i] is an IEEE fp32 divide (q == 0:
+ *       accepted iff p > 0);
+ *   a <  B-1: token = InvCDF(max(0, p[r,a] - q[r,a]), u_samp[r]) (fp32 weights;
+ *             if they are all 0, InvCDF(p[r,a], u_samp[r]));
+ *   a == B-1: token = InvCDF(p[r,B-1], u_samp[r]).
+ * Greedy mode (q == NULL): a = number of leading i with d_i == argmax p[r,i-1]
+ *   (lowest index on ties); token = argmax p[r,a].  u_acc / u_samp are unused.
+ * InvCDF(w, u) = smallest k with C_k > u*S, C_k the cumulative weight in index
+ *   order, S the total; cumulative sums are kept in fp64 (within 2e-7*S of the
+ *   exact sums).
+ * Outputs: accept_len[r] = a, commit_len[r] = a+1,
+ *   out_tokens[r] = [d_1..d_a, token, -1...] ([bs, B]), bonus_id[r] = token,
+ *   new_seq_lens[r] = seq_lens[r] + a + 1.
+ * p, q: fp32; u_acc [bs, B-1], u_samp [bs] fp32 in [0, 1); 2 <= B <= 64 (B = 1
+ * has nothing to verify and is accepted as well); 1 <= V.
+ * A draft id outside [0, V) counts as a rejection and sets dev_status.
+ * Workspace: bdsa_spec_accept_workspace_bytes(...) bytes, 256-byte aligned.
+ */
+size_t bdsa_spec_accept_workspace_bytes(int32_t bs, int32_t B, int32_t V, int32_t num_sms);
+
+int32_t bdsa_spec_accept(const int32_t *block_ids, const float *p, int64_t p_stride_r,
+                         int64_t p_stride_i, const float *q, int64_t q_stride_r,
+                         int64_t q_stride_i, const float *u_acc, const float *u_samp,
+                         const int32_t *seq_lens, int32_t bs, int32_t B, int32_t V,
+                         int32_t *accept_len, int32_t *commit_len, int32_t *out_tokens,
+                         int32_t *bonus_id, int32_t *new_seq_lens, void *workspace,
+                         size_t workspace_bytes, int32_t num_sms, int32_t *dev_status,
+                         void *stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* BDSA_H_ */

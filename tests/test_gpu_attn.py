@@ -1,0 +1,177 @@
+"""GPU parity of bdsa_block_attn_paged against the fp64 oracle.
+
+Tolerance (bf16 inputs, fp32 accumulation, bf16 output): max-abs 1e-2 and
+mean-abs 1e-3 on the output, 1e-3 on the natural-log lse.  Cases span several
+128-key tiles with ragged tails, L = 0, every supported G*B packing, page sizes
+below, at and above the 128-key tile, both masks, and both the single-split and
+the split-KV (combine) paths.  Full-size workloads are checked on sampled
+requests.
+"""
+import numpy as np
+import pytest
+import torch
+
+from block_diffusion_speculative_attn_gb300 import workloads as wl
+from gpu_helpers import (DevAttn, assert_attn_close, oracle_attn_full, oracle_attn_requests,
+                         run_attn)
+
+pytestmark = pytest.mark.gpu
+DRAFT, VERIFY = wl.DRAFT, wl.VERIFY
+FORCE_SPLIT = 4096  # an SM count that makes the planner split every unit's KV range
+
+
+def _cfg(name, bs, Hq, Hkv, D, B, ps, seq_lens, seed=77):
+    return wl.StepConfig(name, bs, Hq, Hkv, D, B, ps, tuple(seq_lens), (DRAFT, VERIFY), seed=seed)
+
+
+SHAPES = [
+    # name, Hq, Hkv, D, B, page_size, seq_lens
+    ("ragged_d128_g2", 4, 2, 128, 8, 16, (0, 1, 127, 120, 129, 300)),
+    ("qwen_like_g4_b16", 32, 8, 128, 16, 64, (1000, 37)),
+    ("llada_like_rows128", 16, 4, 128, 32, 32, (513, 700)),
+    ("long_like_g8", 64, 8, 128, 16, 64, (259, 1500)),
+    ("decode_b1_d64", 8, 8, 64, 1, 8, (50, 400, 0)),
+    ("b64_big_pages", 2, 1, 64, 64, 256, (333,)),
+    ("odd_g3_b3", 6, 2, 64, 3, 128, (240, 17)),
+]
+
+
+@pytest.fixture(scope="module")
+def dev():
+    import block_diffusion_speculative_attn_gb300 as bdsa
+    bdsa.lib()
+    return torch.device("cuda")
+
+
+@pytest.mark.parametrize("mode", [DRAFT, VERIFY])
+@pytest.mark.parametrize("sms", [0, FORCE_SPLIT])
+def test_tiny_config(dev, mode, sms):
+    inp = wl.make_attn_inputs(wl.config("tiny"))
+    d = DevAttn(inp)
+    status = torch.zeros(1, dtype=torch.int32, device=dev)
+    out, lse = run_attn(d, mode, sms=sms, status=status)
+    ref, ref_lse = oracle_attn_full(inp, mode)
+    assert_attn_close(out, ref, lse, ref_lse, tag=f"tiny mode={mode} sms={sms}")
+    assert status.item() == 0
+
+
+@pytest.mark.parametrize("shape", SHAPES, ids=[s[0] for s in SHAPES])
+@pytest.mark.parametrize("mode", [DRAFT, VERIFY])
+@pytest.mark.parametrize("sms", [0, FORCE_SPLIT])
+def test_shapes(dev, shape, mode, sms):
+    name, Hq, Hkv, D, B, ps, lens = shape
+    cfg = _cfg(name, len(lens), Hq, Hkv, D, B, ps, lens)
+    inp = wl.make_attn_inputs(cfg, extra_pages=2)
+    d = DevAttn(inp)
+    status = torch.zeros(1, dtype=torch.int32, device=dev)
+    out, lse = run_attn(d, mode, sms=sms, status=status)
+    ref, ref_lse = oracle_attn_full(inp, mode)
+    assert_attn_close(out, ref, lse, ref_lse, tag=f"{name} mode={mode} sms={sms}")
+    assert status.item() == 0
+
+
+def test_unused_slots_hold_nan(dev):
+    """Slots past L+B in a request's last page, and unowned pages, never leak into the output."""
+    cfg = _cfg("nan_slots", 3, 8, 2, 128, 8, 64, (70, 1, 200))
+    inp = wl.make_attn_inputs(cfg, extra_pages=3)
+    ps = cfg.page_size
+    used = np.zeros(inp.num_pages * ps, bool)
+    for r, L in enumerate(inp.seq_lens):
+        for t in range(int(L) + cfg.B):
+            used[inp.block_table[r, t // ps] * ps + t % ps] = True
+    d_clean = DevAttn(inp)
+    k_nan, v_nan = inp.k_cache.clone(), inp.v_cache.clone()
+    k_nan[torch.from_numpy(~used)] = float("nan")
+    v_nan[torch.from_numpy(~used)] = float("nan")
+    d_nan = DevAttn(wl.AttnInputs(cfg, inp.seq_lens, inp.block_table, inp.num_pages, inp.q,
+                                  k_nan, v_nan, inp.scale))
+    for mode in (DRAFT, VERIFY):
+        for sms in (0, FORCE_SPLIT):
+            a, _ = run_attn(d_clean, mode, sms=sms)
+            b, _ = run_attn(d_nan, mode, sms=sms)
+            assert torch.equal(a, b)
+
+
+def test_page_permutation_is_bit_identical(dev):
+    cfg = _cfg("perm", 2, 16, 4, 128, 16, 32, (900, 333))
+    a = wl.make_attn_inputs(cfg, seed=5)
+    # same logical sequences, pages shuffled differently in the pool
+    rng = np.random.default_rng(99)
+    perm = rng.permutation(a.num_pages)
+    ps = cfg.page_size
+    kp = a.k_cache.view(a.num_pages, ps, cfg.Hkv, cfg.D)
+    vp = a.v_cache.view(a.num_pages, ps, cfg.Hkv, cfg.D)
+    inv = np.argsort(perm)
+    k2 = kp[torch.from_numpy(perm)].reshape_as(a.k_cache).contiguous()
+    v2 = vp[torch.from_numpy(perm)].reshape_as(a.v_cache).contiguous()
+    table2 = np.where(a.block_table >= 0, inv[np.maximum(a.block_table, 0)], -1).astype(np.int32)
+    b = wl.AttnInputs(cfg, a.seq_lens, table2, a.num_pages, a.q, k2, v2, a.scale)
+    for mode in (DRAFT, VERIFY):
+        for sms in (0, FORCE_SPLIT):
+            oa, la = run_attn(DevAttn(a), mode, sms=sms)
+            ob, lb = run_attn(DevAttn(b), mode, sms=sms)
+            assert torch.equal(oa, ob) and torch.equal(la, lb)
+
+
+def test_mode_relations_are_bit_identical(dev):
+    cfg = _cfg("rel", 3, 32, 8, 128, 16, 64, (700, 64, 2000))
+    d = DevAttn(wl.make_attn_inputs(cfg))
+    od, _ = run_attn(d, DRAFT)
+    ov, _ = run_attn(d, VERIFY)
+    B = cfg.B
+    for r in range(cfg.bs):
+        assert torch.equal(od[r * B + B - 1], ov[r * B + B - 1])
+    cfg1 = _cfg("b1", 3, 32, 8, 128, 1, 64, (700, 0, 2000))
+    d1 = DevAttn(wl.make_attn_inputs(cfg1))
+    assert torch.equal(run_attn(d1, DRAFT)[0], run_attn(d1, VERIFY)[0])
+
+
+def test_bad_page_id_sets_status_and_skips_unit(dev):
+    cfg = _cfg("badpage", 3, 8, 2, 128, 8, 16, (100, 200, 50))
+    inp = wl.make_attn_inputs(cfg)
+    table = inp.block_table.copy()
+    table[1, 3] = inp.num_pages + 7  # request 1 references a page outside the pool
+    bad = wl.AttnInputs(cfg, inp.seq_lens, table, inp.num_pages, inp.q, inp.k_cache,
+                        inp.v_cache, inp.scale)
+    d = DevAttn(bad)
+    ref, _ = oracle_attn_full(inp, VERIFY)
+    for sms in (0, FORCE_SPLIT):
+        status = torch.zeros(1, dtype=torch.int32, device=dev)
+        out, _ = run_attn(d, VERIFY, sms=sms, status=status)
+        assert status.item() == 16  # BDSA_DEVICE_OUT_OF_RANGE
+        o = out.float().cpu().numpy()
+        B = cfg.B
+        assert (o[B:2 * B] == 0).all()
+        for r in (0, 2):
+            err = np.abs(o[r * B:(r + 1) * B] - ref[r * B:(r + 1) * B])
+            assert err.max() < 1e-2
+
+
+FULL = ["qwen3_8b_verify", "llada2_block_draft", "uno_1k8k_step", "long_ctx_verify"]
+
+
+@pytest.mark.parametrize("name", FULL)
+def test_full_size_sampled(dev, name):
+    """Full-size workload in the launch configuration the benchmark uses; the oracle
+    recomputes sampled requests (first, last, longest, one random)."""
+    cfg = wl.config(name)
+    inp = wl.make_attn_inputs(cfg, device="cuda")
+    d = DevAttn.__new__(DevAttn)
+    d.inp, d.q, d.k, d.v = inp, inp.q, inp.k_cache, inp.v_cache
+    d.bt = torch.from_numpy(inp.block_table).to(dev)
+    d.sl = torch.from_numpy(inp.seq_lens).to(dev)
+    rng = np.random.default_rng(3)
+    reqs = sorted({0, cfg.bs - 1, int(np.argmax(inp.seq_lens)), int(rng.integers(cfg.bs))})
+    if name == "long_ctx_verify":
+        reqs = [int(rng.integers(cfg.bs))]
+    for mode in cfg.modes:
+        status = torch.zeros(1, dtype=torch.int32, device=dev)
+        out, lse = run_attn(d, mode, status=status)
+        assert status.item() == 0
+        ref, ref_lse, rows = oracle_attn_requests(d, reqs, mode)
+        assert_attn_close(out[torch.from_numpy(rows).to(dev)], ref,
+                          lse[torch.from_numpy(rows).to(dev)], ref_lse,
+                          tag=f"{name} mode={mode}")
+        assert torch.isfinite(out.float()).all()
+    del d, inp
+    torch.cuda.empty_cache()

@@ -1,0 +1,115 @@
+"""CPU checks of the C-ABI library: it loads, exports every symbol that
+include/bdsa.h declares, and its host-side argument checks reject bad calls
+synchronously (no call here reaches a CUDA API: each one fails its checks first
+or only sizes a workspace for an explicit SM count)."""
+import ctypes
+import os
+import re
+
+import pytest
+
+import block_diffusion_speculative_attn_gb300 as bdsa
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "bdsa.h")
+
+
+@pytest.fixture(scope="module")
+def L():
+    from block_diffusion_speculative_attn_gb300 import build
+    build.build()
+    return bdsa.lib()
+
+
+def declared_functions():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(bdsa_[a-z0-9_]+)\s*\(", text)))
+
+
+def test_header_declares_the_three_calls():
+    names = declared_functions()
+    for n in ("bdsa_prepare_block", "bdsa_block_attn_paged", "bdsa_spec_accept"):
+        assert n in names
+
+
+def test_every_declared_symbol_is_exported(L):
+    names = declared_functions()
+    assert set(names) == set(bdsa.EXPORTS)
+    for n in names:
+        assert hasattr(L, n), n
+
+
+def test_status_strings_and_version(L):
+    assert L.bdsa_status_string(0) == b"BDSA_OK"
+    assert L.bdsa_status_string(16).startswith(b"BDSA_DEVICE_OUT_OF_RANGE")
+    assert L.bdsa_status_string(12345) == b"BDSA_UNKNOWN_STATUS"
+    assert re.match(rb"^\d+\.\d+\.\d+$", L.bdsa_version())
+
+
+FAKE = ctypes.c_void_p(0x100000)      # never dereferenced: calls below fail their checks first
+FAKE_ODD = ctypes.c_void_p(0x100002)  # 2-byte aligned only
+
+
+def _attn(L, **kw):
+    a = dict(q=FAKE, k=FAKE, v=FAKE, bt=FAKE, max_pages=4, num_pages=8, sl=FAKE, max_ctx=100,
+             bs=2, B=8, Hq=8, Hkv=2, D=128, ps=16, scale=0.1, mode=1, out=FAKE, lse=None,
+             ws=None, ws_bytes=0, sms=152)
+    a.update(kw)
+    return L.bdsa_block_attn_paged(a["q"], a["k"], a["v"], a["bt"], a["max_pages"],
+                                   a["num_pages"], a["sl"], a["max_ctx"], a["bs"], a["B"],
+                                   a["Hq"], a["Hkv"], a["D"], a["ps"], a["scale"], a["mode"],
+                                   a["out"], a["lse"], a["ws"], a["ws_bytes"], a["sms"], None, None)
+
+
+def test_attn_host_checks(L):
+    assert _attn(L, bs=0) == 0                      # empty batch: nothing to do
+    assert _attn(L, q=None) == 1                    # INVALID_ARG
+    assert _attn(L, mode=2) == 1
+    assert _attn(L, Hq=6, Hkv=4) == 1               # Hq % Hkv
+    assert _attn(L, scale=float("nan")) == 1
+    assert _attn(L, D=96) == 2                      # UNSUPPORTED
+    assert _attn(L, B=65) == 2
+    assert _attn(L, Hq=64, Hkv=2, B=8) == 2         # G*B = 256 > 128
+    assert _attn(L, ps=24) == 2                     # page size not a power of two
+    assert _attn(L, ps=4) == 2
+    assert _attn(L, q=FAKE_ODD) == 3                # MISALIGNED
+
+
+def _accept(L, **kw):
+    a = dict(ids=FAKE, p=FAKE, psr=16000, psi=1000, q=FAKE, qsr=15000, qsi=1000, ua=FAKE,
+             us=FAKE, sl=FAKE, bs=4, B=16, V=1000, outs=FAKE, ws=None, ws_bytes=0, sms=152)
+    a.update(kw)
+    return L.bdsa_spec_accept(a["ids"], a["p"], a["psr"], a["psi"], a["q"], a["qsr"], a["qsi"],
+                              a["ua"], a["us"], a["sl"], a["bs"], a["B"], a["V"], a["outs"],
+                              a["outs"], a["outs"], a["outs"], a["outs"], a["ws"], a["ws_bytes"],
+                              a["sms"], None, None)
+
+
+def test_accept_host_checks(L):
+    assert _accept(L, bs=0) == 0
+    assert _accept(L, p=None) == 1
+    assert _accept(L, V=0) == 1
+    assert _accept(L, psi=-1) == 1
+    assert _accept(L, us=None) == 1                 # stochastic mode needs u_samp
+    assert _accept(L, B=65) == 2
+    assert _accept(L, p=ctypes.c_void_p(0x100001)) == 3
+
+
+def test_prepare_host_checks(L):
+    f = L.bdsa_prepare_block
+    assert f(FAKE, FAKE, FAKE, 4, 8, 0, 8, 16, 0, FAKE, FAKE, FAKE, None, None) == 0
+    assert f(None, FAKE, FAKE, 4, 8, 2, 8, 16, 0, FAKE, FAKE, FAKE, None, None) == 1
+    assert f(FAKE, FAKE, FAKE, 4, 8, 2, 0, 16, 0, FAKE, FAKE, FAKE, None, None) == 1
+    assert f(FAKE, FAKE, FAKE, 4, 8, 2, 8, 0, 0, FAKE, FAKE, FAKE, None, None) == 1
+
+
+def test_workspace_plans(L):
+    # Qwen3-8B-shaped verify (32 x 8 units) on 152 SMs: two splits of 17 tiles.
+    ws = L.bdsa_block_attn_workspace_bytes(32, 16, 32, 8, 128, 4096, 152)
+    assert ws == 2 * 32 * 16 * 32 * 129 * 4
+    # 256 x 8 units already fill the GPU: no split, no workspace.
+    assert L.bdsa_block_attn_workspace_bytes(256, 16, 32, 8, 128, 9216, 152) == 0
+    # long context, 4 x 8 units: split-KV workspace grows with the split count
+    assert L.bdsa_block_attn_workspace_bytes(4, 16, 64, 8, 128, 131072, 152) > 0
+    assert L.bdsa_spec_accept_workspace_bytes(32, 16, 151936, 152) > 32 * 594 * 8
