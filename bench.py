@@ -1,0 +1,507 @@
+#!/usr/bin/env python3
+"""Benchmark one draft/verify step of block-diffusion speculative decoding.
+
+A step is the whole hot path over one batch: prepare_block, block attention
+(every pass the workload names, DRAFT and/or VERIFY) and speculative
+acceptance.  Default workload: the Qwen3-8B-shaped DFlash verify step (32
+requests, 32/8 heads, D 128, contexts U[1024, 4096] in 64-token pages, B = 16,
+acceptance over a 151936-token vocabulary).
+
+Prints one JSON line.  `value` is query tokens per second of whole steps with
+inputs resident in HBM (device time of the step's kernels, CUDA events on the
+launching stream, L2 flushed between steps); `e2e` is the same metric through
+the C ABI with the step's inputs copied from pinned host memory and its result
+read back every step.  `--impl reference` times the CPU oracle instead.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+                  [--workload NAME]
+Multi-GPU (N > 1, torchrun): every rank runs an independent replica on its own
+requests (the step has no cross-request exchange); the slowest rank's time
+counts and value is the total over ranks.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+import numpy as np
+import torch
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+from block_diffusion_speculative_attn_gb300 import workloads as wl  # noqa: E402
+
+METRIC = "draft/verify block-attn query tokens/s + % HBM roofline; accept rows/s"
+L2_FLUSH_BYTES = 512 << 20  # > 129 MB L2
+
+
+def parse_args(argv=None):
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=("ours", "reference"), default="ours")
+    ap.add_argument("--workload", default="qwen3_8b_verify", choices=wl.CONFIG_ORDER)
+    ap.add_argument("--cpu-seconds", type=float, default=15.0,
+                    help="target CPU time of the oracle baseline sample")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-e2e", action="store_true")
+    return ap.parse_args(argv)
+
+
+# ---------------------------------------------------------------------------
+# bookkeeping: algorithmic bytes / flops of one attention pass
+
+def attn_bytes(cfg: wl.StepConfig, seq_lens: np.ndarray) -> int:
+    """Each K/V element of every allowed key read once, Q read and O written once."""
+    kv = int(np.sum(seq_lens.astype(np.int64) + cfg.B)) * cfg.Hkv * cfg.D * 2 * 2
+    qo = 2 * cfg.bs * cfg.B * cfg.Hq * cfg.D * 2
+    return kv + qo
+
+
+def attn_flops(cfg: wl.StepConfig, seq_lens: np.ndarray, mode: int) -> int:
+    blk = cfg.B * cfg.B if mode == wl.DRAFT else cfg.B * (cfg.B + 1) // 2
+    return int(np.sum(4 * cfg.Hq * cfg.D * (cfg.B * seq_lens.astype(np.int64) + blk)))
+
+
+def accept_bytes(cfg: wl.StepConfig) -> int:
+    """One full row of p and q at the resolved position per request (upper bound
+    of the algorithmic bytes: a fully accepted row reads p alone)."""
+    return cfg.bs * 2 * cfg.V * 4 if cfg.V else 0
+
+
+def peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            d = json.load(f)
+        return float(d["hbm_gbs"]), float(d["bf16_tflops"]), "measured"
+    except Exception:
+        return 6800.0, 1900.0, "fallback"
+
+
+# ---------------------------------------------------------------------------
+class ClockSampler:
+    """nvidia-smi clocks / throttle reasons sampled during the timed region."""
+
+    Q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+         "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+         "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index: int):
+        self.index = index
+        self.proc = None
+        self.file = None
+
+    def start(self):
+        try:
+            self.file = tempfile.NamedTemporaryFile("w+", suffix=".csv", delete=False)
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.index}", f"--query-gpu={self.Q}",
+                 "--format=csv,noheader,nounits", "-lms", "100"],
+                stdout=self.file, stderr=subprocess.DEVNULL)
+        except Exception:
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except Exception:
+            self.proc.kill()
+        self.file.flush()
+        self.file.seek(0)
+        rows = [r.split(",") for r in self.file.read().strip().splitlines() if r.strip()]
+        os.unlink(self.file.name)
+        sm, mx, reasons = [], None, set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for r in rows:
+            try:
+                sm.append(float(r[1]))
+                mx = float(r[2])
+                for n, v in zip(names, r[5:9]):
+                    if v.strip().lower() == "active":
+                        reasons.add(n)
+            except (ValueError, IndexError):
+                continue
+        if not sm:
+            return None
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": mx, "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+# ---------------------------------------------------------------------------
+class Step:
+    """Device-resident inputs of one synthetic step and the calls that run it."""
+
+    def __init__(self, cfg: wl.StepConfig, device, seed: int):
+        import block_diffusion_speculative_attn_gb300 as bdsa
+        self.bdsa = bdsa
+        self.cfg = cfg
+        self.dev = device
+        self.attn = wl.make_attn_inputs(cfg, device=device, seed=seed)
+        self.bt = torch.from_numpy(self.attn.block_table).to(device)
+        self.sl = torch.from_numpy(self.attn.seq_lens).to(device)
+        g = torch.Generator(device=device)
+        g.manual_seed(seed + 17)
+        V = max(cfg.V, 1)
+        self.verified = torch.randint(0, V, (cfg.bs,), generator=g, device=device,
+                                      dtype=torch.int32)
+        self.acc = (wl.make_accept_inputs(cfg, device=device, seed=seed,
+                                          seq_lens=self.attn.seq_lens) if cfg.V else None)
+        self.status = torch.zeros(1, dtype=torch.int32, device=device)
+        B, bs = cfg.B, cfg.bs
+        self.prep_out = tuple(torch.empty((bs, B), dtype=torch.int32, device=device)
+                              for _ in range(3))
+        self.o = torch.empty_like(self.attn.q)
+        self.lse = torch.empty((bs * B, cfg.Hq), dtype=torch.float32, device=device)
+        ws = bdsa.block_attn_workspace_bytes(bs, B, cfg.Hq, cfg.Hkv, cfg.D,
+                                             self.attn.max_ctx_len)
+        self.attn_ws = torch.empty(max(ws, 256), dtype=torch.uint8, device=device)
+        self.acc_out = None
+        if cfg.V:
+            self.acc_out = {k: torch.empty(bs, dtype=torch.int32, device=device)
+                            for k in ("accept_len", "commit_len", "bonus_id", "new_seq_lens")}
+            self.acc_out["out_tokens"] = torch.empty((bs, B), dtype=torch.int32, device=device)
+            aws = bdsa.spec_accept_workspace_bytes(bs, B, cfg.V)
+            self.acc_ws = torch.empty(max(aws, 256), dtype=torch.uint8, device=device)
+        plan_splits = ws > 0
+        # kernels of ours per step: prepare, per pass (attention + combine when split), accept
+        self.launches = 1 + len(cfg.modes) * (2 if plan_splits else 1) + (1 if cfg.V else 0)
+
+    def prepare(self):
+        c = self.cfg
+        self.bdsa.prepare_block(self.verified, self.sl, self.bt, self.attn.num_pages, c.B,
+                                c.page_size, c.mask_token_id, out=self.prep_out,
+                                dev_status=self.status)
+
+    def attention(self, mode):
+        c = self.cfg
+        self.bdsa.block_attn_paged(self.attn.q, self.attn.k_cache, self.attn.v_cache, self.bt,
+                                   self.sl, B=c.B, page_size=c.page_size, scale=self.attn.scale,
+                                   mode=mode, max_ctx_len=self.attn.max_ctx_len,
+                                   num_pages=self.attn.num_pages, out=self.o, lse=self.lse,
+                                   workspace=self.attn_ws, dev_status=self.status)
+
+    def accept(self):
+        a = self.acc
+        self.bdsa.spec_accept(a.block_ids, a.p, a.q, a.u_acc, a.u_samp, a.seq_lens,
+                              out=self.acc_out, workspace=self.acc_ws, dev_status=self.status)
+
+    def run(self, ev=None):
+        """One step; ev = optional dict of (start, end) event pairs per stage to record."""
+        self.prepare()
+        for m in self.cfg.modes:
+            if ev is not None:
+                ev["attn"][0].record()
+            self.attention(m)
+            if ev is not None:
+                ev["attn"][1].record()
+        if self.cfg.V:
+            if ev is not None:
+                ev["accept"][0].record()
+            self.accept()
+            if ev is not None:
+                ev["accept"][1].record()
+
+    # host buffers for the end-to-end measurement
+    def host_inputs(self):
+        pin = lambda t: t.detach().cpu().pin_memory()  # noqa: E731
+        h = {"q": pin(self.attn.q), "verified": pin(self.verified), "sl": pin(self.sl),
+             "bt": pin(self.bt)}
+        if self.cfg.V:
+            a = self.acc
+            h.update({"block_ids": pin(a.block_ids), "p": pin(a.p), "qd": pin(a.q),
+                      "u_acc": pin(a.u_acc), "u_samp": pin(a.u_samp)})
+        return h
+
+
+def run_e2e(step: Step, steps: int, warmup: int):
+    """Same step, with every per-step input copied H2D from pinned memory and the
+    acceptance result (or the attention output when there is no acceptance stage)
+    read back D2H, all inside the timed region."""
+    h = step.host_inputs()
+    dev = step.dev
+    d = {k: torch.empty_like(v, device=dev) for k, v in h.items()}
+    res_keys = list(step.acc_out) if step.cfg.V else []
+    res_host = ({k: torch.empty_like(step.acc_out[k], device="cpu").pin_memory()
+                 for k in res_keys} if step.cfg.V else
+                {"o": torch.empty_like(step.o, device="cpu").pin_memory()})
+    h2d = sum(v.numel() * v.element_size() for v in h.values())
+    d2h = sum(v.numel() * v.element_size() for v in res_host.values())
+    c = step.cfg
+
+    def one():
+        for k, v in h.items():
+            d[k].copy_(v, non_blocking=True)
+        step.bdsa.prepare_block(d["verified"], d["sl"], d["bt"], step.attn.num_pages, c.B,
+                                c.page_size, c.mask_token_id, out=step.prep_out)
+        for m in c.modes:
+            step.bdsa.block_attn_paged(d["q"], step.attn.k_cache, step.attn.v_cache, d["bt"],
+                                       d["sl"], B=c.B, page_size=c.page_size,
+                                       scale=step.attn.scale, mode=m,
+                                       max_ctx_len=step.attn.max_ctx_len,
+                                       num_pages=step.attn.num_pages, out=step.o,
+                                       workspace=step.attn_ws)
+        if c.V:
+            step.bdsa.spec_accept(d["block_ids"], d["p"], d["qd"], d["u_acc"], d["u_samp"],
+                                  d["sl"], out=step.acc_out, workspace=step.acc_ws)
+            for k in res_keys:
+                res_host[k].copy_(step.acc_out[k], non_blocking=True)
+        else:
+            res_host["o"].copy_(step.o, non_blocking=True)
+
+    for _ in range(warmup):
+        one()
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record()
+    for _ in range(steps):
+        one()
+    e1.record()
+    torch.cuda.synchronize()
+    ms = e0.elapsed_time(e1) / steps
+    return ms, h2d, d2h
+
+
+# ---------------------------------------------------------------------------
+def oracle_sample(cfg: wl.StepConfig, attn: wl.AttnInputs, acc, reqs, nthreads):
+    """Host copies of the sampled requests' inputs (compact page pool)."""
+    ps = cfg.page_size
+    need = [(int(attn.seq_lens[r]) + cfg.B + ps - 1) // ps for r in reqs]
+    pages = np.concatenate([attn.block_table[r, :n] for r, n in zip(reqs, need)])
+    idx = torch.from_numpy(pages.astype(np.int64)).to(attn.k_cache.device)
+    kc = attn.k_cache.view(-1, ps, cfg.Hkv, cfg.D)[idx].reshape(-1, cfg.Hkv, cfg.D)
+    vc = attn.v_cache.view(-1, ps, cfg.Hkv, cfg.D)[idx].reshape(-1, cfg.Hkv, cfg.D)
+    table = np.full((len(reqs), max(need)), -1, np.int32)
+    at = 0
+    for j, n in enumerate(need):
+        table[j, :n] = np.arange(at, at + n, dtype=np.int32)
+        at += n
+    rows = torch.cat([torch.arange(r * cfg.B, (r + 1) * cfg.B) for r in reqs]).to(attn.q.device)
+    s = {"q": wl.bf16_bits(attn.q[rows]), "k": wl.bf16_bits(kc), "v": wl.bf16_bits(vc),
+         "table": table, "num_pages": at, "seq_lens": attn.seq_lens[reqs].copy(),
+         "verified": np.zeros(len(reqs), np.int32)}
+    if acc is not None:
+        rt = torch.as_tensor(reqs, device=acc.p.device)
+        s.update({"block_ids": acc.block_ids[rt].cpu().numpy(), "p": acc.p[rt].cpu().numpy(),
+                  "qd": acc.q[rt].cpu().numpy(), "u_acc": acc.u_acc[rt].cpu().numpy(),
+                  "u_samp": acc.u_samp[rt].cpu().numpy(),
+                  "acc_sl": acc.seq_lens[rt].cpu().numpy()})
+    return s
+
+
+def oracle_step(cfg: wl.StepConfig, s, scale, nthreads):
+    import oracle
+    oracle.prepare_block(s["verified"], s["seq_lens"], s["table"], s["num_pages"], cfg.B,
+                         cfg.page_size, cfg.mask_token_id)
+    for m in cfg.modes:
+        oracle.block_attn(s["q"], s["k"], s["v"], s["table"], s["seq_lens"], cfg.B, cfg.Hq,
+                          cfg.Hkv, cfg.D, cfg.page_size, scale, m, num_pages=s["num_pages"],
+                          nthreads=nthreads)
+    if cfg.V:
+        oracle.spec_accept(s["block_ids"], s["p"], s["qd"], s["u_acc"], s["u_samp"], s["acc_sl"],
+                           nthreads=nthreads)
+
+
+def cpu_baseline(cfg, attn, acc, target_s: float, reps: int = 1):
+    """Time the oracle on a bounded sample of the same workload on the host cores."""
+    cores = len(os.sched_getaffinity(0))
+    # grow the sample of requests until one oracle step takes a measurable time
+    n = 1
+    while True:
+        reqs = list(range(min(n, cfg.bs)))
+        s = oracle_sample(cfg, attn, acc, reqs, cores)
+        t0 = time.perf_counter()
+        oracle_step(cfg, s, attn.scale, cores)
+        dt = time.perf_counter() - t0
+        if dt * 4 > target_s or n >= cfg.bs:
+            break
+        n = min(cfg.bs, max(n + 1, int(n * max(2.0, 0.5 * target_s / max(dt, 1e-3)))))
+    times = [dt]
+    for _ in range(reps - 1):
+        t0 = time.perf_counter()
+        oracle_step(cfg, s, attn.scale, cores)
+        times.append(time.perf_counter() - t0)
+    best = min(times)
+    tokens = len(reqs) * cfg.B * len(cfg.modes)
+    return {"value": tokens / best, "unit": "query tokens/s", "cores": cores, "kind": "oracle",
+            "sample": f"first {len(reqs)} of {cfg.bs} requests of {cfg.name}, whole step "
+                      f"(prepare, {len(cfg.modes)} attention pass(es)"
+                      f"{', acceptance' if cfg.V else ''}), fp64 C oracle, "
+                      f"{cores} OpenMP threads, best of {len(times)}",
+            "seconds": best, "requests": len(reqs)}
+
+
+# ---------------------------------------------------------------------------
+def dist_setup(args):
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        import torch.distributed as dist
+        os.environ.setdefault("MASTER_ADDR", "127.0.0.1")
+        backend = "nccl" if torch.cuda.is_available() else "gloo"
+        if backend == "nccl":
+            torch.cuda.set_device(local)
+        dist.init_process_group(backend=backend)
+    return world, rank, local
+
+
+def barrier(world):
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+def max_over_ranks(x: float, world: int, device) -> float:
+    if world <= 1:
+        return x
+    import torch.distributed as dist
+    t = torch.tensor([x], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def main_reference(args, world, rank):
+    """Reference arm: the CPU oracle as it stands, on bounded samples of the workload."""
+    if rank != 0:
+        return
+    cfg = wl.config(args.workload)
+    dev = "cuda" if torch.cuda.is_available() else "cpu"
+    attn = wl.make_attn_inputs(cfg, device=dev, seed=cfg.seed)
+    acc = wl.make_accept_inputs(cfg, device=dev, seed=cfg.seed,
+                                seq_lens=attn.seq_lens) if cfg.V else None
+    cores = len(os.sched_getaffinity(0))
+    # sample size: requests whose oracle step takes ~ cpu_seconds / (steps + warmup)
+    per_step = max(0.5, args.cpu_seconds * 8 / max(1, args.steps + args.warmup))
+    probe = cpu_baseline(cfg, attn, acc, per_step)
+    reqs = list(range(probe["requests"]))
+    s = oracle_sample(cfg, attn, acc, reqs, cores)
+    for _ in range(args.warmup):
+        oracle_step(cfg, s, attn.scale, cores)
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        oracle_step(cfg, s, attn.scale, cores)
+    dt = (time.perf_counter() - t0) / args.steps
+    tokens = len(reqs) * cfg.B * len(cfg.modes)
+    value = tokens / dt
+    line = {"impl": "reference", "metric": METRIC, "value": value, "unit": "query tokens/s",
+            "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": dt * 1e3, "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": {"workload": cfg.name, "requests_per_step": len(reqs), "B": cfg.B,
+                       "Hq": cfg.Hq, "Hkv": cfg.Hkv, "D": cfg.D, "page_size": cfg.page_size,
+                       "vocab": cfg.V, "l2": "n/a (CPU)"},
+            "cpu_baseline": {"value": value, "unit": "query tokens/s", "cores": cores,
+                             "kind": "oracle",
+                             "sample": f"first {len(reqs)} of {cfg.bs} requests per step"},
+            "e2e": {"value": value, "unit": "query tokens/s", "h2d_bytes_per_step": 0,
+                    "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+
+
+def main(argv=None):
+    args = parse_args(argv)
+    world, rank, local = dist_setup(args)
+    if args.impl == "reference":
+        main_reference(args, world, rank)
+        return
+    if not torch.cuda.is_available():
+        raise SystemExit("bench.py needs a CUDA GPU (the product path has no CPU fallback)")
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    import block_diffusion_speculative_attn_gb300 as bdsa
+    bdsa.lib()
+    cfg = wl.config(args.workload)
+    step = Step(cfg, dev, seed=cfg.seed + 1000 * rank)
+    flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
+    for _ in range(max(args.warmup, 3)):
+        step.run()
+    torch.cuda.synchronize()
+    assert step.status.item() == 0, bdsa.STATUS.get(step.status.item())
+
+    K = args.steps
+    ev = [{"step": (torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)),
+           "attn": (torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)),
+           "accept": (torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))}
+          for _ in range(K)]
+    clocks = ClockSampler(local)
+    barrier(world)
+    torch.cuda.synchronize()
+    clocks.start()
+    time.sleep(0.3)
+    for i in range(K):
+        flush.zero_()  # evict the previous step's lines from L2 (outside the events)
+        ev[i]["step"][0].record()
+        step.run(ev[i] if len(cfg.modes) == 1 else None)
+        ev[i]["step"][1].record()
+    torch.cuda.synchronize()
+    barrier(world)
+    clk = clocks.stop()
+    step_ms = [e["step"][0].elapsed_time(e["step"][1]) for e in ev]
+    ms = statistics.mean(step_ms)
+    attn_ms = (statistics.mean(e["attn"][0].elapsed_time(e["attn"][1]) for e in ev)
+               if len(cfg.modes) == 1 else None)
+    acc_ms = (statistics.mean(e["accept"][0].elapsed_time(e["accept"][1]) for e in ev)
+              if (cfg.V and len(cfg.modes) == 1) else None)
+    ms_max = max_over_ranks(ms, world, dev)
+
+    tokens = cfg.bs * cfg.B * len(cfg.modes)
+    value = tokens * world / (ms_max / 1e3)
+    hbm, tf, peak_src = peaks()
+    abytes = attn_bytes(cfg, step.attn.seq_lens)
+    roof = None
+    if attn_ms is not None:
+        achieved = abytes / (attn_ms / 1e3) / 1e9
+        roof = {"bound": "hbm", "achieved": achieved, "peak": hbm, "unit": "GB/s",
+                "frac": achieved / hbm, "traffic": None,
+                "kernel": "block_attn_paged (attention + split-KV combine launch)",
+                "algorithmic_bytes_per_launch": abytes, "peak_source": peak_src,
+                "launch_ms": attn_ms}
+
+    e2e = None
+    if not args.no_e2e:
+        e_ms, h2d, d2h = run_e2e(step, max(3, K // 2), 2)
+        e_ms = max_over_ranks(e_ms, world, dev)
+        e2e = {"value": tokens * world / (e_ms / 1e3), "unit": "query tokens/s",
+               "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": e_ms}
+
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        cpu = cpu_baseline(cfg, step.attn, step.acc, args.cpu_seconds)
+
+    line = {"metric": METRIC, "value": value, "unit": "query tokens/s", "n_gpus": world,
+            "steps": K, "warmup": args.warmup, "ms_per_step": ms_max, "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+            "config": {"workload": cfg.name, "batch": cfg.bs, "B": cfg.B, "Hq": cfg.Hq,
+                       "Hkv": cfg.Hkv, "D": cfg.D, "page_size": cfg.page_size,
+                       "ctx": list(cfg.ctx[0]) if isinstance(cfg.ctx[0], tuple) else "fixed",
+                       "modes": ["draft" if m == 0 else "verify" for m in cfg.modes],
+                       "vocab": cfg.V, "l2": "flushed between steps (512 MB write)",
+                       "parallelism": f"replicas x{world}"},
+            "roofline": roof,
+            "attn_query_tokens_per_s": (cfg.bs * cfg.B / (attn_ms / 1e3)) if attn_ms else None,
+            "accept_rows_per_s": (cfg.bs / (acc_ms / 1e3)) if acc_ms else None,
+            "accept_ms": acc_ms,
+            "attn_flops_per_launch": attn_flops(cfg, step.attn.seq_lens, cfg.modes[-1]),
+            "e2e": e2e, "cpu_baseline": cpu, "gpu_launches": step.launches * K,
+            "clocks": clk}
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

@@ -198,8 +198,11 @@ def spec_accept(block_ids, p, q, u_acc, u_samp, seq_lens, *, p_strides=None, q_s
     if workspace is None:
         workspace = torch.empty(max(need, 256), dtype=torch.uint8, device=dev)
     ws_bytes = workspace.numel() * workspace.element_size()
+    # With B == 1 there is no draft and q is never read, but its pointer must stay non-null
+    # to select the stochastic rule; an empty tensor may report a null data pointer.
+    q_ptr = None if q is None else (_ptr(q) if q.numel() > 0 else _ptr(p))
     st = lib().bdsa_spec_accept(_ptr(block_ids), _ptr(p), int(p_strides[0]), int(p_strides[1]),
-                                _ptr(q), int(q_strides[0]), int(q_strides[1]),
+                                q_ptr, int(q_strides[0]), int(q_strides[1]),
                                 _ptr(u_acc) if q is not None else None,
                                 _ptr(u_samp) if q is not None else None, _ptr(seq_lens), bs, B,
                                 V, _ptr(out["accept_len"]), _ptr(out["commit_len"]),

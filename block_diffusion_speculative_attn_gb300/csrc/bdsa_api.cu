@@ -142,7 +142,6 @@ int32_t bdsa_spec_accept(const int32_t *block_ids, const float *p, int64_t p_str
         return BDSA_INVALID_ARG;
     if (bs == 0) return BDSA_OK;
     if (B > 64) return BDSA_UNSUPPORTED;
-    if (bs > 65535) return BDSA_UNSUPPORTED;
     if (!block_ids || !p || !seq_lens || !accept_len || !commit_len || !out_tokens || !bonus_id ||
         !new_seq_lens)
         return BDSA_INVALID_ARG;

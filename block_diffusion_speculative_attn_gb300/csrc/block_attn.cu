@@ -98,6 +98,14 @@ __device__ __forceinline__ uint32_t pack_bf16(float lo, float hi, float &sum) {
     return *reinterpret_cast<uint32_t *>(&v);
 }
 
+// Packs two probabilities to bf16 for the PV product; l_round accumulates the
+// rounded values (the weights the MMA actually applies, so the output is an
+// exact convex combination), l_exact the fp32 values (for the log-sum-exp).
+__device__ __forceinline__ uint32_t pack_p(float lo, float hi, float &l_round, float &l_exact) {
+    l_exact += lo + hi;
+    return pack_bf16(lo, hi, l_round);
+}
+
 template <int D>
 __global__ void __launch_bounds__(kThreads, 1)
     block_attn_kernel(const __grid_constant__ CUtensorMap tm_q,
@@ -122,13 +130,13 @@ __global__ void __launch_bounds__(kThreads, 1)
     const long te = (s == prm.nsplit - 1) ? ntiles : min(ntiles, tb + prm.tps);
     const int nt = (int)max(0L, te - tb);
 
-    // ---- validate the unit's page ids before touching anything else
+    // ---- validate every page id of the request (not only this split's), so a bad
+    // entry skips all splits of the unit alike
     bool bad = (L < 0) || (n_keys > (long)prm.max_pages * ps);
-    if (!bad && nt > 0) {
-        const long first = (tb * kBN) >> prm.log2_ps;
-        const long last = (min(te * kBN, n_keys) - 1) >> prm.log2_ps;
+    if (!bad) {
+        const long last = (n_keys - 1) >> prm.log2_ps;
         const int32_t *bt = prm.block_table + (long)r * prm.max_pages;
-        for (long pi = first + tid; pi <= last; pi += kThreads) {
+        for (long pi = tid; pi <= last; pi += kThreads) {
             const int32_t pg = bt[pi];
             if (pg < 0 || pg >= prm.num_pages) bad = true;
         }
@@ -308,7 +316,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         const uint32_t lane_base = (uint32_t)(warp * 32) << 16;
         const int i_blk = row / G;
         const long limit = (prm.mode == BDSA_MODE_DRAFT) ? n_keys : min(n_keys, (long)L + i_blk + 1);
-        float m_used = -INFINITY, l_sum = 0.f;
+        float m_used = -INFINITY, l_sum = 0.f, l_exact = 0.f;
         bool ok = true;
         for (int jj = 0; jj < nt; ++jj) {
             const long t0 = (tb + jj) * kBN;
@@ -351,6 +359,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 resc = true;
             }
             l_sum *= alpha;
+            l_exact *= alpha;
             uint32_t pk[kBN / 2];
             if (m_used == -INFINITY) {
 #pragma unroll
@@ -358,8 +367,8 @@ __global__ void __launch_bounds__(kThreads, 1)
             } else {
 #pragma unroll
                 for (int k = 0; k < kBN / 2; ++k)
-                    pk[k] = pack_bf16(exp2f(sv[2 * k] - m_used), exp2f(sv[2 * k + 1] - m_used),
-                                      l_sum);
+                    pk[k] = pack_p(exp2f(sv[2 * k] - m_used), exp2f(sv[2 * k + 1] - m_used),
+                                   l_sum, l_exact);
             }
             // PV of the previous tile must be done before P is overwritten or O rescaled.
             if (jj >= 1) {
@@ -447,7 +456,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 }
             }
             if (valid) {
-                const float lse2 = l_sum > 0.f ? m_used + log2f(l_sum) : -INFINITY;
+                const float lse2 = l_exact > 0.f ? m_used + log2f(l_exact) : -INFINITY;
                 if (prm.nsplit == 1) {
                     if (prm.lse) prm.lse[orow] = lse2 * kLn2;
                 } else {

@@ -14,13 +14,13 @@
 // 256-element segments and each chunk is one CTA, so even a handful of rows
 // spreads over the whole GPU.  Every CTA recomputes the accepted length a
 // (B - 1 gathered probability pairs), sweeps its chunk once with 16-byte loads
-// and stores one fp64 total per segment (fp32 pairwise sums of 8 elements per
-// lane, fp64 across lanes).  The last CTA of a row to finish (atomic counter;
-// nothing ever waits) scans the segment totals, re-reads the one segment that
-// holds the crossing point and resolves the token to a single index.
-// Cumulative sums therefore carry at most ~3 * 2^-24 relative error per
-// 8-element group, far inside the 1e-6 band within which the fp64 oracle flags
-// a draw as order-dependent.
+// and stores one fp64 total per segment (error-free TwoSum pairwise sums of 8
+// elements per lane, fp64 across lanes).  The last CTA of a row to finish
+// (atomic counter; nothing ever waits) scans the segment totals, re-reads the
+// one segment that holds the crossing point and resolves the token to a single
+// index.  Cumulative sums stay within ~1e-13 relative of the exact sums, far
+// inside the 1e-9 band within which the fp64 oracle flags a draw as
+// order-dependent.
 #include <cuda_runtime.h>
 #include <limits.h>
 
@@ -87,10 +87,30 @@ __device__ __forceinline__ void load_weights(const float *prow, const float *qro
     }
 }
 
-// Fixed pairwise order; the sweep and the resolve step both use it.
-__device__ __forceinline__ float group_sum(const float (&w)[8]) {
-    return __fadd_rn(__fadd_rn(__fadd_rn(w[0], w[1]), __fadd_rn(w[2], w[3])),
-                     __fadd_rn(__fadd_rn(w[4], w[5]), __fadd_rn(w[6], w[7])));
+// Error-free fp32 addition (Knuth's TwoSum): a + b == s + e exactly.
+__device__ __forceinline__ float two_sum(float a, float b, float &e) {
+    const float s = __fadd_rn(a, b);
+    const float bb = __fsub_rn(s, a);
+    e = __fadd_rn(__fsub_rn(a, __fsub_rn(s, bb)), __fsub_rn(b, bb));
+    return s;
+}
+
+// Sum of 8 weights as an fp64 value within ~2^-46 relative of the exact sum: a
+// pairwise tree of TwoSums keeps every rounding error, and only the (tiny) sum
+// of those errors is rounded.  Fixed order; the sweep and the resolve step
+// both use it.
+__device__ __forceinline__ double group_sum(const float (&w)[8]) {
+    float e0, e1, e2, e3, e4, e5, e6;
+    const float s01 = two_sum(w[0], w[1], e0);
+    const float s23 = two_sum(w[2], w[3], e1);
+    const float s45 = two_sum(w[4], w[5], e2);
+    const float s67 = two_sum(w[6], w[7], e3);
+    const float s03 = two_sum(s01, s23, e4);
+    const float s47 = two_sum(s45, s67, e5);
+    const float s07 = two_sum(s03, s47, e6);
+    const float err = __fadd_rn(__fadd_rn(__fadd_rn(e0, e1), __fadd_rn(e2, e3)),
+                                __fadd_rn(__fadd_rn(e4, e5), e6));
+    return (double)s07 + (double)err;
 }
 
 __device__ __forceinline__ double warp_sum_f64(double v) {
@@ -102,10 +122,12 @@ __device__ __forceinline__ double warp_sum_f64(double v) {
 // Accepted draft count for row r (stochastic mode), computed by one warp.
 __device__ int accepted_len(const Params &P, int r, int lane, bool &bad_id) {
     const int B = P.B;
-    bad_id = false;
+    bool bad_any = false;
+    int a = -1;
     for (int base = 1; base < B; base += 32) {
         const int i = base + lane;
         bool rej = false;
+        bad_id = false;
         if (i < B) {
             const int d = P.block_ids[(long)r * B + i];
             if (d < 0 || d >= P.V) {
@@ -125,14 +147,13 @@ __device__ int accepted_len(const Params &P, int r, int lane, bool &bad_id) {
                 rej = !acc;
             }
         }
+        // any draft id outside the vocabulary is a data error, tested or not
+        bad_any = bad_any || __any_sync(0xffffffffu, bad_id);
         const unsigned m = __ballot_sync(0xffffffffu, rej);
-        if (m != 0u) {
-            const int first = __ffs(m) - 1;
-            bad_id = __shfl_sync(0xffffffffu, bad_id, first);
-            return base + first - 1;
-        }
+        if (m != 0u && a < 0) a = base + (__ffs(m) - 1) - 1;
     }
-    return B - 1;
+    bad_id = bad_any;
+    return a < 0 ? B - 1 : a;
 }
 
 // Segment totals of this CTA's chunk for the chosen distribution.
@@ -141,7 +162,7 @@ __device__ void sweep_chunk(const Params &P, int r, const float *prow, const flo
     for (int seg = seg_begin + warp; seg < seg_end; seg += kWarps) {
         float w[8];
         load_weights(prow, qrow, (long)seg * kSeg + lane * 8, P.V, w);
-        const double t = warp_sum_f64((double)group_sum(w));
+        const double t = warp_sum_f64(group_sum(w));
         if (lane == 0) P.seg_sum[(long)r * P.nseg + seg] = t;
     }
 }
@@ -201,7 +222,7 @@ __device__ int resolve_draw(const Params &P, int r, const float *prow, const flo
     float w[8];
     const long e0 = (long)seg_star * kSeg + lane * 8;
     load_weights(prow, qrow, e0, P.V, w);
-    const double g = (double)group_sum(w);
+    const double g = group_sum(w);
     double ginc = g;
 #pragma unroll
     for (int o = 1; o < 32; o <<= 1) {
@@ -270,7 +291,7 @@ __device__ bool last_cta_of_row(const Params &P, int r) {
 }
 
 __global__ void __launch_bounds__(kThreads) accept_stochastic_kernel(const Params P) {
-    const int r = blockIdx.y, chunk = blockIdx.x;
+    const int r = blockIdx.x / P.nchunk, chunk = blockIdx.x % P.nchunk;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     __shared__ int s_a;
     if (warp == 0) {
@@ -319,7 +340,7 @@ __device__ __forceinline__ void better(float &bv, int &bi, float v, int i) {
 }
 
 __global__ void __launch_bounds__(kThreads) accept_greedy_kernel(const Params P) {
-    const int r = blockIdx.y, chunk = blockIdx.x;
+    const int r = blockIdx.x / P.nchunk, chunk = blockIdx.x % P.nchunk;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     __shared__ float s_v[kWarps];
     __shared__ int s_i[kWarps];
@@ -435,7 +456,9 @@ int launch_spec_accept(const AcceptArgs &a, cudaStream_t stream) {
     P.am_idx = reinterpret_cast<int32_t *>(ws);
     if (cudaMemsetAsync(P.counter, 0, (size_t)a.bs * sizeof(int32_t), stream) != cudaSuccess)
         return BDSA_CUDA_ERROR;
-    const dim3 grid(plan.nchunk, a.bs);
+    const long nblocks = (long)plan.nchunk * a.bs;
+    if (nblocks > 0x7fffffffL) return BDSA_UNSUPPORTED;
+    const unsigned grid = (unsigned)nblocks;
     if (a.q != nullptr)
         accept_stochastic_kernel<<<grid, kThreads, 0, stream>>>(P);
     else

@@ -164,13 +164,15 @@ int32_t bdsa_block_attn_paged(const bdsa_bf16 *q, const bdsa_bf16 *k_cache,
  * Greedy mode (q == NULL): a = number of leading i with d_i == argmax p[r,i-1]
  *   (lowest index on ties); token = argmax p[r,a].  u_acc / u_samp are unused.
  * InvCDF(w, u) = smallest k with C_k > u*S, C_k the cumulative weight in index
- *   order, S the total; cumulative sums are kept in fp64 (within 2e-7*S of the
- *   exact sums).
+ *   order, S the total; cumulative sums are accumulated without fp32 rounding
+ *   loss and kept in fp64 (within ~1e-13*S of the exact sums), so the draw is
+ *   the exact-arithmetic one unless u*S lies within that distance of a boundary.
  * Outputs: accept_len[r] = a, commit_len[r] = a+1,
  *   out_tokens[r] = [d_1..d_a, token, -1...] ([bs, B]), bonus_id[r] = token,
  *   new_seq_lens[r] = seq_lens[r] + a + 1.
- * p, q: fp32; u_acc [bs, B-1], u_samp [bs] fp32 in [0, 1); 2 <= B <= 64 (B = 1
- * has nothing to verify and is accepted as well); 1 <= V.
+ * p, q: fp32; u_acc [bs, B-1], u_samp [bs] fp32 in [0, 1); 1 <= B <= 64; 1 <= V.
+ * With B = 1 there is no draft to test: q is never read but must still be a
+ * non-null pointer to select the stochastic rule (the bonus is then sampled).
  * A draft id outside [0, V) counts as a rejection and sets dev_status.
  * Workspace: bdsa_spec_accept_workspace_bytes(...) bytes, 256-byte aligned.
  */

@@ -218,7 +218,9 @@ int oracle_block_attn(const uint16_t *q, const uint16_t *k_cache,
  * flags[r] (may be NULL) marks rows whose integer result is decided within
  * the fp rounding margin and so is not unique across summation orders:
  *   bit 0: some tested |p/q - u| < 1e-6 (fp64)
- *   bit 1: u*S within 1e-6*S of C_{k-1} or C_k for the chosen k
+ *   bit 1: u*S within 1e-9*S of C_{k-1} or C_k for the chosen k (the fp64
+ *          sequential sums here carry < 2e-11*S error, any other exact-to-
+ *          1e-13 summation order can only disagree inside this band)
  *   bit 2: residual mass was zero, sampled from p
  *   bit 3: a draft id was outside [0, V) (treated as rejected)
  *   bit 4: greedy argmax had a tie at a deciding position
@@ -246,7 +248,7 @@ static int inv_cdf_f32w(const float *w, int V, double u, int *flag_near) {
         if (flag_near) *flag_near = 1;
         return chosen;
     }
-    if (flag_near && ((T - Cprev) < 1e-6 * S || (C - T) < 1e-6 * S)) *flag_near = 1;
+    if (flag_near && ((T - Cprev) < 1e-9 * S || (C - T) < 1e-9 * S)) *flag_near = 1;
     return chosen;
 }
 

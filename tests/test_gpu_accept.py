@@ -1,10 +1,12 @@
 """GPU parity of bdsa_spec_accept against the fp64 oracle.
 
 Accept lengths, emitted tokens and resampled / bonus tokens must be bit-exact.
-The oracle flags rows whose integer result is decided inside the rounding
-margin (|p/q - u| < 1e-6, or u*S within 1e-6*S of a cumulative boundary); such
-rows are excluded from the comparison and counted, and the count must stay a
-tiny fraction of the rows.
+The acceptance test is the same IEEE fp32 divide and compare on both sides,
+so it must match on every row.  The draw compares u*S with cumulative sums; the
+oracle flags rows where u*S lies within 1e-9*S of a boundary of the chosen
+token (there two exact-to-1e-13 summation orders may legitimately differ);
+those rows are excluded from the comparison and counted, and the count must
+stay a tiny fraction of the rows.
 """
 import json
 import os
@@ -32,7 +34,7 @@ def _gpu(acc: wl.AcceptInputs, greedy=False, status=None, sms=0, **kw):
 
 def _compare(got, want, max_flag_frac=1e-3):
     flags = want["flags"]
-    ok = (flags & 3) == 0
+    ok = (flags & 2) == 0
     assert (~ok).mean() <= max_flag_frac, f"{(~ok).sum()} flagged rows"
     for k in KEYS:
         g = got[k].cpu().numpy()
@@ -97,7 +99,7 @@ def test_ragged_vocab_and_block(V, B):
             for k in KEYS:
                 assert (got[k].cpu().numpy()[ok] == want[k][ok]).all(), k
         else:
-            _compare(got, want, max_flag_frac=0.05)
+            _compare(got, want, max_flag_frac=0.02)
 
 
 def test_lossless_million_rows_bit_exact():
