@@ -84,7 +84,7 @@ int32_t bdsa_block_attn_paged(const bdsa_bf16 *q, const bdsa_bf16 *k_cache,
                               void *workspace, size_t workspace_bytes, int32_t num_sms,
                               int32_t *dev_status, void *stream) {
     if (bs < 0 || B < 1 || Hq < 1 || Hkv < 1 || max_pages_per_req < 1 || num_pages < 1 ||
-        max_ctx_len < 0 || !isfinite(softmax_scale) ||
+        max_ctx_len < 0 || !isfinite(softmax_scale) || !(softmax_scale > 0.f) ||
         (mode != BDSA_MODE_DRAFT && mode != BDSA_MODE_VERIFY))
         return BDSA_INVALID_ARG;
     if (bs == 0) return BDSA_OK;

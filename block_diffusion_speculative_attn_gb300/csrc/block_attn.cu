@@ -9,15 +9,20 @@
 //
 // One CTA owns one (request, KV head, KV split) unit:
 //   * the G*B query rows of the unit (GQA heads x block rows, row m = i*G + g)
-//     are packed into one M = 128 tcgen05 tile (zero rows pad it);
+//     form the A operand of one tcgen05 MMA tile: M = 64 when G*B <= 64, else
+//     M = 128 (zero rows pad it).  An M = 64 accumulator spreads its rows over
+//     lanes 0-15 of all four TMEM lane quadrants, so all four SM sub-partitions
+//     take part in the softmax with two threads per row (16x32bx2 TMEM
+//     accesses); an M = 128 accumulator has one thread per row;
 //   * K/V are streamed in 128-key tiles, one TMA box per page (or per 128 keys
-//     of a large page) into 128-byte-swizzled shared memory; a 3-deep K ring
-//     and 2-deep V ring keep ~160 KB of loads in flight per SM;
-//   * S = Q K^T (M128 N128 K16 x D/16) and O += P V (M128 N=D K16 x 8) run on
-//     the tensor cores with fp32 accumulators in TMEM (S double-buffered);
-//   * four softmax warps own one row each per thread: masked online softmax in
-//     the log2 domain, lazy rescale of O in TMEM only when the running max grows
-//     by more than 2^8, P rounded to bf16 and written swizzled for the PV MMA;
+//     of a large page) into 128-byte-swizzled shared memory, through a 3-deep
+//     K ring and a 2-deep V ring;
+//   * S = Q K^T (K = D) and O += P V (K = 128 keys) run on the tensor cores
+//     with fp32 accumulators in TMEM (S double-buffered);
+//   * softmax in the log2 domain: one FFMA + ex2 per score, running max with a
+//     lazy rescale of O in TMEM only when the max grows by more than 2^8, P
+//     rounded to bf16 and written swizzled for the PV MMA (double-buffered in
+//     M = 64 mode so the next tile's P never waits for the previous PV);
 //   * with several splits the CTA writes an fp32 partial (o / l, log2 lse) and
 //     a second kernel merges them, so no CTA ever waits for another.
 // Warp roles: 0-3 softmax/epilogue, 4 TMA producer, 5 MMA issuer + TMEM owner.
@@ -33,9 +38,7 @@
 namespace bdsa {
 namespace {
 
-constexpr int kBM = 128;                  // MMA rows (packed G*B query rows)
 constexpr int kBN = 128;                  // keys per tile
-constexpr int kRegion = 128 * 128;        // 128 rows x 128 bytes: one swizzled 64-wide slab
 constexpr int kThreads = 192;
 constexpr int kProducerWarp = 4;
 constexpr int kMmaWarp = 5;
@@ -45,28 +48,34 @@ constexpr uint32_t kTmemO = 256;          // S buffers at columns 0 and 128, O a
 constexpr float kRescaleLog2 = 8.0f;      // rescale O only when the max grows by > 2^8
 constexpr float kLn2 = 0.6931471805599453f;
 
-template <int D>
+template <int D, int M>
 struct Cfg {
-    static constexpr int DH = D / 64;     // 64-element (128-byte) slabs per row
+    static constexpr int DH = D / 64;               // 64-element (128-byte) slabs per row
+    static constexpr int kSlab = M * 128;           // one M-row slab of 128-byte rows
+    static constexpr int kKVSlab = kBN * 128;       // one 128-key slab
+    static constexpr int NP = (M == 64) ? 2 : 1;    // P buffers
     static constexpr int NK = (D == 128) ? 3 : 4;
     static constexpr int NV = (D == 128) ? 2 : 4;
-    static constexpr int kStage = DH * kRegion;
+    static constexpr int TPR = (M == 64) ? 2 : 1;   // softmax threads per row
+    static constexpr int NC = kBN / TPR;            // score columns per thread
+    static constexpr int kStage = DH * kKVSlab;
+    static constexpr int kPBuf = 2 * kSlab;         // 128 keys = two 64-key slabs
     static constexpr int kOffQ = 0;
-    static constexpr int kOffK = kOffQ + DH * kRegion;
+    static constexpr int kOffK = kOffQ + DH * kSlab;
     static constexpr int kOffV = kOffK + NK * kStage;
     static constexpr int kOffP = kOffV + NV * kStage;
-    static constexpr int kOffBar = kOffP + 2 * kRegion;
+    static constexpr int kOffBar = kOffP + NP * kPBuf;
     // barrier indices
     static constexpr int QF = 0;
     static constexpr int KF = 1;
     static constexpr int KE = KF + NK;
     static constexpr int VF = KE + NK;
     static constexpr int VE = VF + NV;
-    static constexpr int SF = VE + NV;    // 2
-    static constexpr int SR = SF + 2;     // 2 (S buffer released)
-    static constexpr int PF = SR + 2;
-    static constexpr int PV = PF + 1;
-    static constexpr int DR = PV + 1;     // drain
+    static constexpr int SF = VE + NV;    // 2: S buffer full
+    static constexpr int SR = SF + 2;     // 2: S buffer released
+    static constexpr int PF = SR + 2;     // P written (one per tile)
+    static constexpr int PV = PF + 1;     // NP: PV done, per P buffer
+    static constexpr int DR = PV + NP;    // drain
     static constexpr int kNumBars = DR + 1;
     static constexpr int kOffMisc = kOffBar + 8 * kNumBars;
     static constexpr int kSmem = kOffMisc + 16 + 1024;  // + slack to align the base to 1 KB
@@ -92,26 +101,32 @@ __device__ __forceinline__ void st_shared_v4(uint32_t addr, uint32_t a, uint32_t
                  : "memory");
 }
 
-__device__ __forceinline__ uint32_t pack_bf16(float lo, float hi, float &sum) {
+__device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
     __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
-    sum += __low2float(v) + __high2float(v);
     return *reinterpret_cast<uint32_t *>(&v);
 }
 
-// Packs two probabilities to bf16 for the PV product; l_round accumulates the
-// rounded values (the weights the MMA actually applies, so the output is an
-// exact convex combination), l_exact the fp32 values (for the log-sum-exp).
-__device__ __forceinline__ uint32_t pack_p(float lo, float hi, float &l_round, float &l_exact) {
-    l_exact += lo + hi;
-    return pack_bf16(lo, hi, l_round);
+// Loads this thread's share of a 128-column fp32 accumulator block from TMEM:
+// all 128 columns of its lane (M = 128) or its half of the row (M = 64).
+template <int M, int NC>
+__device__ __forceinline__ void load_cols(uint32_t taddr, float (&v)[NC]) {
+    if constexpr (M == 64) {
+#pragma unroll
+        for (int c = 0; c < NC / 32; ++c)
+            tmem_ld16x2_32<NC>(taddr + c * 32, *reinterpret_cast<float(*)[32]>(&v[c * 32]));
+    } else {
+#pragma unroll
+        for (int c = 0; c < NC / 32; ++c)
+            tmem_ld32(taddr + c * 32, *reinterpret_cast<float(*)[32]>(&v[c * 32]));
+    }
 }
 
-template <int D>
+template <int D, int M>
 __global__ void __launch_bounds__(kThreads, 1)
     block_attn_kernel(const __grid_constant__ CUtensorMap tm_q,
                       const __grid_constant__ CUtensorMap tm_k,
                       const __grid_constant__ CUtensorMap tm_v, const Params prm) {
-    using C = Cfg<D>;
+    using C = Cfg<D, M>;
     extern __shared__ uint8_t smem_raw[];
     const uint32_t raw = smem_u32(smem_raw);
     const uint32_t sbase = (raw + 1023u) & ~1023u;
@@ -182,17 +197,17 @@ __global__ void __launch_bounds__(kThreads, 1)
             mbar_init(bar(C::SR + k), kSoftmaxWarps);
         }
         mbar_init(bar(C::PF), kSoftmaxWarps);
-        mbar_init(bar(C::PV), 1);
+        for (int k = 0; k < C::NP; ++k) mbar_init(bar(C::PV + k), 1);
         mbar_init(bar(C::DR), 1);
         *abort_flag = 0;
         fence_mbarrier_init();
     }
     // Zero the padding rows of the Q tile so padded S rows stay finite.
-    if (prm.rows < kBM) {
-        const int pad = kBM - prm.rows;
+    if (prm.rows < M) {
+        const int pad = M - prm.rows;
         for (int idx = tid; idx < pad * C::DH * 8; idx += kThreads) {
             const int u = idx & 7, c = (idx >> 3) % C::DH, m = prm.rows + (idx >> 3) / C::DH;
-            st_shared_v4(sbase + C::kOffQ + c * kRegion + m * 128 + u * 16, 0, 0, 0, 0);
+            st_shared_v4(sbase + C::kOffQ + c * C::kSlab + m * 128 + u * 16, 0, 0, 0, 0);
         }
     }
     fence_proxy_async_smem();
@@ -209,7 +224,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             tma_prefetch_desc(&tm_v);
             mbar_arrive_expect_tx(bar(C::QF), (uint32_t)(prm.rows * D * 2));
             for (int c = 0; c < C::DH; ++c)
-                tma_load_4d(sbase + C::kOffQ + c * kRegion, &tm_q, c * 64, 0, h, r * B,
+                tma_load_4d(sbase + C::kOffQ + c * C::kSlab, &tm_q, c * 64, 0, h, r * B,
                             bar(C::QF));
             const int32_t *bt = prm.block_table + (long)r * prm.max_pages;
             const int rows_box = prm.box_rows;
@@ -226,9 +241,10 @@ __global__ void __launch_bounds__(kThreads, 1)
                 mbar_arrive_expect_tx(bar(C::KF + ks), bytes);
                 for (int b = 0; b < nbox; ++b) {
                     const long t = t0 + (long)b * rows_box;
-                    const int32_t slot = bt[t >> prm.log2_ps] * prm.page_size + (int32_t)(t & (ps - 1));
+                    const int32_t slot =
+                        bt[t >> prm.log2_ps] * prm.page_size + (int32_t)(t & (ps - 1));
                     for (int c = 0; c < C::DH; ++c)
-                        tma_load_2d(sbase + C::kOffK + ks * C::kStage + c * kRegion +
+                        tma_load_2d(sbase + C::kOffK + ks * C::kStage + c * C::kKVSlab +
                                         b * rows_box * 128,
                                     &tm_k, h * D + c * 64, slot, bar(C::KF + ks));
                 }
@@ -241,9 +257,10 @@ __global__ void __launch_bounds__(kThreads, 1)
                 mbar_arrive_expect_tx(bar(C::VF + vs), bytes);
                 for (int b = 0; b < nbox; ++b) {
                     const long t = t0 + (long)b * rows_box;
-                    const int32_t slot = bt[t >> prm.log2_ps] * prm.page_size + (int32_t)(t & (ps - 1));
+                    const int32_t slot =
+                        bt[t >> prm.log2_ps] * prm.page_size + (int32_t)(t & (ps - 1));
                     for (int c = 0; c < C::DH; ++c)
-                        tma_load_2d(sbase + C::kOffV + vs * C::kStage + c * kRegion +
+                        tma_load_2d(sbase + C::kOffV + vs * C::kStage + c * C::kKVSlab +
                                         b * rows_box * 128,
                                     &tm_v, h * D + c * 64, slot, bar(C::VF + vs));
                 }
@@ -261,23 +278,25 @@ __global__ void __launch_bounds__(kThreads, 1)
     } else if (warp == kMmaWarp) {
         // ------------------------------------------------ MMA issuer
         if (lane == 0) {
-            constexpr uint32_t idesc_qk = idesc_bf16_f32(kBM, kBN, 0, 0);
-            constexpr uint32_t idesc_pv = idesc_bf16_f32(kBM, D, 0, 1);
+            constexpr uint32_t idesc_qk = idesc_bf16_f32(M, kBN, 0, 0);
+            constexpr uint32_t idesc_pv = idesc_bf16_f32(M, D, 0, 1);
             auto issue_pv = [&](int j) -> bool {
                 if (!mbar_wait(bar(C::PF), j & 1, abort_flag, prm.dev_status)) return false;
                 const int vs = j % C::NV;
                 if (!mbar_wait(bar(C::VF + vs), (j / C::NV) & 1, abort_flag, prm.dev_status))
                     return false;
                 tc_fence_after();
+                const int pb = j % C::NP;
 #pragma unroll
                 for (int kk = 0; kk < kBN / 16; ++kk) {
                     const uint64_t a = smem_desc_sw128(
-                        sbase + C::kOffP + (kk >> 2) * kRegion + (kk & 3) * 32, 16, 1024);
+                        sbase + C::kOffP + pb * C::kPBuf + (kk >> 2) * C::kSlab + (kk & 3) * 32,
+                        16, 1024);
                     const uint64_t b = smem_desc_sw128(
-                        sbase + C::kOffV + vs * C::kStage + kk * 16 * 128, kRegion, 1024);
+                        sbase + C::kOffV + vs * C::kStage + kk * 16 * 128, C::kKVSlab, 1024);
                     umma_bf16(tmem + kTmemO, a, b, idesc_pv, (j > 0 || kk > 0) ? 1u : 0u);
                 }
-                umma_commit(bar(C::PV));
+                umma_commit(bar(C::PV + pb));
                 umma_commit(bar(C::VE + vs));
                 return true;
             };
@@ -295,10 +314,11 @@ __global__ void __launch_bounds__(kThreads, 1)
                 tc_fence_after();
 #pragma unroll
                 for (int kk = 0; kk < D / 16; ++kk) {
-                    const uint32_t off = (kk >> 2) * kRegion + (kk & 3) * 32;
-                    const uint64_t a = smem_desc_sw128(sbase + C::kOffQ + off, 16, 1024);
-                    const uint64_t b =
-                        smem_desc_sw128(sbase + C::kOffK + ks * C::kStage + off, 16, 1024);
+                    const uint64_t a = smem_desc_sw128(
+                        sbase + C::kOffQ + (kk >> 2) * C::kSlab + (kk & 3) * 32, 16, 1024);
+                    const uint64_t b = smem_desc_sw128(
+                        sbase + C::kOffK + ks * C::kStage + (kk >> 2) * C::kKVSlab + (kk & 3) * 32,
+                        16, 1024);
                     umma_bf16(tmem + sb * 128, a, b, idesc_qk, kk > 0 ? 1u : 0u);
                 }
                 umma_commit(bar(C::SF + sb));
@@ -312,11 +332,19 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
     } else {
         // ------------------------------------------------ softmax + epilogue
-        const int row = tid;  // 0..127, TMEM lane
+        // Thread -> (row, column half).  M = 128: row = tid, all 128 columns.
+        // M = 64: row = 16 * warp + lane % 16, half = lane / 16 owns columns
+        // [64 * half, 64 * half + 64) of every 128-column block.
+        constexpr int NC = C::NC;
+        const int half = (M == 64) ? (lane >> 4) : 0;
+        const int row = (M == 64) ? warp * 16 + (lane & 15) : tid;
         const uint32_t lane_base = (uint32_t)(warp * 32) << 16;
         const int i_blk = row / G;
-        const long limit = (prm.mode == BDSA_MODE_DRAFT) ? n_keys : min(n_keys, (long)L + i_blk + 1);
-        float m_used = -INFINITY, l_sum = 0.f, l_exact = 0.f;
+        const long limit =
+            (prm.mode == BDSA_MODE_DRAFT) ? n_keys : min(n_keys, (long)L + i_blk + 1);
+        const float sl2 = prm.scale_log2;
+        float m_used = -INFINITY;
+        float l4[4] = {0.f, 0.f, 0.f, 0.f};
         bool ok = true;
         for (int jj = 0; jj < nt; ++jj) {
             const long t0 = (tb + jj) * kBN;
@@ -325,76 +353,95 @@ __global__ void __launch_bounds__(kThreads, 1)
             ok = __all_sync(0xffffffffu, ok);
             if (!ok) break;
             tc_fence_after();
-            float sv[kBN];
-#pragma unroll
-            for (int c = 0; c < kBN / 32; ++c)
-                tmem_ld32(tmem + lane_base + sb * 128 + c * 32,
-                          *reinterpret_cast<float(*)[32]>(&sv[c * 32]));
+            float sv[NC];
+            load_cols<M, NC>(tmem + lane_base + sb * 128, sv);
             tmem_wait_ld();
             tc_fence_before();
             __syncwarp();
             if (lane == 0) mbar_arrive(bar(C::SR + sb));
 
-            const long nvalid = limit - t0;
-            float mt = -INFINITY;
-            if (nvalid >= kBN) {
+            // mask the scores past this row's limit (raw scores; scale > 0 keeps the max)
+            const long nvalid = limit - t0 - half * NC;
+            if (nvalid < NC) {
 #pragma unroll
-                for (int k = 0; k < kBN; ++k) {
-                    sv[k] *= prm.scale_log2;
-                    mt = fmaxf(mt, sv[k]);
-                }
-            } else {
-#pragma unroll
-                for (int k = 0; k < kBN; ++k) {
-                    sv[k] = (k < nvalid) ? sv[k] * prm.scale_log2 : -INFINITY;
-                    mt = fmaxf(mt, sv[k]);
-                }
+                for (int k = 0; k < NC; ++k)
+                    if (k >= nvalid) sv[k] = -INFINITY;
             }
-            const float m_new = fmaxf(m_used, mt);
+            float mx[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
+#pragma unroll
+            for (int k = 0; k < NC; ++k) mx[k & 3] = fmaxf(mx[k & 3], sv[k]);
+            float mt = fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3]));
+            if constexpr (M == 64) mt = fmaxf(mt, __shfl_xor_sync(0xffffffffu, mt, 16));
+            const float m_new = mt * sl2;
             float alpha = 1.f;
             bool resc = false;
             if (m_new > m_used + kRescaleLog2) {
-                alpha = exp2f(m_used - m_new);
+                alpha = ex2_approx(m_used - m_new);
                 m_used = m_new;
                 resc = true;
             }
-            l_sum *= alpha;
-            l_exact *= alpha;
-            uint32_t pk[kBN / 2];
+#pragma unroll
+            for (int q = 0; q < 4; ++q) l4[q] *= alpha;
+            uint32_t pk[NC / 2];
             if (m_used == -INFINITY) {
 #pragma unroll
-                for (int k = 0; k < kBN / 2; ++k) pk[k] = 0u;
+                for (int k = 0; k < NC / 2; ++k) pk[k] = 0u;
             } else {
+                const float neg_m = -m_used;
 #pragma unroll
-                for (int k = 0; k < kBN / 2; ++k)
-                    pk[k] = pack_p(exp2f(sv[2 * k] - m_used), exp2f(sv[2 * k + 1] - m_used),
-                                   l_sum, l_exact);
+                for (int k = 0; k < NC / 2; ++k) {
+                    const float p0 = ex2_approx(fmaf(sv[2 * k], sl2, neg_m));
+                    const float p1 = ex2_approx(fmaf(sv[2 * k + 1], sl2, neg_m));
+                    l4[k & 3] += p0 + p1;
+                    pk[k] = pack_bf16x2(p0, p1);
+                }
             }
-            // PV of the previous tile must be done before P is overwritten or O rescaled.
-            if (jj >= 1) {
-                ok = mbar_wait(bar(C::PV), (jj - 1) & 1, abort_flag, prm.dev_status);
+            const int pb = jj % C::NP;
+            // The P buffer must be free: PV of tile jj - NP has read it.
+            if (jj >= C::NP) {
+                const int prev = jj - C::NP;
+                ok = mbar_wait(bar(C::PV + pb), (prev / C::NP) & 1, abort_flag, prm.dev_status);
+                ok = __all_sync(0xffffffffu, ok);
+                if (!ok) break;
+            }
+            // A grown max rescales O, which needs PV of the previous tile to be done.
+            if (jj >= 1 && __any_sync(0xffffffffu, resc)) {
+                const int prev = jj - 1;
+                ok = mbar_wait(bar(C::PV + prev % C::NP), (prev / C::NP) & 1, abort_flag,
+                               prm.dev_status);
                 ok = __all_sync(0xffffffffu, ok);
                 if (!ok) break;
                 tc_fence_after();
-                if (__any_sync(0xffffffffu, resc)) {
 #pragma unroll
-                    for (int c = 0; c < D / 32; ++c) {
-                        float ov[32];
+                for (int c = 0; c < D / (32 * C::TPR); ++c) {
+                    float ov[32];
+                    if constexpr (M == 64) {
+                        tmem_ld16x2_32<D / 2>(tmem + lane_base + kTmemO + c * 32, ov);
+                    } else {
                         tmem_ld32(tmem + lane_base + kTmemO + c * 32, ov);
-                        tmem_wait_ld();
+                    }
+                    tmem_wait_ld();
 #pragma unroll
-                        for (int k = 0; k < 32; ++k) ov[k] *= alpha;
+                    for (int k = 0; k < 32; ++k) ov[k] *= alpha;
+                    if constexpr (M == 64) {
+                        tmem_st16x2_32<D / 2>(tmem + lane_base + kTmemO + c * 32, ov);
+                    } else {
                         tmem_st32(tmem + lane_base + kTmemO + c * 32, ov);
                     }
-                    tmem_wait_st();
                 }
+                tmem_wait_st();
             }
             // P row -> shared memory, K-major with the 128-byte swizzle.
+            {
+                const uint32_t pbase = sbase + C::kOffP + pb * C::kPBuf;
 #pragma unroll
-            for (int u = 0; u < kBN / 8; ++u) {
-                const uint32_t addr = sbase + C::kOffP + (u >> 3) * kRegion + row * 128 +
-                                      ((uint32_t)((u & 7) ^ (row & 7)) << 4);
-                st_shared_v4(addr, pk[4 * u], pk[4 * u + 1], pk[4 * u + 2], pk[4 * u + 3]);
+                for (int u = 0; u < NC / 8; ++u) {
+                    const int slab = (M == 64) ? half : (u >> 3);
+                    const int cu = u & 7;
+                    const uint32_t addr = pbase + slab * C::kSlab + row * 128 +
+                                          ((uint32_t)(cu ^ (row & 7)) << 4);
+                    st_shared_v4(addr, pk[4 * u], pk[4 * u + 1], pk[4 * u + 2], pk[4 * u + 3]);
+                }
             }
             // Ragged last tile: V rows past the request's keys hold stale or unloaded data.
             const long tile_keys = n_keys - t0;
@@ -403,13 +450,13 @@ __global__ void __launch_bounds__(kThreads, 1)
                 ok = mbar_wait(bar(C::VF + vs), (jj / C::NV) & 1, abort_flag, prm.dev_status);
                 ok = __all_sync(0xffffffffu, ok);
                 if (!ok) break;
-                if (row >= tile_keys) {
+                if (tid >= tile_keys) {
 #pragma unroll
                     for (int c = 0; c < C::DH; ++c)
 #pragma unroll
                         for (int u = 0; u < 8; ++u)
-                            st_shared_v4(sbase + C::kOffV + vs * C::kStage + c * kRegion +
-                                             row * 128 + u * 16,
+                            st_shared_v4(sbase + C::kOffV + vs * C::kStage + c * C::kKVSlab +
+                                             tid * 128 + u * 16,
                                          0, 0, 0, 0);
                 }
             }
@@ -419,44 +466,53 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (lane == 0) mbar_arrive(bar(C::PF));
         }
         if (ok) {
-            ok = mbar_wait(bar(C::PV), (nt - 1) & 1, abort_flag, prm.dev_status);
+            const int last = nt - 1;
+            ok = mbar_wait(bar(C::PV + last % C::NP), (last / C::NP) & 1, abort_flag,
+                           prm.dev_status);
             ok = __all_sync(0xffffffffu, ok);
         }
         if (ok) {
             tc_fence_after();
+            float l = (l4[0] + l4[1]) + (l4[2] + l4[3]);
+            if constexpr (M == 64) l += __shfl_xor_sync(0xffffffffu, l, 16);
             const bool valid = row < prm.rows;
             const long token = (long)r * B + i_blk;
             const long orow = token * prm.Hq + (long)h * G + row % G;
-            const float inv_l = l_sum > 0.f ? 1.f / l_sum : 0.f;
+            const float inv_l = l > 0.f ? 1.f / l : 0.f;
+            constexpr int OC = D / C::TPR;  // output columns per thread
 #pragma unroll
-            for (int c = 0; c < D / 32; ++c) {
+            for (int c = 0; c < OC / 32; ++c) {
                 float ov[32];
-                tmem_ld32(tmem + lane_base + kTmemO + c * 32, ov);
+                if constexpr (M == 64) {
+                    tmem_ld16x2_32<D / 2>(tmem + lane_base + kTmemO + c * 32, ov);
+                } else {
+                    tmem_ld32(tmem + lane_base + kTmemO + c * 32, ov);
+                }
                 tmem_wait_ld();
                 if (!valid) continue;
+                const int col0 = half * OC + c * 32;
                 if (prm.nsplit == 1) {
-                    uint4 *dst = reinterpret_cast<uint4 *>(prm.out + orow * D + c * 32);
+                    uint4 *dst = reinterpret_cast<uint4 *>(prm.out + orow * D + col0);
 #pragma unroll
                     for (int v = 0; v < 4; ++v) {
-                        float dummy = 0.f;
                         uint4 w;
-                        w.x = pack_bf16(ov[8 * v + 0] * inv_l, ov[8 * v + 1] * inv_l, dummy);
-                        w.y = pack_bf16(ov[8 * v + 2] * inv_l, ov[8 * v + 3] * inv_l, dummy);
-                        w.z = pack_bf16(ov[8 * v + 4] * inv_l, ov[8 * v + 5] * inv_l, dummy);
-                        w.w = pack_bf16(ov[8 * v + 6] * inv_l, ov[8 * v + 7] * inv_l, dummy);
+                        w.x = pack_bf16x2(ov[8 * v + 0] * inv_l, ov[8 * v + 1] * inv_l);
+                        w.y = pack_bf16x2(ov[8 * v + 2] * inv_l, ov[8 * v + 3] * inv_l);
+                        w.z = pack_bf16x2(ov[8 * v + 4] * inv_l, ov[8 * v + 5] * inv_l);
+                        w.w = pack_bf16x2(ov[8 * v + 6] * inv_l, ov[8 * v + 7] * inv_l);
                         dst[v] = w;
                     }
                 } else {
                     float4 *dst = reinterpret_cast<float4 *>(
-                        prm.part_o + ((long)s * prm.bs * B * prm.Hq + orow) * D + c * 32);
+                        prm.part_o + ((long)s * prm.bs * B * prm.Hq + orow) * D + col0);
 #pragma unroll
                     for (int v = 0; v < 8; ++v)
                         dst[v] = make_float4(ov[4 * v] * inv_l, ov[4 * v + 1] * inv_l,
                                              ov[4 * v + 2] * inv_l, ov[4 * v + 3] * inv_l);
                 }
             }
-            if (valid) {
-                const float lse2 = l_exact > 0.f ? m_used + log2f(l_exact) : -INFINITY;
+            if (valid && half == 0) {
+                const float lse2 = l > 0.f ? m_used + log2f(l) : -INFINITY;
                 if (prm.nsplit == 1) {
                     if (prm.lse) prm.lse[orow] = lse2 * kLn2;
                 } else {
@@ -515,14 +571,13 @@ __global__ void __launch_bounds__(256)
     }
     const float inv = den > 0.f ? 1.f / den : 0.f;
     uint16_t *dst = out + row * D + lane * E;
-    float dummy = 0.f;
     if constexpr (E == 4) {
         uint2 w;
-        w.x = pack_bf16(acc[0] * inv, acc[1] * inv, dummy);
-        w.y = pack_bf16(acc[2] * inv, acc[3] * inv, dummy);
+        w.x = pack_bf16x2(acc[0] * inv, acc[1] * inv);
+        w.y = pack_bf16x2(acc[2] * inv, acc[3] * inv);
         *reinterpret_cast<uint2 *>(dst) = w;
     } else {
-        *reinterpret_cast<uint32_t *>(dst) = pack_bf16(acc[0] * inv, acc[1] * inv, dummy);
+        *reinterpret_cast<uint32_t *>(dst) = pack_bf16x2(acc[0] * inv, acc[1] * inv);
     }
     if (lse && lane == 0) lse[row] = den > 0.f ? (m + log2f(den)) * kLn2 : -INFINITY;
 }
@@ -547,9 +602,9 @@ EncodeTiledFn encode_fn() {
     return fn;
 }
 
-template <int D>
+template <int D, int M>
 int launch_impl(const AttnArgs &a, const AttnPlan &plan, cudaStream_t stream) {
-    using C = Cfg<D>;
+    using C = Cfg<D, M>;
     EncodeTiledFn enc = encode_fn();
     if (enc == nullptr) return BDSA_CUDA_ERROR;
     const int G = a.Hq / a.Hkv;
@@ -613,9 +668,10 @@ int launch_impl(const AttnArgs &a, const AttnPlan &plan, cudaStream_t stream) {
         prm.part_o = nullptr;
         prm.part_lse = nullptr;
     }
-    static bool attr_set = false;  // per D instantiation
+    static bool attr_set = false;  // per (D, M) instantiation
     if (!attr_set) {
-        if (cudaFuncSetAttribute(block_attn_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+        if (cudaFuncSetAttribute(block_attn_kernel<D, M>,
+                                 cudaFuncAttributeMaxDynamicSharedMemorySize,
                                  C::kSmem) != cudaSuccess)
             return BDSA_CUDA_ERROR;
         attr_set = true;
@@ -623,7 +679,7 @@ int launch_impl(const AttnArgs &a, const AttnPlan &plan, cudaStream_t stream) {
     const long grid_l = (long)a.bs * a.Hkv * plan.nsplit;
     if (grid_l > 0x7fffffffL) return BDSA_UNSUPPORTED;
     const unsigned grid = (unsigned)grid_l;
-    block_attn_kernel<D><<<grid, kThreads, C::kSmem, stream>>>(tq, tk, tv, prm);
+    block_attn_kernel<D, M><<<grid, kThreads, C::kSmem, stream>>>(tq, tk, tv, prm);
     if (cudaGetLastError() != cudaSuccess) return BDSA_CUDA_ERROR;
     if (plan.nsplit > 1) {
         const long threads = rows_total * 32;
@@ -661,8 +717,11 @@ int launch_block_attn(const AttnArgs &a, cudaStream_t stream) {
     const AttnPlan plan = attn_plan(a.bs, a.B, a.Hq, a.Hkv, a.D, a.max_ctx_len, a.num_sms);
     if (plan.workspace > 0 && (a.workspace == nullptr || a.workspace_bytes < plan.workspace))
         return BDSA_WORKSPACE_TOO_SMALL;
-    if (a.D == 128) return launch_impl<128>(a, plan, stream);
-    if (a.D == 64) return launch_impl<64>(a, plan, stream);
+    const bool m64 = (a.Hq / a.Hkv) * a.B <= 64;
+    if (a.D == 128)
+        return m64 ? launch_impl<128, 64>(a, plan, stream) : launch_impl<128, 128>(a, plan, stream);
+    if (a.D == 64)
+        return m64 ? launch_impl<64, 64>(a, plan, stream) : launch_impl<64, 128>(a, plan, stream);
     return BDSA_UNSUPPORTED;
 }
 

@@ -116,6 +116,7 @@ int32_t bdsa_prepare_block(const int32_t *verified_id, const int32_t *seq_lens,
  * max_ctx_len  host-side upper bound on every L_r (the scheduler's planning
  *          length); it sizes the split-KV plan.  L_r above it is still handled
  *          correctly, only with less parallelism.
+ * softmax_scale must be finite and > 0.
  * Arithmetic: bf16 products, fp32 accumulation and softmax; P is rounded to
  * bf16 for the PV product.
  * Supported: D in {64, 128}; 1 <= B <= 64; G*B <= 128; page_size a power of two

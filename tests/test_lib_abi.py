@@ -68,6 +68,8 @@ def test_attn_host_checks(L):
     assert _attn(L, mode=2) == 1
     assert _attn(L, Hq=6, Hkv=4) == 1               # Hq % Hkv
     assert _attn(L, scale=float("nan")) == 1
+    assert _attn(L, scale=-0.5) == 1
+    assert _attn(L, scale=0.0) == 1
     assert _attn(L, D=96) == 2                      # UNSUPPORTED
     assert _attn(L, B=65) == 2
     assert _attn(L, Hq=64, Hkv=2, B=8) == 2         # G*B = 256 > 128
