@@ -9,10 +9,15 @@
 namespace bdsa {
 
 // ---------------------------------------------------------------- attention
+// Persistent stream-K style schedule: `grid` CTAs share the concatenated
+// (request, KV head, 128-key tile) sequence in equal contiguous ranges.  The
+// workspace holds the per-request tile prefix, a per-request "bad page" flag,
+// and two fp32 partial slots per CTA for units cut between CTAs.
 struct AttnPlan {
-    int nsplit;           // KV splits per (request, KV head)
-    int tiles_per_split;  // 128-key tiles per split
-    size_t workspace;     // bytes of split partials (0 when nsplit == 1)
+    int grid;
+    int rows;             // packed query rows per unit (G * B)
+    size_t off_prefix, off_bad, off_part_o, off_part_lse;
+    size_t workspace;     // total bytes
 };
 
 AttnPlan attn_plan(int bs, int B, int Hq, int Hkv, int D, int max_ctx_len, int num_sms);

@@ -107,11 +107,13 @@ def test_prepare_host_checks(L):
 
 
 def test_workspace_plans(L):
-    # Qwen3-8B-shaped verify (32 x 8 units) on 152 SMs: two splits of 17 tiles.
-    ws = L.bdsa_block_attn_workspace_bytes(32, 16, 32, 8, 128, 4096, 152)
-    assert ws == 2 * 32 * 16 * 32 * 129 * 4
-    # 256 x 8 units already fill the GPU: no split, no workspace.
-    assert L.bdsa_block_attn_workspace_bytes(256, 16, 32, 8, 128, 9216, 152) == 0
-    # long context, 4 x 8 units: split-KV workspace grows with the split count
-    assert L.bdsa_block_attn_workspace_bytes(4, 16, 64, 8, 128, 131072, 152) > 0
+    # persistent schedule: prefix (bs+1) + bad-page flags (bs) + two partial slots per CTA
+    def al(x):
+        return (x + 255) // 256 * 256
+    bs, B, Hq, Hkv, D, sms = 32, 16, 32, 8, 128, 152
+    rows = Hq // Hkv * B
+    want = al((bs + 1) * 4) + al(bs * 4) + al(2 * sms * rows * 4) + al(2 * sms * rows * D * 4)
+    assert L.bdsa_block_attn_workspace_bytes(bs, B, Hq, Hkv, D, 4096, sms) == want
+    # independent of the context length bound
+    assert L.bdsa_block_attn_workspace_bytes(bs, B, Hq, Hkv, D, 131072, sms) == want
     assert L.bdsa_spec_accept_workspace_bytes(32, 16, 151936, 152) > 32 * 594 * 8
