@@ -30,7 +30,7 @@ STATUS = {0: "BDSA_OK", 1: "BDSA_INVALID_ARG", 2: "BDSA_UNSUPPORTED", 3: "BDSA_M
 # Every symbol include/bdsa.h declares.
 EXPORTS = ("bdsa_status_string", "bdsa_version", "bdsa_prepare_block",
            "bdsa_block_attn_workspace_bytes", "bdsa_block_attn_paged",
-           "bdsa_spec_accept_workspace_bytes", "bdsa_spec_accept")
+           "bdsa_spec_accept_workspace_bytes", "bdsa_spec_accept", "bdsa_spec_accept_noalloc")
 
 _lib = None
 
@@ -68,6 +68,9 @@ def lib() -> ctypes.CDLL:
     L.bdsa_spec_accept.argtypes = [P, P, i64, i64, P, i64, i64, P, P, P, i32, i32, i32, P, P, P,
                                    P, P, P, sz, i32, P, P]
     L.bdsa_spec_accept.restype = i32
+    L.bdsa_spec_accept_noalloc.argtypes = [P, P, i64, i64, P, i64, i64, P, P, P, i32, i32, i32,
+                                           P, P, P, P, P, i32, P, P]
+    L.bdsa_spec_accept_noalloc.restype = i32
     _lib = L
     return L
 

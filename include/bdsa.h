@@ -197,6 +197,37 @@ int32_t bdsa_spec_accept(const int32_t *block_ids, const float *p, int64_t p_str
                          size_t workspace_bytes, int32_t num_sms, int32_t *dev_status,
                          void *stream);
 
+/* ------------------------------------------------------------------------ */
+/* bdsa_spec_accept_noalloc -- no counterpart on the source pages.
+ *
+ * The acceptance step of bdsa_spec_accept (same inputs, outputs, rules and
+ * results) for callers that cannot give this library device memory for
+ * scratch: a serving loop whose memory is planned once at start-up, code that
+ * runs while a CUDA graph is being captured (allocation is not allowed there),
+ * or a framework that owns the allocator and passes only the step's tensors.
+ * Instead of a workspace it uses a fixed 8 MiB array in the library's device
+ * image (present on every GPU that loads the library, until the process exits).
+ *   - Nothing is allocated: no cudaMalloc / cudaFree or allocating call.
+ *   - The first call on each device looks up the array's device address
+ *     (cudaGetSymbolAddress) with that device current; make that first call
+ *     before any stream capture.
+ *   - All calls on a device share the array.  Calls whose kernels may overlap
+ *     on the GPU (unordered streams) race on it; order them on one stream.
+ *     Each call clears the per-row counters it needs at zero (an asynchronous
+ *     memset on `stream`); the rest of the array keeps the last call's values.
+ *   - Returns BDSA_WORKSPACE_TOO_SMALL, launching nothing, when the problem
+ *     needs more than 8 MiB of scratch, i.e. when
+ *     bdsa_spec_accept_workspace_bytes(bs, B, V, num_sms) > 8 MiB (about 1700
+ *     rows at V = 151936).
+ */
+int32_t bdsa_spec_accept_noalloc(const int32_t *block_ids, const float *p, int64_t p_stride_r,
+                                 int64_t p_stride_i, const float *q, int64_t q_stride_r,
+                                 int64_t q_stride_i, const float *u_acc, const float *u_samp,
+                                 const int32_t *seq_lens, int32_t bs, int32_t B, int32_t V,
+                                 int32_t *accept_len, int32_t *commit_len, int32_t *out_tokens,
+                                 int32_t *bonus_id, int32_t *new_seq_lens, int32_t num_sms,
+                                 int32_t *dev_status, void *stream);
+
 #ifdef __cplusplus
 }
 #endif
