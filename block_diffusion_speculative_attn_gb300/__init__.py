@@ -198,9 +198,9 @@ def spec_accept(block_ids, p, q, u_acc, u_samp, seq_lens, *, p_strides=None, q_s
                for k in ("accept_len", "commit_len", "bonus_id", "new_seq_lens")}
         out["out_tokens"] = torch.empty((bs, B), dtype=torch.int32, device=dev)
     need = spec_accept_workspace_bytes(bs, B, V, sms)
-    if workspace is None:
-        workspace = torch.empty(max(need, 256), dtype=torch.uint8, device=dev)
-    ws_bytes = workspace.numel() * workspace.element_size()
+    if workspace is None and need > 0:
+        workspace = torch.empty(need, dtype=torch.uint8, device=dev)
+    ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
     # With B == 1 there is no draft and q is never read, but its pointer must stay non-null
     # to select the stochastic rule; an empty tensor may report a null data pointer.
     q_ptr = None if q is None else (_ptr(q) if q.numel() > 0 else _ptr(p))

@@ -48,7 +48,9 @@ int launch_prepare_block(const int32_t *verified_id, const int32_t *seq_lens,
 struct AcceptPlan {
     int nchunk;       // CTAs per row
     int nseg;         // 256-element segments per vocabulary row
-    size_t workspace; // bytes
+    int spc;          // segments per chunk
+    bool cluster;     // one thread-block cluster per row (no global scratch)
+    size_t workspace; // bytes (0 on the cluster path)
 };
 
 AcceptPlan accept_plan(int bs, int B, int V, int num_sms);

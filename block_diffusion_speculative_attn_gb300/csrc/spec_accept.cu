@@ -13,14 +13,23 @@
 // Layout of the work: a row's vocabulary is cut into `nchunk` chunks of
 // 256-element segments and each chunk is one CTA, so even a handful of rows
 // spreads over the whole GPU.  Every CTA recomputes the accepted length a
-// (B - 1 gathered probability pairs), sweeps its chunk once with 16-byte loads
-// and stores one fp64 total per segment (error-free TwoSum pairwise sums of 8
-// elements per lane, fp64 across lanes).  The last CTA of a row to finish
-// (atomic counter; nothing ever waits) scans the segment totals, re-reads the
-// one segment that holds the crossing point and resolves the token to a single
-// index.  Cumulative sums stay within ~1e-13 relative of the exact sums, far
-// inside the 1e-9 band within which the fp64 oracle flags a draw as
-// order-dependent.
+// (B - 1 gathered probability pairs) and sweeps its chunk once with 16-byte
+// loads, reducing each segment to a float-float total (error-free TwoSum
+// sums, about 48 significant bits, all in fp32 arithmetic).  One CTA per row
+// then scans the segment totals, re-reads the one segment that holds the
+// crossing point and resolves the token to a single index.  Cumulative sums
+// stay within ~1e-12 relative of the exact sums, far inside the 1e-9 band
+// within which the fp64 oracle flags a draw as order-dependent.
+//
+// Two ways to bring a row's chunks together:
+//   cluster path (nseg <= kClusterMaxSeg): the row's CTAs form one thread-block
+//     cluster; each writes its segment totals (or greedy chunk maxima) straight
+//     into the shared memory of the cluster's first CTA, a hardware cluster
+//     barrier publishes them and that CTA resolves.  No global scratch, no
+//     atomics, no memset.
+//   global path (larger vocabularies): totals go to the caller's workspace and
+//     the last CTA of the row to finish (atomic counter, nothing ever waits)
+//     resolves.
 #include <cuda_runtime.h>
 #include <limits.h>
 
@@ -33,6 +42,9 @@ namespace {
 constexpr int kSeg = 256;  // vocabulary elements per segment (32 lanes x 8)
 constexpr int kThreads = 256;
 constexpr int kWarps = kThreads / 32;
+constexpr int kMaxB = 64;
+constexpr int kMaxCluster = 8;         // portable cluster size
+constexpr int kClusterMaxSeg = 8192;   // V <= 2^21 on the cluster path (64 KB of totals)
 
 struct Params {
     const int32_t *block_ids;
@@ -44,13 +56,34 @@ struct Params {
     const int32_t *seq_lens;
     int bs, B, V, nchunk, nseg, spc;
     int32_t *accept_len, *commit_len, *out_tokens, *bonus_id, *new_seq_lens;
-    double *seg_sum;   // [bs, nseg]
-    int32_t *counter;  // [bs], zeroed before the launch
-    float *am_val;     // [bs, B, nchunk]  (greedy)
-    int32_t *am_idx;   // [bs, B, nchunk]  (greedy)
+    float2 *seg_tot;   // global path: [bs, nseg] float-float totals
+    int32_t *counter;  // global path: [bs], zeroed before the launch
+    float *am_val;     // global path, greedy: [bs, B, nchunk]
+    int32_t *am_idx;   // global path, greedy: [bs, B, nchunk]
     int32_t *dev_status;
 };
 
+// ------------------------------------------------------------ cluster helpers
+__device__ __forceinline__ void cluster_arrive_relaxed() {
+    asm volatile("barrier.cluster.arrive.relaxed.aligned;" ::: "memory");
+}
+__device__ __forceinline__ void cluster_arrive_release() {
+    asm volatile("barrier.cluster.arrive.release.aligned;" ::: "memory");
+}
+__device__ __forceinline__ void cluster_wait_acquire() {
+    asm volatile("barrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
+// Generic address of the same shared-memory object in cluster CTA `rank`.
+template <class T>
+__device__ __forceinline__ T *map_to_rank(T *p, uint32_t rank) {
+    uint64_t out;
+    asm volatile("mapa.u64 %0, %1, %2;"
+                 : "=l"(out)
+                 : "l"(reinterpret_cast<uint64_t>(p)), "r"(rank));
+    return reinterpret_cast<T *>(out);
+}
+
+// ------------------------------------------------------------------ weights
 // The 8 weights of one lane: max(0, p - q) (residual) or p (q == nullptr).
 __device__ __forceinline__ void load_weights(const float *prow, const float *qrow, long e0, int V,
                                              float (&w)[8]) {
@@ -87,6 +120,7 @@ __device__ __forceinline__ void load_weights(const float *prow, const float *qro
     }
 }
 
+// --------------------------------------------------------- float-float sums
 // Error-free fp32 addition (Knuth's TwoSum): a + b == s + e exactly.
 __device__ __forceinline__ float two_sum(float a, float b, float &e) {
     const float s = __fadd_rn(a, b);
@@ -95,11 +129,22 @@ __device__ __forceinline__ float two_sum(float a, float b, float &e) {
     return s;
 }
 
-// Sum of 8 weights as an fp64 value within ~2^-46 relative of the exact sum: a
-// pairwise tree of TwoSums keeps every rounding error, and only the (tiny) sum
-// of those errors is rounded.  Fixed order; the sweep and the resolve step
-// both use it.
-__device__ __forceinline__ double group_sum(const float (&w)[8]) {
+// A float-float value hi + lo (|lo| <= ulp(hi) / 2): about 48 significant bits
+// from fp32 arithmetic alone (fp64 throughput on this GPU is a small fraction
+// of fp32's).  Stored as float2 {hi, lo}.
+__device__ __forceinline__ float2 ff_add(float2 a, float2 b) {
+    float e;
+    const float s = two_sum(a.x, b.x, e);
+    const float lo = __fadd_rn(__fadd_rn(a.y, b.y), e);
+    const float hi = __fadd_rn(s, lo);  // renormalise (Fast2Sum, |s| >= |lo|)
+    return make_float2(hi, __fsub_rn(lo, __fsub_rn(hi, s)));
+}
+
+__device__ __forceinline__ double ff_to_double(float2 a) { return (double)a.x + (double)a.y; }
+
+// Sum of 8 weights as a float-float: a pairwise tree of TwoSums keeps every
+// rounding error; only the sum of those tiny errors is rounded.
+__device__ __forceinline__ float2 group_sum_ff(const float (&w)[8]) {
     float e0, e1, e2, e3, e4, e5, e6;
     const float s01 = two_sum(w[0], w[1], e0);
     const float s23 = two_sum(w[2], w[3], e1);
@@ -110,17 +155,38 @@ __device__ __forceinline__ double group_sum(const float (&w)[8]) {
     const float s07 = two_sum(s03, s47, e6);
     const float err = __fadd_rn(__fadd_rn(__fadd_rn(e0, e1), __fadd_rn(e2, e3)),
                                 __fadd_rn(__fadd_rn(e4, e5), e6));
-    return (double)s07 + (double)err;
+    const float hi = __fadd_rn(s07, err);
+    return make_float2(hi, __fsub_rn(err, __fsub_rn(hi, s07)));
 }
 
-__device__ __forceinline__ double warp_sum_f64(double v) {
+__device__ __forceinline__ float2 shfl_xor_ff(float2 v, int o) {
+    return make_float2(__shfl_xor_sync(0xffffffffu, v.x, o), __shfl_xor_sync(0xffffffffu, v.y, o));
+}
+__device__ __forceinline__ float2 shfl_up_ff(float2 v, int o) {
+    return make_float2(__shfl_up_sync(0xffffffffu, v.x, o), __shfl_up_sync(0xffffffffu, v.y, o));
+}
+
+// Warp total (butterfly; every lane gets the total).
+__device__ __forceinline__ float2 warp_sum_ff(float2 v) {
 #pragma unroll
-    for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+    for (int o = 16; o > 0; o >>= 1) v = ff_add(v, shfl_xor_ff(v, o));
     return v;
 }
 
-// Accepted draft count for row r (stochastic mode), computed by one warp.
-__device__ int accepted_len(const Params &P, int r, int lane, bool &bad_id) {
+// Warp inclusive prefix sum.
+__device__ __forceinline__ float2 warp_scan_ff(float2 v, int lane) {
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+        const float2 t = shfl_up_ff(v, o);
+        if (lane >= o) v = ff_add(v, t);
+    }
+    return v;
+}
+
+// ------------------------------------------------------------ acceptance
+// Accepted draft count for row r (stochastic mode), computed by one warp.  The
+// draft ids are also left in s_ids[1..B-1] for the output step.
+__device__ int accepted_len(const Params &P, int r, int lane, bool &bad_id, int *s_ids) {
     const int B = P.B;
     bool bad_any = false;
     int a = -1;
@@ -130,6 +196,7 @@ __device__ int accepted_len(const Params &P, int r, int lane, bool &bad_id) {
         bad_id = false;
         if (i < B) {
             const int d = P.block_ids[(long)r * B + i];
+            s_ids[i] = d;
             if (d < 0 || d >= P.V) {
                 rej = true;
                 bad_id = true;
@@ -156,117 +223,158 @@ __device__ int accepted_len(const Params &P, int r, int lane, bool &bad_id) {
     return a < 0 ? B - 1 : a;
 }
 
-// Segment totals of this CTA's chunk for the chosen distribution.
-__device__ void sweep_chunk(const Params &P, int r, const float *prow, const float *qrow,
-                            int seg_begin, int seg_end, int warp, int lane) {
-    for (int seg = seg_begin + warp; seg < seg_end; seg += kWarps) {
-        float w[8];
-        load_weights(prow, qrow, (long)seg * kSeg + lane * 8, P.V, w);
-        const double t = warp_sum_f64(group_sum(w));
-        if (lane == 0) P.seg_sum[(long)r * P.nseg + seg] = t;
-    }
-}
+// Segment totals of segments [seg_begin, seg_end) of the chosen distribution,
+// written to tot[seg] (shared memory of this or another cluster CTA, or global
+// memory).  Each warp loads kUnroll segments before reducing them, so its
+// loads overlap.
+constexpr int kUnroll = 4;
 
-// Resolve the draw InvCDF(w, u) from the segment totals; executed by warp 0.
-// Returns the token index (or -1 when the weights are all zero).
-__device__ int resolve_draw(const Params &P, int r, const float *prow, const float *qrow,
-                            float u, int lane) {
-    const int nseg = P.nseg;
-    const int per = (nseg + 31) / 32;
-    const int s0 = min(nseg, lane * per), s1 = min(nseg, s0 + per);
-    const double *seg = P.seg_sum + (long)r * nseg;
-    double loc = 0.0;
-    for (int s = s0; s < s1; ++s) loc += __ldcg(seg + s);
-    double inc = loc;
+__device__ void sweep_chunk(const Params &P, const float *prow, const float *qrow, int seg_begin,
+                            int seg_end, int warp, int lane, float2 *tot) {
+    for (int s0 = seg_begin + warp; s0 < seg_end; s0 += kUnroll * kWarps) {
+        float w[kUnroll][8];
 #pragma unroll
-    for (int o = 1; o < 32; o <<= 1) {
-        const double t = __shfl_up_sync(0xffffffffu, inc, o);
-        if (lane >= o) inc += t;
-    }
-    double excl = __shfl_up_sync(0xffffffffu, inc, 1);
-    if (lane == 0) excl = 0.0;
-    const double S = __shfl_sync(0xffffffffu, inc, 31);
-    if (!(S > 0.0)) return -1;
-    double T = (double)u * S;
-
-    // first segment whose cumulative total exceeds T
-    int found = -1;
-    double run = excl;
-    for (int s = s0; s < s1; ++s) {
-        const double v = __ldcg(seg + s);
-        if (run + v > T) {
-            found = s;
-            break;
+        for (int u = 0; u < kUnroll; ++u) {
+            const int seg = s0 + u * kWarps;
+            if (seg < seg_end) load_weights(prow, qrow, (long)seg * kSeg + lane * 8, P.V, w[u]);
         }
-        run += v;
-    }
-    const unsigned any = __ballot_sync(0xffffffffu, found >= 0);
-    int seg_star;
-    double base_seg;
-    if (any != 0u) {
-        const int leader = __ffs(any) - 1;
-        seg_star = __shfl_sync(0xffffffffu, found, leader);
-        base_seg = __shfl_sync(0xffffffffu, run, leader);
-    } else {
-        // rounding fallback: the last segment with positive mass, no crossing inside it
-        int last = -1;
-        for (int s = s0; s < s1; ++s)
-            if (__ldcg(seg + s) > 0.0) last = s;
 #pragma unroll
-        for (int o = 16; o > 0; o >>= 1) last = max(last, __shfl_xor_sync(0xffffffffu, last, o));
-        seg_star = last;
-        base_seg = 0.0;
-        T = INFINITY;
-    }
-    // within the segment: one 8-element group per lane
-    float w[8];
-    const long e0 = (long)seg_star * kSeg + lane * 8;
-    load_weights(prow, qrow, e0, P.V, w);
-    const double g = group_sum(w);
-    double ginc = g;
-#pragma unroll
-    for (int o = 1; o < 32; o <<= 1) {
-        const double t = __shfl_up_sync(0xffffffffu, ginc, o);
-        if (lane >= o) ginc += t;
-    }
-    double gexcl = __shfl_up_sync(0xffffffffu, ginc, 1);
-    if (lane == 0) gexcl = 0.0;
-    const double gb = base_seg + gexcl;
-    const unsigned cross = __ballot_sync(0xffffffffu, gb + g > T);
-    int lane_star;
-    double cum;
-    bool use_cross;
-    if (cross != 0u) {
-        lane_star = __ffs(cross) - 1;
-        use_cross = true;
-    } else {
-        const unsigned pos = __ballot_sync(0xffffffffu, g > 0.0);
-        lane_star = pos ? 31 - __clz(pos) : 0;
-        use_cross = false;
-    }
-    cum = __shfl_sync(0xffffffffu, gb, lane_star);
-    int k = -1;
-    if (lane == lane_star) {
-        int last_pos = -1;
-        for (int e = 0; e < 8; ++e) {
-            if (w[e] > 0.f) last_pos = e;
-            cum += (double)w[e];
-            if (use_cross && cum > T) {
-                k = e;
-                break;
+        for (int u = 0; u < kUnroll; ++u) {
+            const int seg = s0 + u * kWarps;
+            if (seg < seg_end) {
+                const float2 t = warp_sum_ff(group_sum_ff(w[u]));
+                if (lane == 0) tot[seg] = t;
             }
         }
-        if (k < 0) k = last_pos;
-        if (k >= 0) k += (int)e0;
     }
-    return __shfl_sync(0xffffffffu, k, lane_star);
 }
 
-__device__ void write_outputs(const Params &P, int r, int a, int token) {
+// Segment total `i`: plain load from shared memory, or an L2 load of values
+// that other CTAs wrote (global path).
+template <bool kShared>
+__device__ __forceinline__ float2 load_tot(const float2 *tot, int i) {
+    if constexpr (kShared)
+        return tot[i];
+    else
+        return __ldcg(tot + i);
+}
+
+// Resolve the draw InvCDF(w, u) from the segment totals with the whole CTA:
+// a block-wide scan of the totals finds the segment holding the crossing, then
+// warp 0 re-reads that one segment and finds the element.  Every thread
+// returns the token index (-1 when the weights are all zero).
+template <bool kShared>
+__device__ int resolve_draw(const Params &P, const float *prow, const float *qrow, float u,
+                            const float2 *tot) {
+    __shared__ float2 s_wtot[kWarps];
+    __shared__ int s_seg;
+    __shared__ double s_base;
+    __shared__ double s_T;
+    __shared__ int s_last_pos;
+    __shared__ int s_tok;
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const int nseg = P.nseg;
+    const int per = (nseg + kThreads - 1) / kThreads;
+    const int s0 = min(nseg, tid * per), s1 = min(nseg, s0 + per);
+    float2 loc = make_float2(0.f, 0.f);
+    for (int q = s0; q < s1; ++q) loc = ff_add(loc, load_tot<kShared>(tot, q));
+    // block exclusive scan of the per-thread totals
+    const float2 inc = warp_scan_ff(loc, lane);
+    if (lane == 31) s_wtot[warp] = inc;
+    if (tid == 0) {
+        s_seg = INT_MAX;
+        s_last_pos = -1;
+    }
+    __syncthreads();
+    float2 wexcl = make_float2(0.f, 0.f), Sff = make_float2(0.f, 0.f);
+#pragma unroll
+    for (int w = 0; w < kWarps; ++w) {
+        if (w < warp) wexcl = ff_add(wexcl, s_wtot[w]);
+        Sff = ff_add(Sff, s_wtot[w]);
+    }
+    float2 excl = shfl_up_ff(inc, 1);
+    if (lane == 0) excl = make_float2(0.f, 0.f);
+    excl = ff_add(excl, wexcl);
+    const double S = ff_to_double(Sff);
+    if (!(S > 0.0)) return -1;  // uniform: every thread sees the same S
+    const double T = (double)u * S;
+    // first segment whose cumulative total exceeds T
+    double run = ff_to_double(excl);
+    int found = -1;
+    int last_pos = -1;
+    for (int q = s0; q < s1; ++q) {
+        const double v = ff_to_double(load_tot<kShared>(tot, q));
+        if (v > 0.0) last_pos = q;
+        if (found < 0 && run + v > T) found = q;
+        if (found < 0) run += v;
+    }
+    if (found >= 0) atomicMin(&s_seg, found);
+    if (last_pos >= 0) atomicMax(&s_last_pos, last_pos);
+    __syncthreads();
+    if (found >= 0 && found == s_seg) {
+        s_base = run;
+        s_T = T;
+    }
+    if (tid == 0 && s_seg == INT_MAX) {
+        // rounding fallback: the last segment with positive mass, no crossing in it
+        s_seg = s_last_pos;
+        s_base = 0.0;
+        s_T = INFINITY;
+    }
+    __syncthreads();
+    if (warp == 0 && s_seg < 0) {
+        if (lane == 0) s_tok = -1;
+    } else if (warp == 0) {
+        const int seg_star = s_seg;
+        const double base_seg = s_base, Tw = s_T;
+        // within the segment: one 8-element group per lane
+        float w[8];
+        const long e0 = (long)seg_star * kSeg + lane * 8;
+        load_weights(prow, qrow, e0, P.V, w);
+        const float2 gff = group_sum_ff(w);
+        const float2 ginc = warp_scan_ff(gff, lane);
+        float2 gexcl = shfl_up_ff(ginc, 1);
+        if (lane == 0) gexcl = make_float2(0.f, 0.f);
+        const double g = ff_to_double(gff);
+        const double gb = base_seg + ff_to_double(gexcl);
+        const unsigned cross = __ballot_sync(0xffffffffu, gb + g > Tw);
+        int lane_star;
+        bool use_cross;
+        if (cross != 0u) {
+            lane_star = __ffs(cross) - 1;
+            use_cross = true;
+        } else {
+            const unsigned pos = __ballot_sync(0xffffffffu, g > 0.0);
+            lane_star = pos ? 31 - __clz(pos) : 0;
+            use_cross = false;
+        }
+        double cum = __shfl_sync(0xffffffffu, gb, lane_star);
+        if (lane == lane_star) {
+            int k = -1, lp = -1;
+            for (int e = 0; e < 8; ++e) {
+                if (w[e] > 0.f) lp = e;
+                cum += (double)w[e];
+                if (use_cross && cum > Tw) {
+                    k = e;
+                    break;
+                }
+            }
+            if (k < 0) k = lp;
+            if (k >= 0) k += (int)e0;
+            s_tok = k;
+        }
+    }
+    __syncthreads();
+    return s_tok;
+}
+
+// ids[i] holds block_ids[r, i] for 1 <= i < B (shared memory).
+__device__ void write_outputs(const Params &P, int r, int a, int token, const int *ids,
+                              int seq_len) {
     const int B = P.B;
     for (int i = threadIdx.x; i < B; i += blockDim.x) {
         int32_t v = -1;
-        if (i < a) v = P.block_ids[(long)r * B + i + 1];
+        if (i < a) v = ids[i + 1];
         else if (i == a) v = token;
         P.out_tokens[(long)r * B + i] = v;
     }
@@ -274,62 +382,81 @@ __device__ void write_outputs(const Params &P, int r, int a, int token) {
         P.accept_len[r] = a;
         P.commit_len[r] = a + 1;
         P.bonus_id[r] = token;
-        P.new_seq_lens[r] = P.seq_lens[r] + a + 1;
-        P.counter[r] = 0;
+        P.new_seq_lens[r] = seq_len + a + 1;
     }
 }
 
-// True in exactly one CTA per row: the last one to finish its chunk.
+// Global path: true in exactly one CTA per row, the last one to finish its
+// chunk; that CTA also re-arms the row's counter for the next call.
 __device__ bool last_cta_of_row(const Params &P, int r) {
     __shared__ int s_last;
     __threadfence();
     __syncthreads();
     if (threadIdx.x == 0) s_last = (atomicAdd(P.counter + r, 1) == P.nchunk - 1);
     __syncthreads();
-    if (s_last) __threadfence();
+    if (s_last) {
+        __threadfence();
+        if (threadIdx.x == 0) P.counter[r] = 0;
+    }
     return s_last != 0;
 }
 
+// One CTA per (row, chunk); on the cluster path the row's CTAs are one
+// cluster (cluster rank == chunk for a 1-D grid of whole clusters).
+template <bool kCluster>
 __global__ void __launch_bounds__(kThreads) accept_stochastic_kernel(const Params P) {
     const int r = blockIdx.x / P.nchunk, chunk = blockIdx.x % P.nchunk;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    extern __shared__ float2 s_tot[];  // cluster path: [nseg] totals, used in chunk 0
+    __shared__ int s_ids[kMaxB];
     __shared__ int s_a;
+    __shared__ float s_u;
+    __shared__ int s_sl;
+    // First phase of the cluster barrier: once it completes, every CTA of the
+    // row has started, so its shared memory may be written.
+    if constexpr (kCluster) cluster_arrive_relaxed();
     if (warp == 0) {
         bool bad = false;
-        const int a = accepted_len(P, r, lane, bad);
+        const int a = accepted_len(P, r, lane, bad, s_ids);
         if (lane == 0) {
             s_a = a;
             if (bad && chunk == 0) report_status(P.dev_status, BDSA_DEVICE_OUT_OF_RANGE);
         }
+    } else if (warp == 1 && lane == 0) {
+        s_u = __ldg(P.u_samp + r);
+        s_sl = __ldg(P.seq_lens + r);
     }
     __syncthreads();
     const int a = s_a;
     const float *prow = P.p + r * P.psr + a * P.psi;
     const float *qrow = (a < P.B - 1) ? P.q + r * P.qsr + a * P.qsi : nullptr;
     const int sb = chunk * P.spc, se = min(P.nseg, sb + P.spc);
-    sweep_chunk(P, r, prow, qrow, sb, se, warp, lane);
-    if (!last_cta_of_row(P, r)) return;
-
-    __shared__ int s_tok;
-    const float u = __ldg(P.u_samp + r);
-    if (warp == 0) {
-        const int t = resolve_draw(P, r, prow, qrow, u, lane);
-        if (lane == 0) s_tok = t;
+    float2 *tot;
+    if constexpr (kCluster) {
+        cluster_wait_acquire();
+        tot = map_to_rank(s_tot, 0);
+    } else {
+        tot = P.seg_tot + (long)r * P.nseg;
     }
-    __syncthreads();
-    if (s_tok < 0 && qrow != nullptr) {
+    sweep_chunk(P, prow, qrow, sb, se, warp, lane, tot);
+    if constexpr (kCluster) {
+        cluster_arrive_release();
+        cluster_wait_acquire();
+        if (chunk != 0) return;
+        tot = s_tot;
+    } else {
+        if (!last_cta_of_row(P, r)) return;
+    }
+    const float u = s_u;
+    int tok = resolve_draw<kCluster>(P, prow, qrow, u, tot);
+    if (tok < 0 && qrow != nullptr) {
         // residual has no mass (p <= q everywhere in fp32): draw from p instead
         __syncthreads();
-        sweep_chunk(P, r, prow, nullptr, 0, P.nseg, warp, lane);
-        __threadfence_block();
+        sweep_chunk(P, prow, nullptr, 0, P.nseg, warp, lane, tot);
         __syncthreads();
-        if (warp == 0) {
-            const int t = resolve_draw(P, r, prow, nullptr, u, lane);
-            if (lane == 0) s_tok = t;
-        }
-        __syncthreads();
+        tok = resolve_draw<kCluster>(P, prow, nullptr, u, tot);
     }
-    write_outputs(P, r, a, s_tok);
+    write_outputs(P, r, a, tok, s_ids, s_sl);
 }
 
 __device__ __forceinline__ void better(float &bv, int &bi, float v, int i) {
@@ -339,23 +466,45 @@ __device__ __forceinline__ void better(float &bv, int &bi, float v, int i) {
     }
 }
 
+// Greedy: every CTA finds, for each block slot i, the argmax of p[r, i] over
+// its chunk (warps run through the slots independently, kUnroll segments in
+// flight); the resolving CTA combines the chunks and walks the block.
+template <bool kCluster>
 __global__ void __launch_bounds__(kThreads) accept_greedy_kernel(const Params P) {
     const int r = blockIdx.x / P.nchunk, chunk = blockIdx.x % P.nchunk;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    __shared__ float s_v[kWarps];
-    __shared__ int s_i[kWarps];
+    const int B = P.B, C = P.nchunk;
+    __shared__ float s_wv[kWarps][kMaxB];
+    __shared__ int s_wi[kWarps][kMaxB];
+    __shared__ float s_cv[kMaxB * kMaxCluster];  // cluster path: [i][chunk], used in chunk 0
+    __shared__ int s_ci[kMaxB * kMaxCluster];
+    __shared__ int s_ids[kMaxB];
+    __shared__ int s_tp[kMaxB];
+    __shared__ int s_sl;
+    if constexpr (kCluster) cluster_arrive_relaxed();
+    for (int i = threadIdx.x; i < B; i += kThreads) s_ids[i] = P.block_ids[(long)r * B + i];
+    if (threadIdx.x == 0) s_sl = __ldg(P.seq_lens + r);
     const int sb = chunk * P.spc, se = min(P.nseg, sb + P.spc);
-    for (int i = 0; i < P.B; ++i) {
+    for (int i = 0; i < B; ++i) {
         const float *prow = P.p + r * P.psr + (long)i * P.psi;
         float bv = -INFINITY;
         int bi = INT_MAX;
-        for (int seg = sb + warp; seg < se; seg += kWarps) {
-            float w[8];
-            const long e0 = (long)seg * kSeg + lane * 8;
-            load_weights(prow, nullptr, e0, P.V, w);
+        for (int s0 = sb + warp; s0 < se; s0 += kUnroll * kWarps) {
+            float w[kUnroll][8];
 #pragma unroll
-            for (int e = 0; e < 8; ++e)
-                if (e0 + e < P.V) better(bv, bi, w[e], (int)(e0 + e));
+            for (int u = 0; u < kUnroll; ++u) {
+                const int seg = s0 + u * kWarps;
+                if (seg < se) load_weights(prow, nullptr, (long)seg * kSeg + lane * 8, P.V, w[u]);
+            }
+#pragma unroll
+            for (int u = 0; u < kUnroll; ++u) {
+                const long e0 = (long)(s0 + u * kWarps) * kSeg + lane * 8;
+                if (s0 + u * kWarps < se) {
+#pragma unroll
+                    for (int e = 0; e < 8; ++e)
+                        if (e0 + e < P.V) better(bv, bi, w[u][e], (int)(e0 + e));
+                }
+            }
         }
 #pragma unroll
         for (int o = 16; o > 0; o >>= 1) {
@@ -364,26 +513,48 @@ __global__ void __launch_bounds__(kThreads) accept_greedy_kernel(const Params P)
             better(bv, bi, ov, oi);
         }
         if (lane == 0) {
-            s_v[warp] = bv;
-            s_i[warp] = bi;
+            s_wv[warp][i] = bv;
+            s_wi[warp][i] = bi;
         }
-        __syncthreads();
-        if (threadIdx.x == 0) {
-            for (int w = 1; w < kWarps; ++w) better(bv, bi, s_v[w], s_i[w]);
-            const long o = ((long)r * P.B + i) * P.nchunk + chunk;
+    }
+    __syncthreads();
+    float *cv;
+    int *ci;
+    if constexpr (kCluster) {
+        cluster_wait_acquire();
+        cv = map_to_rank(s_cv, 0);
+        ci = map_to_rank(s_ci, 0);
+    }
+    for (int i = threadIdx.x; i < B; i += kThreads) {
+        float bv = -INFINITY;
+        int bi = INT_MAX;
+        for (int w = 0; w < kWarps; ++w) better(bv, bi, s_wv[w][i], s_wi[w][i]);
+        if constexpr (kCluster) {
+            cv[i * C + chunk] = bv;
+            ci[i * C + chunk] = bi;
+        } else {
+            const long o = ((long)r * B + i) * C + chunk;
             P.am_val[o] = bv;
             P.am_idx[o] = bi;
         }
-        __syncthreads();
     }
-    if (!last_cta_of_row(P, r)) return;
-    __shared__ int s_tp[64];
-    for (int i = threadIdx.x; i < P.B; i += blockDim.x) {
+    if constexpr (kCluster) {
+        cluster_arrive_release();
+        cluster_wait_acquire();
+        if (chunk != 0) return;
+    } else {
+        if (!last_cta_of_row(P, r)) return;
+    }
+    for (int i = threadIdx.x; i < B; i += kThreads) {
         float bv = -INFINITY;
         int bi = INT_MAX;
-        for (int c = 0; c < P.nchunk; ++c) {
-            const long o = ((long)r * P.B + i) * P.nchunk + c;
-            better(bv, bi, __ldcg(P.am_val + o), __ldcg(P.am_idx + o));
+        for (int c = 0; c < C; ++c) {
+            if constexpr (kCluster) {
+                better(bv, bi, s_cv[i * C + c], s_ci[i * C + c]);
+            } else {
+                const long o = ((long)r * B + i) * C + c;
+                better(bv, bi, __ldcg(P.am_val + o), __ldcg(P.am_idx + o));
+            }
         }
         s_tp[i] = (bi == INT_MAX) ? 0 : bi;
     }
@@ -391,11 +562,11 @@ __global__ void __launch_bounds__(kThreads) accept_greedy_kernel(const Params P)
     __shared__ int s_a;
     if (threadIdx.x == 0) {
         int a = 0;
-        while (a < P.B - 1 && P.block_ids[(long)r * P.B + a + 1] == s_tp[a]) ++a;
+        while (a < B - 1 && s_ids[a + 1] == s_tp[a]) ++a;
         s_a = a;
     }
     __syncthreads();
-    write_outputs(P, r, s_a, s_tp[s_a]);
+    write_outputs(P, r, s_a, s_tp[s_a], s_ids, s_sl);
 }
 
 size_t align256(size_t x) { return (x + 255) & ~(size_t)255; }
@@ -405,23 +576,30 @@ size_t align256(size_t x) { return (x + 255) & ~(size_t)255; }
 AcceptPlan accept_plan(int bs, int B, int V, int num_sms) {
     AcceptPlan p;
     p.nseg = (V + kSeg - 1) / kSeg;
+    p.cluster = p.nseg <= kClusterMaxSeg;
+    // about two CTAs per SM over the whole batch, at least 8 segments (2048
+    // elements) per CTA, and at most a portable cluster per row on the
+    // cluster path
     long nchunk = bs > 0 ? (2L * num_sms + bs - 1) / bs : 1;
-    const long cap = (p.nseg + 7) / 8;  // at least 8 segments (2048 elements) per CTA
+    const long cap = (p.nseg + 7) / 8;
     if (nchunk > cap) nchunk = cap;
+    if (p.cluster && nchunk > kMaxCluster) nchunk = kMaxCluster;
     if (nchunk < 1) nchunk = 1;
     const long spc = (p.nseg + nchunk - 1) / nchunk;
-    nchunk = (p.nseg + spc - 1) / spc;
+    if (!p.cluster) nchunk = (p.nseg + spc - 1) / spc;
     p.nchunk = (int)nchunk;
-    p.workspace = align256((size_t)bs * sizeof(int32_t)) +
-                  align256((size_t)bs * p.nseg * sizeof(double)) +
-                  2 * align256((size_t)bs * B * p.nchunk * 4);
+    p.spc = (int)spc;
+    p.workspace = p.cluster ? 0
+                            : align256((size_t)bs * sizeof(int32_t)) +
+                                  align256((size_t)bs * p.nseg * sizeof(float2)) +
+                                  2 * align256((size_t)bs * B * p.nchunk * 4);
     return p;
 }
 
 int launch_spec_accept(const AcceptArgs &a, cudaStream_t stream) {
     if (a.bs == 0) return BDSA_OK;
     const AcceptPlan plan = accept_plan(a.bs, a.B, a.V, a.num_sms);
-    if (a.workspace == nullptr || a.workspace_bytes < plan.workspace)
+    if (a.workspace_bytes < plan.workspace || (plan.workspace > 0 && a.workspace == nullptr))
         return BDSA_WORKSPACE_TOO_SMALL;
     Params P;
     P.block_ids = a.block_ids;
@@ -439,30 +617,60 @@ int launch_spec_accept(const AcceptArgs &a, cudaStream_t stream) {
     P.V = a.V;
     P.nchunk = plan.nchunk;
     P.nseg = plan.nseg;
-    P.spc = (plan.nseg + plan.nchunk - 1) / plan.nchunk;
+    P.spc = plan.spc;
     P.accept_len = a.accept_len;
     P.commit_len = a.commit_len;
     P.out_tokens = a.out_tokens;
     P.bonus_id = a.bonus_id;
     P.new_seq_lens = a.new_seq_lens;
     P.dev_status = a.dev_status;
+    P.seg_tot = nullptr;
+    P.counter = nullptr;
+    P.am_val = nullptr;
+    P.am_idx = nullptr;
+    const long nblocks = (long)plan.nchunk * a.bs;
+    if (nblocks > 0x7fffffffL) return BDSA_UNSUPPORTED;
+    const bool greedy = a.q == nullptr;
+    if (plan.cluster) {
+        // segment totals of one row live in the first CTA of its cluster
+        const size_t smem = greedy ? 0 : (size_t)plan.nseg * sizeof(float2);
+        const void *fn = greedy ? reinterpret_cast<const void *>(&accept_greedy_kernel<true>)
+                                : reinterpret_cast<const void *>(&accept_stochastic_kernel<true>);
+        if (smem > 48 * 1024 &&
+            cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) !=
+                cudaSuccess)
+            return BDSA_CUDA_ERROR;
+        cudaLaunchConfig_t cfg = {};
+        cfg.gridDim = dim3((unsigned)nblocks);
+        cfg.blockDim = dim3(kThreads);
+        cfg.dynamicSmemBytes = smem;
+        cfg.stream = stream;
+        cudaLaunchAttribute attr[1];
+        attr[0].id = cudaLaunchAttributeClusterDimension;
+        attr[0].val.clusterDim.x = (unsigned)plan.nchunk;
+        attr[0].val.clusterDim.y = 1;
+        attr[0].val.clusterDim.z = 1;
+        cfg.attrs = attr;
+        cfg.numAttrs = 1;
+        const cudaError_t e = greedy ? cudaLaunchKernelEx(&cfg, accept_greedy_kernel<true>, P)
+                                     : cudaLaunchKernelEx(&cfg, accept_stochastic_kernel<true>, P);
+        return e == cudaSuccess ? BDSA_OK : BDSA_CUDA_ERROR;
+    }
     char *ws = static_cast<char *>(a.workspace);
     P.counter = reinterpret_cast<int32_t *>(ws);
     ws += align256((size_t)a.bs * sizeof(int32_t));
-    P.seg_sum = reinterpret_cast<double *>(ws);
-    ws += align256((size_t)a.bs * plan.nseg * sizeof(double));
+    P.seg_tot = reinterpret_cast<float2 *>(ws);
+    ws += align256((size_t)a.bs * plan.nseg * sizeof(float2));
     P.am_val = reinterpret_cast<float *>(ws);
     ws += align256((size_t)a.bs * a.B * plan.nchunk * 4);
     P.am_idx = reinterpret_cast<int32_t *>(ws);
     if (cudaMemsetAsync(P.counter, 0, (size_t)a.bs * sizeof(int32_t), stream) != cudaSuccess)
         return BDSA_CUDA_ERROR;
-    const long nblocks = (long)plan.nchunk * a.bs;
-    if (nblocks > 0x7fffffffL) return BDSA_UNSUPPORTED;
     const unsigned grid = (unsigned)nblocks;
-    if (a.q != nullptr)
-        accept_stochastic_kernel<<<grid, kThreads, 0, stream>>>(P);
+    if (greedy)
+        accept_greedy_kernel<false><<<grid, kThreads, 0, stream>>>(P);
     else
-        accept_greedy_kernel<<<grid, kThreads, 0, stream>>>(P);
+        accept_stochastic_kernel<false><<<grid, kThreads, 0, stream>>>(P);
     return cudaGetLastError() == cudaSuccess ? BDSA_OK : BDSA_CUDA_ERROR;
 }
 

@@ -19,7 +19,8 @@
 namespace {
 
 // Fixed scratch: 8 MiB on every GPU that loads the library, held until the
-// process exits.  Enough for about 1700 rows at a 151936-token vocabulary.
+// process exits.  Only vocabularies above 2^21 use scratch (about 60 rows at
+// V = 2^22 fit); smaller ones need none.
 constexpr size_t kScratchBytes = size_t(8) << 20;
 static __device__ __align__(256) unsigned char g_accept_scratch[kScratchBytes];
 
@@ -64,8 +65,8 @@ extern "C" int32_t bdsa_spec_accept_noalloc(const int32_t *block_ids, const floa
     void *scratch = nullptr;
     const int st = scratch_address(&scratch);
     if (st != BDSA_OK) return st;
-    // Same checks and kernels as bdsa_spec_accept; the launch clears the
-    // per-row counters it needs at zero before the kernel runs.
+    // Same checks and kernels as bdsa_spec_accept; a launch that uses scratch
+    // clears the per-row counters it needs at zero before the kernel runs.
     return bdsa_spec_accept(block_ids, p, p_stride_r, p_stride_i, q, q_stride_r, q_stride_i,
                             u_acc, u_samp, seq_lens, bs, B, V, accept_len, commit_len,
                             out_tokens, bonus_id, new_seq_lens, scratch, kScratchBytes, num_sms,

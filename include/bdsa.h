@@ -185,6 +185,11 @@ int32_t bdsa_block_attn_paged(const bdsa_bf16 *q, const bdsa_bf16 *k_cache,
  * non-null pointer to select the stochastic rule (the bonus is then sampled).
  * A draft id outside [0, V) counts as a rejection and sets dev_status.
  * Workspace: bdsa_spec_accept_workspace_bytes(...) bytes, 256-byte aligned.
+ *   It is 0 for V <= 2^21: a row's partial sums then stay in the shared memory
+ *   of the thread-block cluster that handles the row, and `workspace` may be
+ *   NULL.  Larger vocabularies need global scratch (per-row float-float
+ *   segment totals and a counter that each call clears with a memset).
+ * Launches: one kernel (plus that memset above V = 2^21).
  */
 size_t bdsa_spec_accept_workspace_bytes(int32_t bs, int32_t B, int32_t V, int32_t num_sms);
 
@@ -213,12 +218,14 @@ int32_t bdsa_spec_accept(const int32_t *block_ids, const float *p, int64_t p_str
  *     before any stream capture.
  *   - All calls on a device share the array.  Calls whose kernels may overlap
  *     on the GPU (unordered streams) race on it; order them on one stream.
- *     Each call clears the per-row counters it needs at zero (an asynchronous
- *     memset on `stream`); the rest of the array keeps the last call's values.
+ *     Problems with V <= 2^21 need no scratch and do not touch the array.
+ *     Above that, each call clears the per-row counters it needs at zero (an
+ *     asynchronous memset on `stream`); the rest of the array keeps the last
+ *     call's values.
  *   - Returns BDSA_WORKSPACE_TOO_SMALL, launching nothing, when the problem
  *     needs more than 8 MiB of scratch, i.e. when
- *     bdsa_spec_accept_workspace_bytes(bs, B, V, num_sms) > 8 MiB (about 1700
- *     rows at V = 151936).
+ *     bdsa_spec_accept_workspace_bytes(bs, B, V, num_sms) > 8 MiB (for
+ *     example 128 rows at V = 2^22).
  */
 int32_t bdsa_spec_accept_noalloc(const int32_t *block_ids, const float *p, int64_t p_stride_r,
                                  int64_t p_stride_i, const float *q, int64_t q_stride_r,

@@ -171,6 +171,40 @@ def test_greedy_full_size():
         assert (got[k].cpu().numpy() == want[k]).all(), k
 
 
+@pytest.mark.parametrize("V", [1 << 21, (1 << 21) + 1000])
+def test_vocab_at_and_beyond_the_cluster_limit(V):
+    # 2^21 is the largest vocabulary whose segment totals sit in one CTA's shared
+    # memory (64 KB, above the 48 KB default); one more segment takes the path
+    # through the global workspace and the last-CTA counter.
+    need = bdsa.spec_accept_workspace_bytes(3, 4, V)
+    assert (need == 0) == (V <= 1 << 21)
+    rng = np.random.default_rng(V)
+    bs, B = 3, 4
+    p = rng.random((bs, B, V), dtype=np.float32) ** 8
+    p /= p.sum(-1, keepdims=True)
+    q = p[:, :B - 1] * rng.uniform(0.5, 1.5, (bs, B - 1, V)).astype(np.float32)
+    q /= q.sum(-1, keepdims=True)
+    ids = np.empty((bs, B), np.int32)
+    ids[:, 0] = rng.integers(0, V, bs)
+    for i in range(1, B):
+        c = np.cumsum(q[:, i - 1].astype(np.float64), -1)
+        u = rng.random(bs)[:, None] * c[:, -1:]
+        ids[:, i] = np.minimum((c <= u).sum(-1), V - 1)
+    acc = wl.AcceptInputs(torch.from_numpy(ids), torch.from_numpy(p), torch.from_numpy(q),
+                          torch.from_numpy(rng.random((bs, B - 1), dtype=np.float32)),
+                          torch.from_numpy(rng.random(bs, dtype=np.float32)),
+                          torch.from_numpy(rng.integers(0, 1000, bs).astype(np.int32)))
+    for greedy in (False, True):
+        got = _gpu(acc, greedy=greedy)
+        want = oracle.spec_accept(ids, p, None if greedy else q, acc.u_acc.numpy(),
+                                  acc.u_samp.numpy(), acc.seq_lens.numpy(),
+                                  nthreads=os.cpu_count() or 1)
+        bad = (want["flags"] & (2 | 16)) != 0
+        assert bad.sum() == 0
+        for k in KEYS:
+            assert (got[k].cpu().numpy() == want[k]).all(), (k, greedy)
+
+
 def test_bad_draft_id_sets_status():
     cfg = wl.config("tiny")
     acc = wl.make_accept_inputs(cfg, bs=4)

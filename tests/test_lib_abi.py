@@ -116,4 +116,9 @@ def test_workspace_plans(L):
     assert L.bdsa_block_attn_workspace_bytes(bs, B, Hq, Hkv, D, 4096, sms) == want
     # independent of the context length bound
     assert L.bdsa_block_attn_workspace_bytes(bs, B, Hq, Hkv, D, 131072, sms) == want
-    assert L.bdsa_spec_accept_workspace_bytes(32, 16, 151936, 152) > 32 * 594 * 8
+    # acceptance: no scratch while a row's segment totals fit one CTA's shared
+    # memory (V <= 2^21); beyond that, float-float totals per segment and more
+    assert L.bdsa_spec_accept_workspace_bytes(32, 16, 151936, 152) == 0
+    assert L.bdsa_spec_accept_workspace_bytes(32, 16, 1 << 21, 152) == 0
+    V = (1 << 21) + 1
+    assert L.bdsa_spec_accept_workspace_bytes(32, 16, V, 152) > 32 * ((V + 255) // 256) * 8

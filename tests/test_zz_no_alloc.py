@@ -69,7 +69,9 @@ def test_small_vocab_and_batch_reuse():
 
 def test_rejects_problems_larger_than_the_fixed_scratch():
     L = bdsa.lib()
-    bs, B, V = 4096, 16, 151936  # needs ~19 MB of scratch, the array holds 8 MiB
+    # vocabularies above 2^21 keep their segment totals in global scratch:
+    # 128 rows of 2^22 needs ~17 MB, the array holds 8 MiB
+    bs, B, V = 128, 16, 1 << 22
     assert L.bdsa_spec_accept_workspace_bytes(bs, B, V, 0) > (8 << 20)
     dummy = torch.zeros(16, dtype=torch.int32, device="cuda")
     st = L.bdsa_spec_accept_noalloc(_ptr(dummy), _ptr(dummy), 0, 0, _ptr(dummy), 0, 0,
