@@ -11,12 +11,13 @@ namespace bdsa {
 // ---------------------------------------------------------------- attention
 // Persistent stream-K style schedule: `grid` CTAs share the concatenated
 // (request, KV head, 128-key tile) sequence in equal contiguous ranges.  The
-// workspace holds the per-request tile prefix, a per-request "bad page" flag,
-// and two fp32 partial slots per CTA for units cut between CTAs.
+// workspace holds two partial slots per CTA for units cut between CTAs (a
+// bad-page flag, the fp32 log2-sum-exp per row and the fp32 normalised output
+// rows).
 struct AttnPlan {
     int grid;
     int rows;             // packed query rows per unit (G * B)
-    size_t off_prefix, off_bad, off_part_o, off_part_lse;
+    size_t off_part_bad, off_part_o, off_part_lse;
     size_t workspace;     // total bytes
 };
 

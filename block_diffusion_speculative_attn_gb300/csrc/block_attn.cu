@@ -7,17 +7,21 @@
 //   "Attention Mask", and used by the draft/verify passes of "From DFlash to
 //   dLLM Self-Spec (II)", sections 2.2.3-2.2.4 and "(IV)", section 4.4.1.
 //
-// One call = three launches chained with programmatic dependent launch:
-//   plan    one CTA: per-request tile counts -> prefix; validates every page id
-//           a request references and flags the request if one is out of range;
+// One call = two launches chained with programmatic dependent launch:
 //   attend  persistent, one CTA per SM.  Every (request, KV head) unit is a run
 //           of 128-key tiles; the runs are concatenated and each CTA takes an
 //           equal contiguous range (stream-K style), so the work is balanced to
-//           one tile.  A unit wholly inside one CTA is written directly; a unit
-//           cut between CTAs leaves an fp32 partial (o / l and log2-sum-exp) in
-//           one of each CTA's two slots;
-//   merge   one CTA per range boundary that cuts a unit: merges the unit's
-//           partials in tile order.
+//           one tile.  Each CTA derives the schedule itself: its threads read
+//           the context lengths, scan the per-request tile counts and locate
+//           the CTA's first unit, then every role walks the units in order.  A
+//           unit wholly inside one CTA is written directly; a unit cut between
+//           CTAs leaves an fp32 partial (o / l and log2-sum-exp) in one of each
+//           CTA's two slots.  The softmax warps check every page id a piece
+//           references; a unit that references one outside the pool is written
+//           as zeros (lse -inf) and reported;
+//   merge   one CTA per range boundary that is a unit's first cut: merges the
+//           unit's partials in tile order, from a descriptor of the cut that
+//           the attention CTA left.
 //
 // Inside a CTA (warp roles: 0-3 softmax + epilogue, 4 Q/K producer, 5 MMA
 // issuer + TMEM owner, 6 V producer):
@@ -100,19 +104,19 @@ struct Cfg {
     static constexpr int DR = OE + 2;     // drain
     static constexpr int kNumBars = DR + 1;
     static constexpr int kOffMisc = kOffBar + 8 * kNumBars;
-    static constexpr int kSmem = kOffMisc + 16 + 1024;  // + slack to align the base to 1 KB
+    static constexpr int kSmem = kOffMisc + 192 + 1024;  // + slack to align the base to 1 KB
 };
 
 struct Params {
     const int32_t *block_table;
     const int32_t *seq_lens;
-    const int32_t *prefix;   // [bs + 1] exclusive prefix of per-request tile counts
-    const int32_t *bad;      // [bs] request references a page id outside the pool
+    int32_t *part_bad;       // [2 * grid] partial slot saw a page id outside the pool
     uint16_t *out;
     float *lse;
     float *part_o;           // [2 * grid, rows, D]
     float *part_lse;         // [2 * grid, rows]
     int32_t *dev_status;
+    uint64_t magic_S;        // floor((2^64 - 1) / grid), see range_start
     int max_pages, num_pages, bs, B, Hq, Hkv, G, rows, page_size, log2_ps, box_rows, mode;
     float scale_log2;
 };
@@ -141,36 +145,160 @@ __device__ __forceinline__ void tmem_store_chunk(uint32_t taddr, const float (&v
     else tmem_st32(taddr, v);
 }
 
-// A maximal run of one unit's tiles inside a CTA's range.
-struct Piece {
-    int r, h, a, e, nt, L;
+// Tiles of a request with context length L (at least one, so that every
+// unit has an epilogue).
+__device__ __forceinline__ int tiles_of(long L, int B) {
+    const long nk = L + B;
+    return nk > 0 ? (int)min((nk + kBN - 1) / kBN, 1L << 24) : 1;
+}
+
+// Schedule.  Units (request, KV head) are concatenated in order; each unit is
+// kUnitCost "virtual" tiles followed by its real tiles, and CTA b takes the
+// cost range [b * Wc / S, (b + 1) * Wc / S).  The virtual tiles carry no work:
+// they charge every unit switch (a Q load, an epilogue, a ragged last tile)
+// about one tile of time, so a CTA that touches more units gets fewer tiles.
+// The real tiles inside a CTA's cost range form its range [x0, x1) of global
+// tile indices.
+constexpr int kUnitCost = 1;
+
+// Schedule state (shared memory).
+struct Sched {
+    uint32_t tmem;           // attention: TMEM base address (written by tcgen05.alloc)
+    int abort;               // attention: a bounded wait gave up
+    int r0, h0, nt0, L0;     // the unit holding the CTA's cost start (if below Wc)
+    long long u_off0;        // its first real tile
+    long long cu0;           // its cost offset
+    long long x0, x1, W, Wc;
+    long long wsum[8];       // per-warp partial sums of the scan (<= 256 threads)
+};
+
+// The unit a role is working through, walked in (request, KV head) order.
+struct Cursor {
+    int r, h, nt, L;
     long u_off;  // global index of the unit's first tile
 };
 
-__device__ __forceinline__ void locate(const int32_t *pre, int bs, int Hkv,
-                                       const int32_t *seq_lens, long x, long x1, Piece &pc) {
-    int lo = 0, hi = bs - 1;
-    while (lo < hi) {
-        const int mid = (lo + hi + 1) >> 1;
-        if ((long)Hkv * __ldg(pre + mid) <= x) lo = mid;
-        else hi = mid - 1;
-    }
-    const long base = (long)Hkv * __ldg(pre + lo);
-    pc.r = lo;
-    pc.nt = __ldg(pre + lo + 1) - __ldg(pre + lo);
-    const long y = x - base;
-    pc.h = (int)(y / pc.nt);
-    pc.a = (int)(y % pc.nt);
-    pc.e = (int)min((long)pc.nt, (long)pc.a + (x1 - x));
-    pc.L = __ldg(seq_lens + lo);
-    pc.u_off = base + (long)pc.h * pc.nt;
+// A maximal run of one unit's tiles inside a CTA's range.
+struct Piece {
+    int r, h, a, e, nt, L;
+    long u_off;
+};
+
+__device__ __forceinline__ Piece piece_at(const Cursor &c, long x, long x1) {
+    Piece pc;
+    pc.r = c.r;
+    pc.h = c.h;
+    pc.nt = c.nt;
+    pc.L = c.L;
+    pc.u_off = c.u_off;
+    pc.a = (int)(x - c.u_off);
+    pc.e = (int)min((long)c.nt, (long)pc.a + (x1 - x));
+    return pc;
 }
 
 // Start of CTA b's range and the CTA whose range holds global tile x.
-__device__ __forceinline__ long range_start(int b, long W, int S) { return (long)b * W / S; }
+// b * W / S without a 64-bit division (which the GPU emulates in software):
+// magic = floor((2^64 - 1) / S) comes from the host, and the multiply-high
+// quotient is at most one short for b * W < 2^63, which one step corrects.
+__device__ __forceinline__ long range_start(int b, long W, int S, uint64_t magic) {
+    if (b <= 0) return 0;
+    const uint64_t n = (uint64_t)b * (uint64_t)W;
+    uint64_t q = __umul64hi(n, magic);
+    if (n - q * (uint64_t)S >= (uint64_t)S) ++q;
+    return (long)q;
+}
+
+// Block-wide schedule of CTA b of S (NT threads): every thread sums the tile
+// counts of a contiguous block of requests, a scan gives each block's first
+// tile, and the threads whose blocks hold the CTA's cost bounds map them to
+// real tiles.  Two __syncthreads; results in *sch.
+template <int NT>
+__device__ void schedule(const Params &prm, int b, int S, Sched *sch) {
+    static_assert(NT % 32 == 0 && NT <= 256, "scan partials hold 8 warps");
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const int bs = prm.bs;
+    const int per = (bs + NT - 1) / NT;
+    const int i0 = min(bs, tid * per), i1 = min(bs, i0 + per);
+    long long sum = 0;
+    for (int i = i0; i < i1; ++i) sum += tiles_of(__ldg(prm.seq_lens + i), prm.B);
+    long long inc = sum;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+        const long long t = __shfl_up_sync(0xffffffffu, inc, o);
+        if (lane >= o) inc += t;
+    }
+    if (lane == 31) sch->wsum[warp] = inc;
+    __syncthreads();
+    long long wex = 0, T = 0;
+#pragma unroll
+    for (int w = 0; w < NT / 32; ++w) {
+        const long long v = sch->wsum[w];
+        if (w < warp) wex += v;
+        T += v;
+    }
+    const long long Hkv = prm.Hkv;
+    const long long W = Hkv * T, Wc = Hkv * (T + (long long)kUnitCost * bs);
+    const long long c0 = range_start(b, Wc, S, prm.magic_S);
+    const long long c1 = range_start(b + 1, Wc, S, prm.magic_S);
+    const long long pre = wex + inc - sum;  // tiles before request i0
+    // cost offset of request i: Hkv * (tiles before it + kUnitCost * i)
+    const long long clo = Hkv * (pre + (long long)kUnitCost * i0);
+    const long long chi = Hkv * (pre + sum + (long long)kUnitCost * i1);
+    for (int which = 0; which < 2; ++which) {
+        const long long c = which == 0 ? c0 : c1;
+        if (!(c < Wc && clo <= c && c < chi)) continue;
+        long long tp = pre;  // tiles before request i
+        for (int i = i0; i < i1; ++i) {
+            const int L = __ldg(prm.seq_lens + i);
+            const int nt = tiles_of(L, prm.B);
+            const long long ci = Hkv * (tp + (long long)kUnitCost * i);
+            const long long span = nt + kUnitCost;  // cost of one unit of request i
+            if (c < ci + Hkv * span) {
+                const int h = (int)((c - ci) / span);
+                const long long pos = (c - ci) - h * span;
+                const long long u_off = Hkv * tp + (long long)h * nt;
+                const long long x = u_off + max(0LL, pos - kUnitCost);
+                if (which == 0) {
+                    sch->r0 = i;
+                    sch->h0 = h;
+                    sch->nt0 = nt;
+                    sch->L0 = L;
+                    sch->u_off0 = u_off;
+                    sch->cu0 = ci + (long long)h * span;
+                    sch->x0 = x;
+                } else {
+                    sch->x1 = x;
+                }
+                break;
+            }
+            tp += nt;
+        }
+    }
+    if (tid == 0) {
+        if (c0 >= Wc) sch->x0 = W;
+        if (c1 >= Wc) sch->x1 = W;
+        sch->W = W;
+        sch->Wc = Wc;
+    }
+    __syncthreads();
+}
+
+// Move the cursor past a finished unit.
+__device__ __forceinline__ void next_unit(Cursor &c, const Params &prm) {
+    c.u_off += c.nt;
+    if (++c.h == prm.Hkv) {
+        c.h = 0;
+        if (++c.r < prm.bs) {
+            c.L = __ldg(prm.seq_lens + c.r);
+            c.nt = tiles_of(c.L, prm.B);
+        }
+    }
+}
 __device__ __forceinline__ int cta_of(long x, long W, int S) {
     return (int)(((x + 1) * (long)S - 1) / W);
 }
+
+constexpr int kMaxBoxes = kBN / 8;  // page_size >= 8
 
 // Number of TMA boxes of tile t0 that hold keys of the request (never past its
 // block-table row).
@@ -197,11 +325,11 @@ __global__ void __launch_bounds__(kThreads, 1)
     const long ps = prm.page_size;
 
     auto bar = [&](int i) -> uint32_t { return sbase + C::kOffBar + 8u * (uint32_t)i; };
-    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + C::kOffMisc);
-    volatile int *abort_flag = reinterpret_cast<volatile int *>(smem + C::kOffMisc + 4);
+    Sched *sch = reinterpret_cast<Sched *>(smem + C::kOffMisc);
+    uint32_t *tmem_slot = &sch->tmem;
+    volatile int *abort_flag = &sch->abort;
 
-    // ---- prologue (overlaps the plan kernel under programmatic dependent launch)
-    grid_launch_dependents();
+    // ---- prologue (overlaps the previous kernel under programmatic dependent launch)
     if (warp == kMmaWarp) {
         tmem_alloc(smem_u32(tmem_slot), kTmemCols);
         tmem_relinquish();
@@ -253,15 +381,32 @@ __global__ void __launch_bounds__(kThreads, 1)
     tc_fence_after();
     const uint32_t tmem = *tmem_slot;
 
-    // ---- the plan kernel's outputs are needed from here on
+    // ---- inputs written by earlier kernels on the stream are read from here on
     grid_dependency_wait();
-    // Warm L1 with the tile prefix: every role's first binary search reads it.
-    for (int i = tid * 32; i <= prm.bs; i += kThreads * 32)
-        asm volatile("prefetch.global.L1 [%0];" ::"l"(prm.prefix + i));
+    // The merge kernel may start now: its schedule reads only this call's inputs.
+    grid_launch_dependents();
     const int S = gridDim.x;
     const int b = blockIdx.x;
-    const long W = (long)prm.Hkv * __ldg(prm.prefix + prm.bs);
-    const long x0 = range_start(b, W, S), x1 = range_start(b + 1, W, S);
+    if (warp == kKProducerWarp) {
+        // Warm L2 with the block-table rows this CTA most likely starts in
+        // (exact when the requests are of similar length), so the first page
+        // lookups overlap the schedule's context-length reads.
+        const long guess = (long)b * prm.bs / S;
+        const long r = guess - 1 + lane / 8;
+        const long e = (long)(lane % 8) * 32;  // 32 entries = one 128-byte line
+        if (lane < 24 && r >= 0 && r < prm.bs && e < prm.max_pages)
+            asm volatile("prefetch.global.L2 [%0];" ::"l"(prm.block_table + r * prm.max_pages + e));
+    }
+    schedule<kThreads>(prm, b, S, sch);
+    const long x0 = sch->x0, x1 = sch->x1;
+    Cursor cur0;
+    if (x0 < x1) {
+        cur0.r = sch->r0;
+        cur0.h = sch->h0;
+        cur0.nt = sch->nt0;
+        cur0.L = sch->L0;
+        cur0.u_off = sch->u_off0;
+    }
 
     if (warp == kKProducerWarp || warp == kVProducerWarp) {
         // ------------------------------------------------ TMA producers
@@ -277,9 +422,9 @@ __global__ void __launch_bounds__(kThreads, 1)
             long g = 0, issued = 0, q_issued = 0;
             int k = 0;
             bool ok = true;
+            Cursor cur = cur0;
             for (long x = x0; ok && x < x1; ++k) {
-                Piece pc;
-                locate(prm.prefix, prm.bs, prm.Hkv, prm.seq_lens, x, x1, pc);
+                const Piece pc = piece_at(cur, x, x1);
                 if (is_k) {
                     const int qb = k % C::NQ;
                     if (k >= C::NQ) {
@@ -298,25 +443,34 @@ __global__ void __launch_bounds__(kThreads, 1)
                 for (int j = pc.a; j < pc.e; ++j, ++g) {
                     const long t0 = (long)j * kBN;
                     const int nbox = boxes_of(n_keys, t0, rows_box, prm.log2_ps, prm.max_pages);
+                    // look the pages up before waiting for the stage
+                    int32_t slot[kMaxBoxes];
+#pragma unroll
+                    for (int bx = 0; bx < kMaxBoxes; ++bx) {
+                        const long t = t0 + (long)bx * rows_box;
+                        if (bx < nbox)
+                            slot[bx] =
+                                bt[t >> prm.log2_ps] * prm.page_size + (int32_t)(t & (ps - 1));
+                    }
                     const int st = (int)(g % NR);
                     ok = mbar_wait(bar(EMPTY + st), (uint32_t)(((g / NR) & 1) ^ 1), abort_flag,
                                    prm.dev_status);
                     if (!ok) break;
                     mbar_arrive_expect_tx(bar(FULL + st),
                                           (uint32_t)(nbox * rows_box * 128 * C::DH));
-                    for (int bx = 0; bx < nbox; ++bx) {
-                        const long t = t0 + (long)bx * rows_box;
-                        const int32_t slot =
-                            bt[t >> prm.log2_ps] * prm.page_size + (int32_t)(t & (ps - 1));
+#pragma unroll
+                    for (int bx = 0; bx < kMaxBoxes; ++bx) {
+                        if (bx >= nbox) break;
                         for (int c = 0; c < C::DH; ++c)
                             tma_load_2d_hint(dst0 + st * C::kStage + c * C::kKVSlab +
                                                  bx * rows_box * 128,
-                                             tmap, pc.h * D + c * 64, slot, bar(FULL + st),
+                                             tmap, pc.h * D + c * 64, slot[bx], bar(FULL + st),
                                              policy);
                     }
                     issued = g + 1;
                 }
                 x += pc.e - pc.a;
+                if (pc.e == pc.nt) next_unit(cur, prm);
             }
             // Drain: the last load issued into each buffer must have landed before exit.
             for (long i = max(0L, q_issued - C::NQ); i < q_issued; ++i)
@@ -370,9 +524,9 @@ __global__ void __launch_bounds__(kThreads, 1)
             long g = 0;
             int k = 0;
             bool ok = true;
+            Cursor cur = cur0;
             for (long x = x0; ok && x < x1; ++k) {
-                Piece pc;
-                locate(prm.prefix, prm.bs, prm.Hkv, prm.seq_lens, x, x1, pc);
+                const Piece pc = piece_at(cur, x, x1);
                 if (have) {
                     ok = issue_pv(pend);
                     have = false;
@@ -412,6 +566,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                     have = true;
                 }
                 x += n;
+                if (pc.e == pc.nt) next_unit(cur, prm);
             }
             if (ok && have) ok = issue_pv(pend);
             // Drain: every MMA issued above has completed before TMEM is released.
@@ -431,14 +586,82 @@ __global__ void __launch_bounds__(kThreads, 1)
         const float sl2 = prm.scale_log2;
         const bool valid_row = row < prm.rows;
         const int i_blk = row / G;
+        // A piece's output: O from TMEM scaled by 1/l, to `out` (bf16) when the
+        // piece is the whole unit, else to the CTA's partial slot (fp32).
+        struct Epi {
+            long lastg, orow;
+            float inv_l, lse2;
+            int ob, slot;
+            bool complete, bad;
+        };
+        auto epilogue = [&](const Epi &e) -> bool {
+            bool okw = mbar_wait(bar(C::PV + (int)(e.lastg % C::NP)),
+                                 (uint32_t)((e.lastg / C::NP) & 1), abort_flag, prm.dev_status);
+            okw = __all_sync(0xffffffffu, okw);
+            if (!okw) return false;
+            tc_fence_after();
+#pragma unroll
+            for (int c = 0; c < OC / 32; ++c) {
+                float ov[32];
+                tmem_load_chunk<M, D / 2>(tmem + lane_base + kTmemO + e.ob * 128 + c * 32, ov);
+                tmem_wait_ld();
+                if (!valid_row) continue;
+                const int col0 = half * OC + c * 32;
+                if (e.complete && e.bad) {
+                    uint4 *dst = reinterpret_cast<uint4 *>(prm.out + e.orow * D + col0);
+#pragma unroll
+                    for (int v = 0; v < 4; ++v) dst[v] = make_uint4(0, 0, 0, 0);
+                } else if (e.complete) {
+                    uint4 *dst = reinterpret_cast<uint4 *>(prm.out + e.orow * D + col0);
+#pragma unroll
+                    for (int v = 0; v < 4; ++v) {
+                        uint4 w;
+                        w.x = pack_bf16x2(ov[8 * v + 0] * e.inv_l, ov[8 * v + 1] * e.inv_l);
+                        w.y = pack_bf16x2(ov[8 * v + 2] * e.inv_l, ov[8 * v + 3] * e.inv_l);
+                        w.z = pack_bf16x2(ov[8 * v + 4] * e.inv_l, ov[8 * v + 5] * e.inv_l);
+                        w.w = pack_bf16x2(ov[8 * v + 6] * e.inv_l, ov[8 * v + 7] * e.inv_l);
+                        dst[v] = w;
+                    }
+                } else {
+                    float4 *dst = reinterpret_cast<float4 *>(
+                        prm.part_o + ((long)e.slot * prm.rows + row) * D + col0);
+#pragma unroll
+                    for (int v = 0; v < 8; ++v)
+                        dst[v] = make_float4(ov[4 * v] * e.inv_l, ov[4 * v + 1] * e.inv_l,
+                                             ov[4 * v + 2] * e.inv_l, ov[4 * v + 3] * e.inv_l);
+                }
+            }
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(bar(C::OE + e.ob));
+            if (valid_row && half == 0) {
+                if (e.complete && e.bad) {
+                    if (prm.lse) prm.lse[e.orow] = -INFINITY;
+                } else if (e.complete) {
+                    if (prm.lse) prm.lse[e.orow] = e.lse2 * kLn2;
+                } else {
+                    prm.part_lse[(long)e.slot * prm.rows + row] = e.lse2;
+                }
+            }
+            if (!e.complete && tid == 0) prm.part_bad[e.slot] = e.bad ? 1 : 0;
+            return true;
+        };
         long g = 0;
         int k = 0;
         bool ok = true;
+        Cursor cur = cur0;
         for (long x = x0; ok && x < x1; ++k) {
-            Piece pc;
-            locate(prm.prefix, prm.bs, prm.Hkv, prm.seq_lens, x, x1, pc);
-            const int bad = __ldg(prm.bad + pc.r);  // used only in the epilogue
+            const Piece pc = piece_at(cur, x, x1);
             const long n_keys = (long)pc.L + B;
+            // Page ids this piece references: a context that needs more pages
+            // than the block-table row holds, or an id outside the pool, makes
+            // the unit's output zeros.  Each tile's ids are loaded during the
+            // tile and checked during the next one (or the epilogue).
+            const bool shape_bad =
+                pc.L < 0 || (n_keys + ps - 1) / ps > (long)prm.max_pages;
+            const int32_t *bt_row = prm.block_table + (long)pc.r * prm.max_pages;
+            bool page_bad = false, pend = false;
+            int32_t pend_pg = 0;
             const long limit =
                 (prm.mode == BDSA_MODE_DRAFT) ? n_keys : min(n_keys, (long)pc.L + i_blk + 1);
             const int ob = k & 1;
@@ -447,6 +670,13 @@ __global__ void __launch_bounds__(kThreads, 1)
             for (int j = pc.a; j < pc.e; ++j, ++g) {
                 const long t0 = (long)j * kBN;
                 const int sb = (int)(g & 1);
+                if (pend) page_bad |= pend_pg < 0 || pend_pg >= prm.num_pages;
+                {
+                    const long kend = min(t0 + kBN, n_keys);
+                    const long p0 = t0 >> prm.log2_ps;
+                    pend = !shape_bad && kend > t0 && p0 + lane <= ((kend - 1) >> prm.log2_ps);
+                    if (pend) pend_pg = __ldg(bt_row + p0 + lane);
+                }
                 ok = mbar_wait(bar(C::SF + sb), (uint32_t)((g >> 1) & 1), abort_flag,
                                prm.dev_status);
                 ok = __all_sync(0xffffffffu, ok);
@@ -566,67 +796,27 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
             if (!ok) break;
 
-            // ---- epilogue of the piece
+            // ---- end of the piece
             {
-                const long lastg = g - 1;
-                ok = mbar_wait(bar(C::PV + (int)(lastg % C::NP)), (uint32_t)((lastg / C::NP) & 1),
-                               abort_flag, prm.dev_status);
-                ok = __all_sync(0xffffffffu, ok);
+                float l = (l4[0] + l4[1]) + (l4[2] + l4[3]);
+                if constexpr (M == 64) l += __shfl_xor_sync(0xffffffffu, l, 16);
+                if (pend) page_bad |= pend_pg < 0 || pend_pg >= prm.num_pages;
+                Epi e;
+                e.lastg = g - 1;
+                e.ob = ob;
+                e.inv_l = l > 0.f ? 1.f / l : 0.f;
+                e.lse2 = l > 0.f ? m_used + log2f(l) : -INFINITY;
+                e.complete = pc.a == 0 && pc.e == pc.nt;
+                // every warp checked every page of the piece
+                e.bad = shape_bad || __any_sync(0xffffffffu, page_bad);
+                e.orow = ((long)pc.r * B + i_blk) * prm.Hq + (long)pc.h * G + row % G;
+                e.slot = 2 * b + (k == 0 ? 0 : 1);
+                if (e.bad && tid == 0) report_status(prm.dev_status, BDSA_DEVICE_OUT_OF_RANGE);
+                ok = epilogue(e);
                 if (!ok) break;
             }
-            tc_fence_after();
-            float l = (l4[0] + l4[1]) + (l4[2] + l4[3]);
-            if constexpr (M == 64) l += __shfl_xor_sync(0xffffffffu, l, 16);
-            const float inv_l = l > 0.f ? 1.f / l : 0.f;
-            const float lse2 = l > 0.f ? m_used + log2f(l) : -INFINITY;
-            const bool complete = (pc.a == 0 && pc.e == pc.nt);
-            const long token = (long)pc.r * B + i_blk;
-            const long orow = token * prm.Hq + (long)pc.h * G + row % G;
-            const int slot = 2 * b + (k == 0 ? 0 : 1);
-#pragma unroll
-            for (int c = 0; c < OC / 32; ++c) {
-                float ov[32];
-                tmem_load_chunk<M, D / 2>(tmem + lane_base + kTmemO + ob * 128 + c * 32, ov);
-                tmem_wait_ld();
-                if (!valid_row) continue;
-                const int col0 = half * OC + c * 32;
-                if (bad) {
-                    uint4 *dst = reinterpret_cast<uint4 *>(prm.out + orow * D + col0);
-#pragma unroll
-                    for (int v = 0; v < 4; ++v) dst[v] = make_uint4(0, 0, 0, 0);
-                } else if (complete) {
-                    uint4 *dst = reinterpret_cast<uint4 *>(prm.out + orow * D + col0);
-#pragma unroll
-                    for (int v = 0; v < 4; ++v) {
-                        uint4 w;
-                        w.x = pack_bf16x2(ov[8 * v + 0] * inv_l, ov[8 * v + 1] * inv_l);
-                        w.y = pack_bf16x2(ov[8 * v + 2] * inv_l, ov[8 * v + 3] * inv_l);
-                        w.z = pack_bf16x2(ov[8 * v + 4] * inv_l, ov[8 * v + 5] * inv_l);
-                        w.w = pack_bf16x2(ov[8 * v + 6] * inv_l, ov[8 * v + 7] * inv_l);
-                        dst[v] = w;
-                    }
-                } else {
-                    float4 *dst = reinterpret_cast<float4 *>(
-                        prm.part_o + ((long)slot * prm.rows + row) * D + col0);
-#pragma unroll
-                    for (int v = 0; v < 8; ++v)
-                        dst[v] = make_float4(ov[4 * v] * inv_l, ov[4 * v + 1] * inv_l,
-                                             ov[4 * v + 2] * inv_l, ov[4 * v + 3] * inv_l);
-                }
-            }
-            tc_fence_before();
-            __syncwarp();
-            if (lane == 0) mbar_arrive(bar(C::OE + ob));
-            if (valid_row && half == 0) {
-                if (bad) {
-                    if (prm.lse) prm.lse[orow] = -INFINITY;
-                } else if (complete) {
-                    if (prm.lse) prm.lse[orow] = lse2 * kLn2;
-                } else {
-                    prm.part_lse[(long)slot * prm.rows + row] = lse2;
-                }
-            }
             x += pc.e - pc.a;
+            if (pc.e == pc.nt) next_unit(cur, prm);
         }
     }
 
@@ -639,184 +829,114 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
 }
 
-// Merge the partials of every unit cut between CTAs.  Blocks (b, sub): b picks
-// the unit whose first interior cut is the start of CTA b's range; the unit's
-// (row, 4-column) items are spread over kMergeSub blocks of 256 threads, one
-// item per thread, with the pieces' loads issued kMB at a time.
-constexpr int kMergeSub = 8;
+// Merge the partials of every unit cut between CTAs.  Block b handles the
+// unit whose first interior cut is the start of attention CTA b's range: it
+// derives that unit and the slots of its pieces from the context lengths (the
+// same schedule as the attention kernel, computed while the attention runs),
+// waits for the attention grid, then merges the pieces in tile order.  Four
+// threads share a row, their 16-byte columns interleaved so each warp load
+// reads whole 32-byte sectors, and walk the pieces with all of a piece's
+// loads in flight.  A unit any of whose pieces saw a page id outside the pool
+// is written as zeros (lse -inf).
 constexpr int kMergeThreads = 256;
+constexpr int kMergeTPR = 4;      // threads per row
+constexpr int kMergeSlots = 32;   // piece slots listed in shared memory
 
 template <int D>
-__global__ void __launch_bounds__(kMergeThreads) attn_merge_kernel(const Params prm, int S) {
-    grid_dependency_wait();
-    const int b = blockIdx.x;
-    const long W = (long)prm.Hkv * __ldg(prm.prefix + prm.bs);
-    if (b == 0 || W == 0) return;
-    const long x = range_start(b, W, S);
-    if (x >= W) return;
-    Piece pc;
-    locate(prm.prefix, prm.bs, prm.Hkv, prm.seq_lens, x, W, pc);
-    // split at this cut, and no earlier cut lies inside the unit
-    if (!(pc.u_off < x && range_start(b - 1, W, S) <= pc.u_off)) return;
-    if (__ldg(prm.bad + pc.r)) return;
-    const int b_first = cta_of(pc.u_off, W, S);
-    const int b_last = cta_of(pc.u_off + pc.nt - 1, W, S);
+__global__ void __launch_bounds__(kMergeThreads) attn_merge_kernel(const Params prm) {
+    __shared__ Sched sch;
+    __shared__ int s_slot[kMergeSlots];
+    __shared__ int s_np;
+    const int b = blockIdx.x, S = gridDim.x;
+    schedule<kMergeThreads>(prm, b, S, &sch);
+    const long W = sch.W, Wc = sch.Wc, x0 = sch.x0;
+    if (x0 >= W) return;
+    const long u_off = sch.u_off0, cu = sch.cu0;
+    // the cut at this CTA's start splits the unit's tiles, and CTA b - 1 holds
+    // the unit's first tile (so this is the unit's first cut)
+    if (!(u_off < x0 && range_start(b - 1, Wc, S, prm.magic_S) <= cu + kUnitCost)) return;
+    const int r = sch.r0, h = sch.h0;
+    const int b_first = cta_of(cu + kUnitCost, Wc, S);
+    const int b_last = cta_of(cu + kUnitCost + sch.nt0 - 1, Wc, S);
+    // Partial slots of the unit's pieces, in tile order.  Every CTA from
+    // b_first to b_last with a non-empty cost range holds one; it is that
+    // CTA's first piece (slot 2bb) unless tiles of an earlier unit precede it
+    // in the range (2bb + 1).
+    if (threadIdx.x == 0) {
+        int n = 0;
+        for (int bb = b_first; bb <= b_last && n < kMergeSlots; ++bb) {
+            const long cb = range_start(bb, Wc, S, prm.magic_S);
+            if (cb < range_start(bb + 1, Wc, S, prm.magic_S))
+                s_slot[n++] = 2 * bb + (cb >= cu ? 0 : 1);
+        }
+        s_np = n;
+    }
+    __syncthreads();
+    const int np = s_np;
+    grid_dependency_wait();  // the attention grid's partials
     constexpr int C4 = D / 4;
-    const int items = prm.rows * C4;
-    constexpr int kMB = 8;  // pieces whose loads are in flight together
-    for (int it = blockIdx.y * kMergeThreads + threadIdx.x; it < items;
-         it += kMergeSub * kMergeThreads) {
-        const int row = it / C4, c4 = it % C4;
-        // running max / sum of the pieces' log2-sum-exp for this row
+    constexpr int F4 = C4 / kMergeTPR;  // 16-byte columns per thread
+    const int items = prm.rows * kMergeTPR;
+    for (int it = threadIdx.x; it < items; it += kMergeThreads) {
+        const int row = it / kMergeTPR, sub = it % kMergeTPR;
         float mmax = -INFINITY, den = 0.f;
-        float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-        for (int b0 = b_first; b0 <= b_last; b0 += kMB) {
-            float ls[kMB];
-            float4 po[kMB];
+        float4 acc[F4];
 #pragma unroll
-            for (int q = 0; q < kMB; ++q) {
-                const int bb = b0 + q;
-                const long fb = range_start(bb, W, S);
-                const bool live = bb <= b_last && fb < range_start(bb + 1, W, S);
-                const int sl = 2 * bb + (fb >= pc.u_off ? 0 : 1);
-                ls[q] = live ? __ldcg(prm.part_lse + (long)sl * prm.rows + row) : -INFINITY;
-                po[q] = live ? __ldcg(reinterpret_cast<const float4 *>(
-                                   prm.part_o + ((long)sl * prm.rows + row) * D) + c4)
-                             : make_float4(0.f, 0.f, 0.f, 0.f);
+        for (int v = 0; v < F4; ++v) acc[v] = make_float4(0.f, 0.f, 0.f, 0.f);
+        bool bad = false;
+        // pieces past the listed ones (only when a unit spans more than
+        // kMergeSlots CTAs) are enumerated on the fly, after the last listed CTA
+        int bb_next = np > 0 ? s_slot[np - 1] / 2 + 1 : b_first;
+        for (int q = 0;; ++q) {
+            int sl;
+            if (q < np) {
+                sl = s_slot[q];
+            } else {
+                if (np < kMergeSlots) break;
+                while (bb_next <= b_last && range_start(bb_next, Wc, S, prm.magic_S) >=
+                                               range_start(bb_next + 1, Wc, S, prm.magic_S))
+                    ++bb_next;
+                if (bb_next > b_last) break;
+                const long cb = range_start(bb_next, Wc, S, prm.magic_S);
+                sl = 2 * bb_next + (cb >= cu ? 0 : 1);
+                ++bb_next;
             }
-            float bm = mmax;
+            const float4 *src =
+                reinterpret_cast<const float4 *>(prm.part_o + ((long)sl * prm.rows + row) * D);
+            float4 po[F4];
 #pragma unroll
-            for (int q = 0; q < kMB; ++q) bm = fmaxf(bm, ls[q]);
-            if (bm == -INFINITY) continue;
-            const float sc = (mmax == -INFINITY) ? 0.f : exp2f(mmax - bm);
-            den *= sc;
-            acc.x *= sc;
-            acc.y *= sc;
-            acc.z *= sc;
-            acc.w *= sc;
+            for (int v = 0; v < F4; ++v) po[v] = __ldcg(src + sub + kMergeTPR * v);
+            const float ls = __ldcg(prm.part_lse + (long)sl * prm.rows + row);
+            bad = bad || __ldcg(prm.part_bad + sl) != 0;
+            if (ls == -INFINITY) continue;  // no key of this piece is visible to the row
+            const float m_new = fmaxf(mmax, ls);
+            const float sc = (mmax == -INFINITY) ? 0.f : exp2f(mmax - m_new);
+            const float w = exp2f(ls - m_new);
+            den = den * sc + w;
 #pragma unroll
-            for (int q = 0; q < kMB; ++q) {
-                if (ls[q] == -INFINITY) continue;
-                const float w = exp2f(ls[q] - bm);
-                den += w;
-                acc.x += w * po[q].x;
-                acc.y += w * po[q].y;
-                acc.z += w * po[q].z;
-                acc.w += w * po[q].w;
+            for (int v = 0; v < F4; ++v) {
+                acc[v].x = acc[v].x * sc + w * po[v].x;
+                acc[v].y = acc[v].y * sc + w * po[v].y;
+                acc[v].z = acc[v].z * sc + w * po[v].z;
+                acc[v].w = acc[v].w * sc + w * po[v].w;
             }
-            mmax = bm;
+            mmax = m_new;
         }
-        const float inv = den > 0.f ? 1.f / den : 0.f;
-        const long orow =
-            ((long)pc.r * prm.B + row / prm.G) * prm.Hq + (long)pc.h * prm.G + row % prm.G;
-        uint2 w;
-        w.x = pack_bf16x2(acc.x * inv, acc.y * inv);
-        w.y = pack_bf16x2(acc.z * inv, acc.w * inv);
-        *reinterpret_cast<uint2 *>(prm.out + orow * D + c4 * 4) = w;
-        if (c4 == 0 && prm.lse) prm.lse[orow] = den > 0.f ? (mmax + log2f(den)) * kLn2 : -INFINITY;
+        const bool ok = den > 0.f && !bad;
+        const float inv = ok ? 1.f / den : 0.f;
+        const long orow = ((long)r * prm.B + row / prm.G) * prm.Hq + (long)h * prm.G + row % prm.G;
+        uint2 *dst = reinterpret_cast<uint2 *>(prm.out + orow * D);
+#pragma unroll
+        for (int v = 0; v < F4; ++v) {
+            uint2 w2 = make_uint2(0u, 0u);  // a bad unit's partials may hold anything
+            if (ok) {
+                w2.x = pack_bf16x2(acc[v].x * inv, acc[v].y * inv);
+                w2.y = pack_bf16x2(acc[v].z * inv, acc[v].w * inv);
+            }
+            dst[sub + kMergeTPR * v] = w2;
+        }
+        if (sub == 0 && prm.lse) prm.lse[orow] = ok ? (mmax + log2f(den)) * kLn2 : -INFINITY;
     }
-}
-
-// Per-request tile counts -> exclusive prefix; per-request page-id validation.
-// One CTA of 1024 threads.
-constexpr int kPlanChunk = 2048;  // requests validated per pass (page prefix in shared memory)
-
-__global__ void __launch_bounds__(1024)
-    attn_plan_kernel(const int32_t *__restrict__ seq_lens, const int32_t *__restrict__ block_table,
-                     int bs, int B, int max_pages, int num_pages, int page_size,
-                     int32_t *__restrict__ prefix, int32_t *__restrict__ bad,
-                     int32_t *dev_status) {
-    grid_launch_dependents();
-    __shared__ int warp_tot[32];
-    __shared__ int carry;
-    __shared__ int page_pre[kPlanChunk + 1];
-    __shared__ int any_bad;
-    const int tid = threadIdx.x, lane = tid & 31, wid = tid >> 5;
-    if (tid == 0) {
-        carry = 0;
-        any_bad = 0;
-    }
-    __syncthreads();
-    for (int base = 0; base < bs; base += 1024) {
-        const int i = base + tid;
-        int nt = 0;
-        if (i < bs) {
-            const long nk = (long)seq_lens[i] + B;
-            nt = nk > 0 ? (int)min((nk + kBN - 1) / kBN, 1L << 24) : 1;
-        }
-        int inc = nt;
-#pragma unroll
-        for (int o = 1; o < 32; o <<= 1) {
-            const int t = __shfl_up_sync(0xffffffffu, inc, o);
-            if (lane >= o) inc += t;
-        }
-        if (lane == 31) warp_tot[wid] = inc;
-        __syncthreads();
-        if (wid == 0) {
-            const int v = warp_tot[lane];
-            int vi = v;
-#pragma unroll
-            for (int o = 1; o < 32; o <<= 1) {
-                const int t = __shfl_up_sync(0xffffffffu, vi, o);
-                if (lane >= o) vi += t;
-            }
-            warp_tot[lane] = vi - v;  // exclusive prefix of warp totals
-        }
-        __syncthreads();
-        const int excl = carry + warp_tot[wid] + inc - nt;
-        if (i < bs) prefix[i] = excl;
-        __syncthreads();
-        if (tid == 1023) carry = excl + nt;
-        __syncthreads();
-    }
-    if (tid == 0) prefix[bs] = carry;
-
-    // Validation: the pages each request references, flattened over a chunk of
-    // requests and split evenly over the threads so the loads are in flight
-    // together.
-    for (int base = 0; base < bs; base += kPlanChunk) {
-        const int n = min(kPlanChunk, bs - base);
-        __syncthreads();
-        if (tid == 0) {
-            int acc = 0;
-            for (int q = 0; q < n; ++q) {
-                const int r = base + q;
-                const long L = seq_lens[r];
-                const long need = (L + B + page_size - 1) / page_size;
-                const bool shape_bad = L < 0 || need > max_pages;
-                page_pre[q] = acc;
-                bad[r] = shape_bad ? 1 : 0;
-                if (shape_bad) any_bad = 1;
-                else acc += (int)need;
-            }
-            page_pre[n] = acc;
-        }
-        __syncthreads();
-        const int total = page_pre[n];
-        const int per = (total + 1023) / 1024;
-        const int p0 = min(total, tid * per), p1 = min(total, p0 + per);
-        int q = 0;
-        {
-            int lo = 0, hi = n - 1;  // request holding flattened page p0
-            while (lo < hi) {
-                const int mid = (lo + hi + 1) >> 1;
-                if (page_pre[mid] <= p0) lo = mid;
-                else hi = mid - 1;
-            }
-            q = lo;
-        }
-        for (int p = p0; p < p1; ++p) {
-            while (q < n - 1 && page_pre[q + 1] <= p) ++q;
-            const int r = base + q;
-            const int32_t pg = __ldg(block_table + (long)r * max_pages + (p - page_pre[q]));
-            if (pg < 0 || pg >= num_pages) {
-                bad[r] = 1;
-                any_bad = 1;
-            }
-        }
-    }
-    __syncthreads();
-    if (tid == 0 && any_bad) report_status(dev_status, BDSA_DEVICE_OUT_OF_RANGE);
 }
 
 // ------------------------------------------------------------------ host side
@@ -896,8 +1016,7 @@ int launch_impl(const AttnArgs &a, const AttnPlan &plan, cudaStream_t stream) {
     Params prm;
     prm.block_table = a.block_table;
     prm.seq_lens = a.seq_lens;
-    prm.prefix = reinterpret_cast<const int32_t *>(ws + plan.off_prefix);
-    prm.bad = reinterpret_cast<const int32_t *>(ws + plan.off_bad);
+    prm.part_bad = reinterpret_cast<int32_t *>(ws + plan.off_part_bad);
     prm.out = a.out;
     prm.lse = a.lse;
     prm.part_o = reinterpret_cast<float *>(ws + plan.off_part_o);
@@ -918,6 +1037,7 @@ int launch_impl(const AttnArgs &a, const AttnPlan &plan, cudaStream_t stream) {
     prm.box_rows = box_rows;
     prm.mode = a.mode;
     prm.scale_log2 = a.scale * 1.4426950408889634f;
+    prm.magic_S = UINT64_MAX / (uint64_t)plan.grid;
     static bool attr_set = false;  // per (D, M) instantiation
     if (!attr_set) {
         if (cudaFuncSetAttribute(block_attn_kernel<D, M>,
@@ -926,16 +1046,11 @@ int launch_impl(const AttnArgs &a, const AttnPlan &plan, cudaStream_t stream) {
             return BDSA_CUDA_ERROR;
         attr_set = true;
     }
-    attn_plan_kernel<<<1, 1024, 0, stream>>>(
-        a.seq_lens, a.block_table, a.bs, a.B, a.max_pages, a.num_pages, a.page_size,
-        reinterpret_cast<int32_t *>(ws + plan.off_prefix),
-        reinterpret_cast<int32_t *>(ws + plan.off_bad), a.dev_status);
-    if (cudaGetLastError() != cudaSuccess) return BDSA_CUDA_ERROR;
     if (launch_pdl(block_attn_kernel<D, M>, dim3(plan.grid), dim3(kThreads), C::kSmem, stream,
                    tq, tk, tv, prm) != cudaSuccess)
         return BDSA_CUDA_ERROR;
-    if (launch_pdl(attn_merge_kernel<D>, dim3(plan.grid, kMergeSub), dim3(kMergeThreads), 0,
-                   stream, prm, plan.grid) != cudaSuccess)
+    if (launch_pdl(attn_merge_kernel<D>, dim3(plan.grid), dim3(kMergeThreads), 0, stream,
+                   prm) != cudaSuccess)
         return BDSA_CUDA_ERROR;
     return BDSA_OK;
 }
@@ -950,10 +1065,9 @@ AttnPlan attn_plan(int bs, int B, int Hq, int Hkv, int D, int max_ctx_len, int n
     p.grid = num_sms > 0 ? num_sms : 1;
     p.rows = (Hq / Hkv) * B;
     size_t off = 0;
-    p.off_prefix = off;
-    off += align256((size_t)(bs + 1) * sizeof(int32_t));
-    p.off_bad = off;
-    off += align256((size_t)bs * sizeof(int32_t));
+    (void)bs;
+    p.off_part_bad = off;
+    off += align256((size_t)2 * p.grid * sizeof(int32_t));
     p.off_part_lse = off;
     off += align256((size_t)2 * p.grid * p.rows * sizeof(float));
     p.off_part_o = off;

@@ -117,21 +117,25 @@ int32_t bdsa_prepare_block(const int32_t *verified_id, const int32_t *seq_lens,
  *          length); checked to be >= 0.  The device-side schedule below reads
  *          the actual seq_lens and does not depend on it.
  * num_sms  number of persistent CTAs (0: the current device's SM count).
- * Schedule: a one-CTA plan kernel turns seq_lens into a tile prefix, then one
- * persistent CTA per SM takes an equal share of the concatenated (request, KV
- * head, 128-key tile) sequence; a unit cut between CTAs is merged by the last
- * CTA to finish it (arrival counter in the workspace; no CTA waits for
- * another).  Two launches per call.
+ * Schedule: one persistent CTA per SM takes an equal share of the concatenated
+ * (request, KV head, 128-key tile) sequence, which each CTA derives from
+ * seq_lens itself; a (request, KV head) unit cut between CTAs leaves partials
+ * that a second kernel merges.  Two launches per call, chained with
+ * programmatic dependent launch (no CTA waits for another).
+ * Pages: a request with L_r < 0, with L_r + B needing more pages than
+ * max_pages_per_req, or with a page id it references (pages 0 ..
+ * ceil((L_r+B)/ps) - 1 of its row) outside [0, num_pages) gets out = 0 and
+ * lse = -inf on all its rows, and dev_status = BDSA_DEVICE_OUT_OF_RANGE.
  * softmax_scale must be finite and > 0.
  * Arithmetic: bf16 products, fp32 accumulation and softmax; P is rounded to
  * bf16 for the PV product.
  * Supported: D in {64, 128}; 1 <= B <= 64; G*B <= 128; page_size a power of two
  * >= 8; q, k_cache, v_cache, out 16-byte aligned.
  * Workspace: at least bdsa_block_attn_workspace_bytes(...) bytes of device
- * memory, 256-byte aligned: the tile prefix, one counter per (request, KV head)
- * and two fp32 partial slots of G*B*(D+1) floats per CTA.  Its contents need no
- * initialisation and are not meaningful after the call; calls that share one
- * workspace must be ordered on the same stream.
+ * memory, 256-byte aligned: two partial slots per CTA (a flag and G*B*(D+1)
+ * fp32 values).  Its contents need no initialisation and are not meaningful
+ * after the call; calls that share one workspace must be ordered on the same
+ * stream.
  */
 size_t bdsa_block_attn_workspace_bytes(int32_t bs, int32_t B, int32_t Hq, int32_t Hkv, int32_t D,
                                        int32_t max_ctx_len, int32_t num_sms);

@@ -33,6 +33,9 @@ SHAPES = [
     ("decode_b1_d64", 8, 8, 64, 1, 8, (50, 400, 0)),
     ("b64_big_pages", 2, 1, 64, 64, 256, (333,)),
     ("odd_g3_b3", 6, 2, 64, 3, 128, (240, 17)),
+    # 63 tiles in one unit: with the forced split it is cut into more pieces than
+    # the merge kernel lists up front
+    ("long_unit_many_pieces", 2, 1, 64, 4, 64, (8000,)),
 ]
 
 
@@ -135,16 +138,43 @@ def test_bad_page_id_sets_status_and_skips_unit(dev):
                         inp.v_cache, inp.scale)
     d = DevAttn(bad)
     ref, _ = oracle_attn_full(inp, VERIFY)
+    # sms = FORCE_SPLIT cuts every unit into one-tile pieces, so only one piece
+    # of each of request 1's units sees the bad page and the merge must zero it
     for sms in (0, FORCE_SPLIT):
         status = torch.zeros(1, dtype=torch.int32, device=dev)
-        out, _ = run_attn(d, VERIFY, sms=sms, status=status)
+        out, lse = run_attn(d, VERIFY, sms=sms, status=status)
         assert status.item() == 16  # BDSA_DEVICE_OUT_OF_RANGE
         o = out.float().cpu().numpy()
         B = cfg.B
         assert (o[B:2 * B] == 0).all()
+        assert (lse[B:2 * B] == float("-inf")).all()
         for r in (0, 2):
             err = np.abs(o[r * B:(r + 1) * B] - ref[r * B:(r + 1) * B])
             assert err.max() < 1e-2
+
+
+@pytest.mark.parametrize("L_bad", [-1, "beyond_table"])
+def test_context_the_table_cannot_hold_sets_status(dev, L_bad):
+    # a negative length, or L + B needing more pages than the block-table row
+    # holds: the request's rows are zeros (lse -inf), nothing past the row is read
+    cfg = _cfg("shapebad", 3, 8, 2, 128, 8, 16, (100, 200, 50))
+    inp = wl.make_attn_inputs(cfg)
+    ref, _ = oracle_attn_full(inp, VERIFY)
+    d = DevAttn(inp)
+    max_pages = inp.block_table.shape[1]
+    L = -1 if L_bad == -1 else max_pages * cfg.page_size - cfg.B + 1
+    d.sl = d.sl.clone()
+    d.sl[2] = L
+    for sms in (0, FORCE_SPLIT):
+        status = torch.zeros(1, dtype=torch.int32, device=dev)
+        out, lse = run_attn(d, VERIFY, sms=sms, status=status)
+        assert status.item() == 16
+        o = out.float().cpu().numpy()
+        B = cfg.B
+        assert (o[2 * B:3 * B] == 0).all()
+        assert (lse[2 * B:3 * B] == float("-inf")).all()
+        err = np.abs(o[:2 * B] - ref[:2 * B])
+        assert err.max() < 1e-2
 
 
 FULL = ["qwen3_8b_verify", "llada2_block_draft", "uno_1k8k_step", "long_ctx_verify"]
