@@ -101,10 +101,18 @@ struct Cfg {
     static constexpr int PF = SR + 2;     // NP
     static constexpr int PV = PF + NP;    // NP: PV done, per P buffer
     static constexpr int OE = PV + NP;    // 2: O buffer read by the epilogue
-    static constexpr int DR = OE + 2;     // drain
+    // M = 64 epilogue staging in the P buffers: every softmax warp wrote its
+    // rows (EW), the tile store has read them (ER); one phase per piece.
+    static constexpr int EW = OE + 2;
+    static constexpr int ER = EW + 1;
+    static constexpr int DR = ER + 1;     // drain
     static constexpr int kNumBars = DR + 1;
     static constexpr int kOffMisc = kOffBar + 8 * kNumBars;
-    static constexpr int kSmem = kOffMisc + 192 + 1024;  // + slack to align the base to 1 KB
+    static constexpr int kOffMiscEnd = kOffMisc + 144;  // the schedule state (Sched)
+    // + slack to align the base to 1 KB.  With D = 128 this is within a few
+    // hundred bytes of the SM's shared memory less one merge CTA's, so that a
+    // merge CTA can wait beside each attention CTA: keep both small.
+    static constexpr int kSmem = kOffMiscEnd + 1024;
 };
 
 struct Params {
@@ -156,7 +164,8 @@ __device__ __forceinline__ int tiles_of(long L, int B) {
 // kUnitCost "virtual" tiles followed by its real tiles, and CTA b takes the
 // cost range [b * Wc / S, (b + 1) * Wc / S).  The virtual tiles carry no work:
 // they charge every unit switch (a Q load, an epilogue, a ragged last tile)
-// about one tile of time, so a CTA that touches more units gets fewer tiles.
+// about the time of kUnitCost tiles, so a CTA that touches more units gets
+// fewer tiles.
 // The real tiles inside a CTA's cost range form its range [x0, x1) of global
 // tile indices.
 constexpr int kUnitCost = 1;
@@ -171,6 +180,7 @@ struct Sched {
     long long x0, x1, W, Wc;
     long long wsum[8];       // per-warp partial sums of the scan (<= 256 threads)
 };
+static_assert(sizeof(Sched) <= 144, "the attention kernel keeps Sched in 144 bytes");
 
 // The unit a role is working through, walked in (request, KV head) order.
 struct Cursor {
@@ -314,7 +324,9 @@ template <int D, int M>
 __global__ void __launch_bounds__(kThreads, 1)
     block_attn_kernel(const __grid_constant__ CUtensorMap tm_q,
                       const __grid_constant__ CUtensorMap tm_k,
-                      const __grid_constant__ CUtensorMap tm_v, const Params prm) {
+                      const __grid_constant__ CUtensorMap tm_v,
+                      const __grid_constant__ CUtensorMap tm_out,
+                      const __grid_constant__ CUtensorMap tm_part, const Params prm) {
     using C = Cfg<D, M>;
     extern __shared__ uint8_t smem_raw[];
     const uint32_t raw = smem_u32(smem_raw);
@@ -356,6 +368,8 @@ __global__ void __launch_bounds__(kThreads, 1)
             mbar_init(bar(C::PF + k), kSoftmaxWarps);
             mbar_init(bar(C::PV + k), 1);
         }
+        mbar_init(bar(C::EW), kSoftmaxWarps);
+        mbar_init(bar(C::ER), 1);
         mbar_init(bar(C::DR), 1);
         *abort_flag = 0;
         fence_mbarrier_init();
@@ -591,8 +605,22 @@ __global__ void __launch_bounds__(kThreads, 1)
         struct Epi {
             long lastg, orow;
             float inv_l, lse2;
-            int ob, slot;
+            int ob, slot, r, h, k;
             bool complete, bad;
+        };
+        // M = 64: a piece's tile store reads the P buffers after the epilogue
+        // returns; they are released before the next write to them.
+        bool stage_busy = false;
+        int stage_k = 0;
+        auto release_stage = [&]() -> bool {
+            if (tid == 0) {
+                bulk_wait_group_read0();
+                mbar_arrive(bar(C::ER));
+            }
+            bool okr = mbar_wait(bar(C::ER), (uint32_t)(stage_k & 1), abort_flag, prm.dev_status);
+            okr = __all_sync(0xffffffffu, okr);
+            stage_busy = false;
+            return okr;
         };
         auto epilogue = [&](const Epi &e) -> bool {
             bool okw = mbar_wait(bar(C::PV + (int)(e.lastg % C::NP)),
@@ -600,40 +628,113 @@ __global__ void __launch_bounds__(kThreads, 1)
             okw = __all_sync(0xffffffffu, okw);
             if (!okw) return false;
             tc_fence_after();
-#pragma unroll
-            for (int c = 0; c < OC / 32; ++c) {
-                float ov[32];
-                tmem_load_chunk<M, D / 2>(tmem + lane_base + kTmemO + e.ob * 128 + c * 32, ov);
+            const float sc = e.inv_l;
+            const bool zero = e.complete && e.bad;  // zeros, whatever O holds (it may be NaN)
+            // This thread's output columns [half * OC, half * OC + OC), read from
+            // TMEM 32 at a time.
+            auto load_chunk = [&](int c, float (&v32)[32]) {
+                tmem_load_chunk<M, D / 2>(tmem + lane_base + kTmemO + e.ob * 128 + c * 32, v32);
                 tmem_wait_ld();
-                if (!valid_row) continue;
-                const int col0 = half * OC + c * 32;
-                if (e.complete && e.bad) {
-                    uint4 *dst = reinterpret_cast<uint4 *>(prm.out + e.orow * D + col0);
+                if (zero) {
 #pragma unroll
-                    for (int v = 0; v < 4; ++v) dst[v] = make_uint4(0, 0, 0, 0);
-                } else if (e.complete) {
-                    uint4 *dst = reinterpret_cast<uint4 *>(prm.out + e.orow * D + col0);
-#pragma unroll
-                    for (int v = 0; v < 4; ++v) {
-                        uint4 w;
-                        w.x = pack_bf16x2(ov[8 * v + 0] * e.inv_l, ov[8 * v + 1] * e.inv_l);
-                        w.y = pack_bf16x2(ov[8 * v + 2] * e.inv_l, ov[8 * v + 3] * e.inv_l);
-                        w.z = pack_bf16x2(ov[8 * v + 4] * e.inv_l, ov[8 * v + 5] * e.inv_l);
-                        w.w = pack_bf16x2(ov[8 * v + 6] * e.inv_l, ov[8 * v + 7] * e.inv_l);
-                        dst[v] = w;
-                    }
-                } else {
-                    float4 *dst = reinterpret_cast<float4 *>(
-                        prm.part_o + ((long)e.slot * prm.rows + row) * D + col0);
-#pragma unroll
-                    for (int v = 0; v < 8; ++v)
-                        dst[v] = make_float4(ov[4 * v] * e.inv_l, ov[4 * v + 1] * e.inv_l,
-                                             ov[4 * v + 2] * e.inv_l, ov[4 * v + 3] * e.inv_l);
+                    for (int q = 0; q < 32; ++q) v32[q] = 0.f;
                 }
+            };
+            if constexpr (M == 64) {
+                // Stage the rows in the two P buffers (free: the piece's last two
+                // PVs are done and the next tile's P is not written before this
+                // returns), 128-byte rows swizzled like the tensor maps, then one
+                // thread stores them with TMA: bf16 to `out` for a whole unit,
+                // fp32 to the partial slot otherwise.
+                const uint32_t stage = sbase + C::kOffP;
+#pragma unroll
+                for (int c = 0; c < OC / 32; ++c) {
+                    float v32[32];
+                    load_chunk(c, v32);
+                    if (!valid_row) continue;
+                    const int col0 = half * OC + c * 32;
+                    if (e.complete) {
+                        // 32 bf16 = four 16-byte chunks of the 64-column slab
+                        const uint32_t rbase = stage + (col0 >> 6) * C::kSlab + row * 128;
+                        const int u0 = (col0 & 63) >> 3;
+#pragma unroll
+                        for (int v = 0; v < 4; ++v)
+                            st_shared_v4(rbase + (((u0 + v) ^ (row & 7)) << 4),
+                                         pack_bf16x2(v32[8 * v + 0] * sc, v32[8 * v + 1] * sc),
+                                         pack_bf16x2(v32[8 * v + 2] * sc, v32[8 * v + 3] * sc),
+                                         pack_bf16x2(v32[8 * v + 4] * sc, v32[8 * v + 5] * sc),
+                                         pack_bf16x2(v32[8 * v + 6] * sc, v32[8 * v + 7] * sc));
+                    } else {
+                        // 32 fp32 = one 128-byte row of a 32-column box
+                        const uint32_t rbase = stage + (col0 >> 5) * C::kSlab + row * 128;
+#pragma unroll
+                        for (int v = 0; v < 8; ++v)
+                            st_shared_v4(rbase + ((v ^ (row & 7)) << 4),
+                                         __float_as_uint(v32[4 * v + 0] * sc),
+                                         __float_as_uint(v32[4 * v + 1] * sc),
+                                         __float_as_uint(v32[4 * v + 2] * sc),
+                                         __float_as_uint(v32[4 * v + 3] * sc));
+                    }
+                }
+                // the O buffer may take the next unit but one as soon as it is read
+                tc_fence_before();
+                fence_proxy_async_smem();
+                __syncwarp();
+                if (lane == 0) {
+                    mbar_arrive(bar(C::OE + e.ob));
+                    mbar_arrive(bar(C::EW));
+                }
+                if (tid == 0) {
+                    const bool okw = mbar_wait(bar(C::EW), (uint32_t)(e.k & 1), abort_flag,
+                                               prm.dev_status);
+                    if (okw) {
+                        if (e.complete) {
+                            for (int sl = 0; sl < D / 64; ++sl)
+                                tma_store_4d(&tm_out, stage + sl * C::kSlab, sl * 64, 0, e.h,
+                                             e.r * B);
+                        } else {
+                            for (int bx = 0; bx < D / 32; ++bx)
+                                tma_store_2d(&tm_part, stage + bx * C::kSlab, bx * 32,
+                                             e.slot * prm.rows);
+                        }
+                        bulk_commit_group();
+                    }
+                }
+                // The staging area is released (ER) before the next P write,
+                // by when the store has long read it.
+                stage_busy = true;
+                stage_k = e.k;
+            } else {
+#pragma unroll
+                for (int c = 0; c < OC / 32; ++c) {
+                    float v32[32];
+                    load_chunk(c, v32);
+                    if (!valid_row) continue;
+                    const int col0 = half * OC + c * 32;
+                    if (e.complete) {
+                        uint4 *dst = reinterpret_cast<uint4 *>(prm.out + e.orow * D + col0);
+#pragma unroll
+                        for (int v = 0; v < 4; ++v) {
+                            uint4 w;
+                            w.x = pack_bf16x2(v32[8 * v + 0] * sc, v32[8 * v + 1] * sc);
+                            w.y = pack_bf16x2(v32[8 * v + 2] * sc, v32[8 * v + 3] * sc);
+                            w.z = pack_bf16x2(v32[8 * v + 4] * sc, v32[8 * v + 5] * sc);
+                            w.w = pack_bf16x2(v32[8 * v + 6] * sc, v32[8 * v + 7] * sc);
+                            dst[v] = w;
+                        }
+                    } else {
+                        float4 *dst = reinterpret_cast<float4 *>(
+                            prm.part_o + ((long)e.slot * prm.rows + row) * D + col0);
+#pragma unroll
+                        for (int v = 0; v < 8; ++v)
+                            dst[v] = make_float4(v32[4 * v] * sc, v32[4 * v + 1] * sc,
+                                                 v32[4 * v + 2] * sc, v32[4 * v + 3] * sc);
+                    }
+                }
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(bar(C::OE + e.ob));
             }
-            tc_fence_before();
-            __syncwarp();
-            if (lane == 0) mbar_arrive(bar(C::OE + e.ob));
             if (valid_row && half == 0) {
                 if (e.complete && e.bad) {
                     if (prm.lse) prm.lse[e.orow] = -INFINITY;
@@ -758,6 +859,10 @@ __global__ void __launch_bounds__(kThreads, 1)
                     tmem_wait_st();
                 }
                 // P row -> shared memory, K-major with the 128-byte swizzle.
+                if (stage_busy) {
+                    ok = release_stage();
+                    if (!ok) break;
+                }
                 {
                     const uint32_t pbase = sbase + C::kOffP + pb * C::kPBuf;
 #pragma unroll
@@ -811,6 +916,9 @@ __global__ void __launch_bounds__(kThreads, 1)
                 e.bad = shape_bad || __any_sync(0xffffffffu, page_bad);
                 e.orow = ((long)pc.r * B + i_blk) * prm.Hq + (long)pc.h * G + row % G;
                 e.slot = 2 * b + (k == 0 ? 0 : 1);
+                e.r = pc.r;
+                e.h = pc.h;
+                e.k = k;
                 if (e.bad && tid == 0) report_status(prm.dev_status, BDSA_DEVICE_OUT_OF_RANGE);
                 ok = epilogue(e);
                 if (!ok) break;
@@ -820,6 +928,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
     }
 
+    if (tid == 0) bulk_wait_group0();  // epilogue tile stores complete
     tc_fence_before();
     __syncthreads();
     if (warp == kMmaWarp) {
@@ -840,7 +949,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 // is written as zeros (lse -inf).
 constexpr int kMergeThreads = 256;
 constexpr int kMergeTPR = 4;      // threads per row
-constexpr int kMergeSlots = 32;   // piece slots listed in shared memory
+constexpr int kMergeSlots = 16;   // piece slots listed in shared memory
 
 template <int D>
 __global__ void __launch_bounds__(kMergeThreads) attn_merge_kernel(const Params prm) {
@@ -1013,6 +1122,33 @@ int launch_impl(const AttnArgs &a, const AttnPlan &plan, cudaStream_t stream) {
             return BDSA_CUDA_ERROR;
     }
     char *ws = static_cast<char *>(a.workspace);
+    CUtensorMap tout, tpart;
+    {
+        // out has q's layout; the epilogue stores a whole unit's rows per box.
+        cuuint64_t dims[4] = {(cuuint64_t)D, (cuuint64_t)G, (cuuint64_t)a.Hkv,
+                              (cuuint64_t)a.bs * a.B};
+        cuuint64_t strides[3] = {(cuuint64_t)D * 2, (cuuint64_t)G * D * 2,
+                                 (cuuint64_t)a.Hq * D * 2};
+        cuuint32_t box[4] = {64, (cuuint32_t)G, 1, (cuuint32_t)a.B};
+        cuuint32_t es[4] = {1, 1, 1, 1};
+        if (enc(&tout, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, a.out, dims, strides, box, es,
+                CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) !=
+            CUDA_SUCCESS)
+            return BDSA_CUDA_ERROR;
+    }
+    {
+        // partial slots [2 * grid * rows, D] fp32, stored 32 columns x rows per box.
+        cuuint64_t dims[2] = {(cuuint64_t)D, (cuuint64_t)2 * plan.grid * plan.rows};
+        cuuint64_t strides[1] = {(cuuint64_t)D * 4};
+        cuuint32_t box[2] = {32, (cuuint32_t)plan.rows};
+        cuuint32_t es[2] = {1, 1};
+        if (enc(&tpart, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2, ws + plan.off_part_o, dims, strides,
+                box, es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) !=
+            CUDA_SUCCESS)
+            return BDSA_CUDA_ERROR;
+    }
     Params prm;
     prm.block_table = a.block_table;
     prm.seq_lens = a.seq_lens;
@@ -1047,7 +1183,7 @@ int launch_impl(const AttnArgs &a, const AttnPlan &plan, cudaStream_t stream) {
         attr_set = true;
     }
     if (launch_pdl(block_attn_kernel<D, M>, dim3(plan.grid), dim3(kThreads), C::kSmem, stream,
-                   tq, tk, tv, prm) != cudaSuccess)
+                   tq, tk, tv, tout, tpart, prm) != cudaSuccess)
         return BDSA_CUDA_ERROR;
     if (launch_pdl(attn_merge_kernel<D>, dim3(plan.grid), dim3(kMergeThreads), 0, stream,
                    prm) != cudaSuccess)
