@@ -39,6 +39,15 @@ sys.path.insert(0, ROOT)
 from block_diffusion_speculative_attn_gb300 import workloads as wl  # noqa: E402
 
 METRIC = "draft/verify block-attn query tokens/s + % HBM roofline; accept rows/s"
+# DRAM bytes (read + write) of one attention call on the Qwen3-8B-shaped verify
+# batch, from one ncu capture of each of its two kernels (summary and commands
+# in profiles/qwen3_8b_verify_step_ncu.md): attention 308.42 + 5.21 MB, merge
+# 8.88 MB (cold under ncu; L2 hits in the timed step).  Valid only for the
+# kernel sources it was taken on: reported as null once they change.
+ATTN_TRAFFIC = {"workload": "qwen3_8b_verify", "bytes_per_call": 322.51e6,
+                "sources_sha256": "1fc4367321d8b9f85228bd0867087a419cf1694f7ab480490e7bd9f1465c0919"}
+ATTN_SOURCES = ("block_diffusion_speculative_attn_gb300/csrc/block_attn.cu",
+                "block_diffusion_speculative_attn_gb300/csrc/bdsa_device.cuh")
 L2_FLUSH_BYTES = 512 << 20  # > 129 MB L2
 L2_CLEAN_BYTES = 256 << 20  # read after the flush: writes its dirty lines back
 
@@ -76,6 +85,18 @@ def accept_bytes(cfg: wl.StepConfig) -> int:
     """One full row of p and q at the resolved position per request (upper bound
     of the algorithmic bytes: a fully accepted row reads p alone)."""
     return cfg.bs * 2 * cfg.V * 4 if cfg.V else 0
+
+
+def attn_traffic(workload: str):
+    import hashlib
+    h = hashlib.sha256()
+    root = os.path.dirname(os.path.abspath(__file__))
+    for f in ATTN_SOURCES:
+        with open(os.path.join(root, f), "rb") as fh:
+            h.update(fh.read())
+    ok = (workload == ATTN_TRAFFIC["workload"] and
+          h.hexdigest() == ATTN_TRAFFIC["sources_sha256"])
+    return ATTN_TRAFFIC["bytes_per_call"] if ok else None
 
 
 def peaks():
@@ -470,7 +491,7 @@ def main(argv=None):
     if attn_ms is not None:
         achieved = abytes / (attn_ms / 1e3) / 1e9
         roof = {"bound": "hbm", "achieved": achieved, "peak": hbm, "unit": "GB/s",
-                "frac": achieved / hbm, "traffic": None,
+                "frac": achieved / hbm, "traffic": attn_traffic(cfg.name),
                 "kernel": "block_attn_paged (attention + split-KV combine launch)",
                 "algorithmic_bytes_per_launch": abytes, "peak_source": peak_src,
                 "launch_ms": attn_ms}
