@@ -165,10 +165,11 @@ __device__ __forceinline__ int tiles_of(long L, int B) {
 // cost range [b * Wc / S, (b + 1) * Wc / S).  The virtual tiles carry no work:
 // they charge every unit switch (a Q load, an epilogue, a ragged last tile)
 // about the time of kUnitCost tiles, so a CTA that touches more units gets
-// fewer tiles.
+// fewer tiles.  Two tiles per switch: per-CTA end times regressed on the
+// schedule (traced) put a switch at one to two tiles, and two measured best.
 // The real tiles inside a CTA's cost range form its range [x0, x1) of global
 // tile indices.
-constexpr int kUnitCost = 1;
+constexpr int kUnitCost = 2;
 
 // Schedule state (shared memory).
 struct Sched {
