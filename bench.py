@@ -41,11 +41,11 @@ from block_diffusion_speculative_attn_gb300 import workloads as wl  # noqa: E402
 METRIC = "draft/verify block-attn query tokens/s + % HBM roofline; accept rows/s"
 # DRAM bytes (read + write) of one attention call on the Qwen3-8B-shaped verify
 # batch, from one ncu capture of each of its two kernels (summary and commands
-# in profiles/qwen3_8b_verify_step_ncu.md): attention 308.42 + 5.21 MB, merge
-# 8.88 MB (cold under ncu; L2 hits in the timed step).  Valid only for the
+# in profiles/qwen3_8b_verify_step_ncu.md): attention 308.42 + 5.03 MB, merge
+# 8.79 MB (cold under ncu; L2 hits in the timed step).  Valid only for the
 # kernel sources it was taken on: reported as null once they change.
-ATTN_TRAFFIC = {"workload": "qwen3_8b_verify", "bytes_per_call": 322.51e6,
-                "sources_sha256": "1fc4367321d8b9f85228bd0867087a419cf1694f7ab480490e7bd9f1465c0919"}
+ATTN_TRAFFIC = {"workload": "qwen3_8b_verify", "bytes_per_call": 322.24e6,
+                "sources_sha256": "b88068f1483fca1b91658d037d3eee30705bb234e47c0fbe2fe017cf7bb532c1"}
 ATTN_SOURCES = ("block_diffusion_speculative_attn_gb300/csrc/block_attn.cu",
                 "block_diffusion_speculative_attn_gb300/csrc/bdsa_device.cuh")
 L2_FLUSH_BYTES = 512 << 20  # > 129 MB L2
@@ -448,21 +448,25 @@ def main(argv=None):
     step = Step(cfg, dev, seed=cfg.seed + 1000 * rank)
     flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
     clean = torch.ones(L2_CLEAN_BYTES // 4, dtype=torch.float32, device=dev)
-    for _ in range(max(args.warmup, 3)):
-        step.run()
-    torch.cuda.synchronize()
-    assert step.status.item() == 0, bdsa.STATUS.get(step.status.item())
-
     K = args.steps
     ev = [{"step": (torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)),
            "attn": (torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)),
            "accept": (torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))}
           for _ in range(K)]
+    # The clock sampler starts first; the warm-up steps then run right before
+    # the timed ones, so the GPU does not sit idle in between (an idle gap made
+    # the first timed step an outlier).
     clocks = ClockSampler(local)
-    barrier(world)
-    torch.cuda.synchronize()
     clocks.start()
     time.sleep(0.3)
+    for _ in range(max(args.warmup, 3)):
+        flush.zero_()
+        clean.sum()
+        step.run()
+    torch.cuda.synchronize()
+    assert step.status.item() == 0, bdsa.STATUS.get(step.status.item())
+    barrier(world)
+    torch.cuda.synchronize()
     for i in range(K):
         # Evict the previous step's lines from L2 (outside the events): write a
         # buffer larger than L2, then read another one so that the write-back
