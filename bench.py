@@ -295,6 +295,45 @@ def run_e2e(step: Step, steps: int, warmup: int):
     return ms, h2d, d2h
 
 
+def time_fused_append(step: Step, flush, clean, iters: int = 20):
+    """The attention call with and without the fused block-KV append (the
+    block's own keys and values written into the paged cache by the same
+    launch), interleaved, L2 flushed before each; mean event times in ms."""
+    c = step.cfg
+    g = torch.Generator(device=step.dev)
+    g.manual_seed(c.seed + 99)
+    shape = (c.bs * c.B, c.Hkv, c.D)
+    k_new = torch.randn(shape, generator=g, device=step.dev).to(torch.bfloat16)
+    v_new = torch.randn(shape, generator=g, device=step.dev).to(torch.bfloat16)
+    mode = c.modes[-1]
+
+    def call(append):
+        step.bdsa.block_attn_paged(step.attn.q, step.attn.k_cache, step.attn.v_cache, step.bt,
+                                   step.sl, B=c.B, page_size=c.page_size, scale=step.attn.scale,
+                                   mode=mode, max_ctx_len=step.attn.max_ctx_len,
+                                   num_pages=step.attn.num_pages, out=step.o, lse=step.lse,
+                                   workspace=step.attn_ws, dev_status=step.status,
+                                   k_new=k_new if append else None,
+                                   v_new=v_new if append else None)
+
+    times = {False: [], True: []}
+    for i in range(iters + 2):
+        for append in ((False, True) if i % 2 == 0 else (True, False)):
+            flush.zero_()
+            clean.sum()
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record()
+            call(append)
+            e1.record()
+            if i >= 2:
+                times[append].append((e0, e1))
+    torch.cuda.synchronize()
+    ms = {a: statistics.mean(x.elapsed_time(y) for x, y in v) for a, v in times.items()}
+    return {"launch_ms": ms[True], "plain_launch_ms": ms[False],
+            "added_us": (ms[True] - ms[False]) * 1e3,
+            "bytes_written": 2 * c.bs * c.B * c.Hkv * c.D * 2, "iters": iters}
+
+
 # ---------------------------------------------------------------------------
 def oracle_sample(cfg: wl.StepConfig, attn: wl.AttnInputs, acc, reqs, nthreads):
     """Host copies of the sampled requests' inputs (compact page pool)."""
@@ -500,6 +539,11 @@ def main(argv=None):
                 "algorithmic_bytes_per_launch": abytes, "peak_source": peak_src,
                 "launch_ms": attn_ms}
 
+    fused_append = None
+    if attn_ms is not None:
+        fused_append = time_fused_append(step, flush, clean)
+        assert step.status.item() == 0, bdsa.STATUS.get(step.status.item())
+
     e2e = None
     if not args.no_e2e:
         e_ms, h2d, d2h = run_e2e(step, max(3, K // 2), 2)
@@ -524,6 +568,7 @@ def main(argv=None):
             "attn_query_tokens_per_s": (cfg.bs * cfg.B / (attn_ms / 1e3)) if attn_ms else None,
             "accept_rows_per_s": (cfg.bs / (acc_ms / 1e3)) if acc_ms else None,
             "accept_ms": acc_ms,
+            "fused_append": fused_append,
             "attn_flops_per_launch": attn_flops(cfg, step.attn.seq_lens, cfg.modes[-1]),
             "e2e": e2e, "cpu_baseline": cpu, "gpu_launches": step.launches * K,
             "clocks": clk}

@@ -30,7 +30,8 @@ STATUS = {0: "BDSA_OK", 1: "BDSA_INVALID_ARG", 2: "BDSA_UNSUPPORTED", 3: "BDSA_M
 # Every symbol include/bdsa.h declares.
 EXPORTS = ("bdsa_status_string", "bdsa_version", "bdsa_prepare_block",
            "bdsa_block_attn_workspace_bytes", "bdsa_block_attn_paged",
-           "bdsa_spec_accept_workspace_bytes", "bdsa_spec_accept", "bdsa_spec_accept_noalloc")
+           "bdsa_block_attn_paged_append", "bdsa_spec_accept_workspace_bytes",
+           "bdsa_spec_accept", "bdsa_spec_accept_noalloc")
 
 _lib = None
 
@@ -63,6 +64,9 @@ def lib() -> ctypes.CDLL:
     L.bdsa_block_attn_paged.argtypes = [P, P, P, P, i32, i32, P, i32, i32, i32, i32, i32, i32,
                                         i32, f32, i32, P, P, P, sz, i32, P, P]
     L.bdsa_block_attn_paged.restype = i32
+    L.bdsa_block_attn_paged_append.argtypes = [P, P, P, P, P, P, i32, i32, P, i32, i32, i32, i32,
+                                               i32, i32, i32, f32, i32, P, P, P, sz, i32, P, P]
+    L.bdsa_block_attn_paged_append.restype = i32
     L.bdsa_spec_accept_workspace_bytes.argtypes = [i32] * 4
     L.bdsa_spec_accept_workspace_bytes.restype = sz
     L.bdsa_spec_accept.argtypes = [P, P, i64, i64, P, i64, i64, P, P, P, i32, i32, i32, P, P, P,
@@ -129,12 +133,21 @@ def block_attn_workspace_bytes(bs, B, Hq, Hkv, D, max_ctx_len, sms: int = 0) -> 
 
 def block_attn_paged(q, k_cache, v_cache, block_table, seq_lens, *, B: int, page_size: int,
                      scale: float, mode: int, max_ctx_len: int, num_pages: int | None = None,
-                     out=None, lse=None, workspace=None, dev_status=None, sms: int = 0):
+                     out=None, lse=None, workspace=None, dev_status=None, sms: int = 0,
+                     k_new=None, v_new=None):
     """bdsa_block_attn_paged.  q [bs*B, Hq, D] bf16, caches [slots, Hkv, D] bf16.
 
-    Returns out [bs*B, Hq, D] bf16 (lse is filled when given, fp32 [bs*B, Hq]).
+    With k_new / v_new ([bs*B, Hkv, D] bf16) it is bdsa_block_attn_paged_append:
+    the block's own keys and values are written into the caches in the same
+    launch.  Returns out [bs*B, Hq, D] bf16 (lse is filled when given, fp32
+    [bs*B, Hq]).
     """
     _dev(q, "q", torch.bfloat16)
+    if (k_new is None) != (v_new is None):
+        raise ValueError("k_new and v_new go together")
+    if k_new is not None:
+        _dev(k_new, "k_new", torch.bfloat16)
+        _dev(v_new, "v_new", torch.bfloat16)
     _dev(k_cache, "k_cache", torch.bfloat16)
     _dev(v_cache, "v_cache", torch.bfloat16)
     _dev(block_table, "block_table", torch.int32)
@@ -153,12 +166,20 @@ def block_attn_paged(q, k_cache, v_cache, block_table, seq_lens, *, B: int, page
     if workspace is None and need > 0:
         workspace = torch.empty(need, dtype=torch.uint8, device=q.device)
     ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
-    st = lib().bdsa_block_attn_paged(_ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(block_table),
-                                     max_pages, num_pages, _ptr(seq_lens), int(max_ctx_len), bs,
-                                     B, Hq, Hkv, D, page_size, float(scale), int(mode), _ptr(out),
-                                     _ptr(lse), _ptr(workspace), ws_bytes, sms, _ptr(dev_status),
-                                     _stream(q.device))
-    _check("bdsa_block_attn_paged", st)
+    if k_new is None:
+        st = lib().bdsa_block_attn_paged(_ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(block_table),
+                                         max_pages, num_pages, _ptr(seq_lens), int(max_ctx_len),
+                                         bs, B, Hq, Hkv, D, page_size, float(scale), int(mode),
+                                         _ptr(out), _ptr(lse), _ptr(workspace), ws_bytes, sms,
+                                         _ptr(dev_status), _stream(q.device))
+        _check("bdsa_block_attn_paged", st)
+    else:
+        st = lib().bdsa_block_attn_paged_append(
+            _ptr(q), _ptr(k_new), _ptr(v_new), _ptr(k_cache), _ptr(v_cache), _ptr(block_table),
+            max_pages, num_pages, _ptr(seq_lens), int(max_ctx_len), bs, B, Hq, Hkv, D, page_size,
+            float(scale), int(mode), _ptr(out), _ptr(lse), _ptr(workspace), ws_bytes, sms,
+            _ptr(dev_status), _stream(q.device))
+        _check("bdsa_block_attn_paged_append", st)
     return out
 
 

@@ -75,20 +75,26 @@ size_t bdsa_block_attn_workspace_bytes(int32_t bs, int32_t B, int32_t Hq, int32_
         .workspace;
 }
 
-int32_t bdsa_block_attn_paged(const bdsa_bf16 *q, const bdsa_bf16 *k_cache,
-                              const bdsa_bf16 *v_cache, const int32_t *block_table,
-                              int32_t max_pages_per_req, int32_t num_pages,
-                              const int32_t *seq_lens, int32_t max_ctx_len, int32_t bs,
-                              int32_t B, int32_t Hq, int32_t Hkv, int32_t D, int32_t page_size,
-                              float softmax_scale, int32_t mode, bdsa_bf16 *out, float *lse,
-                              void *workspace, size_t workspace_bytes, int32_t num_sms,
-                              int32_t *dev_status, void *stream) {
+}  // extern "C"
+
+namespace {
+
+// Checks and dispatch shared by bdsa_block_attn_paged and
+// bdsa_block_attn_paged_append (k_new / v_new null for the former).
+int32_t attn_call(const bdsa_bf16 *q, const bdsa_bf16 *k_new, const bdsa_bf16 *v_new,
+                  const bdsa_bf16 *k_cache, const bdsa_bf16 *v_cache, const int32_t *block_table,
+                  int32_t max_pages_per_req, int32_t num_pages, const int32_t *seq_lens,
+                  int32_t max_ctx_len, int32_t bs, int32_t B, int32_t Hq, int32_t Hkv, int32_t D,
+                  int32_t page_size, float softmax_scale, int32_t mode, bdsa_bf16 *out, float *lse,
+                  void *workspace, size_t workspace_bytes, int32_t num_sms, int32_t *dev_status,
+                  void *stream) {
     if (bs < 0 || B < 1 || Hq < 1 || Hkv < 1 || max_pages_per_req < 1 || num_pages < 1 ||
         max_ctx_len < 0 || !isfinite(softmax_scale) || !(softmax_scale > 0.f) ||
         (mode != BDSA_MODE_DRAFT && mode != BDSA_MODE_VERIFY))
         return BDSA_INVALID_ARG;
     if (bs == 0) return BDSA_OK;
     if (!q || !k_cache || !v_cache || !block_table || !seq_lens || !out) return BDSA_INVALID_ARG;
+    if ((k_new == nullptr) != (v_new == nullptr)) return BDSA_INVALID_ARG;
     if (Hq % Hkv != 0) return BDSA_INVALID_ARG;
     if (D != 64 && D != 128) return BDSA_UNSUPPORTED;
     if (B > 64 || (Hq / Hkv) * B > 128) return BDSA_UNSUPPORTED;
@@ -96,12 +102,15 @@ int32_t bdsa_block_attn_paged(const bdsa_bf16 *q, const bdsa_bf16 *k_cache,
     if ((int64_t)num_pages * page_size > INT32_MAX) return BDSA_UNSUPPORTED;
     if ((int64_t)bs * B > INT32_MAX) return BDSA_UNSUPPORTED;
     if (!aligned(q, 16) || !aligned(k_cache, 16) || !aligned(v_cache, 16) || !aligned(out, 16) ||
+        (k_new && !aligned(k_new, 16)) || (v_new && !aligned(v_new, 16)) ||
         (lse && !aligned(lse, 4)) || (workspace && !aligned(workspace, 256)))
         return BDSA_MISALIGNED;
     bdsa::AttnArgs a;
     a.q = reinterpret_cast<const uint16_t *>(q);
     a.k_cache = reinterpret_cast<const uint16_t *>(k_cache);
     a.v_cache = reinterpret_cast<const uint16_t *>(v_cache);
+    a.k_new = reinterpret_cast<const uint16_t *>(k_new);
+    a.v_new = reinterpret_cast<const uint16_t *>(v_new);
     a.block_table = block_table;
     a.seq_lens = seq_lens;
     a.max_pages = max_pages_per_req;
@@ -122,6 +131,40 @@ int32_t bdsa_block_attn_paged(const bdsa_bf16 *q, const bdsa_bf16 *k_cache,
     a.workspace_bytes = workspace_bytes;
     a.dev_status = dev_status;
     return bdsa::launch_block_attn(a, static_cast<cudaStream_t>(stream));
+}
+
+}  // namespace
+
+extern "C" {
+
+int32_t bdsa_block_attn_paged(const bdsa_bf16 *q, const bdsa_bf16 *k_cache,
+                              const bdsa_bf16 *v_cache, const int32_t *block_table,
+                              int32_t max_pages_per_req, int32_t num_pages,
+                              const int32_t *seq_lens, int32_t max_ctx_len, int32_t bs,
+                              int32_t B, int32_t Hq, int32_t Hkv, int32_t D, int32_t page_size,
+                              float softmax_scale, int32_t mode, bdsa_bf16 *out, float *lse,
+                              void *workspace, size_t workspace_bytes, int32_t num_sms,
+                              int32_t *dev_status, void *stream) {
+    return attn_call(q, nullptr, nullptr, k_cache, v_cache, block_table, max_pages_per_req,
+                     num_pages, seq_lens, max_ctx_len, bs, B, Hq, Hkv, D, page_size,
+                     softmax_scale, mode, out, lse, workspace, workspace_bytes, num_sms,
+                     dev_status, stream);
+}
+
+int32_t bdsa_block_attn_paged_append(const bdsa_bf16 *q, const bdsa_bf16 *k_new,
+                                     const bdsa_bf16 *v_new, bdsa_bf16 *k_cache,
+                                     bdsa_bf16 *v_cache, const int32_t *block_table,
+                                     int32_t max_pages_per_req, int32_t num_pages,
+                                     const int32_t *seq_lens, int32_t max_ctx_len, int32_t bs,
+                                     int32_t B, int32_t Hq, int32_t Hkv, int32_t D,
+                                     int32_t page_size, float softmax_scale, int32_t mode,
+                                     bdsa_bf16 *out, float *lse, void *workspace,
+                                     size_t workspace_bytes, int32_t num_sms, int32_t *dev_status,
+                                     void *stream) {
+    if (bs > 0 && (!k_new || !v_new)) return BDSA_INVALID_ARG;
+    return attn_call(q, k_new, v_new, k_cache, v_cache, block_table, max_pages_per_req, num_pages,
+                     seq_lens, max_ctx_len, bs, B, Hq, Hkv, D, page_size, softmax_scale, mode,
+                     out, lse, workspace, workspace_bytes, num_sms, dev_status, stream);
 }
 
 size_t bdsa_spec_accept_workspace_bytes(int32_t bs, int32_t B, int32_t V, int32_t num_sms) {

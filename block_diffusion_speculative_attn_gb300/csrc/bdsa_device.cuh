@@ -91,6 +91,35 @@ __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, volatil
     }
 }
 
+// Adds v to a shared-memory counter with release semantics (this thread's
+// earlier writes are visible to a thread that reads the sum with acquire).
+__device__ __forceinline__ void red_release_add_shared(int *p, int v) {
+    asm volatile("red.release.cta.shared::cta.add.s32 [%0], %1;" ::"r"(smem_u32(p)), "r"(v)
+                 : "memory");
+}
+
+__device__ __forceinline__ int ld_acquire_shared(const int *p) {
+    int v;
+    asm volatile("ld.acquire.cta.shared::cta.b32 %0, [%1];" : "=r"(v) : "r"(smem_u32(p)) : "memory");
+    return v;
+}
+
+// Waits until the shared counter *p reaches target; bounded like mbar_wait.
+__device__ __forceinline__ bool wait_counter_geq(const int *p, int target, volatile int *abort,
+                                                 int32_t *dev_status) {
+    if (ld_acquire_shared(p) >= target) return true;
+    const uint64_t t0 = global_timer_ns();
+    while (true) {
+        if (ld_acquire_shared(p) >= target) return true;
+        if (*abort) return false;
+        if (global_timer_ns() - t0 > kWaitLimitNs) {
+            *abort = 1;
+            report_status(dev_status, BDSA_DEVICE_TIMEOUT);
+            return false;
+        }
+    }
+}
+
 // Drain-time wait: ignores *abort, still bounded.
 __device__ __forceinline__ bool mbar_wait_drain(uint32_t bar, uint32_t parity) {
     const uint64_t t0 = global_timer_ns();
@@ -101,6 +130,11 @@ __device__ __forceinline__ bool mbar_wait_drain(uint32_t bar, uint32_t parity) {
 }
 
 // ---------------------------------------------------------------- fences
+// Orders this thread's generic-proxy global writes before its (or, after a
+// barrier, another thread's) later async-proxy accesses such as TMA loads.
+__device__ __forceinline__ void fence_proxy_async_global() {
+    asm volatile("fence.proxy.async.global;" ::: "memory");
+}
 __device__ __forceinline__ void fence_proxy_async_smem() {
     asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
 }

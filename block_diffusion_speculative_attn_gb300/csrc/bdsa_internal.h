@@ -25,6 +25,7 @@ AttnPlan attn_plan(int bs, int B, int Hq, int Hkv, int D, int max_ctx_len, int n
 
 struct AttnArgs {
     const uint16_t *q, *k_cache, *v_cache;
+    const uint16_t *k_new, *v_new;  // fused append (bdsa_block_attn_paged_append), or null
     const int32_t *block_table, *seq_lens;
     int max_pages, num_pages, max_ctx_len, bs, B, Hq, Hkv, D, page_size, mode, num_sms;
     float scale;

@@ -55,10 +55,12 @@ namespace {
 
 constexpr int kBN = 128;                  // keys per tile
 constexpr int kThreads = 224;
+constexpr int kThreadsAppend = 256;       // + the append warp
 constexpr int kKProducerWarp = 4;
 constexpr int kMmaWarp = 5;
 constexpr int kVProducerWarp = 6;
 constexpr int kSoftmaxWarps = 4;
+constexpr int kAppendWarp = 7;
 constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kTmemO = 256;          // S at columns 0 / 128, O at 256 / 384
 constexpr float kRescaleLog2 = 8.0f;      // rescale O only when the max grows by > 2^8
@@ -129,6 +131,15 @@ struct Params {
     float scale_log2;
 };
 
+// The fused append's buffers, a kernel argument of their own (left out of
+// Params, which the merge kernel shares).
+struct AppendParams {
+    const uint16_t *k_new;   // the block's own keys / values, [bs * B, Hkv, D]
+    const uint16_t *v_new;
+    uint16_t *k_cache;       // the caches they are written into
+    uint16_t *v_cache;
+};
+
 __device__ __forceinline__ void st_shared_v4(uint32_t addr, uint32_t a, uint32_t b, uint32_t c,
                                              uint32_t d) {
     asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(a), "r"(b), "r"(c),
@@ -180,6 +191,7 @@ struct Sched {
     long long cu0;           // its cost offset
     long long x0, x1, W, Wc;
     long long wsum[8];       // per-warp partial sums of the scan (<= 256 threads)
+    int appended;            // attention with the fused append: 32 x pieces whose rows are written
 };
 static_assert(sizeof(Sched) <= 144, "the attention kernel keeps Sched in 144 bytes");
 
@@ -321,13 +333,57 @@ __device__ __forceinline__ int boxes_of(long n_keys, long t0, int rows_box, int 
     return nbox;
 }
 
-template <int D, int M>
-__global__ void __launch_bounds__(kThreads, 1)
+// Fused append, one warp: the block's own keys and values of request r, KV
+// head h at positions [p_lo, p_hi) -- the part of L..L+B-1 inside one piece of
+// the schedule -- go to their cache slots (slot = page * ps + position % ps
+// from the request's block-table row).  Rows on a page id outside the pool, or
+// past the block-table row, are not written.  Each lane keeps kU 16-byte
+// pieces of K and of V in flight.
+template <int D>
+__device__ void append_piece_rows(const Params &prm, const AppendParams &app, const int32_t *bt,
+                                  int r, int h, long L, long t_lo, long t_hi, int lane) {
+    const long p_lo = max(t_lo, L), p_hi = min(t_hi, L + prm.B);
+    if (L < 0 || p_lo >= p_hi) return;
+    constexpr int kChunks = D / 8;  // 16-byte pieces of one row
+    constexpr int kU = 4;
+    const int total = (int)(p_hi - p_lo) * kChunks;
+    for (int base = 0; base < total; base += 32 * kU) {
+        uint4 kv[kU], vv[kU];
+        long off[kU];
+#pragma unroll
+        for (int u = 0; u < kU; ++u) {
+            off[u] = -1;
+            const int idx = base + u * 32 + lane;
+            if (idx >= total) continue;
+            const long p = p_lo + idx / kChunks;
+            const int c = idx % kChunks;
+            const long src = (((long)r * prm.B + (p - L)) * prm.Hkv + h) * D + c * 8;
+            kv[u] = __ldg(reinterpret_cast<const uint4 *>(app.k_new + src));
+            vv[u] = __ldg(reinterpret_cast<const uint4 *>(app.v_new + src));
+            const long page = p >> prm.log2_ps;
+            if (page >= prm.max_pages) continue;
+            const int32_t pg = __ldg(bt + page);
+            if (pg < 0 || pg >= prm.num_pages) continue;
+            const long slot = (long)pg * prm.page_size + (p & (prm.page_size - 1));
+            off[u] = (slot * prm.Hkv + h) * D + c * 8;
+        }
+#pragma unroll
+        for (int u = 0; u < kU; ++u) {
+            if (off[u] < 0) continue;
+            *reinterpret_cast<uint4 *>(app.k_cache + off[u]) = kv[u];
+            *reinterpret_cast<uint4 *>(app.v_cache + off[u]) = vv[u];
+        }
+    }
+}
+
+template <int D, int M, bool kAppend>
+__global__ void __launch_bounds__(kAppend ? kThreadsAppend : kThreads, 1)
     block_attn_kernel(const __grid_constant__ CUtensorMap tm_q,
                       const __grid_constant__ CUtensorMap tm_k,
                       const __grid_constant__ CUtensorMap tm_v,
                       const __grid_constant__ CUtensorMap tm_out,
-                      const __grid_constant__ CUtensorMap tm_part, const Params prm) {
+                      const __grid_constant__ CUtensorMap tm_part, const Params prm,
+                      const AppendParams app) {
     using C = Cfg<D, M>;
     extern __shared__ uint8_t smem_raw[];
     const uint32_t raw = smem_u32(smem_raw);
@@ -336,6 +392,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int B = prm.B, G = prm.G;
     const long ps = prm.page_size;
+    constexpr int NT = kAppend ? kThreadsAppend : kThreads;
 
     auto bar = [&](int i) -> uint32_t { return sbase + C::kOffBar + 8u * (uint32_t)i; };
     Sched *sch = reinterpret_cast<Sched *>(smem + C::kOffMisc);
@@ -373,6 +430,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         mbar_init(bar(C::ER), 1);
         mbar_init(bar(C::DR), 1);
         *abort_flag = 0;
+        sch->appended = 0;
         fence_mbarrier_init();
     }
     if (warp == kKProducerWarp && lane == 0) {
@@ -383,7 +441,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     // Zero the padding rows of every Q buffer so padded S rows stay finite.
     if (prm.rows < M) {
         const int pad = M - prm.rows;
-        for (int idx = tid; idx < C::NQ * C::DH * pad * 8; idx += kThreads) {
+        for (int idx = tid; idx < C::NQ * C::DH * pad * 8; idx += NT) {
             const int u = idx & 7;
             const int m = prm.rows + (idx >> 3) % pad;
             const int slab = (idx >> 3) / pad;  // qbuf * DH + c
@@ -412,7 +470,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (lane < 24 && r >= 0 && r < prm.bs && e < prm.max_pages)
             asm volatile("prefetch.global.L2 [%0];" ::"l"(prm.block_table + r * prm.max_pages + e));
     }
-    schedule<kThreads>(prm, b, S, sch);
+    schedule<NT>(prm, b, S, sch);
     const long x0 = sch->x0, x1 = sch->x1;
     Cursor cur0;
     if (x0 < x1) {
@@ -455,8 +513,16 @@ __global__ void __launch_bounds__(kThreads, 1)
                 }
                 const long n_keys = (long)pc.L + B;
                 const int32_t *bt = prm.block_table + (long)pc.r * prm.max_pages;
+                // With the fused append, the first tile holding the block's
+                // own rows waits until the append warp has written this piece.
+                const int j_app = (kAppend && pc.L >= 0) ? max(pc.a, pc.L / kBN) : pc.e;
                 for (int j = pc.a; j < pc.e; ++j, ++g) {
                     const long t0 = (long)j * kBN;
+                    if (kAppend && j == j_app) {
+                        ok = wait_counter_geq(&sch->appended, 32 * (k + 1), abort_flag,
+                                              prm.dev_status);
+                        if (!ok) break;
+                    }
                     const int nbox = boxes_of(n_keys, t0, rows_box, prm.log2_ps, prm.max_pages);
                     // look the pages up before waiting for the stage
                     int32_t slot[kMaxBoxes];
@@ -587,6 +653,21 @@ __global__ void __launch_bounds__(kThreads, 1)
             // Drain: every MMA issued above has completed before TMEM is released.
             umma_commit(bar(C::DR));
             mbar_wait_drain(bar(C::DR), 0);
+        }
+    } else if (kAppend && warp == kAppendWarp) {
+        // ------------------------------------------------ fused append
+        // Walks the CTA's pieces ahead of the producers: writes each piece's
+        // block rows, fences them against the async proxy and counts the piece
+        // (a release per lane) for the producers' TMA loads.
+        Cursor cur = cur0;
+        for (long x = x0; x < x1;) {
+            const Piece pc = piece_at(cur, x, x1);
+            append_piece_rows<D>(prm, app, prm.block_table + (long)pc.r * prm.max_pages, pc.r,
+                                 pc.h, pc.L, (long)pc.a * kBN, (long)pc.e * kBN, lane);
+            fence_proxy_async_global();
+            red_release_add_shared(&sch->appended, 1);
+            x += pc.e - pc.a;
+            if (pc.e == pc.nt) next_unit(cur, prm);
         }
     } else if (warp < kSoftmaxWarps) {
         // ------------------------------------------------ softmax + epilogue
@@ -952,8 +1033,12 @@ constexpr int kMergeThreads = 256;
 constexpr int kMergeTPR = 4;      // threads per row
 constexpr int kMergeSlots = 16;   // piece slots listed in shared memory
 
+// At most 64 registers a thread (launch bound of 4 CTAs an SM): two merge warps
+// must fit on each SM sub-partition beside two attention warps, so that the
+// merge CTAs become resident, and compute the schedule, while the attention
+// grid still runs.
 template <int D>
-__global__ void __launch_bounds__(kMergeThreads) attn_merge_kernel(const Params prm) {
+__global__ void __launch_bounds__(kMergeThreads, 4) attn_merge_kernel(const Params prm) {
     __shared__ Sched sch;
     __shared__ int s_slot[kMergeSlots];
     __shared__ int s_np;
@@ -1175,16 +1260,23 @@ int launch_impl(const AttnArgs &a, const AttnPlan &plan, cudaStream_t stream) {
     prm.mode = a.mode;
     prm.scale_log2 = a.scale * 1.4426950408889634f;
     prm.magic_S = UINT64_MAX / (uint64_t)plan.grid;
-    static bool attr_set = false;  // per (D, M) instantiation
-    if (!attr_set) {
-        if (cudaFuncSetAttribute(block_attn_kernel<D, M>,
-                                 cudaFuncAttributeMaxDynamicSharedMemorySize,
+    AppendParams app;
+    app.k_new = a.k_new;
+    app.v_new = a.v_new;
+    app.k_cache = const_cast<uint16_t *>(a.k_cache);
+    app.v_cache = const_cast<uint16_t *>(a.v_cache);
+    const bool append = a.k_new != nullptr;
+    auto kernel = append ? block_attn_kernel<D, M, true> : block_attn_kernel<D, M, false>;
+    static bool attr_set[2] = {false, false};  // per instantiation
+    if (!attr_set[append]) {
+        if (cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                  C::kSmem) != cudaSuccess)
             return BDSA_CUDA_ERROR;
-        attr_set = true;
+        attr_set[append] = true;
     }
-    if (launch_pdl(block_attn_kernel<D, M>, dim3(plan.grid), dim3(kThreads), C::kSmem, stream,
-                   tq, tk, tv, tout, tpart, prm) != cudaSuccess)
+    if (launch_pdl(kernel, dim3(plan.grid), dim3(append ? kThreadsAppend : kThreads), C::kSmem,
+                   stream, tq, tk, tv, tout,
+                   tpart, prm, app) != cudaSuccess)
         return BDSA_CUDA_ERROR;
     if (launch_pdl(attn_merge_kernel<D>, dim3(plan.grid), dim3(kMergeThreads), 0, stream,
                    prm) != cudaSuccess)

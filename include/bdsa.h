@@ -150,6 +150,42 @@ int32_t bdsa_block_attn_paged(const bdsa_bf16 *q, const bdsa_bf16 *k_cache,
                               int32_t *dev_status, void *stream);
 
 /* ------------------------------------------------------------------------ */
+/* bdsa_block_attn_paged_append
+ *
+ * "From DFlash to dLLM Self-Spec (II)", section 2.2.2 (the prepare step builds
+ * the block's positions and the cache locations its K/V go to) and section
+ * 2.2.4 (the verify forward over the block): the block's own keys and values
+ * are written into the paged cache in the same launch as the block attention
+ * that reads them, instead of by a separate write before it.
+ *
+ * k_new, v_new  [bs*B, Hkv, D] bf16: the block's keys (post-RoPE) and values,
+ *          row r*B + i for position L_r + i.
+ * For every r, i < B and KV head h:
+ *   k_cache[slot, h, :] = k_new[r*B + i, h, :] and likewise v, with
+ *   slot = block_table[r, (L_r+i)/ps] * ps + (L_r+i) % ps (the slot
+ *   bdsa_prepare_block's cache_loc names); then the attention is exactly
+ *   that of bdsa_block_attn_paged on the updated caches.
+ * A position whose page is past max_pages_per_req or outside [0, num_pages) is
+ * not written (the request's output is zeros as in bdsa_block_attn_paged);
+ * nothing else in the caches changes.  Each new row is written by the CTA
+ * whose share of the schedule holds it (by a warp of its own, before that
+ * tile's load), so it is read back from the cache in the same launch.  No
+ * other work may read or write the block's cache slots during the call.
+ * Everything else (arguments, schedule, workspace, launches, errors) is as in
+ * bdsa_block_attn_paged; k_new and v_new must be 16-byte aligned.
+ */
+int32_t bdsa_block_attn_paged_append(const bdsa_bf16 *q, const bdsa_bf16 *k_new,
+                                     const bdsa_bf16 *v_new, bdsa_bf16 *k_cache,
+                                     bdsa_bf16 *v_cache, const int32_t *block_table,
+                                     int32_t max_pages_per_req, int32_t num_pages,
+                                     const int32_t *seq_lens, int32_t max_ctx_len, int32_t bs,
+                                     int32_t B, int32_t Hq, int32_t Hkv, int32_t D,
+                                     int32_t page_size, float softmax_scale, int32_t mode,
+                                     bdsa_bf16 *out, float *lse, void *workspace,
+                                     size_t workspace_bytes, int32_t num_sms, int32_t *dev_status,
+                                     void *stream);
+
+/* ------------------------------------------------------------------------ */
 /* bdsa_spec_accept
  *
  * "From DFlash to dLLM Self-Spec (IV)", section 4.3.1: a draft token is

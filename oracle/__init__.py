@@ -10,6 +10,8 @@ source pages' definitions:
   section 2.2.2; "... (IV)", section 4.4.1 (block init).
 * block attention masks -- "SGLang dLLM / LLaDA 2.0", section "Attention Mask";
   "... (IV)", section 4.4.1 (causal verify over the past KV).
+* the block's own K/V appended to the paged cache -- "... (II)", sections 2.2.2
+  and 2.2.4 (numpy indexing in this module).
 * acceptance -- "... (IV)", section 4.3.1 (min(1, p/q), correction token);
   "Unlocking Lossless Speedups in LLMs via Discrete Diffusion", background on
   speculative decoding and the Psi-Spec step (longest accepted prefix, residual
@@ -123,6 +125,42 @@ def block_attn(q_bits, k_bits, v_bits, block_table, seq_lens, B, Hq, Hkv, D, pag
     if bad:
         raise ValueError(f"oracle: {bad} rows referenced out-of-range pages")
     return out, lse
+
+
+def append_block_kv(k_bits, v_bits, k_new_bits, v_new_bits, block_table, seq_lens, B, page_size,
+                    num_pages=None):
+    """The block's own keys and values written into copies of the caches.
+
+    "From DFlash to dLLM Self-Spec (II)", sections 2.2.2 and 2.2.4: row r*B + i of
+    k_new / v_new ([bs*B, Hkv, D]) is position L_r + i of request r and goes to
+    slot block_table[r, (L_r+i) // ps] * ps + (L_r+i) % ps of every KV head.  A
+    position whose page is past the block-table row or outside [0, num_pages) is
+    not written, nor is any position of a request with L_r < 0.
+    Returns (k_bits', v_bits') as new arrays.
+    """
+    k_out = np.array(k_bits, copy=True)
+    v_out = np.array(v_bits, copy=True)
+    bt = np.asarray(block_table)
+    sl = np.asarray(seq_lens)
+    bs, max_pages = bt.shape
+    if num_pages is None:
+        num_pages = k_out.shape[0] // page_size
+    for r in range(bs):
+        L = int(sl[r])
+        if L < 0:
+            continue
+        for i in range(B):
+            t = L + i
+            page = t // page_size
+            if page >= max_pages:
+                continue
+            pg = int(bt[r, page])
+            if pg < 0 or pg >= num_pages:
+                continue
+            slot = pg * page_size + t % page_size
+            k_out[slot] = k_new_bits[r * B + i]
+            v_out[slot] = v_new_bits[r * B + i]
+    return k_out, v_out
 
 
 def spec_accept(block_ids, p, q, u_acc, u_samp, seq_lens, *, p_strides=None, q_strides=None,
