@@ -41,11 +41,11 @@ from block_diffusion_speculative_attn_gb300 import workloads as wl  # noqa: E402
 METRIC = "draft/verify block-attn query tokens/s + % HBM roofline; accept rows/s"
 # DRAM bytes (read + write) of one attention call on the Qwen3-8B-shaped verify
 # batch, from one ncu capture of each of its two kernels (summary and commands
-# in profiles/qwen3_8b_verify_step_ncu.md): attention 308.42 + 5.03 MB, merge
+# in profiles/qwen3_8b_verify_step_ncu.md): attention 308.41 + 4.63 MB, merge
 # 8.79 MB (cold under ncu; L2 hits in the timed step).  Valid only for the
 # kernel sources it was taken on: reported as null once they change.
-ATTN_TRAFFIC = {"workload": "qwen3_8b_verify", "bytes_per_call": 322.24e6,
-                "sources_sha256": "b88068f1483fca1b91658d037d3eee30705bb234e47c0fbe2fe017cf7bb532c1"}
+ATTN_TRAFFIC = {"workload": "qwen3_8b_verify", "bytes_per_call": 321.83e6,
+                "sources_sha256": "5a15aa5d3a57e2dacc8c9b3da4c4c24613ca7d99cc3519161d8d480c71bcf9c4"}
 ATTN_SOURCES = ("block_diffusion_speculative_attn_gb300/csrc/block_attn.cu",
                 "block_diffusion_speculative_attn_gb300/csrc/bdsa_device.cuh")
 L2_FLUSH_BYTES = 512 << 20  # > 129 MB L2
