@@ -12,6 +12,9 @@ source pages' definitions:
   "... (IV)", section 4.4.1 (causal verify over the past KV).
 * the block's own K/V appended to the paged cache -- "... (II)", sections 2.2.2
   and 2.2.4 (numpy indexing in this module).
+* I-DLM Block-N round -- "... (IV)", sections 4.3 and 4.3.1 (2N-1 layout,
+  verify of the carried specs, correction / bonus, new specs from the MASK
+  slots) and 4.6 (KV trim, the request's advance).
 * acceptance -- "... (IV)", section 4.3.1 (min(1, p/q), correction token);
   "Unlocking Lossless Speedups in LLMs via Discrete Diffusion", background on
   speculative decoding and the Psi-Spec step (longest accepted prefix, residual
@@ -63,6 +66,12 @@ def _load():
         lib.oracle_spec_accept.argtypes = [P, P, i64, i64, P, i64, i64, P, P, P, i32, i32, i32,
                                            P, P, P, P, P, P, i32]
         lib.oracle_spec_accept.restype = None
+        lib.oracle_idlm_prepare.argtypes = [P, P, P, P, P, i32, i32, i32, i32, i32, i32, P, P,
+                                            P]
+        lib.oracle_idlm_prepare.restype = i32
+        lib.oracle_idlm_accept.argtypes = [P, P, P, i64, i64, P, i64, i64, P, P, P, P, i32, i32,
+                                           i32, P, P, P, P, P, P, P, P, P, P, i32]
+        lib.oracle_idlm_accept.restype = None
         lib.oracle_inv_cdf.argtypes = [P, i32, f64, P]
         lib.oracle_inv_cdf.restype = i32
         lib.oracle_max_threads.argtypes = []
@@ -195,6 +204,62 @@ def spec_accept(block_ids, p, q, u_acc, u_samp, seq_lens, *, p_strides=None, q_s
                            _ptr(seq_lens), bs, B, V, _ptr(out["accept_len"]),
                            _ptr(out["commit_len"]), _ptr(out["out_tokens"]),
                            _ptr(out["bonus_id"]), _ptr(out["new_seq_lens"]), _ptr(out["flags"]),
+                           int(nthreads))
+    return out
+
+
+def idlm_prepare(pending, specs, mode, seq_lens, block_table, num_pages, N, page_size,
+                 mask_token_id):
+    """I-DLM Block-N layout of 2N-1 slots.  specs: [bs, N-1] (read in verify
+    mode only).  Returns (block_ids, positions, cache_loc, n_out_of_range)."""
+    lib = _load()
+    pending = _c(pending, np.int32)
+    mode = _c(mode, np.int32)
+    seq_lens = _c(seq_lens, np.int32)
+    block_table = _c(block_table, np.int32)
+    bs, max_pages = block_table.shape
+    specs = _c(specs, np.int32).reshape(bs, max(N - 1, 0))
+    blk = 2 * N - 1
+    out = [np.empty((bs, blk), np.int32) for _ in range(3)]
+    bad = lib.oracle_idlm_prepare(_ptr(pending), _ptr(specs), _ptr(mode), _ptr(seq_lens),
+                                  _ptr(block_table), max_pages, num_pages, bs, N, page_size,
+                                  mask_token_id, *[_ptr(o) for o in out])
+    return out[0], out[1], out[2], int(bad)
+
+
+IDLM_KEYS = ("accept_len", "n_out", "next_mode", "next_pending", "next_q_slot",
+             "new_seq_lens", "kv_keep")
+
+
+def idlm_accept(block_ids, mode, p, q_prev, q_slot, u_acc, u_samp, seq_lens, N, *,
+                p_strides=None, q_strides=None, V=None, nthreads=1):
+    """I-DLM verify / sample / trim step.  p, q_prev: fp32 [bs, 2N-1, V] (or
+    addressed through the strides); u_acc [bs, N-1], u_samp [bs, N].  Returns
+    a dict of int32 arrays: IDLM_KEYS [bs], out_tokens [bs, N], next_specs
+    [bs, N-1], flags [bs]."""
+    lib = _load()
+    block_ids = _c(block_ids, np.int32)
+    bs, blk = block_ids.shape
+    assert blk == 2 * N - 1
+    p = np.ascontiguousarray(p, dtype=np.float32)
+    q_prev = np.ascontiguousarray(q_prev, dtype=np.float32)
+    if V is None:
+        V = p.shape[-1]
+    if p_strides is None:
+        p_strides = (blk * V, V)
+    if q_strides is None:
+        q_strides = (blk * V, V)
+    out = {k: np.empty(bs, np.int32) for k in IDLM_KEYS + ("flags",)}
+    out["out_tokens"] = np.empty((bs, N), np.int32)
+    out["next_specs"] = np.empty((bs, max(N - 1, 0)), np.int32)
+    lib.oracle_idlm_accept(_ptr(block_ids), _ptr(_c(mode, np.int32)), _ptr(p), p_strides[0],
+                           p_strides[1], _ptr(q_prev), q_strides[0], q_strides[1],
+                           _ptr(_c(q_slot, np.int32)), _ptr(_c(u_acc, np.float32)),
+                           _ptr(_c(u_samp, np.float32)), _ptr(_c(seq_lens, np.int32)), bs, N, V,
+                           _ptr(out["accept_len"]), _ptr(out["n_out"]), _ptr(out["out_tokens"]),
+                           _ptr(out["next_mode"]), _ptr(out["next_pending"]),
+                           _ptr(out["next_specs"]), _ptr(out["next_q_slot"]),
+                           _ptr(out["new_seq_lens"]), _ptr(out["kv_keep"]), _ptr(out["flags"]),
                            int(nthreads))
     return out
 

@@ -9,7 +9,9 @@
  *
  *   [P1] "From DFlash to dLLM Self-Spec (IV): Self-Spec dLLM & AR Uni-Model",
  *        sections 4.3.1 (p/q acceptance) and 4.4.1 (LinearSpec block init,
- *        causal verify, greedy longest-prefix loop with bonus).
+ *        causal verify, greedy longest-prefix loop with bonus); sections 4.3,
+ *        4.3.1 and 4.6 for the I-DLM Block-N round (2N-1 layout, verify of
+ *        the carried specs, new specs from the MASK positions, KV trim).
  *   [P2] "Unlocking Lossless Speedups in LLMs via Discrete Diffusion",
  *        background on speculative decoding / rejection sampling and the
  *        Psi-Spec sampling step (first token always accepted, longest
@@ -346,6 +348,182 @@ void oracle_spec_accept(const int32_t *block_ids, const float *p, int64_t p_stri
                 out_tokens[(long)r * B + i] = v;
             }
             bonus_id[r] = token;
+            new_seq_lens[r] = seq_lens[r] + a + 1;
+            if (flags) flags[r] = flag;
+        }
+        free(w);
+    }
+}
+
+/* ------------------------------------------------------------------------ */
+/* I-DLM Block-N round  [P1 4.3 (ISD: the specs drawn from MASK positions in
+ * round t are verified in round t+1 against the causal view), 4.3.1 (the
+ * Block-N layouts, p/q acceptance with a correction token, MASK KV freed
+ * after the forward), 4.6 (KV trim info and the request's advance)]
+ *
+ * A round has blk = 2N-1 block slots per request.  Slot j's logits predict
+ * the token at slot j+1 (the causal view with a logit shift), p[r, j] being
+ * their distribution.
+ *   verify (mode 1): [pending, spec_0 .. spec_{N-2}, M x (N-1)]
+ *   cold   (mode 0): [pending, M x (2N-2)]
+ * idlm_prepare writes that layout, positions L_r + j and cache_loc exactly as
+ * prepare_block does for a block of blk slots.  Any mode other than 1 is laid
+ * out as a cold start.
+ */
+int oracle_idlm_prepare(const int32_t *pending, const int32_t *specs, const int32_t *mode,
+                        const int32_t *seq_lens, const int32_t *block_table,
+                        int max_pages_per_req, int num_pages, int bs, int N, int page_size,
+                        int mask_token_id, int32_t *block_ids, int32_t *positions,
+                        int32_t *cache_loc) {
+    const int blk = 2 * N - 1;
+    int bad = 0;
+    for (int r = 0; r < bs; ++r) {
+        for (int j = 0; j < blk; ++j) {
+            int32_t id = mask_token_id;
+            if (j == 0) id = pending[r];
+            else if (mode[r] == 1 && j <= N - 1) id = specs[(long)r * (N - 1) + (j - 1)];
+            long pos = (long)seq_lens[r] + j;
+            block_ids[(long)r * blk + j] = id;
+            positions[(long)r * blk + j] = (int32_t)pos;
+            long page_idx = pos / page_size;
+            int32_t loc = -1;
+            if (seq_lens[r] >= 0 && page_idx < max_pages_per_req) {
+                int32_t page = block_table[(long)r * max_pages_per_req + page_idx];
+                if (page >= 0 && page < num_pages)
+                    loc = (int32_t)((long)page * page_size + pos % page_size);
+            }
+            if (loc < 0) ++bad;
+            cache_loc[(long)r * blk + j] = loc;
+        }
+    }
+    return bad;
+}
+
+/* The verify / sample / trim step of the round, stochastic.
+ *
+ * q_prev[r, q_slot[r] + k] is the distribution spec_k was drawn from in the
+ * previous round (its p rows, kept by the caller); strides in elements.
+ * verify (mode 1):
+ *   spec_k (slot k+1) is tested against p[r, k]: accept iff
+ *     u_acc[r, k] < min(1, p[k][s] / q_prev[q_slot + k][s])   (fp32 ratio;
+ *     q == 0 accepts iff p > 0; an id outside [0, V) is rejected, flag bit 3)
+ *   a = leading accepted specs.
+ *   a < N-1: anchor = InvCDF(max(0, p[a] - q_prev[q_slot + a]), u_samp[r, 0])
+ *            (from p[a] if that has no mass, flag bit 2); no new specs; next
+ *            round is a cold start.
+ *   a = N-1: anchor = InvCDF(p[N-1], u_samp[r, 0]) (the bonus); new specs
+ *            spec'_j = InvCDF(p[N + j], u_samp[r, 1 + j]), j < N-1 (the MASK
+ *            slots N..2N-2 predict the slots after the bonus); next round
+ *            verifies them against q_slot' = N.
+ * cold (mode 0, and mode 1 with q_slot outside [0, N], flag bit 5):
+ *   a = 0; anchor = InvCDF(p[0], u_samp[r, 0]); spec'_j = InvCDF(p[1 + j],
+ *   u_samp[r, 1 + j]); q_slot' = 1.
+ * The KV rows kept are the pending token's and the accepted specs' (kv_keep =
+ * a + 1 block rows from slot 0; every MASK row and rejected spec row, i.e.
+ * cache_loc[r, kv_keep:], is freed); new_seq_lens = L + kv_keep.  The emitted
+ * tokens are the accepted specs then the anchor (n_out = a + 1, -1 padding
+ * to N); the anchor is the next round's pending token.  next_specs holds -1
+ * and next_q_slot -1 when the next round is a cold start.  Any mode other
+ * than 0 or 1 is a cold start with flag bit 6.
+ * Flags as in oracle_spec_accept: bit 0 a tested ratio within 1e-6 of u, bit 1
+ * a draw within 1e-9 * S of a boundary (any of the draws).
+ */
+void oracle_idlm_accept(const int32_t *block_ids, const int32_t *mode, const float *p,
+                        int64_t p_stride_r, int64_t p_stride_i, const float *q_prev,
+                        int64_t q_stride_r, int64_t q_stride_i, const int32_t *q_slot,
+                        const float *u_acc, const float *u_samp, const int32_t *seq_lens, int bs,
+                        int N, int V, int32_t *accept_len, int32_t *n_out, int32_t *out_tokens,
+                        int32_t *next_mode, int32_t *next_pending, int32_t *next_specs,
+                        int32_t *next_q_slot, int32_t *new_seq_lens, int32_t *kv_keep,
+                        int32_t *flags, int nthreads) {
+    const int blk = 2 * N - 1;
+#ifdef _OPENMP
+    if (nthreads < 1) nthreads = 1;
+#pragma omp parallel num_threads(nthreads)
+#endif
+    {
+        float *w = (float *)malloc(sizeof(float) * (size_t)V);
+#ifdef _OPENMP
+#pragma omp for schedule(static)
+#endif
+        for (int r = 0; r < bs; ++r) {
+            int flag = 0;
+            const int32_t *ids = block_ids + (long)r * blk;
+            const float *prow = p + (long)r * p_stride_r;
+            int verify = mode[r] == 1;
+            if (mode[r] != 0 && mode[r] != 1) flag |= 64;
+            if (verify && (q_slot[r] < 0 || q_slot[r] > N)) {
+                verify = 0;
+                flag |= 32;
+            }
+            int a = 0, anchor, near = 0;
+            int draw_specs;   /* slot of p holding spec'_0's distribution, or -1 */
+            if (verify) {
+                const float *qrow = q_prev + (long)r * q_stride_r + (long)q_slot[r] * q_stride_i;
+                for (int k = 0; k < N - 1; ++k) {
+                    int s = ids[1 + k];
+                    if (s < 0 || s >= V) {
+                        flag |= 8;
+                        break;
+                    }
+                    float pv = prow[(long)k * p_stride_i + s];
+                    float qv = qrow[(long)k * q_stride_i + s];
+                    float u = u_acc[(long)r * (N - 1) + k];
+                    int acc;
+                    if (qv == 0.0f) {
+                        acc = pv > 0.0f;
+                    } else {
+                        volatile float ratio = pv / qv; /* fp32, correctly rounded */
+                        acc = u < fminf(1.0f, ratio);
+                        if (fabs((double)ratio - (double)u) < 1e-6) flag |= 1;
+                    }
+                    if (!acc) break;
+                    ++a;
+                }
+                if (a < N - 1) {
+                    const float *pa = prow + (long)a * p_stride_i;
+                    const float *qa = qrow + (long)a * q_stride_i;
+                    double S = 0.0;
+                    for (int k = 0; k < V; ++k) {
+                        float d = pa[k] - qa[k];
+                        w[k] = d > 0.0f ? d : 0.0f;
+                        S += (double)w[k];
+                    }
+                    if (!(S > 0.0)) {
+                        flag |= 4;
+                        for (int k = 0; k < V; ++k) w[k] = pa[k];
+                    }
+                    anchor = inv_cdf_f32w(w, V, (double)u_samp[(long)r * N], &near);
+                    draw_specs = -1;
+                } else {
+                    anchor = inv_cdf_f32w(prow + (long)(N - 1) * p_stride_i, V,
+                                          (double)u_samp[(long)r * N], &near);
+                    draw_specs = N;
+                }
+            } else {
+                anchor = inv_cdf_f32w(prow, V, (double)u_samp[(long)r * N], &near);
+                draw_specs = 1;
+            }
+            for (int j = 0; j < N - 1; ++j) {
+                int32_t t = -1;
+                if (draw_specs >= 0)
+                    t = inv_cdf_f32w(prow + (long)(draw_specs + j) * p_stride_i, V,
+                                     (double)u_samp[(long)r * N + 1 + j], &near);
+                next_specs[(long)r * (N - 1) + j] = t;
+            }
+            if (near) flag |= 2;
+            for (int i = 0; i < N; ++i) {
+                int32_t v = -1;
+                if (i < a) v = ids[1 + i];
+                else if (i == a) v = anchor;
+                out_tokens[(long)r * N + i] = v;
+            }
+            accept_len[r] = a;
+            n_out[r] = a + 1;
+            next_mode[r] = draw_specs >= 0 ? 1 : 0;
+            next_pending[r] = anchor;
+            next_q_slot[r] = draw_specs;
+            kv_keep[r] = a + 1;
             new_seq_lens[r] = seq_lens[r] + a + 1;
             if (flags) flags[r] = flag;
         }
