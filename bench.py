@@ -334,6 +334,70 @@ def time_fused_append(step: Step, flush, clean, iters: int = 20):
             "bytes_written": 2 * c.bs * c.B * c.Hkv * c.D * 2, "iters": iters}
 
 
+def idlm_bytes(mode: np.ndarray, accept_len: np.ndarray, N: int, V: int) -> int:
+    """Algorithmic bytes of one I-DLM round's acceptance: per request, the
+    gathered p / q pairs of the tested specs, then every distribution row a
+    draw reads: p and q_prev at a rejection (the residual), p alone for a bonus
+    or a cold start's clean token, and one p row per new spec drawn."""
+    total = 0
+    for m, a in zip(mode.tolist(), accept_len.tolist()):
+        if m == 1:
+            total += 2 * 4 * (a + 1 if a < N - 1 else N - 1)
+            rows = 2 if a < N - 1 else N
+        else:
+            rows = N
+        total += rows * V * 4
+    return total
+
+
+def time_idlm(cfg: wl.StepConfig, dev, flush, clean, N: int = 8, iters: int = 20):
+    """The I-DLM Block-N round at the workload's batch and vocabulary: layout
+    (idlm_prepare) and verify / correct / new-spec draws (idlm_accept), L2
+    flushed before each round; mean event times in ms."""
+    import block_diffusion_speculative_attn_gb300 as bdsa
+    x = wl.make_idlm_inputs(cfg, N=N, device=dev)
+    blk = 2 * N - 1
+    rng = np.random.default_rng(cfg.seed + 5)
+    table, num_pages = wl.paging_for(x.seq_lens.cpu().numpy(), blk, cfg.page_size, rng)
+    bt = torch.from_numpy(table).to(dev)
+    bs = cfg.bs
+    status = torch.zeros(1, dtype=torch.int32, device=dev)
+    prep = tuple(torch.empty((bs, blk), dtype=torch.int32, device=dev) for _ in range(3))
+    out = {k: torch.empty(bs, dtype=torch.int32, device=dev) for k in bdsa.IDLM_KEYS}
+    out["out_tokens"] = torch.empty((bs, N), dtype=torch.int32, device=dev)
+    out["next_specs"] = torch.empty((bs, N - 1), dtype=torch.int32, device=dev)
+    times = []
+    for i in range(iters + 3):
+        flush.zero_()
+        clean.sum()
+        ev = [torch.cuda.Event(enable_timing=True) for _ in range(3)]
+        ev[0].record()
+        bdsa.idlm_prepare(x.pending, x.specs, x.mode, x.seq_lens, bt, num_pages, N,
+                          cfg.page_size, cfg.mask_token_id, out=prep, dev_status=status)
+        ev[1].record()
+        bdsa.idlm_accept(prep[0], x.mode, x.p, x.q_prev, x.q_slot, x.u_acc, x.u_samp,
+                         x.seq_lens, N, out=out, dev_status=status)
+        ev[2].record()
+        if i >= 3:
+            times.append(ev)
+    torch.cuda.synchronize()
+    assert status.item() == 0, bdsa.STATUS.get(status.item())
+    round_ms = statistics.mean(e[0].elapsed_time(e[2]) for e in times)
+    acc_ms = statistics.mean(e[1].elapsed_time(e[2]) for e in times)
+    mode = x.mode.cpu().numpy()
+    a = out["accept_len"].cpu().numpy()
+    nbytes = idlm_bytes(mode, a, N, cfg.V)
+    hbm, _, src = peaks()
+    achieved = nbytes / (acc_ms / 1e3) / 1e9
+    return {"N": N, "slots": blk, "batch": bs, "vocab": cfg.V,
+            "verify_share": float(mode.mean()), "mean_accept_len": float(a[mode == 1].mean()),
+            "round_ms": round_ms, "accept_ms": acc_ms, "rows_per_s": bs / (acc_ms / 1e3),
+            "accept_roofline": {"bound": "hbm", "achieved": achieved, "peak": hbm,
+                                "unit": "GB/s", "frac": achieved / hbm, "peak_source": src,
+                                "algorithmic_bytes_per_launch": nbytes},
+            "gpu_launches_per_round": 2, "iters": iters}
+
+
 # ---------------------------------------------------------------------------
 def oracle_sample(cfg: wl.StepConfig, attn: wl.AttnInputs, acc, reqs, nthreads):
     """Host copies of the sampled requests' inputs (compact page pool)."""
@@ -543,6 +607,7 @@ def main(argv=None):
     if attn_ms is not None:
         fused_append = time_fused_append(step, flush, clean)
         assert step.status.item() == 0, bdsa.STATUS.get(step.status.item())
+    idlm = time_idlm(cfg, dev, flush, clean) if (cfg.V and attn_ms is not None) else None
 
     e2e = None
     if not args.no_e2e:
@@ -569,6 +634,7 @@ def main(argv=None):
             "accept_rows_per_s": (cfg.bs / (acc_ms / 1e3)) if acc_ms else None,
             "accept_ms": acc_ms,
             "fused_append": fused_append,
+            "idlm_round": idlm,
             "attn_flops_per_launch": attn_flops(cfg, step.attn.seq_lens, cfg.modes[-1]),
             "e2e": e2e, "cpu_baseline": cpu, "gpu_launches": step.launches * K,
             "clocks": clk}

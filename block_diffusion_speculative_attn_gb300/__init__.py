@@ -11,6 +11,8 @@ Calls (all asynchronous on the current stream):
   prepare_block     block ids / positions / cache slots of each request's block
   block_attn_paged  block attention over the paged cache, DRAFT or VERIFY mask
   spec_accept       lossless speculative acceptance (stochastic or greedy)
+  idlm_prepare      I-DLM Block-N layout of 2N-1 slots (pending, carried specs, masks)
+  idlm_accept       I-DLM Block-N verify / correct / draw-new-specs / KV-trim step
 """
 from __future__ import annotations
 
@@ -31,7 +33,8 @@ STATUS = {0: "BDSA_OK", 1: "BDSA_INVALID_ARG", 2: "BDSA_UNSUPPORTED", 3: "BDSA_M
 EXPORTS = ("bdsa_status_string", "bdsa_version", "bdsa_prepare_block",
            "bdsa_block_attn_workspace_bytes", "bdsa_block_attn_paged",
            "bdsa_block_attn_paged_append", "bdsa_spec_accept_workspace_bytes",
-           "bdsa_spec_accept", "bdsa_spec_accept_noalloc")
+           "bdsa_spec_accept", "bdsa_spec_accept_noalloc", "bdsa_idlm_prepare",
+           "bdsa_idlm_accept")
 
 _lib = None
 
@@ -75,6 +78,11 @@ def lib() -> ctypes.CDLL:
     L.bdsa_spec_accept_noalloc.argtypes = [P, P, i64, i64, P, i64, i64, P, P, P, i32, i32, i32,
                                            P, P, P, P, P, i32, P, P]
     L.bdsa_spec_accept_noalloc.restype = i32
+    L.bdsa_idlm_prepare.argtypes = [P, P, P, P, P, i32, i32, i32, i32, i32, i32, P, P, P, P, P]
+    L.bdsa_idlm_prepare.restype = i32
+    L.bdsa_idlm_accept.argtypes = [P, P, P, i64, i64, P, i64, i64, P, P, P, P, i32, i32, i32,
+                                   P, P, P, P, P, P, P, P, P, i32, P, P]
+    L.bdsa_idlm_accept.restype = i32
     _lib = L
     return L
 
@@ -234,4 +242,84 @@ def spec_accept(block_ids, p, q, u_acc, u_samp, seq_lens, *, p_strides=None, q_s
                                 _ptr(out["new_seq_lens"]), _ptr(workspace), ws_bytes, sms,
                                 _ptr(dev_status), _stream(dev))
     _check("bdsa_spec_accept", st)
+    return out
+
+
+# ---------------------------------------------------------------------------
+IDLM_KEYS = ("accept_len", "n_out", "next_mode", "next_pending", "next_q_slot",
+             "new_seq_lens", "kv_keep")
+
+
+def idlm_prepare(pending, specs, mode, seq_lens, block_table, num_pages: int, N: int,
+                 page_size: int, mask_token_id: int, out=None, dev_status=None):
+    """bdsa_idlm_prepare.  specs [bs, N-1] int32 (read in verify mode only).
+
+    Returns (block_ids, positions, cache_loc), int32 [bs, 2N-1].
+    """
+    _dev(pending, "pending", torch.int32)
+    _dev(mode, "mode", torch.int32)
+    _dev(seq_lens, "seq_lens", torch.int32)
+    _dev(block_table, "block_table", torch.int32)
+    if specs is not None:
+        _dev(specs, "specs", torch.int32)
+    bs, max_pages = block_table.shape
+    blk = 2 * N - 1
+    if out is None:
+        out = tuple(torch.empty((bs, blk), dtype=torch.int32, device=block_table.device)
+                    for _ in range(3))
+    for name, t in zip(("block_ids", "positions", "cache_loc"), out):
+        _dev(t, name, torch.int32)
+    specs_ptr = _ptr(specs) if specs is not None and specs.numel() > 0 else None
+    st = lib().bdsa_idlm_prepare(_ptr(pending), specs_ptr, _ptr(mode), _ptr(seq_lens),
+                                 _ptr(block_table), max_pages, num_pages, bs, N, page_size,
+                                 mask_token_id, _ptr(out[0]), _ptr(out[1]), _ptr(out[2]),
+                                 _ptr(dev_status), _stream(block_table.device))
+    _check("bdsa_idlm_prepare", st)
+    return out
+
+
+def idlm_accept(block_ids, mode, p, q_prev, q_slot, u_acc, u_samp, seq_lens, N: int, *,
+                p_strides=None, q_strides=None, V: int | None = None, out=None,
+                dev_status=None, sms: int = 0):
+    """bdsa_idlm_accept.  p, q_prev fp32 [bs, 2N-1, V] (or addressed through
+    the element strides (row, slot)); u_acc [bs, N-1], u_samp [bs, N].
+
+    Returns a dict of int32 tensors: IDLM_KEYS [bs], out_tokens [bs, N] and
+    next_specs [bs, N-1].
+    """
+    _dev(block_ids, "block_ids", torch.int32)
+    _dev(mode, "mode", torch.int32)
+    _dev(q_slot, "q_slot", torch.int32)
+    _dev(seq_lens, "seq_lens", torch.int32)
+    _dev(u_samp, "u_samp", torch.float32)
+    bs, blk = block_ids.shape
+    if blk != 2 * N - 1:
+        raise ValueError(f"block_ids has {blk} slots, want 2N-1 = {2 * N - 1}")
+    for name, t in (("p", p), ("q_prev", q_prev)):
+        if not (t.is_cuda and t.dtype == torch.float32):
+            raise TypeError(f"{name} must be a CUDA float32 tensor")
+    V = p.shape[-1] if V is None else V
+    if p_strides is None:
+        _dev(p, "p", torch.float32)
+        p_strides = (blk * V, V)
+    if q_strides is None:
+        _dev(q_prev, "q_prev", torch.float32)
+        q_strides = (blk * V, V)
+    if N > 1:
+        _dev(u_acc, "u_acc", torch.float32)
+    dev = block_ids.device
+    if out is None:
+        out = {k: torch.empty(bs, dtype=torch.int32, device=dev) for k in IDLM_KEYS}
+        out["out_tokens"] = torch.empty((bs, N), dtype=torch.int32, device=dev)
+        out["next_specs"] = torch.empty((bs, max(N - 1, 0)), dtype=torch.int32, device=dev)
+    ns = out["next_specs"]
+    st = lib().bdsa_idlm_accept(
+        _ptr(block_ids), _ptr(mode), _ptr(p), int(p_strides[0]), int(p_strides[1]),
+        _ptr(q_prev), int(q_strides[0]), int(q_strides[1]), _ptr(q_slot),
+        _ptr(u_acc) if N > 1 else None, _ptr(u_samp), _ptr(seq_lens), bs, N, V,
+        _ptr(out["accept_len"]), _ptr(out["n_out"]), _ptr(out["out_tokens"]),
+        _ptr(out["next_mode"]), _ptr(out["next_pending"]), _ptr(ns) if ns.numel() > 0 else None,
+        _ptr(out["next_q_slot"]), _ptr(out["new_seq_lens"]), _ptr(out["kv_keep"]), sms,
+        _ptr(dev_status), _stream(dev))
+    _check("bdsa_idlm_accept", st)
     return out

@@ -167,6 +167,73 @@ int32_t bdsa_block_attn_paged_append(const bdsa_bf16 *q, const bdsa_bf16 *k_new,
                      out, lse, workspace, workspace_bytes, num_sms, dev_status, stream);
 }
 
+int32_t bdsa_idlm_prepare(const int32_t *pending, const int32_t *specs, const int32_t *mode,
+                          const int32_t *seq_lens, const int32_t *block_table,
+                          int32_t max_pages_per_req, int32_t num_pages, int32_t bs, int32_t N,
+                          int32_t page_size, int32_t mask_token_id, int32_t *block_ids,
+                          int32_t *positions, int32_t *cache_loc, int32_t *dev_status,
+                          void *stream) {
+    if (bs < 0 || N < 1 || page_size < 1 || max_pages_per_req < 1 || num_pages < 1)
+        return BDSA_INVALID_ARG;
+    if (bs == 0) return BDSA_OK;
+    if (!pending || !mode || !seq_lens || !block_table || !block_ids || !positions ||
+        !cache_loc || (N > 1 && !specs))
+        return BDSA_INVALID_ARG;
+    if ((int64_t)bs * (2 * (int64_t)N - 1) > INT32_MAX) return BDSA_UNSUPPORTED;
+    return bdsa::launch_idlm_prepare(pending, specs, mode, seq_lens, block_table,
+                                     max_pages_per_req, num_pages, bs, N, page_size,
+                                     mask_token_id, block_ids, positions, cache_loc, dev_status,
+                                     static_cast<cudaStream_t>(stream));
+}
+
+int32_t bdsa_idlm_accept(const int32_t *block_ids, const int32_t *mode, const float *p,
+                         int64_t p_stride_r, int64_t p_stride_i, const float *q_prev,
+                         int64_t q_stride_r, int64_t q_stride_i, const int32_t *q_slot,
+                         const float *u_acc, const float *u_samp, const int32_t *seq_lens,
+                         int32_t bs, int32_t N, int32_t V, int32_t *accept_len, int32_t *n_out,
+                         int32_t *out_tokens, int32_t *next_mode, int32_t *next_pending,
+                         int32_t *next_specs, int32_t *next_q_slot, int32_t *new_seq_lens,
+                         int32_t *kv_keep, int32_t num_sms, int32_t *dev_status, void *stream) {
+    if (bs < 0 || N < 1 || V < 1 || p_stride_r < 0 || p_stride_i < 0 || q_stride_r < 0 ||
+        q_stride_i < 0)
+        return BDSA_INVALID_ARG;
+    if (bs == 0) return BDSA_OK;
+    if (N > 32 || V > (1 << 21)) return BDSA_UNSUPPORTED;
+    if (!block_ids || !mode || !p || !q_slot || !u_samp || !seq_lens || !accept_len || !n_out ||
+        !out_tokens || !next_mode || !next_pending || !next_q_slot || !new_seq_lens || !kv_keep)
+        return BDSA_INVALID_ARG;
+    if (N > 1 && (!q_prev || !u_acc || !next_specs)) return BDSA_INVALID_ARG;
+    if (!aligned(p, 4) || (q_prev && !aligned(q_prev, 4))) return BDSA_MISALIGNED;
+    bdsa::IdlmArgs a;
+    a.block_ids = block_ids;
+    a.mode = mode;
+    a.q_slot = q_slot;
+    a.seq_lens = seq_lens;
+    a.p = p;
+    a.q = q_prev;
+    a.psr = p_stride_r;
+    a.psi = p_stride_i;
+    a.qsr = q_stride_r;
+    a.qsi = q_stride_i;
+    a.u_acc = u_acc;
+    a.u_samp = u_samp;
+    a.bs = bs;
+    a.N = N;
+    a.V = V;
+    a.num_sms = bdsa::device_num_sms(num_sms);
+    a.accept_len = accept_len;
+    a.n_out = n_out;
+    a.out_tokens = out_tokens;
+    a.next_mode = next_mode;
+    a.next_pending = next_pending;
+    a.next_specs = next_specs;
+    a.next_q_slot = next_q_slot;
+    a.new_seq_lens = new_seq_lens;
+    a.kv_keep = kv_keep;
+    a.dev_status = dev_status;
+    return bdsa::launch_idlm_accept(a, static_cast<cudaStream_t>(stream));
+}
+
 size_t bdsa_spec_accept_workspace_bytes(int32_t bs, int32_t B, int32_t V, int32_t num_sms) {
     if (bs <= 0 || B <= 0 || V <= 0) return 0;
     return bdsa::accept_plan(bs, B, V, bdsa::device_num_sms(num_sms)).workspace;

@@ -72,6 +72,26 @@ struct AcceptArgs {
 
 int launch_spec_accept(const AcceptArgs &a, cudaStream_t stream);
 
+// I-DLM Block-N round: layout of 2N-1 slots, verify / sample / trim.
+int launch_idlm_prepare(const int32_t *pending, const int32_t *specs, const int32_t *mode,
+                        const int32_t *seq_lens, const int32_t *block_table, int max_pages,
+                        int num_pages, int bs, int N, int page_size, int mask_token_id,
+                        int32_t *block_ids, int32_t *positions, int32_t *cache_loc,
+                        int32_t *dev_status, cudaStream_t stream);
+
+struct IdlmArgs {
+    const int32_t *block_ids, *mode, *q_slot, *seq_lens;
+    const float *p, *q;
+    int64_t psr, psi, qsr, qsi;
+    const float *u_acc, *u_samp;
+    int bs, N, V, num_sms;
+    int32_t *accept_len, *n_out, *out_tokens, *next_mode, *next_pending, *next_specs,
+        *next_q_slot, *new_seq_lens, *kv_keep;
+    int32_t *dev_status;
+};
+
+int launch_idlm_accept(const IdlmArgs &a, cudaStream_t stream);
+
 // ---------------------------------------------------------------- misc
 int device_num_sms(int requested);
 

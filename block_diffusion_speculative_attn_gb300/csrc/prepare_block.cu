@@ -36,7 +36,53 @@ __global__ void __launch_bounds__(256)
     cache_loc[idx] = loc;
 }
 
+// I-DLM Block-N layout ("From DFlash to dLLM Self-Spec (IV)", section 4.3.1):
+// 2N-1 slots, [pending, spec_0 .. spec_{N-2}, mask ...] in verify mode (mode
+// 1), [pending, mask ...] otherwise; positions and cache locations as above.
+__global__ void __launch_bounds__(256)
+    idlm_prepare_kernel(const int32_t *__restrict__ pending, const int32_t *__restrict__ specs,
+                        const int32_t *__restrict__ mode, const int32_t *__restrict__ seq_lens,
+                        const int32_t *__restrict__ block_table, int max_pages, int num_pages,
+                        int bs, int N, int page_size, int mask_token_id,
+                        int32_t *__restrict__ block_ids, int32_t *__restrict__ positions,
+                        int32_t *__restrict__ cache_loc, int32_t *dev_status) {
+    const int blk = 2 * N - 1;
+    const long idx = (long)blockIdx.x * blockDim.x + threadIdx.x;
+    if (idx >= (long)bs * blk) return;
+    const int r = (int)(idx / blk), i = (int)(idx % blk);
+    const int L = seq_lens[r];
+    const long pos = (long)L + i;
+    int32_t id = mask_token_id;
+    if (i == 0) id = pending[r];
+    else if (i < N && mode[r] == 1) id = specs[(long)r * (N - 1) + i - 1];
+    block_ids[idx] = id;
+    positions[idx] = (int32_t)pos;
+    int32_t loc = -1;
+    const long page_idx = pos / page_size;
+    if (L >= 0 && page_idx < max_pages) {
+        const int32_t page = block_table[(long)r * max_pages + page_idx];
+        if (page >= 0 && page < num_pages) loc = (int32_t)((long)page * page_size + pos % page_size);
+    }
+    if (loc < 0) report_status(dev_status, BDSA_DEVICE_OUT_OF_RANGE);
+    cache_loc[idx] = loc;
+}
+
 }  // namespace
+
+int launch_idlm_prepare(const int32_t *pending, const int32_t *specs, const int32_t *mode,
+                        const int32_t *seq_lens, const int32_t *block_table, int max_pages,
+                        int num_pages, int bs, int N, int page_size, int mask_token_id,
+                        int32_t *block_ids, int32_t *positions, int32_t *cache_loc,
+                        int32_t *dev_status, cudaStream_t stream) {
+    const long n = (long)bs * (2 * N - 1);
+    if (n == 0) return BDSA_OK;
+    const unsigned grid = (unsigned)((n + 255) / 256);
+    idlm_prepare_kernel<<<grid, 256, 0, stream>>>(pending, specs, mode, seq_lens, block_table,
+                                                  max_pages, num_pages, bs, N, page_size,
+                                                  mask_token_id, block_ids, positions, cache_loc,
+                                                  dev_status);
+    return cudaGetLastError() == cudaSuccess ? BDSA_OK : BDSA_CUDA_ERROR;
+}
 
 int launch_prepare_block(const int32_t *verified_id, const int32_t *seq_lens,
                          const int32_t *block_table, int max_pages, int num_pages, int bs, int B,

@@ -229,7 +229,8 @@ __device__ int accepted_len(const Params &P, int r, int lane, bool &bad_id, int 
 // loads overlap.
 constexpr int kUnroll = 4;
 
-__device__ void sweep_chunk(const Params &P, const float *prow, const float *qrow, int seg_begin,
+template <class PT>
+__device__ void sweep_chunk(const PT &P, const float *prow, const float *qrow, int seg_begin,
                             int seg_end, int warp, int lane, float2 *tot) {
     for (int s0 = seg_begin + warp; s0 < seg_end; s0 += kUnroll * kWarps) {
         float w[kUnroll][8];
@@ -263,8 +264,8 @@ __device__ __forceinline__ float2 load_tot(const float2 *tot, int i) {
 // a block-wide scan of the totals finds the segment holding the crossing, then
 // warp 0 re-reads that one segment and finds the element.  Every thread
 // returns the token index (-1 when the weights are all zero).
-template <bool kShared>
-__device__ int resolve_draw(const Params &P, const float *prow, const float *qrow, float u,
+template <bool kShared, class PT>
+__device__ int resolve_draw(const PT &P, const float *prow, const float *qrow, float u,
                             const float2 *tot) {
     __shared__ float2 s_wtot[kWarps];
     __shared__ int s_seg;
@@ -569,6 +570,155 @@ __global__ void __launch_bounds__(kThreads) accept_greedy_kernel(const Params P)
     write_outputs(P, r, s_a, s_tp[s_a], s_ids, s_sl);
 }
 
+// ------------------------------------------------------------ I-DLM round
+// "From DFlash to dLLM Self-Spec (IV)", sections 4.3 and 4.3.1 (Block-N
+// round: the specs carried from the previous round's MASK slots are verified
+// left to right against the causal view, a rejection is corrected from the
+// residual, a fully verified block draws its bonus and N-1 new specs from the
+// MASK slots, a cold start draws one clean token and N-1 specs) and 4.6 (the
+// KV rows to keep and the request's advance).  Slot j's distribution p[j]
+// predicts slot j + 1.
+struct IdlmParams {
+    const int32_t *block_ids;  // [bs, 2N-1]
+    const int32_t *mode;       // [bs]: 1 verify, 0 cold start
+    const float *p;
+    const float *q;            // previous round's p rows
+    int64_t psr, psi, qsr, qsi;
+    const int32_t *q_slot;     // [bs]: q row of spec_0
+    const float *u_acc;        // [bs, N-1]
+    const float *u_samp;       // [bs, N]: the anchor's, then spec'_j's
+    const int32_t *seq_lens;
+    int bs, N, V, nchunk, nseg, spc;
+    int32_t *accept_len, *n_out, *out_tokens, *next_mode, *next_pending, *next_specs,
+        *next_q_slot, *new_seq_lens, *kv_keep;
+    int32_t *dev_status;
+};
+
+// Leading verified specs of row r (one warp); spec ids are left in
+// s_ids[1..N-1].  An id outside the vocabulary is a rejection and a data error.
+__device__ int idlm_accepted(const IdlmParams &P, int r, int qs, int lane, bool &bad,
+                             int *s_ids) {
+    const int N = P.N, blk = 2 * N - 1;
+    bool bad_any = false;
+    int a = -1;
+    for (int base = 0; base < N - 1; base += 32) {
+        const int k = base + lane;
+        bool rej = false, bad_id = false;
+        if (k < N - 1) {
+            const int s = P.block_ids[(long)r * blk + 1 + k];
+            s_ids[1 + k] = s;
+            if (s < 0 || s >= P.V) {
+                rej = bad_id = true;
+            } else {
+                const float pv = __ldg(P.p + r * P.psr + (long)k * P.psi + s);
+                const float qv = __ldg(P.q + r * P.qsr + (long)(qs + k) * P.qsi + s);
+                const float u = __ldg(P.u_acc + (long)r * (N - 1) + k);
+                rej = (qv == 0.f) ? !(pv > 0.f) : !(u < fminf(1.f, __fdiv_rn(pv, qv)));
+            }
+        }
+        bad_any = bad_any || __any_sync(0xffffffffu, bad_id);
+        const unsigned m = __ballot_sync(0xffffffffu, rej);
+        if (m != 0u && a < 0) a = base + (__ffs(m) - 1);
+    }
+    bad = bad_any;
+    return a < 0 ? N - 1 : a;
+}
+
+// One thread-block cluster per (row r, draw j), its CTAs = the vocabulary
+// chunks.  Draw 0 is the anchor (correction, bonus or clean token) and writes
+// the row's outputs; draw j > 0 is spec'_{j-1}, drawn only when the next round
+// verifies.
+__global__ void __launch_bounds__(kThreads) idlm_accept_kernel(const IdlmParams P) {
+    const int unit = blockIdx.x / P.nchunk, chunk = blockIdx.x % P.nchunk;
+    const int r = unit / P.N, j = unit % P.N;
+    const int N = P.N;
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    extern __shared__ float2 s_tot[];  // [nseg] totals, used in chunk 0
+    __shared__ int s_ids[kMaxB];
+    __shared__ int s_a, s_verify, s_qs, s_sl;
+    __shared__ float s_u;
+    cluster_arrive_relaxed();
+    if (warp == 0) {
+        const int m = __ldg(P.mode + r);
+        const int qs = __ldg(P.q_slot + r);
+        const bool verify = m == 1 && qs >= 0 && qs <= N;
+        bool bad = false;
+        const int a = verify ? idlm_accepted(P, r, qs, lane, bad, s_ids) : 0;
+        if (lane == 0) {
+            s_a = a;
+            s_verify = verify;
+            s_qs = qs;
+            const bool bad_state = (m != 0 && m != 1) || (m == 1 && !verify);
+            if (chunk == 0 && j == 0 && (bad || bad_state))
+                report_status(P.dev_status, BDSA_DEVICE_OUT_OF_RANGE);
+        }
+    } else if (warp == 1 && lane == 0) {
+        s_u = __ldg(P.u_samp + (long)r * N + j);
+        s_sl = __ldg(P.seq_lens + r);
+    }
+    __syncthreads();
+    const int a = s_a;
+    const bool verify = s_verify != 0;
+    int slot = -1;  // p row this draw samples
+    const float *qrow = nullptr;
+    if (j == 0) {
+        if (!verify) {
+            slot = 0;
+        } else if (a < N - 1) {
+            slot = a;
+            qrow = P.q + r * P.qsr + (long)(s_qs + a) * P.qsi;
+        } else {
+            slot = N - 1;
+        }
+    } else if (!verify) {
+        slot = j;
+    } else if (a == N - 1) {
+        slot = N + j - 1;
+    }
+    if (slot < 0) {
+        // the next round is a cold start: no spec to draw
+        cluster_wait_acquire();
+        if (chunk == 0 && threadIdx.x == 0) P.next_specs[(long)r * (N - 1) + j - 1] = -1;
+        return;
+    }
+    const float *prow = P.p + r * P.psr + (long)slot * P.psi;
+    const int sb = chunk * P.spc, se = min(P.nseg, sb + P.spc);
+    cluster_wait_acquire();
+    sweep_chunk(P, prow, qrow, sb, se, warp, lane, map_to_rank(s_tot, 0));
+    cluster_arrive_release();
+    cluster_wait_acquire();
+    if (chunk != 0) return;
+    const float u = s_u;
+    int tok = resolve_draw<true>(P, prow, qrow, u, s_tot);
+    if (tok < 0 && qrow != nullptr) {
+        // residual has no mass (p <= q everywhere in fp32): draw from p instead
+        __syncthreads();
+        sweep_chunk(P, prow, nullptr, 0, P.nseg, warp, lane, s_tot);
+        __syncthreads();
+        tok = resolve_draw<true>(P, prow, nullptr, u, s_tot);
+    }
+    if (j > 0) {
+        if (threadIdx.x == 0) P.next_specs[(long)r * (N - 1) + j - 1] = tok;
+        return;
+    }
+    for (int i = threadIdx.x; i < N; i += kThreads) {
+        int32_t v = -1;
+        if (i < a) v = s_ids[i + 1];
+        else if (i == a) v = tok;
+        P.out_tokens[(long)r * N + i] = v;
+    }
+    if (threadIdx.x == 0) {
+        const bool next_verify = !verify || a == N - 1;
+        P.accept_len[r] = a;
+        P.n_out[r] = a + 1;
+        P.next_pending[r] = tok;
+        P.next_mode[r] = next_verify ? 1 : 0;
+        P.next_q_slot[r] = !verify ? 1 : (a == N - 1 ? N : -1);
+        P.kv_keep[r] = a + 1;
+        P.new_seq_lens[r] = s_sl + a + 1;
+    }
+}
+
 size_t align256(size_t x) { return (x + 255) & ~(size_t)255; }
 
 }  // namespace
@@ -594,6 +744,62 @@ AcceptPlan accept_plan(int bs, int B, int V, int num_sms) {
                                   align256((size_t)bs * p.nseg * sizeof(float2)) +
                                   2 * align256((size_t)bs * B * p.nchunk * 4);
     return p;
+}
+
+int launch_idlm_accept(const IdlmArgs &a, cudaStream_t stream) {
+    if (a.bs == 0) return BDSA_OK;
+    const AcceptPlan plan = accept_plan(a.bs * a.N, 2 * a.N - 1, a.V, a.num_sms);
+    if (!plan.cluster) return BDSA_UNSUPPORTED;
+    IdlmParams P;
+    P.block_ids = a.block_ids;
+    P.mode = a.mode;
+    P.p = a.p;
+    P.q = a.q;
+    P.psr = a.psr;
+    P.psi = a.psi;
+    P.qsr = a.qsr;
+    P.qsi = a.qsi;
+    P.q_slot = a.q_slot;
+    P.u_acc = a.u_acc;
+    P.u_samp = a.u_samp;
+    P.seq_lens = a.seq_lens;
+    P.bs = a.bs;
+    P.N = a.N;
+    P.V = a.V;
+    P.nchunk = plan.nchunk;
+    P.nseg = plan.nseg;
+    P.spc = plan.spc;
+    P.accept_len = a.accept_len;
+    P.n_out = a.n_out;
+    P.out_tokens = a.out_tokens;
+    P.next_mode = a.next_mode;
+    P.next_pending = a.next_pending;
+    P.next_specs = a.next_specs;
+    P.next_q_slot = a.next_q_slot;
+    P.new_seq_lens = a.new_seq_lens;
+    P.kv_keep = a.kv_keep;
+    P.dev_status = a.dev_status;
+    const long nblocks = (long)plan.nchunk * a.bs * a.N;
+    if (nblocks > 0x7fffffffL) return BDSA_UNSUPPORTED;
+    const size_t smem = (size_t)plan.nseg * sizeof(float2);
+    if (smem > 48 * 1024 &&
+        cudaFuncSetAttribute(idlm_accept_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             (int)smem) != cudaSuccess)
+        return BDSA_CUDA_ERROR;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)nblocks);
+    cfg.blockDim = dim3(kThreads);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = (unsigned)plan.nchunk;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, idlm_accept_kernel, P) == cudaSuccess ? BDSA_OK
+                                                                          : BDSA_CUDA_ERROR;
 }
 
 int launch_spec_accept(const AcceptArgs &a, cudaStream_t stream) {

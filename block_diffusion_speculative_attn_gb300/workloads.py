@@ -195,6 +195,61 @@ def make_accept_inputs(cfg: StepConfig, device="cpu", seed: int | None = None,
     return AcceptInputs(block_ids, p.contiguous(), q.contiguous(), u_acc, u_samp, seq_lens)
 
 
+@dataclasses.dataclass
+class IdlmInputs:
+    """Inputs of one I-DLM Block-N round (blk = 2N - 1 slots per request)."""
+    N: int
+    pending: torch.Tensor       # [bs] int32, the token whose KV the round writes first
+    specs: torch.Tensor         # [bs, N-1] int32, carried specs (meaningful where mode == 1)
+    mode: torch.Tensor          # [bs] int32, 1 verify / 0 cold start
+    q_slot: torch.Tensor        # [bs] int32, q_prev row of spec_0
+    p: torch.Tensor             # [bs, blk, V] fp32, this round's distributions
+    q_prev: torch.Tensor        # [bs, blk, V] fp32, the previous round's distributions
+    u_acc: torch.Tensor         # [bs, N-1] fp32
+    u_samp: torch.Tensor        # [bs, N] fp32
+    seq_lens: torch.Tensor      # [bs] int32
+
+
+def make_idlm_inputs(cfg: StepConfig, N: int = 8, device="cpu", seed: int | None = None,
+                     bs: int | None = None, verify_frac: float = 0.75) -> IdlmInputs:
+    """A round shaped like cfg's acceptance stage: p = softmax(3 N(0,1) logits);
+    the previous round's rows that drew the carried specs are p's logits plus
+    N(0,1) noise (the draft is close to the verifier), the other q_prev rows
+    independent; a verify_frac share of requests verify carried specs, drawn
+    from their q_prev rows at q_slot in {1, N} (after a cold start or after a
+    fully verified round); the rest start cold."""
+    seed = (cfg.seed if seed is None else seed) + 104729
+    bs = cfg.bs if bs is None else bs
+    V, blk = cfg.V, 2 * N - 1
+    g = _gen(device, seed)
+    f32 = torch.float32
+    logits = 3.0 * torch.randn((bs, blk, V), generator=g, device=device, dtype=f32)
+    p = torch.softmax(logits, -1)
+    q_prev = torch.softmax(3.0 * torch.randn((bs, blk, V), generator=g, device=device,
+                                             dtype=f32), -1)
+    mode = (torch.rand((bs,), generator=g, device=device) < verify_frac).to(torch.int32)
+    q_slot = torch.where(torch.rand((bs,), generator=g, device=device) < 0.5,
+                         torch.ones((bs,), device=device, dtype=torch.int32),
+                         torch.full((bs,), N, device=device, dtype=torch.int32))
+    specs = torch.randint(0, V, (bs, max(N - 1, 0)), generator=g, device=device,
+                          dtype=torch.int32)
+    for r in range(bs):
+        if int(mode[r]) != 1 or N == 1:
+            continue
+        qs = int(q_slot[r])
+        noise = torch.randn((N - 1, V), generator=g, device=device, dtype=f32)
+        rows = torch.softmax(logits[r, :N - 1] + noise, -1)
+        q_prev[r, qs:qs + N - 1] = rows
+        specs[r] = torch.multinomial(rows, 1, generator=g).reshape(N - 1).to(torch.int32)
+    del logits
+    pending = torch.randint(0, V, (bs,), generator=g, device=device, dtype=torch.int32)
+    u_acc = torch.rand((bs, max(N - 1, 0)), generator=g, device=device, dtype=f32)
+    u_samp = torch.rand((bs, N), generator=g, device=device, dtype=f32)
+    seq_lens = torch.randint(1, 4096, (bs,), generator=g, device=device).to(torch.int32)
+    return IdlmInputs(N, pending, specs.contiguous(), mode, q_slot.to(torch.int32),
+                      p.contiguous(), q_prev.contiguous(), u_acc, u_samp, seq_lens)
+
+
 def draft_from(q_rows: np.ndarray, u: np.ndarray) -> np.ndarray:
     """Inverse-CDF draws from rows of q (numpy, for small host-side workloads)."""
     c = np.cumsum(q_rows.astype(np.float64), axis=-1)

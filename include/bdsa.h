@@ -275,6 +275,84 @@ int32_t bdsa_spec_accept_noalloc(const int32_t *block_ids, const float *p, int64
                                  int32_t *bonus_id, int32_t *new_seq_lens, int32_t num_sms,
                                  int32_t *dev_status, void *stream);
 
+/* ------------------------------------------------------------------------ */
+/* bdsa_idlm_prepare
+ *
+ * "From DFlash to dLLM Self-Spec (IV)", section 4.3.1: an I-DLM Block-N
+ * round lays out blk = 2N-1 slots per request, [pending, spec_0 .. spec_{N-2},
+ * M .. M] when it verifies the specs carried from the previous round (mode 1)
+ * and [pending, M .. M] on a cold start (any other mode).
+ *
+ * pending [bs], mode [bs], specs [bs, N-1] (read only in mode 1; may be NULL
+ * when N == 1), seq_lens [bs] (L_r, the committed length; the pending token's
+ * KV is not yet in the cache), block_table [bs, max_pages_per_req].
+ * Outputs [bs, blk]: block_ids as above, positions L_r + j, cache_loc exactly
+ * as bdsa_prepare_block computes it for a block of blk slots (-1 and
+ * *dev_status = BDSA_DEVICE_OUT_OF_RANGE where the page lookup fails).
+ * Host checks: bs >= 0, 1 <= N, bs * blk <= INT32_MAX, page_size >= 1,
+ * max_pages_per_req >= 1, num_pages >= 1, non-null buffers.  One launch.
+ */
+int32_t bdsa_idlm_prepare(const int32_t *pending, const int32_t *specs, const int32_t *mode,
+                          const int32_t *seq_lens, const int32_t *block_table,
+                          int32_t max_pages_per_req, int32_t num_pages, int32_t bs, int32_t N,
+                          int32_t page_size, int32_t mask_token_id, int32_t *block_ids,
+                          int32_t *positions, int32_t *cache_loc, int32_t *dev_status,
+                          void *stream);
+
+/* ------------------------------------------------------------------------ */
+/* bdsa_idlm_accept
+ *
+ * "From DFlash to dLLM Self-Spec (IV)", sections 4.3 and 4.3.1 (the specs
+ * drawn from MASK slots in one round are verified in the next against the
+ * causal view with min(1, p/q), a rejection is corrected from the anchor
+ * distribution and falls back to a cold start, the same forward drafts the
+ * next specs) and 4.6 (which KV rows to free, how far the request advances).
+ *
+ * p [bs, 2N-1, V] fp32: p[r, j] (at p + r*p_stride_r + j*p_stride_i) is the
+ *   distribution predicted at slot j, i.e. for slot j + 1's token.
+ * q_prev: the previous round's p rows; spec_k of row r was drawn from
+ *   q_prev[r, q_slot[r] + k] (at q_prev + r*q_stride_r + (q_slot[r]+k)*q_stride_i).
+ * block_ids [bs, 2N-1] as written by bdsa_idlm_prepare; mode [bs];
+ * u_acc [bs, N-1], u_samp [bs, N] fp32 uniforms in [0, 1); seq_lens [bs].
+ * Row r, verify (mode 1 with 0 <= q_slot <= N):
+ *   a = leading k with u_acc[r,k] < min(1, p[k][s_k] / q_prev[q_slot+k][s_k])
+ *       (IEEE fp32 divide; q == 0 accepts iff p > 0; an id outside [0, V)
+ *       rejects and sets *dev_status = BDSA_DEVICE_OUT_OF_RANGE);
+ *   a < N-1: anchor = InvCDF(max(0, p[a] - q_prev[q_slot+a]), u_samp[r,0])
+ *            (from p[a] if those weights are all 0); next round: cold start;
+ *   a = N-1: anchor = InvCDF(p[N-1], u_samp[r,0]) (bonus); new specs
+ *            next_specs[r,j] = InvCDF(p[N+j], u_samp[r,1+j]); next_q_slot = N.
+ * Row r, cold start (mode 0; mode 1 with q_slot outside [0, N] and any other
+ *   mode too, with *dev_status = BDSA_DEVICE_OUT_OF_RANGE): a = 0, anchor =
+ *   InvCDF(p[0], u_samp[r,0]), next_specs[r,j] = InvCDF(p[1+j], u_samp[r,1+j]),
+ *   next_q_slot = 1.
+ * InvCDF(w, u) = smallest k with sum_{i<=k} w_i > u * sum_i w_i.
+ * Outputs: accept_len = a; n_out = a + 1; out_tokens [bs, N] = s_0..s_{a-1},
+ *   anchor, -1 padding; next_pending = anchor; next_mode = 1 if specs were
+ *   drawn else 0; next_specs [bs, N-1] (-1 when not drawn; may be NULL when
+ *   N == 1); next_q_slot (-1 when not drawn); kv_keep = a + 1, the block rows
+ *   from slot 0 whose KV stays (cache_loc[r, kv_keep:] are freed: every MASK
+ *   row and every rejected spec); new_seq_lens = seq_lens + kv_keep.
+ * Limits: 1 <= N <= 32, V <= 2^21 (BDSA_UNSUPPORTED above).  No workspace.
+ * Host checks: bs >= 0, V >= 1, non-negative strides, non-null buffers
+ *   (q_prev, u_acc and next_specs may be NULL only when N == 1), p and q_prev
+ *   4-byte aligned.  All buffers are device memory owned by the caller.
+ * num_sms: SM count the vocabulary chunking is sized for (0: the current
+ *   device's).  dev_status (nullable) receives BDSA_DEVICE_OUT_OF_RANGE by
+ *   atomicCAS from 0 on the data errors above; the kernel never traps.
+ * Launch: one kernel of bs * N thread-block clusters (one per row and draw),
+ * each cluster = that draw's vocabulary chunks; draws that the row does not
+ * need exit at once.  Asynchronous on `stream`.
+ */
+int32_t bdsa_idlm_accept(const int32_t *block_ids, const int32_t *mode, const float *p,
+                         int64_t p_stride_r, int64_t p_stride_i, const float *q_prev,
+                         int64_t q_stride_r, int64_t q_stride_i, const int32_t *q_slot,
+                         const float *u_acc, const float *u_samp, const int32_t *seq_lens,
+                         int32_t bs, int32_t N, int32_t V, int32_t *accept_len, int32_t *n_out,
+                         int32_t *out_tokens, int32_t *next_mode, int32_t *next_pending,
+                         int32_t *next_specs, int32_t *next_q_slot, int32_t *new_seq_lens,
+                         int32_t *kv_keep, int32_t num_sms, int32_t *dev_status, void *stream);
+
 #ifdef __cplusplus
 }
 #endif

@@ -123,3 +123,38 @@ def test_workspace_plans(L):
     assert L.bdsa_spec_accept_workspace_bytes(32, 16, 1 << 21, 152) == 0
     V = (1 << 21) + 1
     assert L.bdsa_spec_accept_workspace_bytes(32, 16, V, 152) > 32 * ((V + 255) // 256) * 8
+
+
+def _idlm_accept(L, **kw):
+    a = dict(ids=FAKE, mode=FAKE, p=FAKE, psr=15000, psi=1000, q=FAKE, qsr=15000, qsi=1000,
+             qs=FAKE, ua=FAKE, us=FAKE, sl=FAKE, bs=4, N=8, V=1000, outs=FAKE, ns=FAKE, sms=152)
+    a.update(kw)
+    o = a["outs"]
+    return L.bdsa_idlm_accept(a["ids"], a["mode"], a["p"], a["psr"], a["psi"], a["q"], a["qsr"],
+                              a["qsi"], a["qs"], a["ua"], a["us"], a["sl"], a["bs"], a["N"],
+                              a["V"], o, o, o, o, o, a["ns"], o, o, o, a["sms"], None, None)
+
+
+def test_idlm_accept_host_checks(L):
+    assert _idlm_accept(L, bs=0) == 0
+    assert _idlm_accept(L, bs=-1) == 1
+    assert _idlm_accept(L, N=0) == 1
+    assert _idlm_accept(L, V=0) == 1
+    assert _idlm_accept(L, qsi=-1) == 1
+    assert _idlm_accept(L, p=None) == 1
+    assert _idlm_accept(L, qs=None) == 1
+    assert _idlm_accept(L, q=None) == 1           # N > 1 verifies against q_prev
+    assert _idlm_accept(L, ns=None) == 1          # N > 1 draws new specs
+    assert _idlm_accept(L, N=33) == 2             # UNSUPPORTED
+    assert _idlm_accept(L, V=(1 << 21) + 1) == 2
+    assert _idlm_accept(L, p=ctypes.c_void_p(0x100001)) == 3
+
+
+def test_idlm_prepare_host_checks(L):
+    f = L.bdsa_idlm_prepare
+    # pending, specs, mode, seq_lens, block_table, max_pages, num_pages, bs, N, ps, mask, outs
+    assert f(FAKE, FAKE, FAKE, FAKE, FAKE, 4, 8, 0, 8, 16, 0, FAKE, FAKE, FAKE, None, None) == 0
+    assert f(None, FAKE, FAKE, FAKE, FAKE, 4, 8, 2, 8, 16, 0, FAKE, FAKE, FAKE, None, None) == 1
+    assert f(FAKE, None, FAKE, FAKE, FAKE, 4, 8, 2, 8, 16, 0, FAKE, FAKE, FAKE, None, None) == 1
+    assert f(FAKE, FAKE, FAKE, FAKE, FAKE, 4, 8, 2, 0, 16, 0, FAKE, FAKE, FAKE, None, None) == 1
+    assert f(FAKE, FAKE, FAKE, FAKE, FAKE, 4, 8, 2, 8, 0, 0, FAKE, FAKE, FAKE, None, None) == 1
