@@ -594,34 +594,37 @@ struct IdlmParams {
     int32_t *dev_status;
 };
 
-// Leading verified specs of row r (one warp); spec ids are left in
-// s_ids[1..N-1].  An id outside the vocabulary is a rejection and a data error.
-__device__ int idlm_accepted(const IdlmParams &P, int r, int qs, int lane, bool &bad,
-                             int *s_ids) {
+// Leading verified specs of row r (one warp, N - 1 <= 31 specs: one lane
+// each); spec ids are left in s_ids[1..N-1].  The row's mode, q slot, spec
+// ids and uniforms are loaded together, then the p / q pairs: two dependent
+// global round trips.  An id outside the vocabulary is a rejection and a data
+// error.  Returns -1 for a row that does not verify (cold start).
+__device__ int idlm_accepted(const IdlmParams &P, int r, int lane, int &m_out, int &qs_out,
+                             bool &bad, int *s_ids) {
     const int N = P.N, blk = 2 * N - 1;
-    bool bad_any = false;
-    int a = -1;
-    for (int base = 0; base < N - 1; base += 32) {
-        const int k = base + lane;
-        bool rej = false, bad_id = false;
-        if (k < N - 1) {
-            const int s = P.block_ids[(long)r * blk + 1 + k];
-            s_ids[1 + k] = s;
-            if (s < 0 || s >= P.V) {
-                rej = bad_id = true;
-            } else {
-                const float pv = __ldg(P.p + r * P.psr + (long)k * P.psi + s);
-                const float qv = __ldg(P.q + r * P.qsr + (long)(qs + k) * P.qsi + s);
-                const float u = __ldg(P.u_acc + (long)r * (N - 1) + k);
-                rej = (qv == 0.f) ? !(pv > 0.f) : !(u < fminf(1.f, __fdiv_rn(pv, qv)));
-            }
+    const bool has = lane < N - 1;
+    const int m = __ldg(P.mode + r);
+    const int qs = __ldg(P.q_slot + r);
+    const int s = has ? __ldg(P.block_ids + (long)r * blk + 1 + lane) : 0;
+    const float u = has ? __ldg(P.u_acc + (long)r * (N - 1) + lane) : 0.f;
+    m_out = m;
+    qs_out = qs;
+    bad = false;
+    if (!(m == 1 && qs >= 0 && qs <= N)) return -1;
+    bool rej = false, bad_id = false;
+    if (has) {
+        s_ids[1 + lane] = s;
+        if (s < 0 || s >= P.V) {
+            rej = bad_id = true;
+        } else {
+            const float pv = __ldg(P.p + r * P.psr + (long)lane * P.psi + s);
+            const float qv = __ldg(P.q + r * P.qsr + (long)(qs + lane) * P.qsi + s);
+            rej = (qv == 0.f) ? !(pv > 0.f) : !(u < fminf(1.f, __fdiv_rn(pv, qv)));
         }
-        bad_any = bad_any || __any_sync(0xffffffffu, bad_id);
-        const unsigned m = __ballot_sync(0xffffffffu, rej);
-        if (m != 0u && a < 0) a = base + (__ffs(m) - 1);
     }
-    bad = bad_any;
-    return a < 0 ? N - 1 : a;
+    bad = __any_sync(0xffffffffu, bad_id);
+    const unsigned msk = __ballot_sync(0xffffffffu, rej);
+    return msk != 0u ? __ffs(msk) - 1 : N - 1;
 }
 
 // One thread-block cluster per (row r, draw j), its CTAs = the vocabulary
@@ -639,11 +642,11 @@ __global__ void __launch_bounds__(kThreads) idlm_accept_kernel(const IdlmParams 
     __shared__ float s_u;
     cluster_arrive_relaxed();
     if (warp == 0) {
-        const int m = __ldg(P.mode + r);
-        const int qs = __ldg(P.q_slot + r);
-        const bool verify = m == 1 && qs >= 0 && qs <= N;
-        bool bad = false;
-        const int a = verify ? idlm_accepted(P, r, qs, lane, bad, s_ids) : 0;
+        int m, qs;
+        bool bad;
+        const int av = idlm_accepted(P, r, lane, m, qs, bad, s_ids);
+        const bool verify = av >= 0;
+        const int a = verify ? av : 0;
         if (lane == 0) {
             s_a = a;
             s_verify = verify;
@@ -748,7 +751,9 @@ AcceptPlan accept_plan(int bs, int B, int V, int num_sms) {
 
 int launch_idlm_accept(const IdlmArgs &a, cudaStream_t stream) {
     if (a.bs == 0) return BDSA_OK;
-    const AcceptPlan plan = accept_plan(a.bs * a.N, 2 * a.N - 1, a.V, a.num_sms);
+    // Most (row, draw) clusters of a round find nothing to draw and exit: the
+    // chunks are sized for about four CTAs an SM over all of them.
+    const AcceptPlan plan = accept_plan(a.bs * a.N, 2 * a.N - 1, a.V, 2 * a.num_sms);
     if (!plan.cluster) return BDSA_UNSUPPORTED;
     IdlmParams P;
     P.block_ids = a.block_ids;
