@@ -250,6 +250,65 @@ def make_idlm_inputs(cfg: StepConfig, N: int = 8, device="cpu", seed: int | None
                       p.contiguous(), q_prev.contiguous(), u_acc, u_samp, seq_lens)
 
 
+@dataclasses.dataclass
+class KvMatInputs:
+    """Inputs of the draft-KV materialisation of one verify step's committed rows."""
+    B: int
+    n_layers: int
+    Hkv: int
+    D: int
+    hidden: torch.Tensor        # [bs*B, H] bf16, target hidden rows
+    w_kv: torch.Tensor          # [n_layers, 2, Hkv*D, H] bf16, K rows then V rows per layer
+    k_norm_w: torch.Tensor      # [n_layers, D] bf16
+    rope_cos: torch.Tensor      # [max_pos, D/2] fp32
+    rope_sin: torch.Tensor      # [max_pos, D/2] fp32
+    commit_len: torch.Tensor    # [bs] int32 in [1, B]
+    seq_lens: np.ndarray        # [bs] int32, committed length before the block
+    block_table: np.ndarray     # [bs, max_pages] int32
+    num_pages: int
+    eps: float = 1e-6
+
+
+def rope_tables(max_pos: int, D: int, base: float = 1e6):
+    """cos / sin tables [max_pos, D/2] of the model's rotary embedding (the
+    usual frequencies base^(-2d/D), computed in fp64 and stored as fp32):
+    model data handed to the call like the weights."""
+    inv = base ** (-np.arange(0, D, 2, dtype=np.float64) / D)
+    ang = np.arange(max_pos, dtype=np.float64)[:, None] * inv[None, :]
+    return (torch.from_numpy(np.cos(ang).astype(np.float32)),
+            torch.from_numpy(np.sin(ang).astype(np.float32)))
+
+
+def make_kvmat_inputs(cfg: StepConfig, n_layers: int = 5, H: int = 4096, device="cpu",
+                      seed: int | None = None, bs: int | None = None,
+                      max_ctx: int | None = None) -> KvMatInputs:
+    """A drafter shaped like cfg's model (Hkv, D), n_layers draft layers of
+    hidden size H: hidden rows N(0, 1), projection weights N(0, 1/H) (so
+    projections are about unit scale), K-norm gains 1 + 0.1 N(0, 1), all bf16;
+    commit lengths uniform in [1, B]; contexts and paging as cfg's."""
+    seed = (cfg.seed if seed is None else seed) + 15485863
+    bs = cfg.bs if bs is None else bs
+    B, Hkv, D = cfg.B, cfg.Hkv, cfg.D
+    rng = np.random.default_rng(seed)
+    if max_ctx is not None:
+        seq_lens = rng.integers(0, max_ctx + 1, bs).astype(np.int32)
+    elif bs == cfg.bs:
+        seq_lens = seq_lens_for(cfg, rng)
+    else:
+        lo, hi = cfg.ctx[0] if isinstance(cfg.ctx[0], tuple) else (min(cfg.ctx), max(cfg.ctx))
+        seq_lens = rng.integers(lo, hi + 1, bs).astype(np.int32)
+    table, num_pages = paging_for(seq_lens, B, cfg.page_size, rng)
+    g = _gen(device, seed)
+    hidden = randn_bf16((bs * B, H), g, device)
+    w = (torch.randn((n_layers, 2, Hkv * D, H), generator=g, device=device) /
+         math.sqrt(H)).to(torch.bfloat16)
+    kn = (1.0 + 0.1 * torch.randn((n_layers, D), generator=g, device=device)).to(torch.bfloat16)
+    cos, sin = rope_tables(int(seq_lens.max()) + B + 1, D)
+    commit = torch.from_numpy(rng.integers(1, B + 1, bs).astype(np.int32)).to(device)
+    return KvMatInputs(B, n_layers, Hkv, D, hidden, w, kn, cos.to(device), sin.to(device),
+                       commit, seq_lens, table, num_pages)
+
+
 def draft_from(q_rows: np.ndarray, u: np.ndarray) -> np.ndarray:
     """Inverse-CDF draws from rows of q (numpy, for small host-side workloads)."""
     c = np.cumsum(q_rows.astype(np.float64), axis=-1)

@@ -15,6 +15,9 @@ source pages' definitions:
 * I-DLM Block-N round -- "... (IV)", sections 4.3 and 4.3.1 (2N-1 layout,
   verify of the carried specs, correction / bonus, new specs from the MASK
   slots) and 4.6 (KV trim, the request's advance).
+* KV materialisation of the committed prefix -- "... (II)", section 2.2.6 and
+  the DFlash engineering notes (projection across draft layers, K RMS norm,
+  rotate-half RoPE from a cos / sin table, write at the verify cache slots).
 * acceptance -- "... (IV)", section 4.3.1 (min(1, p/q), correction token);
   "Unlocking Lossless Speedups in LLMs via Discrete Diffusion", background on
   speculative decoding and the Psi-Spec step (longest accepted prefix, residual
@@ -72,6 +75,9 @@ def _load():
         lib.oracle_idlm_accept.argtypes = [P, P, P, i64, i64, P, i64, i64, P, P, P, P, i32, i32,
                                            i32, P, P, P, P, P, P, P, P, P, P, i32]
         lib.oracle_idlm_accept.restype = None
+        lib.oracle_kv_materialize.argtypes = [P, P, P, P, P, P, P, P, i32, f64, i32, i32, i32,
+                                               i32, i32, i32, i64, P, P, P, i32]
+        lib.oracle_kv_materialize.restype = i32
         lib.oracle_inv_cdf.argtypes = [P, i32, f64, P]
         lib.oracle_inv_cdf.restype = i32
         lib.oracle_max_threads.argtypes = []
@@ -271,3 +277,34 @@ def inv_cdf(w, u):
     flag = np.zeros(1, np.int32)
     k = lib.oracle_inv_cdf(_ptr(w), w.shape[0], float(u), _ptr(flag))
     return int(k), bool(flag[0])
+
+
+def kv_materialize(hidden_bits, commit_len, positions, cache_loc, w_bits, k_norm_bits, cos_tab,
+                   sin_tab, eps, B, n_layers, Hkv, D, num_slots, nthreads=1):
+    """fp64 K/V of the committed rows.
+
+    hidden_bits [bs*B, H] and w_bits [n_layers, 2, Hkv*D, H], k_norm_bits
+    [n_layers, D]: uint16 bf16 bit patterns; cos_tab / sin_tab [max_pos, D/2]
+    fp32.  Returns (k [bs*B, n_layers, Hkv, D] fp64, v (same), status [bs*B]
+    int32: 1 written, 0 not committed, -1 skipped for a bad slot / position);
+    rows not written hold NaN.
+    """
+    lib = _load()
+    hidden_bits = _c(hidden_bits, np.uint16)
+    rows, H = hidden_bits.shape
+    bs = rows // B
+    w_bits = _c(w_bits, np.uint16)
+    assert w_bits.size == n_layers * 2 * Hkv * D * H
+    k_norm_bits = _c(k_norm_bits, np.uint16)
+    cos_tab = _c(cos_tab, np.float32)
+    sin_tab = _c(sin_tab, np.float32)
+    max_pos = cos_tab.shape[0]
+    k = np.full((rows, n_layers, Hkv, D), np.nan)
+    v = np.full((rows, n_layers, Hkv, D), np.nan)
+    status = np.empty(rows, np.int32)
+    lib.oracle_kv_materialize(_ptr(hidden_bits), _ptr(_c(commit_len, np.int32)),
+                              _ptr(_c(positions, np.int32)), _ptr(_c(cache_loc, np.int32)),
+                              _ptr(w_bits), _ptr(k_norm_bits), _ptr(cos_tab), _ptr(sin_tab),
+                              max_pos, float(eps), bs, B, H, n_layers, Hkv, D, int(num_slots),
+                              _ptr(k), _ptr(v), _ptr(status), int(nthreads))
+    return k, v, status

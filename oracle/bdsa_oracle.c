@@ -22,6 +22,9 @@
  *   [P4] "SGLang dLLM / LLaDA 2.0", section "Attention Mask" (context query
  *        sees the whole cache; intra-block query is a rectangle in block
  *        diffusion, a token-causal trapezoid in chunked prefill).
+ *   [P3] section 2.2.6 and the DFlash engineering notes of "From DFlash to
+ *        dLLM Self-Spec" for the KV materialisation of the committed prefix
+ *        (projection across draft layers, K norm, RoPE, paged write).
  *
  * Every floating-point quantity is computed in fp64 from inputs widened
  * exactly (bf16 -> fp64, fp32 -> fp64), except the two decisions whose
@@ -529,6 +532,109 @@ void oracle_idlm_accept(const int32_t *block_ids, const int32_t *mode, const flo
         }
         free(w);
     }
+}
+
+/* ------------------------------------------------------------------------ */
+/* KV materialisation of the committed prefix  [P3 2.2.6 (after verify, the
+ * target hidden states of the committed prefix are written into the draft KV
+ * cache at the verify step's cache locations); "From DFlash to dLLM
+ * Self-Spec", DFlash engineering notes (KV injection is materialised right
+ * before the draft forward: a batched linear projection across layers, then K
+ * norm and RoPE, then the write into the KV pool)]
+ *
+ * Row (r, i) = r*B + i of `hidden` is committed when i < commit_len[r]
+ * (commit_len clamped to [0, B]).  For every committed row x, draft layer l,
+ * KV head h and d in [0, D):
+ *   k[d] = sum_c W[l][0][h*D + d][c] * x[c]      (K projection)
+ *   v[d] = sum_c W[l][1][h*D + d][c] * x[c]      (V projection)
+ *   kn[d] = k[d] / sqrt(mean_d(k^2) + eps) * g[l][d]           (RMS K norm)
+ *   for d < D/2, with c = cos_tab[pos][d], s = sin_tab[pos][d]:
+ *     ko[d]       = kn[d] * c - kn[d + D/2] * s                 (RoPE, the
+ *     ko[d + D/2] = kn[d + D/2] * c + kn[d] * s                  rotate-half pairing)
+ * pos = positions[row].  Outputs, fp64: k_out / v_out [bs*B, L, Hkv, D] for the
+ * committed rows; rows not written are left as they are.  status[row] = 1
+ * for a written row, 0 for an uncommitted one, -1 for a committed row whose
+ * cache_loc is outside [0, num_slots) or whose position is outside
+ * [0, max_pos) (skipped).  Returns the number of such rows.
+ */
+int oracle_kv_materialize(const uint16_t *hidden, const int32_t *commit_len,
+                          const int32_t *positions, const int32_t *cache_loc,
+                          const uint16_t *w_kv, const uint16_t *k_norm_w, const float *cos_tab,
+                          const float *sin_tab, int max_pos, double eps, int bs, int B, int H,
+                          int n_layers, int Hkv, int D, int64_t num_slots, double *k_out,
+                          double *v_out, int32_t *status, int nthreads) {
+    const int half = D / 2;
+    const long rows = (long)bs * B;
+    int bad = 0;
+    for (long row = 0; row < rows; ++row) {
+        const int r = (int)(row / B), i = (int)(row % B);
+        int cl = commit_len[r];
+        if (cl < 0) cl = 0;
+        if (cl > B) cl = B;
+        if (i >= cl) {
+            status[row] = 0;
+            continue;
+        }
+        const int32_t loc = cache_loc[row], pos = positions[row];
+        if (loc < 0 || (int64_t)loc >= num_slots || pos < 0 || pos >= max_pos) {
+            status[row] = -1;
+            ++bad;
+            continue;
+        }
+        status[row] = 1;
+    }
+#ifdef _OPENMP
+    if (nthreads < 1) nthreads = 1;
+#pragma omp parallel num_threads(nthreads)
+#endif
+    {
+        double *x = (double *)malloc(sizeof(double) * (size_t)H);
+        double *y = (double *)malloc(sizeof(double) * (size_t)D);
+        double *kn = (double *)malloc(sizeof(double) * (size_t)D);
+#ifdef _OPENMP
+#pragma omp for schedule(dynamic)
+#endif
+        for (long row = 0; row < rows; ++row) {
+            if (status[row] != 1) continue;
+            for (int c = 0; c < H; ++c) x[c] = bf16_to_f64(hidden[row * H + c]);
+            const int pos = positions[row];
+            for (int l = 0; l < n_layers; ++l) {
+                for (int kv = 0; kv < 2; ++kv) {
+                    for (int h = 0; h < Hkv; ++h) {
+                        for (int d = 0; d < D; ++d) {
+                            const uint16_t *wr =
+                                w_kv + ((((long)l * 2 + kv) * Hkv + h) * D + d) * (long)H;
+                            double acc = 0.0;
+                            for (int c = 0; c < H; ++c) acc += bf16_to_f64(wr[c]) * x[c];
+                            y[d] = acc;
+                        }
+                        double *dst = (kv == 0 ? k_out : v_out) +
+                                      (((row * n_layers + l) * Hkv + h) * (long)D);
+                        if (kv == 1) {
+                            for (int d = 0; d < D; ++d) dst[d] = y[d];
+                            continue;
+                        }
+                        double ms = 0.0;
+                        for (int d = 0; d < D; ++d) ms += y[d] * y[d];
+                        ms /= (double)D;
+                        const double inv = 1.0 / sqrt(ms + eps);
+                        for (int d = 0; d < D; ++d)
+                            kn[d] = y[d] * inv * bf16_to_f64(k_norm_w[(long)l * D + d]);
+                        for (int d = 0; d < half; ++d) {
+                            const double c = (double)cos_tab[(long)pos * half + d];
+                            const double s = (double)sin_tab[(long)pos * half + d];
+                            dst[d] = kn[d] * c - kn[d + half] * s;
+                            dst[d + half] = kn[d + half] * c + kn[d] * s;
+                        }
+                    }
+                }
+            }
+        }
+        free(x);
+        free(y);
+        free(kn);
+    }
+    return bad;
 }
 
 /* Exposed for tests of the sampling rule itself. */
