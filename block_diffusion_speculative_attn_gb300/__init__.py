@@ -13,6 +13,7 @@ Calls (all asynchronous on the current stream):
   spec_accept       lossless speculative acceptance (stochastic or greedy)
   idlm_prepare      I-DLM Block-N layout of 2N-1 slots (pending, carried specs, masks)
   idlm_accept       I-DLM Block-N verify / correct / draw-new-specs / KV-trim step
+  kv_materialize    draft K/V of the committed rows (projection, K norm, RoPE, paged write)
 """
 from __future__ import annotations
 
@@ -34,7 +35,7 @@ EXPORTS = ("bdsa_status_string", "bdsa_version", "bdsa_prepare_block",
            "bdsa_block_attn_workspace_bytes", "bdsa_block_attn_paged",
            "bdsa_block_attn_paged_append", "bdsa_spec_accept_workspace_bytes",
            "bdsa_spec_accept", "bdsa_spec_accept_noalloc", "bdsa_idlm_prepare",
-           "bdsa_idlm_accept")
+           "bdsa_idlm_accept", "bdsa_kv_materialize_workspace_bytes", "bdsa_kv_materialize")
 
 _lib = None
 
@@ -83,6 +84,11 @@ def lib() -> ctypes.CDLL:
     L.bdsa_idlm_accept.argtypes = [P, P, P, i64, i64, P, i64, i64, P, P, P, P, i32, i32, i32,
                                    P, P, P, P, P, P, P, P, P, i32, P, P]
     L.bdsa_idlm_accept.restype = i32
+    L.bdsa_kv_materialize_workspace_bytes.argtypes = [i32, i32, i32]
+    L.bdsa_kv_materialize_workspace_bytes.restype = sz
+    L.bdsa_kv_materialize.argtypes = [P, P, P, P, i32, i32, i32, P, P, i32, i32, i32, P, P, i32,
+                                      f32, P, P, i64, P, sz, P, P]
+    L.bdsa_kv_materialize.restype = i32
     _lib = L
     return L
 
@@ -323,3 +329,41 @@ def idlm_accept(block_ids, mode, p, q_prev, q_slot, u_acc, u_samp, seq_lens, N: 
         _ptr(dev_status), _stream(dev))
     _check("bdsa_idlm_accept", st)
     return out
+
+
+# ---------------------------------------------------------------------------
+def kv_materialize_workspace_bytes(bs, B, H) -> int:
+    return int(lib().bdsa_kv_materialize_workspace_bytes(bs, B, H))
+
+
+def kv_materialize(hidden, commit_len, positions, cache_loc, w_kv, k_norm_w, rope_cos, rope_sin,
+                   k_cache, v_cache, *, B: int, eps: float, workspace=None, dev_status=None):
+    """bdsa_kv_materialize: the committed rows' K (RMS norm, RoPE) and V of every
+    draft layer, written into k_cache / v_cache [n_layers, slots, Hkv, D] at
+    cache_loc.  hidden [bs*B, H] bf16; w_kv [n_layers, 2, Hkv*D, H] bf16;
+    k_norm_w [n_layers, D] bf16; rope_cos / rope_sin [max_pos, D/2] fp32."""
+    _dev(hidden, "hidden", torch.bfloat16)
+    for name, t in (("commit_len", commit_len), ("positions", positions),
+                    ("cache_loc", cache_loc)):
+        _dev(t, name, torch.int32)
+    for name, t in (("w_kv", w_kv), ("k_norm_w", k_norm_w), ("k_cache", k_cache),
+                    ("v_cache", v_cache)):
+        _dev(t, name, torch.bfloat16)
+    _dev(rope_cos, "rope_cos", torch.float32)
+    _dev(rope_sin, "rope_sin", torch.float32)
+    rows, H = hidden.shape
+    bs = commit_len.shape[0]
+    if rows != bs * B:
+        raise ValueError(f"hidden has {rows} rows, want bs*B = {bs * B}")
+    n_layers, _, HD, _ = w_kv.shape
+    _, num_slots, Hkv, D = k_cache.shape
+    need = kv_materialize_workspace_bytes(bs, B, H)
+    if workspace is None and need > 0:
+        workspace = torch.empty(need, dtype=torch.uint8, device=hidden.device)
+    ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    st = lib().bdsa_kv_materialize(
+        _ptr(hidden), _ptr(commit_len), _ptr(positions), _ptr(cache_loc), bs, B, H, _ptr(w_kv),
+        _ptr(k_norm_w), n_layers, Hkv, D, _ptr(rope_cos), _ptr(rope_sin), rope_cos.shape[0],
+        float(eps), _ptr(k_cache), _ptr(v_cache), int(num_slots), _ptr(workspace), ws_bytes,
+        _ptr(dev_status), _stream(hidden.device))
+    _check("bdsa_kv_materialize", st)

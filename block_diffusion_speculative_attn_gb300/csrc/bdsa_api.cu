@@ -284,4 +284,58 @@ int32_t bdsa_spec_accept(const int32_t *block_ids, const float *p, int64_t p_str
     return bdsa::launch_spec_accept(a, static_cast<cudaStream_t>(stream));
 }
 
+size_t bdsa_kv_materialize_workspace_bytes(int32_t bs, int32_t B, int32_t H) {
+    if (bs <= 0 || B <= 0 || H <= 0) return 0;
+    return bdsa::kvmat_workspace_bytes(bs, B, H);
+}
+
+int32_t bdsa_kv_materialize(const bdsa_bf16 *hidden, const int32_t *commit_len,
+                            const int32_t *positions, const int32_t *cache_loc, int32_t bs,
+                            int32_t B, int32_t H, const bdsa_bf16 *w_kv,
+                            const bdsa_bf16 *k_norm_w, int32_t n_layers, int32_t Hkv, int32_t D,
+                            const float *rope_cos, const float *rope_sin, int32_t max_pos,
+                            float rms_eps, bdsa_bf16 *k_cache, bdsa_bf16 *v_cache,
+                            int64_t num_slots, void *workspace, size_t workspace_bytes,
+                            int32_t *dev_status, void *stream) {
+    if (bs < 0 || B < 1 || H < 1 || n_layers < 1 || Hkv < 1 || D < 1 || max_pos < 1 ||
+        num_slots < 1 || !(rms_eps >= 0.f) || !isfinite(rms_eps))
+        return BDSA_INVALID_ARG;
+    if (D != 128 || H % 128 != 0) return BDSA_UNSUPPORTED;
+    if ((int64_t)bs * B > (1 << 24) || (int64_t)n_layers * 2 * Hkv * D > (1LL << 31) ||
+        num_slots > (1LL << 31))
+        return BDSA_UNSUPPORTED;
+    if (bs == 0) return BDSA_OK;
+    if (!hidden || !commit_len || !positions || !cache_loc || !w_kv || !k_norm_w || !rope_cos ||
+        !rope_sin || !k_cache || !v_cache || !workspace)
+        return BDSA_INVALID_ARG;
+    if (!aligned(hidden, 16) || !aligned(w_kv, 16) || !aligned(k_cache, 16) ||
+        !aligned(v_cache, 16) || !aligned(k_norm_w, 2) || !aligned(rope_cos, 4) ||
+        !aligned(rope_sin, 4) || !aligned(workspace, 256))
+        return BDSA_MISALIGNED;
+    if (workspace_bytes < bdsa::kvmat_workspace_bytes(bs, B, H)) return BDSA_WORKSPACE_TOO_SMALL;
+    bdsa::KvMatArgs a;
+    a.hidden = reinterpret_cast<const uint16_t *>(hidden);
+    a.commit_len = commit_len;
+    a.positions = positions;
+    a.cache_loc = cache_loc;
+    a.w_kv = reinterpret_cast<const uint16_t *>(w_kv);
+    a.k_norm_w = reinterpret_cast<const uint16_t *>(k_norm_w);
+    a.cos_tab = rope_cos;
+    a.sin_tab = rope_sin;
+    a.max_pos = max_pos;
+    a.eps = rms_eps;
+    a.bs = bs;
+    a.B = B;
+    a.H = H;
+    a.n_layers = n_layers;
+    a.Hkv = Hkv;
+    a.D = D;
+    a.k_cache = reinterpret_cast<uint16_t *>(k_cache);
+    a.v_cache = reinterpret_cast<uint16_t *>(v_cache);
+    a.num_slots = num_slots;
+    a.workspace = workspace;
+    a.dev_status = dev_status;
+    return bdsa::launch_kv_materialize(a, static_cast<cudaStream_t>(stream));
+}
+
 }  // extern "C"

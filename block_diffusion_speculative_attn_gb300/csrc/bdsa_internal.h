@@ -92,6 +92,28 @@ struct IdlmArgs {
 
 int launch_idlm_accept(const IdlmArgs &a, cudaStream_t stream);
 
+// ---------------------------------------------------------------- KV materialisation
+// Committed rows of the verify block -> every draft layer's K (RMS norm, RoPE)
+// and V at the rows' cache slots.  Workspace: the gathered row count, one
+// (slot, position) pair and one dense copy of the hidden row per block row.
+struct KvMatArgs {
+    const uint16_t *hidden;    // [bs*B, H]
+    const int32_t *commit_len, *positions, *cache_loc;
+    const uint16_t *w_kv;      // [n_layers, 2, Hkv*D, H]
+    const uint16_t *k_norm_w;  // [n_layers, D]
+    const float *cos_tab, *sin_tab;
+    int max_pos;
+    float eps;
+    int bs, B, H, n_layers, Hkv, D;
+    uint16_t *k_cache, *v_cache;
+    long long num_slots;
+    void *workspace;
+    int32_t *dev_status;
+};
+
+size_t kvmat_workspace_bytes(int bs, int B, int H);
+int launch_kv_materialize(const KvMatArgs &a, cudaStream_t stream);
+
 // ---------------------------------------------------------------- misc
 int device_num_sms(int requested);
 

@@ -353,6 +353,59 @@ int32_t bdsa_idlm_accept(const int32_t *block_ids, const int32_t *mode, const fl
                          int32_t *next_specs, int32_t *next_q_slot, int32_t *new_seq_lens,
                          int32_t *kv_keep, int32_t num_sms, int32_t *dev_status, void *stream);
 
+/* ------------------------------------------------------------------------ */
+/* bdsa_kv_materialize
+ *
+ * "From DFlash to dLLM Self-Spec (II): SGLang Spec V2", section 2.2.6: after
+ * verify, the target hidden states of each request's committed prefix are
+ * written into the draft model's KV cache at the verify step's cache
+ * locations (DFlash KV injection); the DFlash engineering notes of "From
+ * DFlash to dLLM Self-Spec": this is materialised right before the draft
+ * forward as one batched linear projection across the draft layers followed
+ * by K norm and RoPE, then the write into the KV pool.
+ *
+ * Row (r, i) = r*B + i of `hidden` is committed when i < commit_len[r]
+ * (clamped to [0, B]).  For every committed row x, layer l, KV head h, d < D:
+ *   k[d] = sum_c w_kv[l][0][h*D + d][c] x[c],  v[d] = sum_c w_kv[l][1][h*D + d][c] x[c]
+ *   kn[d] = k[d] / sqrt(mean_d k^2 + rms_eps) * k_norm_w[l][d]
+ *   for d < D/2, c = rope_cos[pos][d], s = rope_sin[pos][d], pos = positions[row]:
+ *     k_cache[l][slot][h][d]       = kn[d] c - kn[d + D/2] s
+ *     k_cache[l][slot][h][d + D/2] = kn[d + D/2] c + kn[d] s
+ *   v_cache[l][slot][h][d] = v[d], slot = cache_loc[row].
+ * Uncommitted rows write nothing.  A committed row whose slot is outside
+ * [0, num_slots) or whose position is outside [0, max_pos) writes nothing and
+ * sets *dev_status = BDSA_DEVICE_OUT_OF_RANGE.
+ *
+ * hidden      [bs*B, H] bf16, 16-byte aligned
+ * commit_len  [bs] int32 (e.g. bdsa_spec_accept's commit_len)
+ * positions, cache_loc  [bs*B] int32 (e.g. bdsa_prepare_block's outputs)
+ * w_kv        [n_layers, 2, Hkv*D, H] bf16 (per layer: the K projection's
+ *             rows, then the V projection's; row-major like a linear layer's
+ *             weight), 16-byte aligned
+ * k_norm_w    [n_layers, D] bf16
+ * rope_cos, rope_sin  [max_pos, D/2] fp32: the rotary table (angle of pair d
+ *             at position p)
+ * k_cache, v_cache  [n_layers, num_slots, Hkv, D] bf16, 16-byte aligned
+ * Arithmetic: bf16 products with fp32 accumulation on the tensor cores; norm
+ * and rotation in fp32; one rounding to bf16 at the store.
+ * Supported: D == 128, H a multiple of 128, bs*B <= 2^24.
+ * Workspace: bdsa_kv_materialize_workspace_bytes(bs, B, H) bytes, 256-byte
+ * aligned (the gathered rows: a count, (slot, position) per row and a dense
+ * copy of each committed hidden row); no initialisation needed.
+ * Launches: a gather kernel (one CTA per request) and a projection kernel of
+ * n_layers * 2 * Hkv CTA pairs (thread-block clusters of 2 that split the
+ * hidden dimension), chained with programmatic dependent launch.
+ */
+size_t bdsa_kv_materialize_workspace_bytes(int32_t bs, int32_t B, int32_t H);
+int32_t bdsa_kv_materialize(const bdsa_bf16 *hidden, const int32_t *commit_len,
+                            const int32_t *positions, const int32_t *cache_loc, int32_t bs,
+                            int32_t B, int32_t H, const bdsa_bf16 *w_kv,
+                            const bdsa_bf16 *k_norm_w, int32_t n_layers, int32_t Hkv, int32_t D,
+                            const float *rope_cos, const float *rope_sin, int32_t max_pos,
+                            float rms_eps, bdsa_bf16 *k_cache, bdsa_bf16 *v_cache,
+                            int64_t num_slots, void *workspace, size_t workspace_bytes,
+                            int32_t *dev_status, void *stream);
+
 #ifdef __cplusplus
 }
 #endif

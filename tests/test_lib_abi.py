@@ -158,3 +158,31 @@ def test_idlm_prepare_host_checks(L):
     assert f(FAKE, None, FAKE, FAKE, FAKE, 4, 8, 2, 8, 16, 0, FAKE, FAKE, FAKE, None, None) == 1
     assert f(FAKE, FAKE, FAKE, FAKE, FAKE, 4, 8, 2, 0, 16, 0, FAKE, FAKE, FAKE, None, None) == 1
     assert f(FAKE, FAKE, FAKE, FAKE, FAKE, 4, 8, 2, 8, 0, 0, FAKE, FAKE, FAKE, None, None) == 1
+
+
+def _kvmat(L, **kw):
+    a = dict(hidden=FAKE, cl=FAKE, pos=FAKE, loc=FAKE, bs=2, B=16, H=4096, w=FAKE, g=FAKE,
+             layers=5, Hkv=8, D=128, cos=FAKE, sin=FAKE, max_pos=8192, eps=1e-6, kc=FAKE,
+             vc=FAKE, slots=1 << 20, ws=FAKE, ws_bytes=0)
+    a.update(kw)
+    return L.bdsa_kv_materialize(a["hidden"], a["cl"], a["pos"], a["loc"], a["bs"], a["B"],
+                                 a["H"], a["w"], a["g"], a["layers"], a["Hkv"], a["D"],
+                                 a["cos"], a["sin"], a["max_pos"], a["eps"], a["kc"], a["vc"],
+                                 a["slots"], a["ws"], a["ws_bytes"], None, None)
+
+
+def test_kv_materialize_host_checks(L):
+    assert _kvmat(L, bs=0) == 0
+    assert _kvmat(L, bs=-1) == 1
+    assert _kvmat(L, B=0) == 1
+    assert _kvmat(L, eps=float("nan")) == 1
+    assert _kvmat(L, eps=-1.0) == 1
+    assert _kvmat(L, hidden=None) == 1
+    assert _kvmat(L, ws=None) == 1
+    assert _kvmat(L, D=64) == 2                      # UNSUPPORTED
+    assert _kvmat(L, H=4000) == 2
+    assert _kvmat(L, hidden=FAKE_ODD) == 3           # MISALIGNED
+    assert _kvmat(L, ws_bytes=16) == 4               # WORKSPACE_TOO_SMALL
+    # gathered rows: a count, (slot, position) per row, a dense copy of each row
+    need = L.bdsa_kv_materialize_workspace_bytes(32, 16, 4096)
+    assert need == 256 + 32 * 16 * 8 + 32 * 16 * 4096 * 2
