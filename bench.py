@@ -398,6 +398,58 @@ def time_idlm(cfg: wl.StepConfig, dev, flush, clean, N: int = 8, iters: int = 20
             "gpu_launches_per_round": 2, "iters": iters}
 
 
+def kvmat_bytes(rows: int, H: int, n_layers: int, Hkv: int, D: int) -> int:
+    """Algorithmic bytes of one KV materialisation: every projection weight
+    read once, each committed hidden row read once, its K and V written once."""
+    return (n_layers * 2 * Hkv * D * H * 2 + rows * H * 2 + rows * n_layers * 2 * Hkv * D * 2)
+
+
+def time_kvmat(step: "Step", flush, clean, n_layers: int = 5, H: int = 4096, iters: int = 20):
+    """The draft KV materialisation of this step's committed rows (commit_len
+    from the step's acceptance, positions and slots from its prepare_block)
+    for a drafter of n_layers layers of hidden size H with the model's KV
+    heads, into a draft pool paged like the target cache; L2 flushed before
+    each call; mean event time in ms."""
+    import block_diffusion_speculative_attn_gb300 as bdsa
+    c = step.cfg
+    x = wl.make_kvmat_inputs(c, n_layers=n_layers, H=H, device=step.dev)
+    slots = step.attn.num_pages * c.page_size
+    kc = torch.empty((n_layers, slots, c.Hkv, c.D), dtype=torch.bfloat16, device=step.dev)
+    vc = torch.empty_like(kc)
+    ws = torch.empty(bdsa.kv_materialize_workspace_bytes(c.bs, c.B, H), dtype=torch.uint8,
+                     device=step.dev)
+    commit = step.acc_out["commit_len"]
+    pos = step.prep_out[1].reshape(-1)
+    loc = step.prep_out[2].reshape(-1)
+    status = torch.zeros(1, dtype=torch.int32, device=step.dev)
+    times = []
+    for i in range(iters + 3):
+        flush.zero_()
+        clean.sum()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record()
+        bdsa.kv_materialize(x.hidden, commit, pos, loc, x.w_kv, x.k_norm_w, x.rope_cos,
+                            x.rope_sin, kc, vc, B=c.B, eps=x.eps, workspace=ws,
+                            dev_status=status)
+        e1.record()
+        if i >= 3:
+            times.append((e0, e1))
+    torch.cuda.synchronize()
+    assert status.item() == 0, bdsa.STATUS.get(status.item())
+    ms = statistics.mean(a.elapsed_time(b) for a, b in times)
+    rows = int(commit.sum().item())
+    nbytes = kvmat_bytes(rows, H, n_layers, c.Hkv, c.D)
+    flops = 2 * rows * H * n_layers * 2 * c.Hkv * c.D
+    hbm, tf, src = peaks()
+    achieved = nbytes / (ms / 1e3) / 1e9
+    return {"n_layers": n_layers, "hidden": H, "committed_rows": rows, "launch_ms": ms,
+            "rows_per_s": rows / (ms / 1e3), "tflops": flops / (ms / 1e3) / 1e12,
+            "roofline": {"bound": "hbm", "achieved": achieved, "peak": hbm, "unit": "GB/s",
+                         "frac": achieved / hbm, "peak_source": src,
+                         "algorithmic_bytes_per_launch": nbytes, "flops_per_launch": flops},
+            "gpu_launches_per_call": 2, "iters": iters}
+
+
 # ---------------------------------------------------------------------------
 def oracle_sample(cfg: wl.StepConfig, attn: wl.AttnInputs, acc, reqs, nthreads):
     """Host copies of the sampled requests' inputs (compact page pool)."""
@@ -608,6 +660,7 @@ def main(argv=None):
         fused_append = time_fused_append(step, flush, clean)
         assert step.status.item() == 0, bdsa.STATUS.get(step.status.item())
     idlm = time_idlm(cfg, dev, flush, clean) if (cfg.V and attn_ms is not None) else None
+    kvmat = time_kvmat(step, flush, clean) if (cfg.V and attn_ms is not None) else None
 
     e2e = None
     if not args.no_e2e:
@@ -635,6 +688,7 @@ def main(argv=None):
             "accept_ms": acc_ms,
             "fused_append": fused_append,
             "idlm_round": idlm,
+            "kv_materialize": kvmat,
             "attn_flops_per_launch": attn_flops(cfg, step.attn.seq_lens, cfg.modes[-1]),
             "e2e": e2e, "cpu_baseline": cpu, "gpu_launches": step.launches * K,
             "clocks": clk}

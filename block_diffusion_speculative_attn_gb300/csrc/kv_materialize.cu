@@ -11,8 +11,8 @@
 //   with c = cos[pos][d], s = sin[pos][d] (d < D/2), stored as bf16.
 //
 // Two launches, chained with programmatic dependent launch:
-//   gather  one CTA per request: copies the committed hidden rows into a
-//           dense buffer in the workspace and lists (slot, position) per row;
+//   gather  four CTAs per request: copy the committed hidden rows into a
+//           dense buffer in the workspace and list (slot, position) per row;
 //   project one CTA pair (a thread-block cluster of 2) per (layer, K or V,
 //           head): the two CTAs take the two halves of the hidden dimension.
 //           Each streams its 128 x H/2 weight block once by TMA (128-byte
@@ -37,25 +37,27 @@ namespace bdsa {
 namespace {
 
 constexpr int kD = 128;              // head dim (the accumulator's 128 lanes)
-constexpr int kTok = 128;            // rows per pass (MMA N, TMEM columns)
+constexpr int kBox = 64;             // gathered rows per X box (TMA box, MMA N <= 64)
+constexpr int kMaxBoxes = 4;         // boxes per weight stream: 256 rows, 256 TMEM columns
+constexpr int kStreamRows = kBox * kMaxBoxes;
+constexpr int kTmemCols = kStreamRows;
 constexpr int kThreads = 192;        // warps 0-3 epilogue, 4 TMA producer, 5 MMA
 constexpr int kEpiThreads = 128;
 constexpr int kProducerWarp = 4;
 constexpr int kMmaWarp = 5;
 constexpr int kWStages = 4;
-constexpr int kXStages = 2;
+constexpr int kXStages = 5;
 constexpr int kWSlab = kD * 128;     // 128 weight rows x 64 hidden elements (16 KB)
-constexpr int kXSlab = kTok * 128;   // 128 rows x 64 hidden elements (16 KB)
-constexpr int kXBox = 64;            // rows per X TMA box
+constexpr int kXSlab = kBox * 128;   // 64 gathered rows x 64 hidden elements (8 KB)
 constexpr int kOffW = 0;
 constexpr int kOffX = kOffW + kWStages * kWSlab;
 constexpr int kOffBar = kOffX + kXStages * kXSlab;
 // barriers
 constexpr int kWF = 0;                  // weight stage full
 constexpr int kWE = kWF + kWStages;     // weight stage free
-constexpr int kXF = kWE + kWStages;     // row stage full
-constexpr int kXE = kXF + kXStages;     // row stage free
-constexpr int kAF = kXE + kXStages;     // accumulator of the pass complete
+constexpr int kXF = kWE + kWStages;     // row box full
+constexpr int kXE = kXF + kXStages;     // row box free
+constexpr int kAF = kXE + kXStages;     // accumulators of the stream complete
 constexpr int kTF = kAF + 1;            // epilogue done with TMEM and T
 constexpr int kPR = kTF + 1;            // the partner's T may be written (remote arrive)
 constexpr int kRX = kPR + 1;            // the partner's chunks have landed here
@@ -65,9 +67,10 @@ constexpr int kNumBars = kDR + 1;
 constexpr int kOffMisc = kOffBar + 8 * kNumBars;
 constexpr int kSmem = kOffMisc + 64 + 1024;  // + slack to align the base to 1 KB
 // The epilogue's T tile, [64 rows][128 dims] fp32 (32 KB), aliases the row
-// ring: it is used only between a pass's last MMA and the next pass's first
-// row load.
+// ring: it is used only between a stream's last MMA and the next stream's
+// first row load.  Two CTAs fit one SM (shared memory, 256 TMEM columns each).
 static_assert(kXStages * kXSlab >= 64 * kD * 4, "T fits the row ring");
+static_assert(2 * (kSmem + 1024) <= 228 * 1024, "two CTAs an SM");
 
 struct Params {
     const int32_t *count;      // workspace: number of gathered rows
@@ -149,8 +152,13 @@ __device__ __forceinline__ uint32_t pack2_bf16(float lo, float hi) {
 // Request r's committed rows r*B .. r*B + cl - 1 (cl = commit_len clamped to
 // [0, B]) go to dense rows pre .. pre + cl - 1, pre = the committed rows of
 // the requests before r.  A row whose slot or position is out of range is
-// listed with slot -1 (not written) and reported.
-__global__ void __launch_bounds__(128)
+// listed with slot -1 (not written) and reported.  Grid (bs, kGatherParts):
+// part p of request r copies the p-th share of its rows' 16-byte pieces, four
+// loads in flight a thread.
+constexpr int kGatherParts = 4;
+constexpr int kGatherThreads = 256;
+
+__global__ void __launch_bounds__(kGatherThreads)
     kvmat_gather_kernel(const uint4 *__restrict__ hidden, const int32_t *__restrict__ commit_len,
                         const int32_t *__restrict__ positions,
                         const int32_t *__restrict__ cache_loc, int bs, int B, int H, int max_pos,
@@ -158,39 +166,59 @@ __global__ void __launch_bounds__(128)
                         int32_t *dev_status) {
     // the projection kernel may start streaming weights now
     grid_launch_dependents();
-    __shared__ int s_part[4];
-    const int r = blockIdx.x, tid = threadIdx.x;
+    __shared__ int s_part[kGatherThreads / 32];
+    const int r = blockIdx.x, part = blockIdx.y, tid = threadIdx.x;
     int pre = 0;
-    for (int q = tid; q < r; q += 128) pre += min(max(__ldg(commit_len + q), 0), B);
+    for (int q = tid; q < r; q += kGatherThreads) pre += min(max(__ldg(commit_len + q), 0), B);
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) pre += __shfl_xor_sync(0xffffffffu, pre, o);
     if ((tid & 31) == 0) s_part[tid >> 5] = pre;
     __syncthreads();
-    pre = s_part[0] + s_part[1] + s_part[2] + s_part[3];
+    pre = 0;
+#pragma unroll
+    for (int w = 0; w < kGatherThreads / 32; ++w) pre += s_part[w];
     const int cl = min(max(__ldg(commit_len + r), 0), B);
-    for (int i = tid; i < cl; i += 128) {
-        const long row = (long)r * B + i;
-        int slot = __ldg(cache_loc + row);
-        const int pos = __ldg(positions + row);
-        if (slot < 0 || (long long)slot >= num_slots || pos < 0 || pos >= max_pos) {
-            report_status(dev_status, BDSA_DEVICE_OUT_OF_RANGE);
-            slot = -1;
+    if (part == 0) {
+        for (int i = tid; i < cl; i += kGatherThreads) {
+            const long row = (long)r * B + i;
+            int slot = __ldg(cache_loc + row);
+            const int pos = __ldg(positions + row);
+            if (slot < 0 || (long long)slot >= num_slots || pos < 0 || pos >= max_pos) {
+                report_status(dev_status, BDSA_DEVICE_OUT_OF_RANGE);
+                slot = -1;
+            }
+            meta[pre + i] = make_int2(slot, pos);
         }
-        meta[pre + i] = make_int2(slot, pos);
+        if (r == bs - 1 && tid == 0) *count = pre + cl;
     }
-    const int v = H / 8;  // 16-byte pieces per row
-    const long n = (long)cl * v;
-    const uint4 *src = hidden + (long)r * B * v;
-    uint4 *dst = xc + (long)pre * v;
-    for (long e = tid; e < n; e += 128) dst[e] = __ldg(src + e);
-    if (r == bs - 1 && tid == 0) *count = pre + cl;
+    const long n = (long)cl * (H / 8);  // 16-byte pieces of the request's committed rows
+    const long e0 = n * part / kGatherParts, e1 = n * (part + 1) / kGatherParts;
+    const uint4 *src = hidden + (long)r * B * (H / 8);
+    uint4 *dst = xc + (long)pre * (H / 8);
+    constexpr int kU = 4;
+    for (long e = e0 + tid; e < e1; e += (long)kU * kGatherThreads) {
+        uint4 v[kU];
+#pragma unroll
+        for (int u = 0; u < kU; ++u) {
+            const long k = e + (long)u * kGatherThreads;
+            if (k < e1) v[u] = __ldg(src + k);
+        }
+#pragma unroll
+        for (int u = 0; u < kU; ++u) {
+            const long k = e + (long)u * kGatherThreads;
+            if (k < e1) dst[k] = v[u];
+        }
+    }
 }
 
 // ------------------------------------------------------------------ project
 // CTA (cluster rank `rank`) of head `head` = (l * 2 + kv) * Hkv + h handles
-// hidden elements [rank * H/2, (rank + 1) * H/2).  Pass g covers gathered rows
-// [g * 128, g * 128 + 128).  Its 32-row chunk c is finished by the CTA of rank
-// c % 2, in row (c / 2) * 32 + j of that CTA's T tile.
+// hidden elements [rank * H/2, (rank + 1) * H/2).  Weight stream g covers
+// gathered rows [g * 256, g * 256 + 256) as up to four 64-row boxes, box b
+// accumulating into TMEM columns [64 b, 64 b + 64).  Its 32-row chunk c is
+// finished by the CTA of rank c % 2; the epilogue works in rounds of four
+// chunks (two a CTA), chunk 4 rho + 2 i + rank landing in T rows
+// [32 i, 32 i + 32).
 __global__ void __launch_bounds__(kThreads, 2)
     kvmat_project_kernel(const __grid_constant__ CUtensorMap tm_w,
                          const __grid_constant__ CUtensorMap tm_x, const Params P) {
@@ -214,7 +242,7 @@ __global__ void __launch_bounds__(kThreads, 2)
     const int w_row = head * kD;
 
     if (warp == kMmaWarp) {
-        tmem_alloc(smem_u32(tmem_slot), kTok);
+        tmem_alloc(smem_u32(tmem_slot), kTmemCols);
         tmem_relinquish();
     }
     if (tid == 0) {
@@ -256,13 +284,13 @@ __global__ void __launch_bounds__(kThreads, 2)
             }
             grid_dependency_wait();
             const int M = __ldcg(P.count);
-            const int npass = (M + kTok - 1) / kTok;
-            long issued_w = pre, issued_x = 0;
+            const int nstream = (M + kStreamRows - 1) / kStreamRows;
+            long issued_w = pre, xb = 0;  // weight slabs / row boxes issued so far
             bool ok = true;
-            for (int g = 0; ok && g < npass; ++g) {
-                const int ntok = min(kTok, M - g * kTok);
-                const int nbox = (ntok + kXBox - 1) / kXBox;
-                for (int s = 0; s < nslab; ++s) {
+            for (int g = 0; ok && g < nstream; ++g) {
+                const int nrows = min(kStreamRows, M - g * kStreamRows);
+                const int nbox = (nrows + kBox - 1) / kBox;
+                for (int s = 0; ok && s < nslab; ++s) {
                     const long gs = (long)g * nslab + s;
                     if (gs >= issued_w) {
                         const int st = (int)(gs % kWStages);
@@ -280,21 +308,21 @@ __global__ void __launch_bounds__(kThreads, 2)
                                        P.dev_status);
                         if (!ok) break;
                     }
-                    const int xs = (int)(gs % kXStages);
-                    ok = mbar_wait(bar(kXE + xs), (uint32_t)(((gs / kXStages) & 1) ^ 1),
-                                   abort_flag, P.dev_status);
-                    if (!ok) break;
-                    mbar_arrive_expect_tx(bar(kXF + xs), (uint32_t)(nbox * kXBox * 128));
-                    for (int bx = 0; bx < nbox; ++bx)
-                        tma_load_2d(sbase + kOffX + xs * kXSlab + bx * kXBox * 128, &tm_x,
-                                    k0 + s * 64, g * kTok + bx * kXBox, bar(kXF + xs));
-                    issued_x = gs + 1;
+                    for (int b = 0; b < nbox; ++b, ++xb) {
+                        const int xs = (int)(xb % kXStages);
+                        ok = mbar_wait(bar(kXE + xs), (uint32_t)(((xb / kXStages) & 1) ^ 1),
+                                       abort_flag, P.dev_status);
+                        if (!ok) break;
+                        mbar_arrive_expect_tx(bar(kXF + xs), (uint32_t)kXSlab);
+                        tma_load_2d(sbase + kOffX + xs * kXSlab, &tm_x, k0 + s * 64,
+                                    g * kStreamRows + b * kBox, bar(kXF + xs));
+                    }
                 }
             }
             // drain: the last load into each stage has landed before exit
             for (long i = max(0L, issued_w - kWStages); i < issued_w; ++i)
                 mbar_wait_drain(bar(kWF + (int)(i % kWStages)), (uint32_t)((i / kWStages) & 1));
-            for (long i = max(0L, issued_x - kXStages); i < issued_x; ++i)
+            for (long i = max(0L, xb - kXStages); i < xb; ++i)
                 mbar_wait_drain(bar(kXF + (int)(i % kXStages)), (uint32_t)((i / kXStages) & 1));
         }
     } else if (warp == kMmaWarp) {
@@ -302,36 +330,43 @@ __global__ void __launch_bounds__(kThreads, 2)
         if (lane == 0) {
             grid_dependency_wait();
             const int M = __ldcg(P.count);
-            const int npass = (M + kTok - 1) / kTok;
+            const int nstream = (M + kStreamRows - 1) / kStreamRows;
+            long xb = 0;
             bool ok = true;
-            for (int g = 0; ok && g < npass; ++g) {
-                const int ntok = min(kTok, M - g * kTok);
-                const uint32_t idesc = idesc_bf16_f32(128, (uint32_t)((ntok + 15) & ~15), 0, 0);
+            for (int g = 0; ok && g < nstream; ++g) {
+                const int nrows = min(kStreamRows, M - g * kStreamRows);
+                const int nbox = (nrows + kBox - 1) / kBox;
                 if (g > 0) {
-                    // the epilogue has read the previous pass out of TMEM
+                    // the epilogue has read the previous stream out of TMEM
                     ok = mbar_wait(bar(kTF), (uint32_t)((g - 1) & 1), abort_flag, P.dev_status);
                     if (!ok) break;
                 }
-                for (int s = 0; s < nslab; ++s) {
+                for (int s = 0; ok && s < nslab; ++s) {
                     const long gs = (long)g * nslab + s;
-                    const int ws = (int)(gs % kWStages), xs = (int)(gs % kXStages);
+                    const int ws = (int)(gs % kWStages);
                     ok = mbar_wait(bar(kWF + ws), (uint32_t)((gs / kWStages) & 1), abort_flag,
                                    P.dev_status);
-                    if (ok)
-                        ok = mbar_wait(bar(kXF + xs), (uint32_t)((gs / kXStages) & 1),
-                                       abort_flag, P.dev_status);
-                    if (!ok) break;
-                    tc_fence_after();
+                    for (int b = 0; ok && b < nbox; ++b, ++xb) {
+                        const int xs = (int)(xb % kXStages);
+                        ok = mbar_wait(bar(kXF + xs), (uint32_t)((xb / kXStages) & 1), abort_flag,
+                                       P.dev_status);
+                        if (!ok) break;
+                        tc_fence_after();
+                        const int rows_b = min(kBox, nrows - b * kBox);
+                        const uint32_t idesc =
+                            idesc_bf16_f32(128, (uint32_t)((rows_b + 15) & ~15), 0, 0);
 #pragma unroll
-                    for (int kk = 0; kk < 4; ++kk) {
-                        const uint64_t a =
-                            smem_desc_sw128(sbase + kOffW + ws * kWSlab + kk * 32, 16, 1024);
-                        const uint64_t b =
-                            smem_desc_sw128(sbase + kOffX + xs * kXSlab + kk * 32, 16, 1024);
-                        umma_bf16(tmem, a, b, idesc, (s > 0 || kk > 0) ? 1u : 0u);
+                        for (int kk = 0; kk < 4; ++kk) {
+                            const uint64_t a =
+                                smem_desc_sw128(sbase + kOffW + ws * kWSlab + kk * 32, 16, 1024);
+                            const uint64_t bd =
+                                smem_desc_sw128(sbase + kOffX + xs * kXSlab + kk * 32, 16, 1024);
+                            umma_bf16(tmem + (uint32_t)(b * kBox), a, bd, idesc,
+                                      (s > 0 || kk > 0) ? 1u : 0u);
+                        }
+                        umma_commit(bar(kXE + xs));
                     }
-                    umma_commit(bar(kWE + ws));
-                    umma_commit(bar(kXE + xs));
+                    if (ok) umma_commit(bar(kWE + ws));
                 }
                 if (ok) umma_commit(bar(kAF));
             }
@@ -341,10 +376,10 @@ __global__ void __launch_bounds__(kThreads, 2)
         }
     } else {
         // ------------------------------------------------ epilogue (warps 0-3)
-        // Thread tid holds TMEM lane tid = head dim d of the accumulator.
+        // Thread tid holds TMEM lane tid = head dim d of the accumulators.
         grid_dependency_wait();
         const int M = __ldcg(P.count);
-        const int npass = (M + kTok - 1) / kTok;
+        const int nstream = (M + kStreamRows - 1) / kStreamRows;
         const int d = tid;
         const uint32_t lane_base = (uint32_t)(warp * 32) << 16;
         float *T = reinterpret_cast<float *>(smem + kOffX);  // [64][kD]
@@ -363,7 +398,8 @@ __global__ void __launch_bounds__(kThreads, 2)
                 gain[16 + e] = bf16_to_f32(__ldg(P.k_norm_w + (long)l * kD + 64 + 16 * q + e));
             }
         }
-        int eb = 0;  // phases of kEB so far
+        int eb = 0;     // phases of kEB so far
+        int round = 0;  // exchange rounds so far (phases of kPR and kRX)
         auto epi_sync = [&]() -> bool {
             __syncwarp();
             if (lane == 0) mbar_arrive(bar(kEB));
@@ -373,91 +409,107 @@ __global__ void __launch_bounds__(kThreads, 2)
             return r;
         };
         bool ok = true;
-        for (int g = 0; ok && g < npass; ++g) {
-            const int ntok = min(kTok, M - g * kTok);
-            const int nchunk = (ntok + 31) / 32;
+        for (int g = 0; ok && g < nstream; ++g) {
+            const int nrows = min(kStreamRows, M - g * kStreamRows);
+            const int nchunk = (nrows + 31) / 32;
             ok = __all_sync(0xffffffffu,
                             mbar_wait(bar(kAF), (uint32_t)(g & 1), abort_flag, P.dev_status));
             if (!ok) break;
             tc_fence_after();
-            // this CTA's T may take the partner's chunks now (its MMAs are done)
-            if (tid == 0) mbar_arrive_remote_release(pr_peer);
-            ok = __all_sync(0xffffffffu, mbar_wait_cluster(bar(kPR), (uint32_t)(g & 1),
-                                                           abort_flag, P.dev_status));
-            if (!ok) break;
-            for (int c = (int)peer; c < nchunk; c += 2) {
-                float v[32];
-                tmem_ld32(tmem + lane_base + (uint32_t)(c * 32), v);
-                tmem_wait_ld();
-                const uint32_t base = t_peer + (uint32_t)(((c >> 1) * 32 * kD + d) * 4);
-#pragma unroll
-                for (int j = 0; j < 32; ++j) st_cluster_f32(base + (uint32_t)(j * kD * 4), v[j]);
-            }
-            mbar_arrive_remote_release(rx_peer);
-            ok = __all_sync(0xffffffffu, mbar_wait_cluster(bar(kRX), (uint32_t)(g & 1),
-                                                           abort_flag, P.dev_status));
-            if (!ok) break;
-            for (int c = (int)rank; c < nchunk; c += 2) {
-                float v[32];
-                tmem_ld32(tmem + lane_base + (uint32_t)(c * 32), v);
-                tmem_wait_ld();
-                float *col = T + (c >> 1) * 32 * kD + d;
-#pragma unroll
-                for (int j = 0; j < 32; ++j) col[j * kD] += v[j];
-            }
-            tc_fence_before();
-            ok = epi_sync();  // T complete: every epilogue warp has added its dims
-            if (!ok) break;
-            // finish this CTA's rows, four threads a row
-            for (int it = 0; it < 2; ++it) {
-                const int tl = it * 32 + (tid >> 2);       // row of T
-                const int c = 2 * (tl >> 5) + (int)rank;   // its chunk of the pass
-                const int t = c * 32 + (tl & 31);          // its row in the pass
-                const bool live = t < ntok;
-                float v[32];
-                const float *row = T + tl * kD;
-#pragma unroll
-                for (int e = 0; e < 16; e += 4) {
-                    const float4 lo = *reinterpret_cast<const float4 *>(row + 16 * q + e);
-                    const float4 hi = *reinterpret_cast<const float4 *>(row + 64 + 16 * q + e);
-                    v[e] = lo.x; v[e + 1] = lo.y; v[e + 2] = lo.z; v[e + 3] = lo.w;
-                    v[16 + e] = hi.x; v[17 + e] = hi.y; v[18 + e] = hi.z; v[19 + e] = hi.w;
+            for (int c0 = 0; ok && c0 < nchunk; c0 += 4, ++round) {
+                // This CTA's T may take the partner's chunks: its MMAs are done
+                // and (after the first round) its warps have finished reading T.
+                if (c0 > 0) {
+                    ok = epi_sync();
+                    if (!ok) break;
                 }
-                const int2 m = live ? __ldcg(P.meta + (long)g * kTok + t) : make_int2(-1, 0);
-                if (kv == 0) {
-                    float ss = 0.f;
+                if (tid == 0) mbar_arrive_remote_release(pr_peer);
+                ok = __all_sync(0xffffffffu, mbar_wait_cluster(bar(kPR), (uint32_t)(round & 1),
+                                                               abort_flag, P.dev_status));
+                if (!ok) break;
+                for (int i = 0; i < 2; ++i) {
+                    const int c = c0 + 2 * i + (int)peer;
+                    if (c >= nchunk) break;
+                    float v[32];
+                    tmem_ld32(tmem + lane_base + (uint32_t)(c * 32), v);
+                    tmem_wait_ld();
+                    const uint32_t base = t_peer + (uint32_t)((i * 32 * kD + d) * 4);
 #pragma unroll
-                    for (int e = 0; e < 32; ++e) ss = fmaf(v[e], v[e], ss);
-                    ss += __shfl_xor_sync(0xffffffffu, ss, 1);
-                    ss += __shfl_xor_sync(0xffffffffu, ss, 2);
-                    const float inv = rsqrtf(ss * (1.f / kD) + P.eps);
+                    for (int j = 0; j < 32; ++j)
+                        st_cluster_f32(base + (uint32_t)(j * kD * 4), v[j]);
+                }
+                mbar_arrive_remote_release(rx_peer);
+                ok = __all_sync(0xffffffffu, mbar_wait_cluster(bar(kRX), (uint32_t)(round & 1),
+                                                               abort_flag, P.dev_status));
+                if (!ok) break;
+                for (int i = 0; i < 2; ++i) {
+                    const int c = c0 + 2 * i + (int)rank;
+                    if (c >= nchunk) break;
+                    float v[32];
+                    tmem_ld32(tmem + lane_base + (uint32_t)(c * 32), v);
+                    tmem_wait_ld();
+                    float *col = T + i * 32 * kD + d;
 #pragma unroll
-                    for (int e = 0; e < 32; ++e) v[e] = v[e] * inv * gain[e];
-                    if (live && m.x >= 0) {
-                        const float *cs = P.cos_tab + (long)m.y * (kD / 2) + 16 * q;
-                        const float *sn = P.sin_tab + (long)m.y * (kD / 2) + 16 * q;
+                    for (int j = 0; j < 32; ++j) col[j * kD] += v[j];
+                }
+                tc_fence_before();
+                ok = epi_sync();  // T complete: every epilogue warp has added its dims
+                if (!ok) break;
+                // finish this CTA's rows of the round, four threads a row
+                for (int i = 0; i < 2; ++i) {
+                    const int tl = i * 32 + (tid >> 2);             // row of T
+                    const int c = c0 + 2 * i + (int)rank;           // its chunk
+                    const int t = c * 32 + (tl & 31);               // its row in the stream
+                    const bool live = t < nrows;
+                    float v[32];
+                    const float *row = T + tl * kD;
 #pragma unroll
-                        for (int e = 0; e < 16; ++e) {
-                            const float cv = __ldg(cs + e), sv = __ldg(sn + e);
-                            const float a0 = v[e], a1 = v[16 + e];
-                            v[e] = a0 * cv - a1 * sv;
-                            v[16 + e] = a1 * cv + a0 * sv;
+                    for (int e = 0; e < 16; e += 4) {
+                        const float4 lo = *reinterpret_cast<const float4 *>(row + 16 * q + e);
+                        const float4 hi =
+                            *reinterpret_cast<const float4 *>(row + 64 + 16 * q + e);
+                        v[e] = lo.x; v[e + 1] = lo.y; v[e + 2] = lo.z; v[e + 3] = lo.w;
+                        v[16 + e] = hi.x; v[17 + e] = hi.y; v[18 + e] = hi.z; v[19 + e] = hi.w;
+                    }
+                    const int2 m = live ? __ldcg(P.meta + (long)g * kStreamRows + t)
+                                        : make_int2(-1, 0);
+                    if (kv == 0) {
+                        float ss = 0.f;
+#pragma unroll
+                        for (int e = 0; e < 32; ++e) ss = fmaf(v[e], v[e], ss);
+                        ss += __shfl_xor_sync(0xffffffffu, ss, 1);
+                        ss += __shfl_xor_sync(0xffffffffu, ss, 2);
+                        const float inv = rsqrtf(ss * (1.f / kD) + P.eps);
+#pragma unroll
+                        for (int e = 0; e < 32; ++e) v[e] = v[e] * inv * gain[e];
+                        if (live && m.x >= 0) {
+                            const float *cs = P.cos_tab + (long)m.y * (kD / 2) + 16 * q;
+                            const float *sn = P.sin_tab + (long)m.y * (kD / 2) + 16 * q;
+#pragma unroll
+                            for (int e = 0; e < 16; ++e) {
+                                const float cv = __ldg(cs + e), sv = __ldg(sn + e);
+                                const float a0 = v[e], a1 = v[16 + e];
+                                v[e] = a0 * cv - a1 * sv;
+                                v[16 + e] = a1 * cv + a0 * sv;
+                            }
                         }
                     }
-                }
-                if (live && m.x >= 0) {
-                    uint16_t *dst = cache + (((long)l * P.num_slots + m.x) * Hkv + h) * kD;
-                    uint4 w[4];
-                    uint32_t *wp = reinterpret_cast<uint32_t *>(w);
+                    if (live && m.x >= 0) {
+                        uint16_t *dst = cache + (((long)l * P.num_slots + m.x) * Hkv + h) * kD;
+                        uint4 w[4];
+                        uint32_t *wp = reinterpret_cast<uint32_t *>(w);
 #pragma unroll
-                    for (int e = 0; e < 16; ++e) wp[e] = pack2_bf16(v[2 * e], v[2 * e + 1]);
-                    *reinterpret_cast<uint4 *>(dst + 16 * q) = w[0];
-                    *reinterpret_cast<uint4 *>(dst + 16 * q + 8) = w[1];
-                    *reinterpret_cast<uint4 *>(dst + 64 + 16 * q) = w[2];
-                    *reinterpret_cast<uint4 *>(dst + 64 + 16 * q + 8) = w[3];
+                        for (int e = 0; e < 16; ++e) wp[e] = pack2_bf16(v[2 * e], v[2 * e + 1]);
+                        *reinterpret_cast<uint4 *>(dst + 16 * q) = w[0];
+                        *reinterpret_cast<uint4 *>(dst + 16 * q + 8) = w[1];
+                        *reinterpret_cast<uint4 *>(dst + 64 + 16 * q) = w[2];
+                        *reinterpret_cast<uint4 *>(dst + 64 + 16 * q + 8) = w[3];
+                    }
                 }
             }
-            // this warp is done with TMEM and with T for this pass
+            if (!ok) break;
+            // this warp is done with TMEM and with T for this stream
+            tc_fence_before();
             __syncwarp();
             if (lane == 0) mbar_arrive(bar(kTF));
         }
@@ -470,7 +522,7 @@ __global__ void __launch_bounds__(kThreads, 2)
     cluster_sync_all();
     if (warp == kMmaWarp) {
         tc_fence_after();
-        tmem_dealloc(tmem, kTok);
+        tmem_dealloc(tmem, kTmemCols);
     }
 }
 
@@ -538,9 +590,9 @@ int launch_kv_materialize(const KvMatArgs &a, cudaStream_t stream) {
     const long heads = (long)a.n_layers * 2 * a.Hkv;
     CUtensorMap tm_w, tm_x;
     if (!encode_rows(enc, &tm_w, a.w_kv, (uint64_t)heads * kD, (uint64_t)a.H, kD) ||
-        !encode_rows(enc, &tm_x, xc, (uint64_t)a.bs * a.B, (uint64_t)a.H, kXBox))
+        !encode_rows(enc, &tm_x, xc, (uint64_t)a.bs * a.B, (uint64_t)a.H, kBox))
         return BDSA_CUDA_ERROR;
-    kvmat_gather_kernel<<<a.bs, 128, 0, stream>>>(
+    kvmat_gather_kernel<<<dim3((unsigned)a.bs, kGatherParts), kGatherThreads, 0, stream>>>(
         reinterpret_cast<const uint4 *>(a.hidden), a.commit_len, a.positions, a.cache_loc, a.bs,
         a.B, a.H, a.max_pos, a.num_slots, count, meta, reinterpret_cast<uint4 *>(xc),
         a.dev_status);
@@ -562,8 +614,12 @@ int launch_kv_materialize(const KvMatArgs &a, cudaStream_t stream) {
     P.dev_status = a.dev_status;
     static bool attr_set = false;
     if (!attr_set) {
+        // two CTAs an SM need the largest shared-memory carve-out
         if (cudaFuncSetAttribute(kvmat_project_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                 kSmem) != cudaSuccess)
+                                 kSmem) != cudaSuccess ||
+            cudaFuncSetAttribute(kvmat_project_kernel,
+                                 cudaFuncAttributePreferredSharedMemoryCarveout,
+                                 cudaSharedmemCarveoutMaxShared) != cudaSuccess)
             return BDSA_CUDA_ERROR;
         attr_set = true;
     }

@@ -392,7 +392,7 @@ int32_t bdsa_idlm_accept(const int32_t *block_ids, const int32_t *mode, const fl
  * Workspace: bdsa_kv_materialize_workspace_bytes(bs, B, H) bytes, 256-byte
  * aligned (the gathered rows: a count, (slot, position) per row and a dense
  * copy of each committed hidden row); no initialisation needed.
- * Launches: a gather kernel (one CTA per request) and a projection kernel of
+ * Launches: a gather kernel (four CTAs per request) and a projection kernel of
  * n_layers * 2 * Hkv CTA pairs (thread-block clusters of 2 that split the
  * hidden dimension), chained with programmatic dependent launch.
  */
