@@ -18,6 +18,10 @@ source pages' definitions:
 * KV materialisation of the committed prefix -- "... (II)", section 2.2.6 and
   the DFlash engineering notes (projection across draft layers, K RMS norm,
   rotate-half RoPE from a cos / sin table, write at the verify cache slots).
+* tree verify -- "Unlocking Lossless Speedups in LLMs via Discrete Diffusion",
+  the Psi-Spec Tree sampler (a token tree verified in parallel with tree
+  attention, lossless rejection sampling); "SGLang dLLM / LLaDA 2.0",
+  "Attention Mask" (the intra-block mask follows the verify structure).
 * acceptance -- "... (IV)", section 4.3.1 (min(1, p/q), correction token);
   "Unlocking Lossless Speedups in LLMs via Discrete Diffusion", background on
   speculative decoding and the Psi-Spec step (longest accepted prefix, residual
@@ -78,6 +82,14 @@ def _load():
         lib.oracle_kv_materialize.argtypes = [P, P, P, P, P, P, P, P, i32, f64, i32, i32, i32,
                                                i32, i32, i32, i64, P, P, P, i32]
         lib.oracle_kv_materialize.restype = i32
+        lib.oracle_tree_prepare.argtypes = [P, P, P, i32, i32, i32, i32, i32, P, P, P, P]
+        lib.oracle_tree_prepare.restype = i32
+        lib.oracle_block_attn_tree.argtypes = [P, P, P, P, i32, i32, P, P, i32, i32, i32, i32,
+                                               i32, i32, f64, P, P, i32]
+        lib.oracle_block_attn_tree.restype = i32
+        lib.oracle_tree_accept.argtypes = [P, P, P, i64, i64, P, P, i32, i32, i32, P, P, P, P, P,
+                                           P, i32]
+        lib.oracle_tree_accept.restype = None
         lib.oracle_inv_cdf.argtypes = [P, i32, f64, P]
         lib.oracle_inv_cdf.restype = i32
         lib.oracle_max_threads.argtypes = []
@@ -308,3 +320,66 @@ def kv_materialize(hidden_bits, commit_len, positions, cache_loc, w_bits, k_norm
                               max_pos, float(eps), bs, B, H, n_layers, Hkv, D, int(num_slots),
                               _ptr(k), _ptr(v), _ptr(status), int(nthreads))
     return k, v, status
+
+
+def tree_prepare(parent, seq_lens, block_table, num_pages, page_size):
+    """Token tree of B nodes per request (parent [bs, B], node 0 the root with
+    parent -1).  Returns (depth, positions, cache_loc [bs, B] int32, mask
+    [bs, B] uint64 ancestor-or-self bits, n_bad)."""
+    lib = _load()
+    parent = _c(parent, np.int32)
+    bs, B = parent.shape
+    block_table = _c(block_table, np.int32)
+    out = [np.empty((bs, B), np.int32) for _ in range(3)]
+    mask = np.empty((bs, B), np.uint64)
+    bad = lib.oracle_tree_prepare(_ptr(parent), _ptr(_c(seq_lens, np.int32)), _ptr(block_table),
+                                  block_table.shape[1], num_pages, bs, B, page_size,
+                                  *[_ptr(o) for o in out], _ptr(mask))
+    return out[0], out[1], out[2], mask, int(bad)
+
+
+def block_attn_tree(q_bits, k_bits, v_bits, block_table, seq_lens, parent, B, Hq, Hkv, D,
+                    page_size, scale, num_pages=None, nthreads=1):
+    """fp64 tree attention: block row i sees the context and its ancestors-or-self."""
+    lib = _load()
+    q_bits = _c(q_bits, np.uint16)
+    k_bits = _c(k_bits, np.uint16)
+    v_bits = _c(v_bits, np.uint16)
+    block_table = _c(block_table, np.int32)
+    bs, max_pages = block_table.shape
+    if num_pages is None:
+        num_pages = k_bits.shape[0] // page_size
+    out = np.empty((bs * B, Hq, D), np.float64)
+    lse = np.empty((bs * B, Hq), np.float64)
+    bad = lib.oracle_block_attn_tree(_ptr(q_bits), _ptr(k_bits), _ptr(v_bits), _ptr(block_table),
+                                     max_pages, num_pages, _ptr(_c(seq_lens, np.int32)),
+                                     _ptr(_c(parent, np.int32)), bs, B, Hq, Hkv, D, page_size,
+                                     float(scale), _ptr(out), _ptr(lse), int(nthreads))
+    if bad:
+        raise ValueError(f"oracle: {bad} rows referenced out-of-range pages")
+    return out, lse
+
+
+TREE_KEYS = ("accept_len", "bonus_id", "new_seq_lens")
+
+
+def tree_accept(block_ids, parent, p, u, seq_lens, *, p_strides=None, V=None, nthreads=1):
+    """Tree acceptance (u None: greedy).  p: fp32 [bs, B, V].  Returns a dict of
+    int32 arrays: TREE_KEYS [bs], path [bs, B], out_tokens [bs, B], flags [bs]."""
+    lib = _load()
+    block_ids = _c(block_ids, np.int32)
+    bs, B = block_ids.shape
+    p = np.ascontiguousarray(p, dtype=np.float32)
+    if V is None:
+        V = p.shape[-1]
+    if p_strides is None:
+        p_strides = (B * V, V)
+    out = {k: np.empty(bs, np.int32) for k in TREE_KEYS + ("flags",)}
+    out["path"] = np.empty((bs, B), np.int32)
+    out["out_tokens"] = np.empty((bs, B), np.int32)
+    lib.oracle_tree_accept(_ptr(block_ids), _ptr(_c(parent, np.int32)), _ptr(p), p_strides[0],
+                           p_strides[1], None if u is None else _ptr(_c(u, np.float32)),
+                           _ptr(_c(seq_lens, np.int32)), bs, B, V, _ptr(out["accept_len"]),
+                           _ptr(out["path"]), _ptr(out["out_tokens"]), _ptr(out["bonus_id"]),
+                           _ptr(out["new_seq_lens"]), _ptr(out["flags"]), int(nthreads))
+    return out

@@ -637,6 +637,203 @@ int oracle_kv_materialize(const uint16_t *hidden, const int32_t *commit_len,
     return bad;
 }
 
+/* ------------------------------------------------------------------------ */
+/* Tree verify  ["Unlocking Lossless Speedups in LLMs via Discrete Diffusion",
+ * Psi-Spec Tree sampler (per position the top-K tokens, the top-V prefixes by
+ * log-probability kept, the tree verified in parallel with tree attention);
+ * "SGLang dLLM / LLaDA 2.0", "Attention Mask" (the block's queries see the
+ * whole context; inside the block the mask is set by the verify structure)]
+ *
+ * A request's block holds a token tree of B nodes in topological order: node 0
+ * is the root (the verified token, parent -1), node i > 0 has a parent in
+ * [0, i).  A parent outside that range makes the node a root of its own
+ * (reported).  Node i sits at block slot i (cache position L + i) and at
+ * sequence position L + depth(i).
+ */
+static int tree_parent(const int32_t *par, int i) {
+    if (i <= 0) return -1;
+    int p = par[i];
+    return (p >= 0 && p < i) ? p : -1;
+}
+
+static int tree_is_ancestor(const int32_t *par, int j, int i) {  /* j == i counts */
+    for (int k = i; k >= 0; k = tree_parent(par, k))
+        if (k == j) return 1;
+    return 0;
+}
+
+/* depth, positions L + depth, cache_loc of block slot i (as prepare_block),
+ * mask[i] = bit j set iff node j is node i or one of its ancestors.  Returns
+ * the number of invalid parents plus failed page lookups. */
+int oracle_tree_prepare(const int32_t *parent, const int32_t *seq_lens,
+                        const int32_t *block_table, int max_pages_per_req, int num_pages, int bs,
+                        int B, int page_size, int32_t *depth, int32_t *positions,
+                        int32_t *cache_loc, uint64_t *mask) {
+    int bad = 0;
+    for (int r = 0; r < bs; ++r) {
+        const int32_t *par = parent + (long)r * B;
+        for (int i = 0; i < B; ++i) {
+            const long row = (long)r * B + i;
+            if (i == 0 ? par[0] != -1 : tree_parent(par, i) < 0) ++bad;
+            int d = -1;
+            uint64_t m = 0;
+            for (int k = i; k >= 0; k = tree_parent(par, k)) {
+                ++d;
+                m |= (uint64_t)1 << k;
+            }
+            depth[row] = d;
+            mask[row] = m;
+            const long L = seq_lens[r];
+            positions[row] = (int32_t)(L + d);
+            const long t = L + i;
+            int32_t loc = -1;
+            if (L >= 0 && t / page_size < max_pages_per_req) {
+                int32_t page = block_table[(long)r * max_pages_per_req + t / page_size];
+                if (page >= 0 && page < num_pages) loc = (int32_t)((long)page * page_size + t % page_size);
+            }
+            if (loc < 0) ++bad;
+            cache_loc[row] = loc;
+        }
+    }
+    return bad;
+}
+
+/* Tree attention: as oracle_block_attn, with the intra-block mask "block key
+ * j is visible to block row i iff j is i or an ancestor of i". */
+int oracle_block_attn_tree(const uint16_t *q, const uint16_t *k_cache, const uint16_t *v_cache,
+                           const int32_t *block_table, int max_pages_per_req, int num_pages,
+                           const int32_t *seq_lens, const int32_t *parent, int bs, int B, int Hq,
+                           int Hkv, int D, int page_size, double scale, double *out,
+                           double *lse, int nthreads) {
+    long max_keys = 0;
+    for (int r = 0; r < bs; ++r)
+        if ((long)seq_lens[r] + B > max_keys) max_keys = (long)seq_lens[r] + B;
+    int bad = 0;
+    const long units = (long)bs * Hq;
+    const int G = Hq / Hkv;
+#ifdef _OPENMP
+    if (nthreads < 1) nthreads = 1;
+#pragma omp parallel num_threads(nthreads) reduction(+ : bad)
+#endif
+    {
+        double *scores = (double *)malloc(sizeof(double) * (size_t)(max_keys > 0 ? max_keys : 1));
+#ifdef _OPENMP
+#pragma omp for schedule(dynamic, 1)
+#endif
+        for (long u = 0; u < units; ++u) {
+            const int r = (int)(u / Hq), j = (int)(u % Hq), h = j / G;
+            const int32_t *par = parent + (long)r * B;
+            const long L = seq_lens[r];
+            for (int i = 0; i < B; ++i) {
+                const long row = ((long)r * B + i) * Hq + j;
+                const uint16_t *qrow = q + row * D;
+                double smax = -INFINITY;
+                int rc = 0;
+                for (long t = 0; t < L + B; ++t) {
+                    scores[t] = -INFINITY;
+                    if (!(t < L || tree_is_ancestor(par, (int)(t - L), i))) continue;
+                    const long page_idx = t / page_size;
+                    int32_t page = page_idx < max_pages_per_req
+                                       ? block_table[(long)r * max_pages_per_req + page_idx]
+                                       : -1;
+                    if (page < 0 || page >= num_pages) {
+                        rc = -1;
+                        break;
+                    }
+                    const uint16_t *krow = k_cache + (((long)page * page_size + t % page_size) * Hkv + h) * D;
+                    double dot = 0.0;
+                    for (int d = 0; d < D; ++d) dot += bf16_to_f64(qrow[d]) * bf16_to_f64(krow[d]);
+                    scores[t] = scale * dot;
+                    if (scores[t] > smax) smax = scores[t];
+                }
+                double *o = out + row * D;
+                if (rc != 0) {
+                    ++bad;
+                    for (int d = 0; d < D; ++d) o[d] = NAN;
+                    if (lse) lse[row] = NAN;
+                    continue;
+                }
+                double denom = 0.0;
+                for (long t = 0; t < L + B; ++t)
+                    if (scores[t] != -INFINITY) denom += exp(scores[t] - smax);
+                for (int d = 0; d < D; ++d) o[d] = 0.0;
+                for (long t = 0; t < L + B; ++t) {
+                    if (scores[t] == -INFINITY) continue;
+                    const double w = exp(scores[t] - smax) / denom;
+                    const int32_t page = block_table[(long)r * max_pages_per_req + t / page_size];
+                    const uint16_t *vrow = v_cache + (((long)page * page_size + t % page_size) * Hkv + h) * D;
+                    for (int d = 0; d < D; ++d) o[d] += w * bf16_to_f64(vrow[d]);
+                }
+                if (lse) lse[row] = smax + log(denom);
+            }
+        }
+        free(scores);
+    }
+    return bad;
+}
+
+/* Tree acceptance.  p[r, n] (strides in elements) is the verifier's
+ * distribution after node n, i.e. for n's children.  Walk from the root: at
+ * node n of depth d draw x = InvCDF(p[r, n], u[r, d]) (stochastic) or x =
+ * argmax p[r, n] (greedy, u == NULL; lowest index on ties); if a child of n
+ * carries token x (the lowest-index such child) it is accepted and the walk
+ * goes on from it, else x is emitted (the correction, or the bonus when n is a
+ * leaf) and the walk ends.  With deterministic drafts (the tree's tokens are
+ * chosen, not sampled) this is rejection sampling with one-hot draft
+ * distributions: the emitted sequence follows the verifier exactly.
+ * Outputs: accept_len = accepted nodes below the root; path[r] = node indices
+ * root, accepted nodes, -1 padding; out_tokens[r] = accepted tokens then x,
+ * -1 padding; bonus_id = x; new_seq_lens = L + accept_len + 1.
+ * flags: bit 1 a draw within 1e-9 * S of a boundary of its token, bit 4 an
+ * argmax tie (greedy). */
+void oracle_tree_accept(const int32_t *block_ids, const int32_t *parent, const float *p,
+                        int64_t p_stride_r, int64_t p_stride_n, const float *u,
+                        const int32_t *seq_lens, int bs, int B, int V, int32_t *accept_len,
+                        int32_t *path, int32_t *out_tokens, int32_t *bonus_id,
+                        int32_t *new_seq_lens, int32_t *flags, int nthreads) {
+#ifdef _OPENMP
+    if (nthreads < 1) nthreads = 1;
+#pragma omp parallel for num_threads(nthreads) schedule(static)
+#endif
+    for (int r = 0; r < bs; ++r) {
+        const int32_t *ids = block_ids + (long)r * B;
+        const int32_t *par = parent + (long)r * B;
+        int flag = 0, n = 0, depth = 0, x = -1;
+        for (int i = 0; i < B; ++i) {
+            path[(long)r * B + i] = -1;
+            out_tokens[(long)r * B + i] = -1;
+        }
+        path[(long)r * B] = 0;
+        for (;;) {
+            const float *pn = p + (long)r * p_stride_r + (long)n * p_stride_n;
+            if (u != NULL) {
+                int near = 0;
+                x = inv_cdf_f32w(pn, V, (double)u[(long)r * B + depth], &near);
+                if (near) flag |= 2;
+            } else {
+                int tie = 0;
+                x = argmax_lowest(pn, V, &tie);
+                if (tie) flag |= 16;
+            }
+            int child = -1;
+            for (int c = n + 1; c < B; ++c)
+                if (tree_parent(par, c) == n && ids[c] == x) {
+                    child = c;
+                    break;
+                }
+            out_tokens[(long)r * B + depth] = x;
+            if (child < 0) break;
+            ++depth;
+            path[(long)r * B + depth] = child;
+            n = child;
+        }
+        accept_len[r] = depth;
+        bonus_id[r] = x;
+        new_seq_lens[r] = seq_lens[r] + depth + 1;
+        if (flags) flags[r] = flag;
+    }
+}
+
 /* Exposed for tests of the sampling rule itself. */
 int oracle_inv_cdf(const float *w, int V, double u, int32_t *flag_near) {
     int near = 0;
