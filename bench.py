@@ -450,6 +450,75 @@ def time_kvmat(step: "Step", flush, clean, n_layers: int = 5, H: int = 4096, ite
             "gpu_launches_per_call": 2, "iters": iters}
 
 
+def time_tree(cfg: wl.StepConfig, dev, flush, clean, n_nodes: int = 32, iters: int = 20):
+    """Tree verify at the workload's shape with token trees of n_nodes nodes:
+    the layout (tree_prepare) plus tree attention over the paged cache, and
+    the tree acceptance walk over the vocabulary; L2 flushed before each call;
+    mean event times in ms."""
+    import dataclasses
+
+    import block_diffusion_speculative_attn_gb300 as bdsa
+    c = dataclasses.replace(cfg, B=n_nodes)
+    attn = wl.make_attn_inputs(c, device=dev, seed=c.seed + 77)
+    bt = torch.from_numpy(attn.block_table).to(dev)
+    sl = torch.from_numpy(attn.seq_lens).to(dev)
+    x = wl.make_tree_inputs(cfg, n_nodes, device=dev)
+    par = torch.from_numpy(x.parent).to(dev)
+    status = torch.zeros(1, dtype=torch.int32, device=dev)
+    prep = tuple(torch.empty((c.bs, n_nodes), dtype=torch.int32, device=dev) for _ in range(3)) \
+        + (torch.empty((c.bs, n_nodes), dtype=torch.int64, device=dev),)
+    out = torch.empty_like(attn.q)
+    ws = torch.empty(max(bdsa.block_attn_workspace_bytes(c.bs, c.B, c.Hq, c.Hkv, c.D,
+                                                         attn.max_ctx_len), 256),
+                     dtype=torch.uint8, device=dev)
+    acc = {k: torch.empty(c.bs, dtype=torch.int32, device=dev) for k in bdsa.TREE_KEYS}
+    acc["path"] = torch.empty((c.bs, n_nodes), dtype=torch.int32, device=dev)
+    acc["out_tokens"] = torch.empty((c.bs, n_nodes), dtype=torch.int32, device=dev)
+    t_attn, t_acc = [], []
+    for i in range(iters + 3):
+        flush.zero_()
+        clean.sum()
+        ev = [torch.cuda.Event(enable_timing=True) for _ in range(3)]
+        ev[0].record()
+        bdsa.tree_prepare(par, sl, bt, attn.num_pages, c.page_size, out=prep, dev_status=status)
+        bdsa.block_attn_paged(attn.q, attn.k_cache, attn.v_cache, bt, sl, B=c.B,
+                              page_size=c.page_size, scale=attn.scale, mode=wl.VERIFY,
+                              max_ctx_len=attn.max_ctx_len, num_pages=attn.num_pages, out=out,
+                              workspace=ws, dev_status=status, tree_mask=prep[3])
+        ev[1].record()
+        flush.zero_()
+        clean.sum()
+        ev2 = [torch.cuda.Event(enable_timing=True) for _ in range(2)]
+        ev2[0].record()
+        bdsa.tree_accept(x.block_ids, par, x.p, x.u, x.seq_lens, out=acc, dev_status=status)
+        ev2[1].record()
+        if i >= 3:
+            t_attn.append(ev[:2])
+            t_acc.append(ev2)
+    torch.cuda.synchronize()
+    assert status.item() == 0, bdsa.STATUS.get(status.item())
+    attn_ms = statistics.mean(a.elapsed_time(b) for a, b in t_attn)
+    acc_ms = statistics.mean(a.elapsed_time(b) for a, b in t_acc)
+    hbm, _, src = peaks()
+    abytes = attn_bytes(c, attn.seq_lens)
+    depth = acc["accept_len"].cpu().numpy()
+    accbytes = int((depth + 1).sum()) * cfg.V * 4
+    return {"nodes": n_nodes, "batch": c.bs, "vocab": cfg.V,
+            "attn_ms": attn_ms, "attn_query_tokens_per_s": c.bs * n_nodes / (attn_ms / 1e3),
+            "attn_roofline": {"bound": "hbm", "achieved": abytes / (attn_ms / 1e3) / 1e9,
+                              "peak": hbm, "unit": "GB/s",
+                              "frac": abytes / (attn_ms / 1e3) / 1e9 / hbm, "peak_source": src,
+                              "algorithmic_bytes_per_launch": abytes,
+                              "kernels": "tree_prepare + block attention (TREE) + merge"},
+            "accept_ms": acc_ms, "accept_rows_per_s": c.bs / (acc_ms / 1e3),
+            "mean_accept_len": float(depth.mean()),
+            "accept_roofline": {"bound": "hbm", "achieved": accbytes / (acc_ms / 1e3) / 1e9,
+                                "peak": hbm, "unit": "GB/s",
+                                "frac": accbytes / (acc_ms / 1e3) / 1e9 / hbm,
+                                "peak_source": src, "algorithmic_bytes_per_launch": accbytes},
+            "iters": iters}
+
+
 # ---------------------------------------------------------------------------
 def oracle_sample(cfg: wl.StepConfig, attn: wl.AttnInputs, acc, reqs, nthreads):
     """Host copies of the sampled requests' inputs (compact page pool)."""
@@ -661,6 +730,7 @@ def main(argv=None):
         assert step.status.item() == 0, bdsa.STATUS.get(step.status.item())
     idlm = time_idlm(cfg, dev, flush, clean) if (cfg.V and attn_ms is not None) else None
     kvmat = time_kvmat(step, flush, clean) if (cfg.V and attn_ms is not None) else None
+    tree = time_tree(cfg, dev, flush, clean) if (cfg.V and attn_ms is not None) else None
 
     e2e = None
     if not args.no_e2e:
@@ -689,6 +759,7 @@ def main(argv=None):
             "fused_append": fused_append,
             "idlm_round": idlm,
             "kv_materialize": kvmat,
+            "tree_verify": tree,
             "attn_flops_per_launch": attn_flops(cfg, step.attn.seq_lens, cfg.modes[-1]),
             "e2e": e2e, "cpu_baseline": cpu, "gpu_launches": step.launches * K,
             "clocks": clk}

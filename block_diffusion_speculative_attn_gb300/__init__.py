@@ -14,6 +14,9 @@ Calls (all asynchronous on the current stream):
   idlm_prepare      I-DLM Block-N layout of 2N-1 slots (pending, carried specs, masks)
   idlm_accept       I-DLM Block-N verify / correct / draw-new-specs / KV-trim step
   kv_materialize    draft K/V of the committed rows (projection, K norm, RoPE, paged write)
+  tree_prepare      token-tree layout: depths, positions, cache slots, ancestor masks
+  block_attn_paged(tree_mask=...)  tree attention (block row sees its ancestors)
+  tree_accept       lossless tree acceptance walk (stochastic or greedy)
 """
 from __future__ import annotations
 
@@ -35,7 +38,8 @@ EXPORTS = ("bdsa_status_string", "bdsa_version", "bdsa_prepare_block",
            "bdsa_block_attn_workspace_bytes", "bdsa_block_attn_paged",
            "bdsa_block_attn_paged_append", "bdsa_spec_accept_workspace_bytes",
            "bdsa_spec_accept", "bdsa_spec_accept_noalloc", "bdsa_idlm_prepare",
-           "bdsa_idlm_accept", "bdsa_kv_materialize_workspace_bytes", "bdsa_kv_materialize")
+           "bdsa_idlm_accept", "bdsa_kv_materialize_workspace_bytes", "bdsa_kv_materialize",
+           "bdsa_tree_prepare", "bdsa_block_attn_paged_tree", "bdsa_tree_accept")
 
 _lib = None
 
@@ -89,6 +93,14 @@ def lib() -> ctypes.CDLL:
     L.bdsa_kv_materialize.argtypes = [P, P, P, P, i32, i32, i32, P, P, i32, i32, i32, P, P, i32,
                                       f32, P, P, i64, P, sz, P, P]
     L.bdsa_kv_materialize.restype = i32
+    L.bdsa_tree_prepare.argtypes = [P, P, P, i32, i32, i32, i32, i32, P, P, P, P, P, P]
+    L.bdsa_tree_prepare.restype = i32
+    L.bdsa_block_attn_paged_tree.argtypes = [P, P, P, P, i32, i32, P, i32, i32, i32, i32, i32,
+                                             i32, i32, f32, P, P, P, P, sz, i32, P, P]
+    L.bdsa_block_attn_paged_tree.restype = i32
+    L.bdsa_tree_accept.argtypes = [P, P, P, i64, i64, P, P, i32, i32, i32, P, P, P, P, P, i32,
+                                   P, P]
+    L.bdsa_tree_accept.restype = i32
     _lib = L
     return L
 
@@ -148,7 +160,7 @@ def block_attn_workspace_bytes(bs, B, Hq, Hkv, D, max_ctx_len, sms: int = 0) -> 
 def block_attn_paged(q, k_cache, v_cache, block_table, seq_lens, *, B: int, page_size: int,
                      scale: float, mode: int, max_ctx_len: int, num_pages: int | None = None,
                      out=None, lse=None, workspace=None, dev_status=None, sms: int = 0,
-                     k_new=None, v_new=None):
+                     k_new=None, v_new=None, tree_mask=None):
     """bdsa_block_attn_paged.  q [bs*B, Hq, D] bf16, caches [slots, Hkv, D] bf16.
 
     With k_new / v_new ([bs*B, Hkv, D] bf16) it is bdsa_block_attn_paged_append:
@@ -180,7 +192,17 @@ def block_attn_paged(q, k_cache, v_cache, block_table, seq_lens, *, B: int, page
     if workspace is None and need > 0:
         workspace = torch.empty(need, dtype=torch.uint8, device=q.device)
     ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
-    if k_new is None:
+    if tree_mask is not None:
+        _dev(tree_mask, "tree_mask", torch.int64)
+        if k_new is not None:
+            raise ValueError("the tree call has no fused append")
+        st = lib().bdsa_block_attn_paged_tree(
+            _ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(block_table), max_pages, num_pages,
+            _ptr(seq_lens), int(max_ctx_len), bs, B, Hq, Hkv, D, page_size, float(scale),
+            _ptr(tree_mask), _ptr(out), _ptr(lse), _ptr(workspace), ws_bytes, sms,
+            _ptr(dev_status), _stream(q.device))
+        _check("bdsa_block_attn_paged_tree", st)
+    elif k_new is None:
         st = lib().bdsa_block_attn_paged(_ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(block_table),
                                          max_pages, num_pages, _ptr(seq_lens), int(max_ctx_len),
                                          bs, B, Hq, Hkv, D, page_size, float(scale), int(mode),
@@ -367,3 +389,58 @@ def kv_materialize(hidden, commit_len, positions, cache_loc, w_kv, k_norm_w, rop
         float(eps), _ptr(k_cache), _ptr(v_cache), int(num_slots), _ptr(workspace), ws_bytes,
         _ptr(dev_status), _stream(hidden.device))
     _check("bdsa_kv_materialize", st)
+
+
+# ---------------------------------------------------------------------------
+TREE_KEYS = ("accept_len", "bonus_id", "new_seq_lens")
+
+
+def tree_prepare(parent, seq_lens, block_table, num_pages: int, page_size: int, out=None,
+                 dev_status=None):
+    """bdsa_tree_prepare.  parent [bs, B] int32 (node 0 the root, parent -1).
+    Returns (depth, positions, cache_loc) int32 [bs, B] and tree_mask int64
+    [bs, B] (uint64 ancestor-or-self bits)."""
+    _dev(parent, "parent", torch.int32)
+    _dev(seq_lens, "seq_lens", torch.int32)
+    _dev(block_table, "block_table", torch.int32)
+    bs, B = parent.shape
+    dev = parent.device
+    if out is None:
+        out = tuple(torch.empty((bs, B), dtype=torch.int32, device=dev) for _ in range(3)) + \
+            (torch.empty((bs, B), dtype=torch.int64, device=dev),)
+    st = lib().bdsa_tree_prepare(_ptr(parent), _ptr(seq_lens), _ptr(block_table),
+                                 block_table.shape[1], num_pages, bs, B, page_size, _ptr(out[0]),
+                                 _ptr(out[1]), _ptr(out[2]), _ptr(out[3]), _ptr(dev_status),
+                                 _stream(dev))
+    _check("bdsa_tree_prepare", st)
+    return out
+
+
+def tree_accept(block_ids, parent, p, u, seq_lens, *, p_strides=None, V: int | None = None,
+                out=None, dev_status=None, sms: int = 0):
+    """bdsa_tree_accept (u None: greedy).  p fp32 [bs, B, V].  Returns a dict:
+    TREE_KEYS [bs], path [bs, B], out_tokens [bs, B] (int32)."""
+    _dev(block_ids, "block_ids", torch.int32)
+    _dev(parent, "parent", torch.int32)
+    _dev(seq_lens, "seq_lens", torch.int32)
+    if not (p.is_cuda and p.dtype == torch.float32):
+        raise TypeError("p must be a CUDA float32 tensor")
+    bs, B = block_ids.shape
+    V = p.shape[-1] if V is None else V
+    if p_strides is None:
+        _dev(p, "p", torch.float32)
+        p_strides = (B * V, V)
+    if u is not None:
+        _dev(u, "u", torch.float32)
+    dev = block_ids.device
+    if out is None:
+        out = {k: torch.empty(bs, dtype=torch.int32, device=dev) for k in TREE_KEYS}
+        out["path"] = torch.empty((bs, B), dtype=torch.int32, device=dev)
+        out["out_tokens"] = torch.empty((bs, B), dtype=torch.int32, device=dev)
+    st = lib().bdsa_tree_accept(_ptr(block_ids), _ptr(parent), _ptr(p), int(p_strides[0]),
+                                int(p_strides[1]), _ptr(u), _ptr(seq_lens), bs, B, V,
+                                _ptr(out["accept_len"]), _ptr(out["path"]),
+                                _ptr(out["out_tokens"]), _ptr(out["bonus_id"]),
+                                _ptr(out["new_seq_lens"]), sms, _ptr(dev_status), _stream(dev))
+    _check("bdsa_tree_accept", st)
+    return out

@@ -85,12 +85,14 @@ int32_t attn_call(const bdsa_bf16 *q, const bdsa_bf16 *k_new, const bdsa_bf16 *v
                   const bdsa_bf16 *k_cache, const bdsa_bf16 *v_cache, const int32_t *block_table,
                   int32_t max_pages_per_req, int32_t num_pages, const int32_t *seq_lens,
                   int32_t max_ctx_len, int32_t bs, int32_t B, int32_t Hq, int32_t Hkv, int32_t D,
-                  int32_t page_size, float softmax_scale, int32_t mode, bdsa_bf16 *out, float *lse,
-                  void *workspace, size_t workspace_bytes, int32_t num_sms, int32_t *dev_status,
-                  void *stream) {
+                  int32_t page_size, float softmax_scale, int32_t mode, const uint64_t *tree_mask,
+                  bdsa_bf16 *out, float *lse, void *workspace, size_t workspace_bytes,
+                  int32_t num_sms, int32_t *dev_status, void *stream) {
+    const bool mode_ok = tree_mask == nullptr
+                             ? (mode == BDSA_MODE_DRAFT || mode == BDSA_MODE_VERIFY)
+                             : mode == BDSA_MODE_TREE;
     if (bs < 0 || B < 1 || Hq < 1 || Hkv < 1 || max_pages_per_req < 1 || num_pages < 1 ||
-        max_ctx_len < 0 || !isfinite(softmax_scale) || !(softmax_scale > 0.f) ||
-        (mode != BDSA_MODE_DRAFT && mode != BDSA_MODE_VERIFY))
+        max_ctx_len < 0 || !isfinite(softmax_scale) || !(softmax_scale > 0.f) || !mode_ok)
         return BDSA_INVALID_ARG;
     if (bs == 0) return BDSA_OK;
     if (!q || !k_cache || !v_cache || !block_table || !seq_lens || !out) return BDSA_INVALID_ARG;
@@ -103,7 +105,8 @@ int32_t attn_call(const bdsa_bf16 *q, const bdsa_bf16 *k_new, const bdsa_bf16 *v
     if ((int64_t)bs * B > INT32_MAX) return BDSA_UNSUPPORTED;
     if (!aligned(q, 16) || !aligned(k_cache, 16) || !aligned(v_cache, 16) || !aligned(out, 16) ||
         (k_new && !aligned(k_new, 16)) || (v_new && !aligned(v_new, 16)) ||
-        (lse && !aligned(lse, 4)) || (workspace && !aligned(workspace, 256)))
+        (lse && !aligned(lse, 4)) || (workspace && !aligned(workspace, 256)) ||
+        (tree_mask && !aligned(tree_mask, 8)))
         return BDSA_MISALIGNED;
     bdsa::AttnArgs a;
     a.q = reinterpret_cast<const uint16_t *>(q);
@@ -127,6 +130,7 @@ int32_t attn_call(const bdsa_bf16 *q, const bdsa_bf16 *k_new, const bdsa_bf16 *v
     a.scale = softmax_scale;
     a.out = reinterpret_cast<uint16_t *>(out);
     a.lse = lse;
+    a.tree_mask = tree_mask;
     a.workspace = workspace;
     a.workspace_bytes = workspace_bytes;
     a.dev_status = dev_status;
@@ -147,8 +151,24 @@ int32_t bdsa_block_attn_paged(const bdsa_bf16 *q, const bdsa_bf16 *k_cache,
                               int32_t *dev_status, void *stream) {
     return attn_call(q, nullptr, nullptr, k_cache, v_cache, block_table, max_pages_per_req,
                      num_pages, seq_lens, max_ctx_len, bs, B, Hq, Hkv, D, page_size,
-                     softmax_scale, mode, out, lse, workspace, workspace_bytes, num_sms,
+                     softmax_scale, mode, nullptr, out, lse, workspace, workspace_bytes, num_sms,
                      dev_status, stream);
+}
+
+int32_t bdsa_block_attn_paged_tree(const bdsa_bf16 *q, const bdsa_bf16 *k_cache,
+                                   const bdsa_bf16 *v_cache, const int32_t *block_table,
+                                   int32_t max_pages_per_req, int32_t num_pages,
+                                   const int32_t *seq_lens, int32_t max_ctx_len, int32_t bs,
+                                   int32_t B, int32_t Hq, int32_t Hkv, int32_t D,
+                                   int32_t page_size, float softmax_scale,
+                                   const uint64_t *tree_mask, bdsa_bf16 *out, float *lse,
+                                   void *workspace, size_t workspace_bytes, int32_t num_sms,
+                                   int32_t *dev_status, void *stream) {
+    if (bs > 0 && !tree_mask) return BDSA_INVALID_ARG;
+    return attn_call(q, nullptr, nullptr, k_cache, v_cache, block_table, max_pages_per_req,
+                     num_pages, seq_lens, max_ctx_len, bs, B, Hq, Hkv, D, page_size,
+                     softmax_scale, BDSA_MODE_TREE, tree_mask, out, lse, workspace,
+                     workspace_bytes, num_sms, dev_status, stream);
 }
 
 int32_t bdsa_block_attn_paged_append(const bdsa_bf16 *q, const bdsa_bf16 *k_new,
@@ -164,7 +184,7 @@ int32_t bdsa_block_attn_paged_append(const bdsa_bf16 *q, const bdsa_bf16 *k_new,
     if (bs > 0 && (!k_new || !v_new)) return BDSA_INVALID_ARG;
     return attn_call(q, k_new, v_new, k_cache, v_cache, block_table, max_pages_per_req, num_pages,
                      seq_lens, max_ctx_len, bs, B, Hq, Hkv, D, page_size, softmax_scale, mode,
-                     out, lse, workspace, workspace_bytes, num_sms, dev_status, stream);
+                     nullptr, out, lse, workspace, workspace_bytes, num_sms, dev_status, stream);
 }
 
 int32_t bdsa_idlm_prepare(const int32_t *pending, const int32_t *specs, const int32_t *mode,
@@ -336,6 +356,58 @@ int32_t bdsa_kv_materialize(const bdsa_bf16 *hidden, const int32_t *commit_len,
     a.workspace = workspace;
     a.dev_status = dev_status;
     return bdsa::launch_kv_materialize(a, static_cast<cudaStream_t>(stream));
+}
+
+int32_t bdsa_tree_prepare(const int32_t *parent, const int32_t *seq_lens,
+                          const int32_t *block_table, int32_t max_pages_per_req,
+                          int32_t num_pages, int32_t bs, int32_t B, int32_t page_size,
+                          int32_t *depth, int32_t *positions, int32_t *cache_loc,
+                          uint64_t *tree_mask, int32_t *dev_status, void *stream) {
+    if (bs < 0 || B < 1 || page_size < 1 || max_pages_per_req < 1 || num_pages < 1)
+        return BDSA_INVALID_ARG;
+    if (B > 64) return BDSA_UNSUPPORTED;
+    if (bs == 0) return BDSA_OK;
+    if (!parent || !seq_lens || !block_table || !depth || !positions || !cache_loc || !tree_mask)
+        return BDSA_INVALID_ARG;
+    if ((int64_t)bs * B > INT32_MAX) return BDSA_UNSUPPORTED;
+    if (!aligned(tree_mask, 8)) return BDSA_MISALIGNED;
+    return bdsa::launch_tree_prepare(parent, seq_lens, block_table, max_pages_per_req, num_pages,
+                                     bs, B, page_size, depth, positions, cache_loc, tree_mask,
+                                     dev_status, static_cast<cudaStream_t>(stream));
+}
+
+int32_t bdsa_tree_accept(const int32_t *block_ids, const int32_t *parent, const float *p,
+                         int64_t p_stride_r, int64_t p_stride_n, const float *u,
+                         const int32_t *seq_lens, int32_t bs, int32_t B, int32_t V,
+                         int32_t *accept_len, int32_t *path, int32_t *out_tokens,
+                         int32_t *bonus_id, int32_t *new_seq_lens, int32_t num_sms,
+                         int32_t *dev_status, void *stream) {
+    if (bs < 0 || B < 1 || V < 1 || p_stride_r < 0 || p_stride_n < 0) return BDSA_INVALID_ARG;
+    if (B > 64 || V > (1 << 21)) return BDSA_UNSUPPORTED;
+    if (bs == 0) return BDSA_OK;
+    if (!block_ids || !parent || !p || !seq_lens || !accept_len || !path || !out_tokens ||
+        !bonus_id || !new_seq_lens)
+        return BDSA_INVALID_ARG;
+    if (!aligned(p, 4) || (u && !aligned(u, 4))) return BDSA_MISALIGNED;
+    bdsa::TreeArgs a;
+    a.block_ids = block_ids;
+    a.parent = parent;
+    a.seq_lens = seq_lens;
+    a.p = p;
+    a.psr = p_stride_r;
+    a.psn = p_stride_n;
+    a.u = u;
+    a.bs = bs;
+    a.B = B;
+    a.V = V;
+    a.num_sms = bdsa::device_num_sms(num_sms);
+    a.accept_len = accept_len;
+    a.path = path;
+    a.out_tokens = out_tokens;
+    a.bonus_id = bonus_id;
+    a.new_seq_lens = new_seq_lens;
+    a.dev_status = dev_status;
+    return bdsa::launch_tree_accept(a, static_cast<cudaStream_t>(stream));
 }
 
 }  // extern "C"

@@ -31,6 +31,7 @@ struct AttnArgs {
     float scale;
     uint16_t *out;
     float *lse;
+    const uint64_t *tree_mask;      // TREE mode only
     void *workspace;
     size_t workspace_bytes;
     int32_t *dev_status;
@@ -91,6 +92,24 @@ struct IdlmArgs {
 };
 
 int launch_idlm_accept(const IdlmArgs &a, cudaStream_t stream);
+
+// ---------------------------------------------------------------- tree verify
+int launch_tree_prepare(const int32_t *parent, const int32_t *seq_lens, const int32_t *block_table,
+                        int max_pages, int num_pages, int bs, int B, int page_size,
+                        int32_t *depth, int32_t *positions, int32_t *cache_loc,
+                        uint64_t *tree_mask, int32_t *dev_status, cudaStream_t stream);
+
+struct TreeArgs {
+    const int32_t *block_ids, *parent, *seq_lens;
+    const float *p;
+    int64_t psr, psn;
+    const float *u;  // [bs, B] uniforms by depth, or null for greedy
+    int bs, B, V, num_sms;
+    int32_t *accept_len, *path, *out_tokens, *bonus_id, *new_seq_lens;
+    int32_t *dev_status;
+};
+
+int launch_tree_accept(const TreeArgs &a, cudaStream_t stream);
 
 // ---------------------------------------------------------------- KV materialisation
 // Committed rows of the verify block -> every draft layer's K (RMS norm, RoPE)

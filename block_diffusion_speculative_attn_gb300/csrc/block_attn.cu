@@ -5,7 +5,10 @@
 //   limit(i) = L_r + B (DRAFT: rectangular intra-block mask) or L_r + i + 1
 //   (VERIFY: token-causal), as defined on "SGLang dLLM / LLaDA 2.0", section
 //   "Attention Mask", and used by the draft/verify passes of "From DFlash to
-//   dLLM Self-Spec (II)", sections 2.2.3-2.2.4 and "(IV)", section 4.4.1.
+//   dLLM Self-Spec (II)", sections 2.2.3-2.2.4 and "(IV)", section 4.4.1; or
+//   (TREE) block key j visible to block row i iff bit j of tree_mask[r, i] is
+//   set (the node and its ancestors: the tree attention of the Psi-Spec Tree
+//   sampler, "Unlocking Lossless Speedups in LLMs via Discrete Diffusion").
 //
 // One call = two launches chained with programmatic dependent launch:
 //   attend  persistent, one CTA per SM.  Every (request, KV head) unit is a run
@@ -123,6 +126,7 @@ struct Params {
     int32_t *part_bad;       // [2 * grid] partial slot saw a page id outside the pool
     uint16_t *out;
     float *lse;
+    const uint64_t *tree_mask;  // TREE mode: [bs * B] block keys visible to each block row
     float *part_o;           // [2 * grid, rows, D]
     float *part_lse;         // [2 * grid, rows]
     int32_t *dev_status;
@@ -376,7 +380,9 @@ __device__ void append_piece_rows(const Params &prm, const AppendParams &app, co
     }
 }
 
-template <int D, int M, bool kAppend>
+// kTree: the TREE mask (block keys by tree_mask bits), in an instantiation of
+// its own so that the DRAFT / VERIFY tile loop carries none of its code.
+template <int D, int M, bool kAppend, bool kTree>
 __global__ void __launch_bounds__(kAppend ? kThreadsAppend : kThreads, 1)
     block_attn_kernel(const __grid_constant__ CUtensorMap tm_q,
                       const __grid_constant__ CUtensorMap tm_k,
@@ -845,10 +851,21 @@ __global__ void __launch_bounds__(kAppend ? kThreadsAppend : kThreads, 1)
             const int32_t *bt_row = prm.block_table + (long)pc.r * prm.max_pages;
             bool page_bad = false, pend = false;
             int32_t pend_pg = 0;
-            const long limit =
-                (prm.mode == BDSA_MODE_DRAFT) ? n_keys : min(n_keys, (long)pc.L + i_blk + 1);
+            const long limit = (kTree || prm.mode == BDSA_MODE_DRAFT)
+                                   ? n_keys
+                                   : min(n_keys, (long)pc.L + i_blk + 1);
+            // TREE: the block keys this row's node sees (itself and its ancestors)
+            uint64_t amask = ~0ull;
+            if constexpr (kTree) {
+                if (valid_row) amask = __ldg(prm.tree_mask + (long)pc.r * B + i_blk);
+            }
             const int ob = k & 1;
             float m_used = -INFINITY;
+            // Partial sums of the scores' exponentials.  TREE: l4[0..1] hold
+            // them (the lse) and l4[2..3] the same values rounded to bf16 as
+            // the PV product sees them (the normalisation, so that o is a
+            // convex combination of V rows: a row that sees few keys, as in a
+            // short tree, is then within rounding of its dominant V row).
             float l4[4] = {0.f, 0.f, 0.f, 0.f};
             for (int j = pc.a; j < pc.e; ++j, ++g) {
                 const long t0 = (long)j * kBN;
@@ -882,6 +899,15 @@ __global__ void __launch_bounds__(kAppend ? kThreadsAppend : kThreads, 1)
                     for (int c = 0; c < NC; ++c)
                         if (c >= nvalid) sv[c] = -INFINITY;
                 }
+                if constexpr (kTree) {
+                    if (t0 + half * NC + NC > pc.L) {
+#pragma unroll
+                        for (int c = 0; c < NC; ++c) {
+                            const long j = t0 + half * NC + c - pc.L;  // block slot of the key
+                            if (j >= 0 && j < 64 && !((amask >> j) & 1ull)) sv[c] = -INFINITY;
+                        }
+                    }
+                }
                 float mx[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
 #pragma unroll
                 for (int c = 0; c < NC; ++c) mx[c & 3] = fmaxf(mx[c & 3], sv[c]);
@@ -907,8 +933,15 @@ __global__ void __launch_bounds__(kAppend ? kThreadsAppend : kThreads, 1)
                     for (int c = 0; c < NC / 2; ++c) {
                         const float p0 = ex2_approx(fmaf(sv[2 * c], sl2, neg_m));
                         const float p1 = ex2_approx(fmaf(sv[2 * c + 1], sl2, neg_m));
-                        l4[c & 3] += p0 + p1;
-                        pk[c] = pack_bf16x2(p0, p1);
+                        const uint32_t pr = pack_bf16x2(p0, p1);
+                        pk[c] = pr;
+                        if constexpr (kTree) {
+                            l4[c & 1] += p0 + p1;
+                            l4[2 + (c & 1)] +=
+                                __uint_as_float(pr << 16) + __uint_as_float(pr & 0xffff0000u);
+                        } else {
+                            l4[c & 3] += p0 + p1;
+                        }
                     }
                 }
                 const int pb = (int)(g % C::NP);
@@ -985,13 +1018,21 @@ __global__ void __launch_bounds__(kAppend ? kThreadsAppend : kThreads, 1)
 
             // ---- end of the piece
             {
-                float l = (l4[0] + l4[1]) + (l4[2] + l4[3]);
+                float l, lr;
+                if constexpr (kTree) {
+                    l = l4[0] + l4[1];
+                    lr = l4[2] + l4[3];
+                    if constexpr (M == 64) lr += __shfl_xor_sync(0xffffffffu, lr, 16);
+                } else {
+                    l = (l4[0] + l4[1]) + (l4[2] + l4[3]);
+                }
                 if constexpr (M == 64) l += __shfl_xor_sync(0xffffffffu, l, 16);
+                if constexpr (!kTree) lr = l;
                 if (pend) page_bad |= pend_pg < 0 || pend_pg >= prm.num_pages;
                 Epi e;
                 e.lastg = g - 1;
                 e.ob = ob;
-                e.inv_l = l > 0.f ? 1.f / l : 0.f;
+                e.inv_l = lr > 0.f ? 1.f / lr : 0.f;
                 e.lse2 = l > 0.f ? m_used + log2f(l) : -INFINITY;
                 e.complete = pc.a == 0 && pc.e == pc.nt;
                 // every warp checked every page of the piece
@@ -1241,6 +1282,7 @@ int launch_impl(const AttnArgs &a, const AttnPlan &plan, cudaStream_t stream) {
     prm.part_bad = reinterpret_cast<int32_t *>(ws + plan.off_part_bad);
     prm.out = a.out;
     prm.lse = a.lse;
+    prm.tree_mask = a.tree_mask;
     prm.part_o = reinterpret_cast<float *>(ws + plan.off_part_o);
     prm.part_lse = reinterpret_cast<float *>(ws + plan.off_part_lse);
     prm.dev_status = a.dev_status;
@@ -1266,13 +1308,17 @@ int launch_impl(const AttnArgs &a, const AttnPlan &plan, cudaStream_t stream) {
     app.k_cache = const_cast<uint16_t *>(a.k_cache);
     app.v_cache = const_cast<uint16_t *>(a.v_cache);
     const bool append = a.k_new != nullptr;
-    auto kernel = append ? block_attn_kernel<D, M, true> : block_attn_kernel<D, M, false>;
-    static bool attr_set[2] = {false, false};  // per instantiation
-    if (!attr_set[append]) {
+    const bool tree = a.mode == BDSA_MODE_TREE;
+    auto kernel = tree ? block_attn_kernel<D, M, false, true>
+                       : (append ? block_attn_kernel<D, M, true, false>
+                                 : block_attn_kernel<D, M, false, false>);
+    const int inst = tree ? 2 : (append ? 1 : 0);
+    static bool attr_set[3] = {false, false, false};  // per instantiation
+    if (!attr_set[inst]) {
         if (cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                  C::kSmem) != cudaSuccess)
             return BDSA_CUDA_ERROR;
-        attr_set[append] = true;
+        attr_set[inst] = true;
     }
     if (launch_pdl(kernel, dim3(plan.grid), dim3(append ? kThreadsAppend : kThreads), C::kSmem,
                    stream, tq, tk, tv, tout,

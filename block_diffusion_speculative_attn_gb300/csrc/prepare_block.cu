@@ -67,6 +67,46 @@ __global__ void __launch_bounds__(256)
     cache_loc[idx] = loc;
 }
 
+// Tree verify layout ("Unlocking Lossless Speedups in LLMs via Discrete
+// Diffusion", Psi-Spec Tree sampler): node i of request r sits at block slot i
+// (cache location of position L + i) and at sequence position L + depth(i);
+// tree_mask bit j is set iff node j is node i or one of its ancestors.  A
+// parent outside [0, i) (or node 0's parent other than -1) makes the node a
+// root and is reported.
+__global__ void __launch_bounds__(256)
+    tree_prepare_kernel(const int32_t *__restrict__ parent, const int32_t *__restrict__ seq_lens,
+                        const int32_t *__restrict__ block_table, int max_pages, int num_pages,
+                        int bs, int B, int page_size, int32_t *__restrict__ depth,
+                        int32_t *__restrict__ positions, int32_t *__restrict__ cache_loc,
+                        uint64_t *__restrict__ tree_mask, int32_t *dev_status) {
+    const long idx = (long)blockIdx.x * blockDim.x + threadIdx.x;
+    if (idx >= (long)bs * B) return;
+    const int r = (int)(idx / B), i = (int)(idx % B);
+    const int32_t *par = parent + (long)r * B;
+    const int p_i = __ldg(par + i);
+    if (i == 0 ? p_i != -1 : (p_i < 0 || p_i >= i)) report_status(dev_status, BDSA_DEVICE_OUT_OF_RANGE);
+    int d = -1;
+    uint64_t m = 0;
+    for (int k = i; k >= 0;) {
+        ++d;
+        m |= 1ull << k;
+        const int pk = k > 0 ? __ldg(par + k) : -1;
+        k = (pk >= 0 && pk < k) ? pk : -1;
+    }
+    const int L = __ldg(seq_lens + r);
+    depth[idx] = d;
+    tree_mask[idx] = m;
+    positions[idx] = L + d;
+    const long t = (long)L + i;
+    int32_t loc = -1;
+    if (L >= 0 && t / page_size < max_pages) {
+        const int32_t page = block_table[(long)r * max_pages + t / page_size];
+        if (page >= 0 && page < num_pages) loc = (int32_t)((long)page * page_size + t % page_size);
+    }
+    if (loc < 0) report_status(dev_status, BDSA_DEVICE_OUT_OF_RANGE);
+    cache_loc[idx] = loc;
+}
+
 }  // namespace
 
 int launch_idlm_prepare(const int32_t *pending, const int32_t *specs, const int32_t *mode,
@@ -81,6 +121,18 @@ int launch_idlm_prepare(const int32_t *pending, const int32_t *specs, const int3
                                                   max_pages, num_pages, bs, N, page_size,
                                                   mask_token_id, block_ids, positions, cache_loc,
                                                   dev_status);
+    return cudaGetLastError() == cudaSuccess ? BDSA_OK : BDSA_CUDA_ERROR;
+}
+
+int launch_tree_prepare(const int32_t *parent, const int32_t *seq_lens, const int32_t *block_table,
+                        int max_pages, int num_pages, int bs, int B, int page_size,
+                        int32_t *depth, int32_t *positions, int32_t *cache_loc,
+                        uint64_t *tree_mask, int32_t *dev_status, cudaStream_t stream) {
+    const long n = (long)bs * B;
+    if (n == 0) return BDSA_OK;
+    tree_prepare_kernel<<<(unsigned)((n + 255) / 256), 256, 0, stream>>>(
+        parent, seq_lens, block_table, max_pages, num_pages, bs, B, page_size, depth, positions,
+        cache_loc, tree_mask, dev_status);
     return cudaGetLastError() == cudaSuccess ? BDSA_OK : BDSA_CUDA_ERROR;
 }
 

@@ -722,6 +722,147 @@ __global__ void __launch_bounds__(kThreads) idlm_accept_kernel(const IdlmParams 
     }
 }
 
+// ------------------------------------------------------------ tree verify
+// "Unlocking Lossless Speedups in LLMs via Discrete Diffusion", Psi-Spec Tree
+// sampler: the drafted token tree is verified in one forward and rejection
+// sampling keeps the verifier's distribution.  The tree's tokens are chosen,
+// not sampled, so each draft distribution is one-hot: at node n of depth d the
+// verifier draws x from p[n] (InvCDF with u[d], or the argmax when greedy); a
+// child of n carrying x is accepted and the walk goes on from it, otherwise x
+// is emitted (correction, or bonus at a leaf).
+struct TreeParams {
+    const int32_t *block_ids, *parent, *seq_lens;
+    const float *p;
+    int64_t psr, psn;
+    const float *u;  // [bs, B] by depth; null = greedy
+    int bs, B, V, nchunk, nseg, spc;
+    int32_t *accept_len, *path, *out_tokens, *bonus_id, *new_seq_lens;
+    int32_t *dev_status;
+};
+
+// One thread-block cluster per request, its CTAs the vocabulary chunks.  Each
+// step of the walk sweeps p[n] (segment totals, or chunk maxima when greedy,
+// into the first CTA's shared memory), the first CTA resolves x and finds the
+// child, and writes the next node into every CTA of the cluster; two cluster
+// barriers a step.  The walk ends within B steps (a child's index exceeds its
+// parent's).
+__global__ void __launch_bounds__(kThreads) tree_accept_kernel(const TreeParams P) {
+    const int r = blockIdx.x / P.nchunk, chunk = blockIdx.x % P.nchunk;
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int B = P.B;
+    extern __shared__ float2 s_tot[];  // [nseg], used in chunk 0
+    __shared__ int s_ids[kMaxB], s_par[kMaxB], s_path[kMaxB], s_tok[kMaxB];
+    __shared__ float s_cv[kMaxCluster];
+    __shared__ int s_ci[kMaxCluster];
+    __shared__ float s_wv[kWarps];
+    __shared__ int s_wi[kWarps];
+    __shared__ int s_next, s_x;
+    if (chunk == 0) {
+        for (int i = tid; i < B; i += kThreads) {
+            s_ids[i] = __ldg(P.block_ids + (long)r * B + i);
+            const int pi = __ldg(P.parent + (long)r * B + i);
+            const bool ok = i == 0 ? pi == -1 : (pi >= 0 && pi < i);
+            if (!ok) report_status(P.dev_status, BDSA_DEVICE_OUT_OF_RANGE);
+            s_par[i] = (i > 0 && ok) ? pi : -1;
+            s_path[i] = -1;
+            s_tok[i] = -1;
+        }
+        if (tid == 0) s_path[0] = 0;
+    }
+    // every CTA of the cluster has started: its shared memory may be written
+    cluster_arrive_relaxed();
+    cluster_wait_acquire();
+    const bool greedy = P.u == nullptr;
+    const int sb = chunk * P.spc, se = min(P.nseg, sb + P.spc);
+    int n = 0, depth = 0;
+    for (int step = 0; step < B; ++step) {
+        const float *prow = P.p + r * P.psr + (long)n * P.psn;
+        if (!greedy) {
+            sweep_chunk(P, prow, nullptr, sb, se, warp, lane, map_to_rank(s_tot, 0));
+        } else {
+            float bv = -INFINITY;
+            int bi = INT_MAX;
+            for (int s0 = sb + warp; s0 < se; s0 += kUnroll * kWarps) {
+                float w[kUnroll][8];
+#pragma unroll
+                for (int uu = 0; uu < kUnroll; ++uu) {
+                    const int seg = s0 + uu * kWarps;
+                    if (seg < se) load_weights(prow, nullptr, (long)seg * kSeg + lane * 8, P.V, w[uu]);
+                }
+#pragma unroll
+                for (int uu = 0; uu < kUnroll; ++uu) {
+                    const long e0 = (long)(s0 + uu * kWarps) * kSeg + lane * 8;
+                    if (s0 + uu * kWarps < se) {
+#pragma unroll
+                        for (int e = 0; e < 8; ++e)
+                            if (e0 + e < P.V) better(bv, bi, w[uu][e], (int)(e0 + e));
+                    }
+                }
+            }
+#pragma unroll
+            for (int o = 16; o > 0; o >>= 1) {
+                const float ov = __shfl_xor_sync(0xffffffffu, bv, o);
+                const int oi = __shfl_xor_sync(0xffffffffu, bi, o);
+                better(bv, bi, ov, oi);
+            }
+            if (lane == 0) {
+                s_wv[warp] = bv;
+                s_wi[warp] = bi;
+            }
+            __syncthreads();
+            if (tid == 0) {
+                for (int w = 1; w < kWarps; ++w) better(bv, bi, s_wv[w], s_wi[w]);
+                *map_to_rank(&s_cv[chunk], 0) = bv;
+                *map_to_rank(&s_ci[chunk], 0) = bi;
+            }
+        }
+        cluster_arrive_release();
+        cluster_wait_acquire();
+        if (chunk == 0) {
+            int x;
+            if (!greedy) {
+                x = resolve_draw<true>(P, prow, nullptr, __ldg(P.u + (long)r * B + depth), s_tot);
+            } else {
+                if (tid == 0) {
+                    float bv = -INFINITY;
+                    int bi = INT_MAX;
+                    for (int c = 0; c < P.nchunk; ++c) better(bv, bi, s_cv[c], s_ci[c]);
+                    s_x = (bi == INT_MAX) ? 0 : bi;
+                }
+                __syncthreads();
+                x = s_x;
+            }
+            if (tid == 0) {
+                int child = -1;
+                for (int c = n + 1; c < B; ++c)
+                    if (s_par[c] == n && s_ids[c] == x) {
+                        child = c;
+                        break;
+                    }
+                s_tok[depth] = x;
+                if (child >= 0) s_path[depth + 1] = child;
+                for (int rk = 0; rk < P.nchunk; ++rk) *map_to_rank(&s_next, (uint32_t)rk) = child;
+            }
+        }
+        cluster_arrive_release();
+        cluster_wait_acquire();
+        const int next = s_next;
+        if (next < 0) break;
+        n = next;
+        ++depth;
+    }
+    if (chunk != 0) return;
+    for (int i = tid; i < B; i += kThreads) {
+        P.path[(long)r * B + i] = s_path[i];
+        P.out_tokens[(long)r * B + i] = s_tok[i];
+    }
+    if (tid == 0) {
+        P.accept_len[r] = depth;
+        P.bonus_id[r] = s_tok[depth];
+        P.new_seq_lens[r] = __ldg(P.seq_lens + r) + depth + 1;
+    }
+}
+
 size_t align256(size_t x) { return (x + 255) & ~(size_t)255; }
 
 }  // namespace
@@ -804,6 +945,53 @@ int launch_idlm_accept(const IdlmArgs &a, cudaStream_t stream) {
     cfg.attrs = attr;
     cfg.numAttrs = 1;
     return cudaLaunchKernelEx(&cfg, idlm_accept_kernel, P) == cudaSuccess ? BDSA_OK
+                                                                          : BDSA_CUDA_ERROR;
+}
+
+int launch_tree_accept(const TreeArgs &a, cudaStream_t stream) {
+    if (a.bs == 0) return BDSA_OK;
+    const AcceptPlan plan = accept_plan(a.bs, a.B, a.V, a.num_sms);
+    if (!plan.cluster) return BDSA_UNSUPPORTED;
+    TreeParams P;
+    P.block_ids = a.block_ids;
+    P.parent = a.parent;
+    P.seq_lens = a.seq_lens;
+    P.p = a.p;
+    P.psr = a.psr;
+    P.psn = a.psn;
+    P.u = a.u;
+    P.bs = a.bs;
+    P.B = a.B;
+    P.V = a.V;
+    P.nchunk = plan.nchunk;
+    P.nseg = plan.nseg;
+    P.spc = plan.spc;
+    P.accept_len = a.accept_len;
+    P.path = a.path;
+    P.out_tokens = a.out_tokens;
+    P.bonus_id = a.bonus_id;
+    P.new_seq_lens = a.new_seq_lens;
+    P.dev_status = a.dev_status;
+    const long nblocks = (long)plan.nchunk * a.bs;
+    if (nblocks > 0x7fffffffL) return BDSA_UNSUPPORTED;
+    const size_t smem = (size_t)plan.nseg * sizeof(float2);
+    if (smem > 48 * 1024 &&
+        cudaFuncSetAttribute(tree_accept_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             (int)smem) != cudaSuccess)
+        return BDSA_CUDA_ERROR;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)nblocks);
+    cfg.blockDim = dim3(kThreads);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = (unsigned)plan.nchunk;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, tree_accept_kernel, P) == cudaSuccess ? BDSA_OK
                                                                           : BDSA_CUDA_ERROR;
 }
 

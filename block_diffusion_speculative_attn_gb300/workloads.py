@@ -309,6 +309,61 @@ def make_kvmat_inputs(cfg: StepConfig, n_layers: int = 5, H: int = 4096, device=
                        commit, seq_lens, table, num_pages)
 
 
+@dataclasses.dataclass
+class TreeInputs:
+    """A token tree per request and its verifier distributions."""
+    parent: np.ndarray          # [bs, n] int32, node 0 the root (parent -1)
+    block_ids: torch.Tensor     # [bs, n] int32 node tokens (root: the verified token)
+    p: torch.Tensor             # [bs, n, V] fp32, verifier distribution after each node
+    u: torch.Tensor             # [bs, n] fp32 uniforms by depth
+    seq_lens: torch.Tensor      # [bs] int32
+
+
+def random_tree_parents(rng: np.random.Generator, bs: int, n: int, window: int = 8) -> np.ndarray:
+    """Bushy token trees in topological order: node i's parent is drawn from
+    the `window` nodes before it, so early nodes branch and paths run deep."""
+    par = np.empty((bs, n), np.int32)
+    par[:, 0] = -1
+    for i in range(1, n):
+        lo = max(0, i - window)
+        par[:, i] = rng.integers(lo, i, bs)
+    return par
+
+
+def make_tree_inputs(cfg: StepConfig, n_nodes: int, device="cpu", seed: int | None = None,
+                     bs: int | None = None) -> TreeInputs:
+    """Trees of n_nodes nodes shaped like a top-K expansion: the children of a
+    node carry the most likely tokens of its verifier distribution in rank
+    order (a drafter close to the verifier).  p = softmax(2 N(0, 1) logits
+    with one random token per node raised by 15), a confident verifier whose
+    top token holds about three quarters of the mass at V = 151936."""
+    seed = (cfg.seed if seed is None else seed) + 32452843
+    bs = cfg.bs if bs is None else bs
+    V = cfg.V
+    rng = np.random.default_rng(seed)
+    par = random_tree_parents(rng, bs, n_nodes)
+    g = _gen(device, seed)
+    logits = 2.0 * torch.randn((bs, n_nodes, V), generator=g, device=device)
+    hot = torch.randint(0, V, (bs, n_nodes, 1), generator=g, device=device)
+    logits.scatter_add_(-1, hot, torch.full((bs, n_nodes, 1), 15.0, device=device))
+    p = torch.softmax(logits, -1)
+    del logits
+    kmax = int(max(np.bincount(par[r, 1:], minlength=n_nodes).max() for r in range(bs)))
+    k = min(max(kmax, 1), V)
+    top = torch.topk(p, k, dim=-1).indices.cpu().numpy()  # [bs, n, k]
+    ids = np.empty((bs, n_nodes), np.int32)
+    ids[:, 0] = rng.integers(0, V, bs)
+    for r in range(bs):
+        rank = np.zeros(n_nodes, np.int64)
+        for i in range(1, n_nodes):
+            pa = par[r, i]
+            ids[r, i] = top[r, pa, rank[pa] % k]
+            rank[pa] += 1
+    u = torch.rand((bs, n_nodes), generator=g, device=device)
+    seq_lens = torch.randint(1, 4096, (bs,), generator=g, device=device).to(torch.int32)
+    return TreeInputs(par, torch.from_numpy(ids).to(device), p.contiguous(), u, seq_lens)
+
+
 def draft_from(q_rows: np.ndarray, u: np.ndarray) -> np.ndarray:
     """Inverse-CDF draws from rows of q (numpy, for small host-side workloads)."""
     c = np.cumsum(q_rows.astype(np.float64), axis=-1)

@@ -58,7 +58,7 @@ typedef enum bdsa_status {
 
 typedef struct bdsa_bf16 { uint16_t bits; } bdsa_bf16; /* IEEE bfloat16 storage */
 
-enum { BDSA_MODE_DRAFT = 0, BDSA_MODE_VERIFY = 1 };
+enum { BDSA_MODE_DRAFT = 0, BDSA_MODE_VERIFY = 1, BDSA_MODE_TREE = 2 /* bdsa_block_attn_paged_tree */ };
 
 /* Human-readable name of a status code (static string, never NULL). */
 const char *bdsa_status_string(int32_t status);
@@ -405,6 +405,73 @@ int32_t bdsa_kv_materialize(const bdsa_bf16 *hidden, const int32_t *commit_len,
                             float rms_eps, bdsa_bf16 *k_cache, bdsa_bf16 *v_cache,
                             int64_t num_slots, void *workspace, size_t workspace_bytes,
                             int32_t *dev_status, void *stream);
+
+/* ------------------------------------------------------------------------ */
+/* Tree verify
+ *
+ * "Unlocking Lossless Speedups in LLMs via Discrete Diffusion", the Psi-Spec
+ * Tree sampler: a token tree drafted by keeping the top candidates per
+ * position is verified in one forward with tree attention, and rejection
+ * sampling keeps the verifier's output distribution; "SGLang dLLM / LLaDA
+ * 2.0", section "Attention Mask": the block's queries see the whole context,
+ * the intra-block mask follows the verify structure.
+ *
+ * A request's block holds a token tree of B <= 64 nodes in topological order:
+ * parent [bs, B] int32, node 0 the root (the last verified token, parent -1),
+ * node i > 0 with a parent in [0, i).  A parent outside that range makes the
+ * node a root of its own and sets *dev_status = BDSA_DEVICE_OUT_OF_RANGE.
+ *
+ * bdsa_tree_prepare: node i sits at block slot i (cache_loc of position
+ *   L_r + i, as bdsa_prepare_block computes it, -1 and OUT_OF_RANGE when the
+ *   lookup fails) and at sequence position L_r + depth(i) (positions, for
+ *   RoPE); tree_mask[r, i] (uint64, 8-byte aligned) has bit j set iff node j
+ *   is node i or one of its ancestors.  Outputs [bs, B].  One launch.
+ *
+ * bdsa_block_attn_paged_tree: bdsa_block_attn_paged with the intra-block mask
+ *   "block key j is visible to block row i iff bit j of tree_mask[r, i] is
+ *   set" (mode BDSA_MODE_TREE); everything else (layouts, workspace, schedule,
+ *   limits, errors) as bdsa_block_attn_paged.
+ *
+ * bdsa_tree_accept: p [bs, B, V] fp32 (p + r*p_stride_r + n*p_stride_n) is
+ *   the verifier's distribution after node n, i.e. for n's children; u [bs, B]
+ *   fp32 uniforms in [0, 1) indexed by depth, or NULL for greedy.  Walk from
+ *   the root: at node n of depth d, x = InvCDF(p[r, n], u[r, d]) (the smallest
+ *   k whose cumulative weight exceeds u times the total; -1 if p[r, n] has no
+ *   mass) or x = argmax p[r, n] (lowest index on ties); the lowest-index child
+ *   of n carrying token x is accepted and the walk continues from it,
+ *   otherwise x is emitted (the correction, or the bonus at a leaf) and the
+ *   walk ends.  The tree's tokens are chosen rather than sampled, so this is
+ *   rejection sampling with one-hot draft distributions: lossless.
+ *   Outputs: accept_len [bs] (accepted nodes below the root), path [bs, B]
+ *   (node indices: the root, then the accepted nodes; -1 padding),
+ *   out_tokens [bs, B] (the accepted nodes' tokens, then x; -1 padding),
+ *   bonus_id [bs] = x, new_seq_lens [bs] = seq_lens + accept_len + 1.  The KV
+ *   rows of the path's nodes are the ones to keep.
+ *   Limits: B <= 64, V <= 2^21.  No workspace.  Launch: one thread-block
+ *   cluster per request (its CTAs the vocabulary chunks; num_sms sizes them,
+ *   0 = the current device's SM count); two cluster barriers per step of the
+ *   walk, at most B steps.
+ */
+int32_t bdsa_tree_prepare(const int32_t *parent, const int32_t *seq_lens,
+                          const int32_t *block_table, int32_t max_pages_per_req,
+                          int32_t num_pages, int32_t bs, int32_t B, int32_t page_size,
+                          int32_t *depth, int32_t *positions, int32_t *cache_loc,
+                          uint64_t *tree_mask, int32_t *dev_status, void *stream);
+int32_t bdsa_block_attn_paged_tree(const bdsa_bf16 *q, const bdsa_bf16 *k_cache,
+                                   const bdsa_bf16 *v_cache, const int32_t *block_table,
+                                   int32_t max_pages_per_req, int32_t num_pages,
+                                   const int32_t *seq_lens, int32_t max_ctx_len, int32_t bs,
+                                   int32_t B, int32_t Hq, int32_t Hkv, int32_t D,
+                                   int32_t page_size, float softmax_scale,
+                                   const uint64_t *tree_mask, bdsa_bf16 *out, float *lse,
+                                   void *workspace, size_t workspace_bytes, int32_t num_sms,
+                                   int32_t *dev_status, void *stream);
+int32_t bdsa_tree_accept(const int32_t *block_ids, const int32_t *parent, const float *p,
+                         int64_t p_stride_r, int64_t p_stride_n, const float *u,
+                         const int32_t *seq_lens, int32_t bs, int32_t B, int32_t V,
+                         int32_t *accept_len, int32_t *path, int32_t *out_tokens,
+                         int32_t *bonus_id, int32_t *new_seq_lens, int32_t num_sms,
+                         int32_t *dev_status, void *stream);
 
 #ifdef __cplusplus
 }
