@@ -229,18 +229,18 @@ __device__ int accepted_len(const Params &P, int r, int lane, bool &bad_id, int 
 // loads overlap.
 constexpr int kUnroll = 4;
 
-template <class PT>
+template <class PT, int U = kUnroll>
 __device__ void sweep_chunk(const PT &P, const float *prow, const float *qrow, int seg_begin,
                             int seg_end, int warp, int lane, float2 *tot) {
-    for (int s0 = seg_begin + warp; s0 < seg_end; s0 += kUnroll * kWarps) {
-        float w[kUnroll][8];
+    for (int s0 = seg_begin + warp; s0 < seg_end; s0 += U * kWarps) {
+        float w[U][8];
 #pragma unroll
-        for (int u = 0; u < kUnroll; ++u) {
+        for (int u = 0; u < U; ++u) {
             const int seg = s0 + u * kWarps;
             if (seg < seg_end) load_weights(prow, qrow, (long)seg * kSeg + lane * 8, P.V, w[u]);
         }
 #pragma unroll
-        for (int u = 0; u < kUnroll; ++u) {
+        for (int u = 0; u < U; ++u) {
             const int seg = s0 + u * kWarps;
             if (seg < seg_end) {
                 const float2 t = warp_sum_ff(group_sum_ff(w[u]));
@@ -740,20 +740,27 @@ struct TreeParams {
     int32_t *dev_status;
 };
 
+// Each step of the walk is one dependent sweep, so a step's latency is what
+// counts: five segments in flight a warp (two rounds for a 75-segment chunk
+// instead of three), with registers for two CTAs an SM so that every
+// request's cluster is resident at once.
+constexpr int kTreeMaxCluster = kMaxCluster;
+constexpr int kTreeUnroll = 5;
+
 // One thread-block cluster per request, its CTAs the vocabulary chunks.  Each
 // step of the walk sweeps p[n] (segment totals, or chunk maxima when greedy,
 // into the first CTA's shared memory), the first CTA resolves x and finds the
 // child, and writes the next node into every CTA of the cluster; two cluster
 // barriers a step.  The walk ends within B steps (a child's index exceeds its
 // parent's).
-__global__ void __launch_bounds__(kThreads) tree_accept_kernel(const TreeParams P) {
+__global__ void __launch_bounds__(kThreads, 2) tree_accept_kernel(const TreeParams P) {
     const int r = blockIdx.x / P.nchunk, chunk = blockIdx.x % P.nchunk;
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int B = P.B;
     extern __shared__ float2 s_tot[];  // [nseg], used in chunk 0
     __shared__ int s_ids[kMaxB], s_par[kMaxB], s_path[kMaxB], s_tok[kMaxB];
-    __shared__ float s_cv[kMaxCluster];
-    __shared__ int s_ci[kMaxCluster];
+    __shared__ float s_cv[kTreeMaxCluster];
+    __shared__ int s_ci[kTreeMaxCluster];
     __shared__ float s_wv[kWarps];
     __shared__ int s_wi[kWarps];
     __shared__ int s_next, s_x;
@@ -778,19 +785,20 @@ __global__ void __launch_bounds__(kThreads) tree_accept_kernel(const TreeParams 
     for (int step = 0; step < B; ++step) {
         const float *prow = P.p + r * P.psr + (long)n * P.psn;
         if (!greedy) {
-            sweep_chunk(P, prow, nullptr, sb, se, warp, lane, map_to_rank(s_tot, 0));
+            sweep_chunk<TreeParams, kTreeUnroll>(P, prow, nullptr, sb, se, warp, lane,
+                                                 map_to_rank(s_tot, 0));
         } else {
             float bv = -INFINITY;
             int bi = INT_MAX;
-            for (int s0 = sb + warp; s0 < se; s0 += kUnroll * kWarps) {
-                float w[kUnroll][8];
+            for (int s0 = sb + warp; s0 < se; s0 += kTreeUnroll * kWarps) {
+                float w[kTreeUnroll][8];
 #pragma unroll
-                for (int uu = 0; uu < kUnroll; ++uu) {
+                for (int uu = 0; uu < kTreeUnroll; ++uu) {
                     const int seg = s0 + uu * kWarps;
                     if (seg < se) load_weights(prow, nullptr, (long)seg * kSeg + lane * 8, P.V, w[uu]);
                 }
 #pragma unroll
-                for (int uu = 0; uu < kUnroll; ++uu) {
+                for (int uu = 0; uu < kTreeUnroll; ++uu) {
                     const long e0 = (long)(s0 + uu * kWarps) * kSeg + lane * 8;
                     if (s0 + uu * kWarps < se) {
 #pragma unroll
@@ -952,6 +960,7 @@ int launch_tree_accept(const TreeArgs &a, cudaStream_t stream) {
     if (a.bs == 0) return BDSA_OK;
     const AcceptPlan plan = accept_plan(a.bs, a.B, a.V, a.num_sms);
     if (!plan.cluster) return BDSA_UNSUPPORTED;
+
     TreeParams P;
     P.block_ids = a.block_ids;
     P.parent = a.parent;
