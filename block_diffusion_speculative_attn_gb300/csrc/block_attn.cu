@@ -900,11 +900,25 @@ __global__ void __launch_bounds__(kAppend ? kThreadsAppend : kThreads, 1)
                         if (c >= nvalid) sv[c] = -INFINITY;
                 }
                 if constexpr (kTree) {
-                    if (t0 + half * NC + NC > pc.L) {
+                    const long off = t0 + half * NC - pc.L;  // block slot of column 0
+                    if (off + NC > 0) {
+                        // visibility of this thread's columns, 64 to a word: context
+                        // keys (slot < 0) visible, block keys by the row's mask,
+                        // keys past the block already masked by the limit
 #pragma unroll
-                        for (int c = 0; c < NC; ++c) {
-                            const long j = t0 + half * NC + c - pc.L;  // block slot of the key
-                            if (j >= 0 && j < 64 && !((amask >> j) & 1ull)) sv[c] = -INFINITY;
+                        for (int wd = 0; wd < NC / 64; ++wd) {
+                            const long o = off + 64 * wd;
+                            uint64_t vis = ~0ull;
+                            if (o >= 0 && o < 64)
+                                vis = (amask >> o) | (o > 0 ? ~0ull << (64 - o) : 0ull);
+                            else if (o < 0 && o > -64)
+                                vis = (amask << (-o)) | ((1ull << (-o)) - 1ull);
+                            const uint32_t vlo = (uint32_t)vis, vhi = (uint32_t)(vis >> 32);
+#pragma unroll
+                            for (int c = 0; c < 32; ++c) {
+                                if (!((vlo >> c) & 1u)) sv[64 * wd + c] = -INFINITY;
+                                if (!((vhi >> c) & 1u)) sv[64 * wd + 32 + c] = -INFINITY;
+                            }
                         }
                     }
                 }
