@@ -350,7 +350,8 @@ def idlm_bytes(mode: np.ndarray, accept_len: np.ndarray, N: int, V: int) -> int:
     return total
 
 
-def time_idlm(cfg: wl.StepConfig, dev, flush, clean, N: int = 8, iters: int = 20):
+def time_idlm(cfg: wl.StepConfig, dev, flush, clean, N: int = 8, iters: int = 20,
+              cpu: bool = False):
     """The I-DLM Block-N round at the workload's batch and vocabulary: layout
     (idlm_prepare) and verify / correct / new-spec draws (idlm_accept), L2
     flushed before each round; mean event times in ms."""
@@ -389,8 +390,22 @@ def time_idlm(cfg: wl.StepConfig, dev, flush, clean, N: int = 8, iters: int = 20
     nbytes = idlm_bytes(mode, a, N, cfg.V)
     hbm, _, src = peaks()
     achieved = nbytes / (acc_ms / 1e3) / 1e9
+    base = None
+    if cpu:
+        # the oracle on every row of the same round, on the host cores
+        import oracle
+        cores = len(os.sched_getaffinity(0))
+        host = [t.cpu().numpy() for t in (prep[0], x.mode, x.p, x.q_prev, x.q_slot, x.u_acc,
+                                          x.u_samp, x.seq_lens)]
+        t0 = time.perf_counter()
+        oracle.idlm_accept(*host, N, nthreads=cores)
+        dt = time.perf_counter() - t0
+        base = {"value": bs / dt, "unit": "rows/s", "cores": cores, "kind": "oracle",
+                "sample": f"all {bs} rows of the round, fp64/fp32 C oracle, {cores} threads",
+                "seconds": dt}
     return {"N": N, "slots": blk, "batch": bs, "vocab": cfg.V,
             "verify_share": float(mode.mean()), "mean_accept_len": float(a[mode == 1].mean()),
+            "cpu_baseline": base,
             "round_ms": round_ms, "accept_ms": acc_ms, "rows_per_s": bs / (acc_ms / 1e3),
             "accept_roofline": {"bound": "hbm", "achieved": achieved, "peak": hbm,
                                 "unit": "GB/s", "frac": achieved / hbm, "peak_source": src,
@@ -404,7 +419,8 @@ def kvmat_bytes(rows: int, H: int, n_layers: int, Hkv: int, D: int) -> int:
     return (n_layers * 2 * Hkv * D * H * 2 + rows * H * 2 + rows * n_layers * 2 * Hkv * D * 2)
 
 
-def time_kvmat(step: "Step", flush, clean, n_layers: int = 5, H: int = 4096, iters: int = 20):
+def time_kvmat(step: "Step", flush, clean, n_layers: int = 5, H: int = 4096, iters: int = 20,
+               cpu: bool = False):
     """The draft KV materialisation of this step's committed rows (commit_len
     from the step's acceptance, positions and slots from its prepare_block)
     for a drafter of n_layers layers of hidden size H with the model's KV
@@ -442,7 +458,32 @@ def time_kvmat(step: "Step", flush, clean, n_layers: int = 5, H: int = 4096, ite
     flops = 2 * rows * H * n_layers * 2 * c.Hkv * c.D
     hbm, tf, src = peaks()
     achieved = nbytes / (ms / 1e3) / 1e9
+    base = None
+    if cpu:
+        # the oracle on the committed rows of the first requests (about 2 s)
+        import oracle
+        cores = len(os.sched_getaffinity(0))
+        cl = commit.cpu().numpy()
+        hb, wb, gb = wl.bf16_bits(x.hidden), wl.bf16_bits(x.w_kv), wl.bf16_bits(x.k_norm_w)
+        args = (pos.cpu().numpy(), loc.cpu().numpy())
+        keep = np.zeros_like(cl)
+        n, dt = 0, 0.0
+        while n < c.bs and dt < 0.5:
+            n = min(c.bs, max(1, 2 * n))
+            keep[:] = 0
+            keep[:n] = cl[:n]
+            t0 = time.perf_counter()
+            oracle.kv_materialize(hb, keep, *args, wb, gb, x.rope_cos.cpu().numpy(),
+                                  x.rope_sin.cpu().numpy(), x.eps, c.B, n_layers, c.Hkv, c.D,
+                                  slots, nthreads=cores)
+            dt = time.perf_counter() - t0
+        base = {"value": int(keep.sum()) / dt, "unit": "rows/s", "cores": cores,
+                "kind": "oracle",
+                "sample": f"the committed rows of the first {n} of {c.bs} requests "
+                          f"({int(keep.sum())} rows), fp64 C oracle, {cores} threads",
+                "seconds": dt}
     return {"n_layers": n_layers, "hidden": H, "committed_rows": rows, "launch_ms": ms,
+            "cpu_baseline": base,
             "rows_per_s": rows / (ms / 1e3), "tflops": flops / (ms / 1e3) / 1e12,
             "roofline": {"bound": "hbm", "achieved": achieved, "peak": hbm, "unit": "GB/s",
                          "frac": achieved / hbm, "peak_source": src,
@@ -450,7 +491,8 @@ def time_kvmat(step: "Step", flush, clean, n_layers: int = 5, H: int = 4096, ite
             "gpu_launches_per_call": 2, "iters": iters}
 
 
-def time_tree(cfg: wl.StepConfig, dev, flush, clean, n_nodes: int = 32, iters: int = 20):
+def time_tree(cfg: wl.StepConfig, dev, flush, clean, n_nodes: int = 32, iters: int = 20,
+              cpu: bool = False):
     """Tree verify at the workload's shape with token trees of n_nodes nodes:
     the layout (tree_prepare) plus tree attention over the paged cache, and
     the tree acceptance walk over the vocabulary; L2 flushed before each call;
@@ -503,7 +545,34 @@ def time_tree(cfg: wl.StepConfig, dev, flush, clean, n_nodes: int = 32, iters: i
     abytes = attn_bytes(c, attn.seq_lens)
     depth = acc["accept_len"].cpu().numpy()
     accbytes = int((depth + 1).sum()) * cfg.V * 4
-    return {"nodes": n_nodes, "batch": c.bs, "vocab": cfg.V,
+    base = None
+    if cpu:
+        # the oracle: tree attention of the first request, acceptance of all rows
+        import oracle
+        cores = len(os.sched_getaffinity(0))
+        ps = c.page_size
+        need = (int(attn.seq_lens[0]) + c.B + ps - 1) // ps
+        idx = torch.from_numpy(attn.block_table[0, :need].astype(np.int64)).to(dev)
+        kc = attn.k_cache.view(-1, ps, c.Hkv, c.D)[idx].reshape(-1, c.Hkv, c.D)
+        vc = attn.v_cache.view(-1, ps, c.Hkv, c.D)[idx].reshape(-1, c.Hkv, c.D)
+        qb = wl.bf16_bits(attn.q[:c.B])
+        kb, vb = wl.bf16_bits(kc), wl.bf16_bits(vc)
+        t0 = time.perf_counter()
+        oracle.block_attn_tree(qb, kb, vb, np.arange(need, dtype=np.int32)[None],
+                               attn.seq_lens[:1], x.parent[:1], c.B, c.Hq, c.Hkv, c.D, ps,
+                               attn.scale, num_pages=need, nthreads=cores)
+        dt_attn = time.perf_counter() - t0
+        host = [x.block_ids.cpu().numpy(), x.parent, x.p.cpu().numpy(), x.u.cpu().numpy(),
+                x.seq_lens.cpu().numpy()]
+        t0 = time.perf_counter()
+        oracle.tree_accept(*host, nthreads=cores)
+        dt_acc = time.perf_counter() - t0
+        base = {"value": n_nodes / dt_attn, "unit": "query tokens/s (tree attention)",
+                "accept_rows_per_s": c.bs / dt_acc, "cores": cores, "kind": "oracle",
+                "sample": f"tree attention of 1 of {c.bs} requests, acceptance of all "
+                          f"{c.bs} rows, fp64 C oracle, {cores} threads",
+                "seconds": dt_attn + dt_acc}
+    return {"nodes": n_nodes, "batch": c.bs, "vocab": cfg.V, "cpu_baseline": base,
             "attn_ms": attn_ms, "attn_query_tokens_per_s": c.bs * n_nodes / (attn_ms / 1e3),
             "attn_roofline": {"bound": "hbm", "achieved": abytes / (attn_ms / 1e3) / 1e9,
                               "peak": hbm, "unit": "GB/s",
@@ -728,9 +797,11 @@ def main(argv=None):
     if attn_ms is not None:
         fused_append = time_fused_append(step, flush, clean)
         assert step.status.item() == 0, bdsa.STATUS.get(step.status.item())
-    idlm = time_idlm(cfg, dev, flush, clean) if (cfg.V and attn_ms is not None) else None
-    kvmat = time_kvmat(step, flush, clean) if (cfg.V and attn_ms is not None) else None
-    tree = time_tree(cfg, dev, flush, clean) if (cfg.V and attn_ms is not None) else None
+    side = cfg.V and attn_ms is not None
+    cpu_side = rank == 0 and world == 1 and not args.no_cpu_baseline
+    idlm = time_idlm(cfg, dev, flush, clean, cpu=cpu_side) if side else None
+    kvmat = time_kvmat(step, flush, clean, cpu=cpu_side) if side else None
+    tree = time_tree(cfg, dev, flush, clean, cpu=cpu_side) if side else None
 
     e2e = None
     if not args.no_e2e:
