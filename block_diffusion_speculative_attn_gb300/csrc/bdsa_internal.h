@@ -53,6 +53,7 @@ struct AcceptPlan {
     int nseg;         // 256-element segments per vocabulary row
     int spc;          // segments per chunk
     bool cluster;     // one thread-block cluster per row (no global scratch)
+    bool prefetch;    // fewer CTAs than SMs: bulk-prefetch each chunk into L2
     size_t workspace; // bytes (0 on the cluster path)
 };
 

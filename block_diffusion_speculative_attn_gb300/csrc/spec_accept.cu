@@ -55,6 +55,7 @@ struct Params {
     const float *u_samp;
     const int32_t *seq_lens;
     int bs, B, V, nchunk, nseg, spc;
+    int prefetch;  // bulk-prefetch each chunk into L2 (grids smaller than the GPU)
     int32_t *accept_len, *commit_len, *out_tokens, *bonus_id, *new_seq_lens;
     float2 *seg_tot;   // global path: [bs, nseg] float-float totals
     int32_t *counter;  // global path: [bs], zeroed before the launch
@@ -140,8 +141,6 @@ __device__ __forceinline__ float2 ff_add(float2 a, float2 b) {
     return make_float2(hi, __fsub_rn(lo, __fsub_rn(hi, s)));
 }
 
-__device__ __forceinline__ double ff_to_double(float2 a) { return (double)a.x + (double)a.y; }
-
 // Sum of 8 weights as a float-float: a pairwise tree of TwoSums keeps every
 // rounding error; only the sum of those tiny errors is rounded.
 __device__ __forceinline__ float2 group_sum_ff(const float (&w)[8]) {
@@ -165,6 +164,9 @@ __device__ __forceinline__ float2 shfl_xor_ff(float2 v, int o) {
 __device__ __forceinline__ float2 shfl_up_ff(float2 v, int o) {
     return make_float2(__shfl_up_sync(0xffffffffu, v.x, o), __shfl_up_sync(0xffffffffu, v.y, o));
 }
+__device__ __forceinline__ float2 shfl_ff(float2 v, int src) {
+    return make_float2(__shfl_sync(0xffffffffu, v.x, src), __shfl_sync(0xffffffffu, v.y, src));
+}
 
 // Warp total (butterfly; every lane gets the total).
 __device__ __forceinline__ float2 warp_sum_ff(float2 v) {
@@ -181,6 +183,44 @@ __device__ __forceinline__ float2 warp_scan_ff(float2 v, int lane) {
         if (lane >= o) v = ff_add(v, t);
     }
     return v;
+}
+
+// Warp totals of four values at once: the first two butterfly levels halve
+// the number of values a lane carries (each lane sends the half it gives
+// away), so four totals cost 12 shuffles and 6 additions instead of 40 and
+// 20.  Lane l ends with the total of g[l >> 3].
+__device__ __forceinline__ float2 warp_sum4_ff(const float2 (&g)[4], int lane) {
+    const bool h16 = (lane & 16) != 0, h8 = (lane & 8) != 0;
+    const float2 k0 = ff_add(h16 ? g[2] : g[0], shfl_xor_ff(h16 ? g[0] : g[2], 16));
+    const float2 k1 = ff_add(h16 ? g[3] : g[1], shfl_xor_ff(h16 ? g[1] : g[3], 16));
+    float2 k = ff_add(h8 ? k1 : k0, shfl_xor_ff(h8 ? k0 : k1, 8));
+#pragma unroll
+    for (int o = 4; o > 0; o >>= 1) k = ff_add(k, shfl_xor_ff(k, o));
+    return k;
+}
+
+// a + w for a float-float a and a float w.
+__device__ __forceinline__ float2 ff_add_f(float2 a, float w) {
+    float e;
+    const float s = two_sum(a.x, w, e);
+    const float lo = __fadd_rn(a.y, e);
+    const float hi = __fadd_rn(s, lo);
+    return make_float2(hi, __fsub_rn(lo, __fsub_rn(hi, s)));
+}
+
+// u * a for a float u and a float-float a (the product's rounding error from
+// one fused multiply-add).
+__device__ __forceinline__ float2 ff_mul_f(float2 a, float u) {
+    const float p = __fmul_rn(u, a.x);
+    const float lo = __fadd_rn(__fmaf_rn(u, a.x, -p), __fmul_rn(u, a.y));
+    const float hi = __fadd_rn(p, lo);
+    return make_float2(hi, __fsub_rn(lo, __fsub_rn(hi, p)));
+}
+
+// a > b for normalised float-float values (hi == fl(hi + lo)): compare the
+// high parts, then the low parts.
+__device__ __forceinline__ bool ff_gt(float2 a, float2 b) {
+    return a.x > b.x || (a.x == b.x && a.y > b.y);
 }
 
 // ------------------------------------------------------------ acceptance
@@ -223,24 +263,56 @@ __device__ int accepted_len(const Params &P, int r, int lane, bool &bad_id, int 
     return a < 0 ? B - 1 : a;
 }
 
+// Starts pulling elements [seg_begin * kSeg, seg_end * kSeg) of a row into L2
+// with one bulk prefetch (a hint: nothing waits on it), so the whole chunk is
+// in flight from DRAM while the warps' own loads work through it.  Used when
+// the grid has fewer CTAs than the GPU has SMs: one CTA's own loads then
+// cannot keep DRAM busy (with two CTAs an SM the prefetch measured slower).
+__device__ __forceinline__ void prefetch_chunk_l2(const float *row, int seg_begin, int seg_end,
+                                                  int V) {
+    if (row == nullptr || seg_begin >= seg_end) return;
+    const long e0 = (long)seg_begin * kSeg, e1 = min((long)seg_end * kSeg, (long)V);
+    const uintptr_t a = reinterpret_cast<uintptr_t>(row + e0);
+    const uint32_t bytes = (uint32_t)(((e1 - e0) * 4) & ~15L);
+    if ((a & 15) != 0 || bytes == 0) return;
+    asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(a), "r"(bytes) : "memory");
+}
+
 // Segment totals of segments [seg_begin, seg_end) of the chosen distribution,
 // written to tot[seg] (shared memory of this or another cluster CTA, or global
-// memory).  Each warp loads kUnroll segments before reducing them, so its
-// loads overlap.
+// memory).  Each warp loads U segments before reducing them, so its loads
+// overlap; each group of four segments is reduced across the warp together.
 constexpr int kUnroll = 4;
 
 template <class PT, int U = kUnroll>
 __device__ void sweep_chunk(const PT &P, const float *prow, const float *qrow, int seg_begin,
                             int seg_end, int warp, int lane, float2 *tot) {
+    if (P.prefetch && threadIdx.x == 0) {
+        prefetch_chunk_l2(prow, seg_begin, seg_end, P.V);
+        prefetch_chunk_l2(qrow, seg_begin, seg_end, P.V);
+    }
     for (int s0 = seg_begin + warp; s0 < seg_end; s0 += U * kWarps) {
         float w[U][8];
 #pragma unroll
         for (int u = 0; u < U; ++u) {
             const int seg = s0 + u * kWarps;
             if (seg < seg_end) load_weights(prow, qrow, (long)seg * kSeg + lane * 8, P.V, w[u]);
+            else {
+#pragma unroll
+                for (int e = 0; e < 8; ++e) w[u][e] = 0.f;
+            }
         }
 #pragma unroll
-        for (int u = 0; u < U; ++u) {
+        for (int u0 = 0; u0 + 4 <= U; u0 += 4) {
+            float2 g[4];
+#pragma unroll
+            for (int k = 0; k < 4; ++k) g[k] = group_sum_ff(w[u0 + k]);
+            const float2 t = warp_sum4_ff(g, lane);
+            const int seg = s0 + (u0 + (lane >> 3)) * kWarps;
+            if ((lane & 7) == 0 && seg < seg_end) tot[seg] = t;
+        }
+#pragma unroll
+        for (int u = U & ~3; u < U; ++u) {
             const int seg = s0 + u * kWarps;
             if (seg < seg_end) {
                 const float2 t = warp_sum_ff(group_sum_ff(w[u]));
@@ -262,15 +334,16 @@ __device__ __forceinline__ float2 load_tot(const float2 *tot, int i) {
 
 // Resolve the draw InvCDF(w, u) from the segment totals with the whole CTA:
 // a block-wide scan of the totals finds the segment holding the crossing, then
-// warp 0 re-reads that one segment and finds the element.  Every thread
-// returns the token index (-1 when the weights are all zero).
+// warp 0 re-reads that one segment and finds the element.  All comparisons are
+// made on float-float values (about 48 significant bits), in fp32 arithmetic.
+// Every thread returns the token index (-1 when the weights are all zero).
 template <bool kShared, class PT>
 __device__ int resolve_draw(const PT &P, const float *prow, const float *qrow, float u,
                             const float2 *tot) {
     __shared__ float2 s_wtot[kWarps];
     __shared__ int s_seg;
-    __shared__ double s_base;
-    __shared__ double s_T;
+    __shared__ float2 s_base;
+    __shared__ float2 s_T;
     __shared__ int s_last_pos;
     __shared__ int s_tok;
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
@@ -287,27 +360,29 @@ __device__ int resolve_draw(const PT &P, const float *prow, const float *qrow, f
         s_last_pos = -1;
     }
     __syncthreads();
-    float2 wexcl = make_float2(0.f, 0.f), Sff = make_float2(0.f, 0.f);
+    float2 wexcl = make_float2(0.f, 0.f), S = make_float2(0.f, 0.f);
 #pragma unroll
     for (int w = 0; w < kWarps; ++w) {
         if (w < warp) wexcl = ff_add(wexcl, s_wtot[w]);
-        Sff = ff_add(Sff, s_wtot[w]);
+        S = ff_add(S, s_wtot[w]);
     }
     float2 excl = shfl_up_ff(inc, 1);
     if (lane == 0) excl = make_float2(0.f, 0.f);
     excl = ff_add(excl, wexcl);
-    const double S = ff_to_double(Sff);
-    if (!(S > 0.0)) return -1;  // uniform: every thread sees the same S
-    const double T = (double)u * S;
+    if (!(S.x > 0.f)) return -1;  // uniform: every thread sees the same S
+    const float2 T = ff_mul_f(S, u);
     // first segment whose cumulative total exceeds T
-    double run = ff_to_double(excl);
+    float2 run = excl;
     int found = -1;
     int last_pos = -1;
     for (int q = s0; q < s1; ++q) {
-        const double v = ff_to_double(load_tot<kShared>(tot, q));
-        if (v > 0.0) last_pos = q;
-        if (found < 0 && run + v > T) found = q;
-        if (found < 0) run += v;
+        const float2 v = load_tot<kShared>(tot, q);
+        if (v.x > 0.f) last_pos = q;
+        if (found < 0) {
+            const float2 next = ff_add(run, v);
+            if (ff_gt(next, T)) found = q;
+            else run = next;
+        }
     }
     if (found >= 0) atomicMin(&s_seg, found);
     if (last_pos >= 0) atomicMax(&s_last_pos, last_pos);
@@ -319,15 +394,15 @@ __device__ int resolve_draw(const PT &P, const float *prow, const float *qrow, f
     if (tid == 0 && s_seg == INT_MAX) {
         // rounding fallback: the last segment with positive mass, no crossing in it
         s_seg = s_last_pos;
-        s_base = 0.0;
-        s_T = INFINITY;
+        s_base = make_float2(0.f, 0.f);
+        s_T = make_float2(INFINITY, 0.f);
     }
     __syncthreads();
     if (warp == 0 && s_seg < 0) {
         if (lane == 0) s_tok = -1;
     } else if (warp == 0) {
         const int seg_star = s_seg;
-        const double base_seg = s_base, Tw = s_T;
+        const float2 base_seg = s_base, Tw = s_T;
         // within the segment: one 8-element group per lane
         float w[8];
         const long e0 = (long)seg_star * kSeg + lane * 8;
@@ -336,26 +411,25 @@ __device__ int resolve_draw(const PT &P, const float *prow, const float *qrow, f
         const float2 ginc = warp_scan_ff(gff, lane);
         float2 gexcl = shfl_up_ff(ginc, 1);
         if (lane == 0) gexcl = make_float2(0.f, 0.f);
-        const double g = ff_to_double(gff);
-        const double gb = base_seg + ff_to_double(gexcl);
-        const unsigned cross = __ballot_sync(0xffffffffu, gb + g > Tw);
+        const float2 gb = ff_add(base_seg, gexcl);
+        const unsigned cross = __ballot_sync(0xffffffffu, ff_gt(ff_add(gb, gff), Tw));
         int lane_star;
         bool use_cross;
         if (cross != 0u) {
             lane_star = __ffs(cross) - 1;
             use_cross = true;
         } else {
-            const unsigned pos = __ballot_sync(0xffffffffu, g > 0.0);
+            const unsigned pos = __ballot_sync(0xffffffffu, gff.x > 0.f);
             lane_star = pos ? 31 - __clz(pos) : 0;
             use_cross = false;
         }
-        double cum = __shfl_sync(0xffffffffu, gb, lane_star);
+        float2 cum = shfl_ff(gb, lane_star);
         if (lane == lane_star) {
             int k = -1, lp = -1;
             for (int e = 0; e < 8; ++e) {
                 if (w[e] > 0.f) lp = e;
-                cum += (double)w[e];
-                if (use_cross && cum > Tw) {
+                cum = ff_add_f(cum, w[e]);
+                if (use_cross && ff_gt(cum, Tw)) {
                     k = e;
                     break;
                 }
@@ -406,6 +480,7 @@ __device__ bool last_cta_of_row(const Params &P, int r) {
 // cluster (cluster rank == chunk for a 1-D grid of whole clusters).
 template <bool kCluster>
 __global__ void __launch_bounds__(kThreads) accept_stochastic_kernel(const Params P) {
+    grid_dependency_wait();  // the previous kernel's writes (launched with PDL)
     const int r = blockIdx.x / P.nchunk, chunk = blockIdx.x % P.nchunk;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     extern __shared__ float2 s_tot[];  // cluster path: [nseg] totals, used in chunk 0
@@ -472,6 +547,7 @@ __device__ __forceinline__ void better(float &bv, int &bi, float v, int i) {
 // flight); the resolving CTA combines the chunks and walks the block.
 template <bool kCluster>
 __global__ void __launch_bounds__(kThreads) accept_greedy_kernel(const Params P) {
+    grid_dependency_wait();  // the previous kernel's writes (launched with PDL)
     const int r = blockIdx.x / P.nchunk, chunk = blockIdx.x % P.nchunk;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int B = P.B, C = P.nchunk;
@@ -589,6 +665,7 @@ struct IdlmParams {
     const float *u_samp;       // [bs, N]: the anchor's, then spec'_j's
     const int32_t *seq_lens;
     int bs, N, V, nchunk, nseg, spc;
+    int prefetch;
     int32_t *accept_len, *n_out, *out_tokens, *next_mode, *next_pending, *next_specs,
         *next_q_slot, *new_seq_lens, *kv_keep;
     int32_t *dev_status;
@@ -632,6 +709,7 @@ __device__ int idlm_accepted(const IdlmParams &P, int r, int lane, int &m_out, i
 // the row's outputs; draw j > 0 is spec'_{j-1}, drawn only when the next round
 // verifies.
 __global__ void __launch_bounds__(kThreads) idlm_accept_kernel(const IdlmParams P) {
+    grid_dependency_wait();  // the previous kernel's writes (launched with PDL)
     const int unit = blockIdx.x / P.nchunk, chunk = blockIdx.x % P.nchunk;
     const int r = unit / P.N, j = unit % P.N;
     const int N = P.N;
@@ -736,6 +814,7 @@ struct TreeParams {
     int64_t psr, psn;
     const float *u;  // [bs, B] by depth; null = greedy
     int bs, B, V, nchunk, nseg, spc;
+    int prefetch;
     int32_t *accept_len, *path, *out_tokens, *bonus_id, *new_seq_lens;
     int32_t *dev_status;
 };
@@ -754,6 +833,7 @@ constexpr int kTreeUnroll = 5;
 // barriers a step.  The walk ends within B steps (a child's index exceeds its
 // parent's).
 __global__ void __launch_bounds__(kThreads, 2) tree_accept_kernel(const TreeParams P) {
+    grid_dependency_wait();  // the previous kernel's writes (launched with PDL)
     const int r = blockIdx.x / P.nchunk, chunk = blockIdx.x % P.nchunk;
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int B = P.B;
@@ -891,6 +971,7 @@ AcceptPlan accept_plan(int bs, int B, int V, int num_sms) {
     if (!p.cluster) nchunk = (p.nseg + spc - 1) / spc;
     p.nchunk = (int)nchunk;
     p.spc = (int)spc;
+    p.prefetch = (long)p.nchunk * bs < num_sms;
     p.workspace = p.cluster ? 0
                             : align256((size_t)bs * sizeof(int32_t)) +
                                   align256((size_t)bs * p.nseg * sizeof(float2)) +
@@ -923,6 +1004,7 @@ int launch_idlm_accept(const IdlmArgs &a, cudaStream_t stream) {
     P.nchunk = plan.nchunk;
     P.nseg = plan.nseg;
     P.spc = plan.spc;
+    P.prefetch = plan.prefetch;
     P.accept_len = a.accept_len;
     P.n_out = a.n_out;
     P.out_tokens = a.out_tokens;
@@ -945,13 +1027,17 @@ int launch_idlm_accept(const IdlmArgs &a, cudaStream_t stream) {
     cfg.blockDim = dim3(kThreads);
     cfg.dynamicSmemBytes = smem;
     cfg.stream = stream;
-    cudaLaunchAttribute attr[1];
+    cudaLaunchAttribute attr[2];
     attr[0].id = cudaLaunchAttributeClusterDimension;
     attr[0].val.clusterDim.x = (unsigned)plan.nchunk;
     attr[0].val.clusterDim.y = 1;
     attr[0].val.clusterDim.z = 1;
+    // may start while the previous kernel in the stream finishes; the kernel
+    // waits for it (griddepcontrol.wait) before its first global read
+    attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[1].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
-    cfg.numAttrs = 1;
+    cfg.numAttrs = 2;
     return cudaLaunchKernelEx(&cfg, idlm_accept_kernel, P) == cudaSuccess ? BDSA_OK
                                                                           : BDSA_CUDA_ERROR;
 }
@@ -975,6 +1061,7 @@ int launch_tree_accept(const TreeArgs &a, cudaStream_t stream) {
     P.nchunk = plan.nchunk;
     P.nseg = plan.nseg;
     P.spc = plan.spc;
+    P.prefetch = plan.prefetch;
     P.accept_len = a.accept_len;
     P.path = a.path;
     P.out_tokens = a.out_tokens;
@@ -993,13 +1080,17 @@ int launch_tree_accept(const TreeArgs &a, cudaStream_t stream) {
     cfg.blockDim = dim3(kThreads);
     cfg.dynamicSmemBytes = smem;
     cfg.stream = stream;
-    cudaLaunchAttribute attr[1];
+    cudaLaunchAttribute attr[2];
     attr[0].id = cudaLaunchAttributeClusterDimension;
     attr[0].val.clusterDim.x = (unsigned)plan.nchunk;
     attr[0].val.clusterDim.y = 1;
     attr[0].val.clusterDim.z = 1;
+    // may start while the previous kernel in the stream finishes; the kernel
+    // waits for it (griddepcontrol.wait) before its first global read
+    attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[1].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
-    cfg.numAttrs = 1;
+    cfg.numAttrs = 2;
     return cudaLaunchKernelEx(&cfg, tree_accept_kernel, P) == cudaSuccess ? BDSA_OK
                                                                           : BDSA_CUDA_ERROR;
 }
@@ -1026,6 +1117,7 @@ int launch_spec_accept(const AcceptArgs &a, cudaStream_t stream) {
     P.nchunk = plan.nchunk;
     P.nseg = plan.nseg;
     P.spc = plan.spc;
+    P.prefetch = plan.prefetch;
     P.accept_len = a.accept_len;
     P.commit_len = a.commit_len;
     P.out_tokens = a.out_tokens;
@@ -1053,13 +1145,17 @@ int launch_spec_accept(const AcceptArgs &a, cudaStream_t stream) {
         cfg.blockDim = dim3(kThreads);
         cfg.dynamicSmemBytes = smem;
         cfg.stream = stream;
-        cudaLaunchAttribute attr[1];
+        cudaLaunchAttribute attr[2];
         attr[0].id = cudaLaunchAttributeClusterDimension;
         attr[0].val.clusterDim.x = (unsigned)plan.nchunk;
         attr[0].val.clusterDim.y = 1;
         attr[0].val.clusterDim.z = 1;
+        // may start while the previous kernel in the stream finishes; the kernel
+        // waits for it (griddepcontrol.wait) before its first global read
+        attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+        attr[1].val.programmaticStreamSerializationAllowed = 1;
         cfg.attrs = attr;
-        cfg.numAttrs = 1;
+        cfg.numAttrs = 2;
         const cudaError_t e = greedy ? cudaLaunchKernelEx(&cfg, accept_greedy_kernel<true>, P)
                                      : cudaLaunchKernelEx(&cfg, accept_stochastic_kernel<true>, P);
         return e == cudaSuccess ? BDSA_OK : BDSA_CUDA_ERROR;
