@@ -767,11 +767,20 @@ def main(argv=None):
         flush.zero_()
         clean.sum()
         ev[i]["step"][0].record()
-        step.run(ev[i] if len(cfg.modes) == 1 else None)
+        step.run()
         ev[i]["step"][1].record()
     torch.cuda.synchronize()
     barrier(world)
     clk = clocks.stop()
+    # The stages' own times come from a second pass of K steps with events
+    # between the stages (an event between two kernels keeps the second from
+    # starting while the first finishes, so the step time above has none).
+    if len(cfg.modes) == 1:
+        for i in range(K):
+            flush.zero_()
+            clean.sum()
+            step.run(ev[i])
+        torch.cuda.synchronize()
     step_ms = [e["step"][0].elapsed_time(e["step"][1]) for e in ev]
     ms = statistics.mean(step_ms)
     attn_ms = (statistics.mean(e["attn"][0].elapsed_time(e["attn"][1]) for e in ev)
