@@ -220,14 +220,15 @@ class Step:
                               out=self.acc_out, workspace=self.acc_ws, dev_status=self.status)
 
     def run(self, ev=None):
-        """One step; ev = optional dict of (start, end) event pairs per stage to record."""
+        """One step; ev = optional dict of (start, end) event pairs per stage to
+        record ("attn": one pair per attention pass)."""
         self.prepare()
-        for m in self.cfg.modes:
+        for i, m in enumerate(self.cfg.modes):
             if ev is not None:
-                ev["attn"][0].record()
+                ev["attn"][i][0].record()
             self.attention(m)
             if ev is not None:
-                ev["attn"][1].record()
+                ev["attn"][i][1].record()
         if self.cfg.V:
             if ev is not None:
                 ev["accept"][0].record()
@@ -500,6 +501,9 @@ def time_tree(cfg: wl.StepConfig, dev, flush, clean, n_nodes: int = 32, iters: i
     import dataclasses
 
     import block_diffusion_speculative_attn_gb300 as bdsa
+    # the tree attention keeps a request's G x nodes query rows in one
+    # 128-row tile: 32 nodes at G = 4, 16 at G = 8
+    n_nodes = min(n_nodes, 128 // (cfg.Hq // cfg.Hkv))
     c = dataclasses.replace(cfg, B=n_nodes)
     attn = wl.make_attn_inputs(c, device=dev, seed=c.seed + 77)
     bt = torch.from_numpy(attn.block_table).to(dev)
@@ -743,7 +747,8 @@ def main(argv=None):
     clean = torch.ones(L2_CLEAN_BYTES // 4, dtype=torch.float32, device=dev)
     K = args.steps
     ev = [{"step": (torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)),
-           "attn": (torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)),
+           "attn": [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+                    for _ in cfg.modes],
            "accept": (torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))}
           for _ in range(K)]
     # The clock sampler starts first; the warm-up steps then run right before
@@ -775,18 +780,17 @@ def main(argv=None):
     # The stages' own times come from a second pass of K steps with events
     # between the stages (an event between two kernels keeps the second from
     # starting while the first finishes, so the step time above has none).
-    if len(cfg.modes) == 1:
-        for i in range(K):
-            flush.zero_()
-            clean.sum()
-            step.run(ev[i])
-        torch.cuda.synchronize()
+    for i in range(K):
+        flush.zero_()
+        clean.sum()
+        step.run(ev[i])
+    torch.cuda.synchronize()
     step_ms = [e["step"][0].elapsed_time(e["step"][1]) for e in ev]
     ms = statistics.mean(step_ms)
-    attn_ms = (statistics.mean(e["attn"][0].elapsed_time(e["attn"][1]) for e in ev)
-               if len(cfg.modes) == 1 else None)
+    # mean time of one attention call (over the steps and the step's passes)
+    attn_ms = statistics.mean(a.elapsed_time(b) for e in ev for a, b in e["attn"])
     acc_ms = (statistics.mean(e["accept"][0].elapsed_time(e["accept"][1]) for e in ev)
-              if (cfg.V and len(cfg.modes) == 1) else None)
+              if cfg.V else None)
     ms_max = max_over_ranks(ms, world, dev)
 
     tokens = cfg.bs * cfg.B * len(cfg.modes)
@@ -802,11 +806,13 @@ def main(argv=None):
                 "algorithmic_bytes_per_launch": abytes, "peak_source": peak_src,
                 "launch_ms": attn_ms}
 
+    # the side lines run on single-pass workloads (the default one included)
+    single = len(cfg.modes) == 1
     fused_append = None
-    if attn_ms is not None:
+    if single:
         fused_append = time_fused_append(step, flush, clean)
         assert step.status.item() == 0, bdsa.STATUS.get(step.status.item())
-    side = cfg.V and attn_ms is not None
+    side = cfg.V and single
     cpu_side = rank == 0 and world == 1 and not args.no_cpu_baseline
     idlm = time_idlm(cfg, dev, flush, clean, cpu=cpu_side) if side else None
     kvmat = time_kvmat(step, flush, clean, cpu=cpu_side) if side else None
