@@ -40,8 +40,9 @@
 //   * S = Q K^T and O += P V run on the tensor cores with fp32 accumulators in
 //     TMEM: two S buffers and two O buffers (512 columns), so consecutive units
 //     overlap;
-//   * softmax in the log2 domain: one FFMA + ex2 per score, running max with a
-//     lazy rescale of O in TMEM only when the max grows by more than 2^8, P
+//   * softmax in the log2 domain: one ex2 per score, the scale, the row max
+//     (three-input max) and the row sum on packed fp32 pairs, running max with
+//     a lazy rescale of O in TMEM only when the max grows by more than 2^8, P
 //     rounded to bf16 and written swizzled for the PV MMA.
 #include <cuda.h>
 #include <cuda_bf16.h>
@@ -154,6 +155,41 @@ __device__ __forceinline__ void st_shared_v4(uint32_t addr, uint32_t a, uint32_t
 __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
     __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
     return *reinterpret_cast<uint32_t *>(&v);
+}
+
+// Pairs of fp32 values in one 64-bit register, for the f32x2 arithmetic of
+// the sm_100 family (two results per instruction), and the three-input max:
+// the softmax at 128 columns a thread is bound by instruction issue, and
+// these halve its max, scale and sum instructions.
+__device__ __forceinline__ uint64_t f2_pack(float a, float b) {
+    uint64_t r;
+    asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(a), "f"(b));
+    return r;
+}
+__device__ __forceinline__ float2 f2_unpack(uint64_t r) {
+    float2 v;
+    asm("mov.b64 {%0, %1}, %2;" : "=f"(v.x), "=f"(v.y) : "l"(r));
+    return v;
+}
+__device__ __forceinline__ uint64_t f2_fma(uint64_t a, uint64_t b, uint64_t c) {
+    uint64_t d;
+    asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(d) : "l"(a), "l"(b), "l"(c));
+    return d;
+}
+__device__ __forceinline__ uint64_t f2_add(uint64_t a, uint64_t b) {
+    uint64_t d;
+    asm("add.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+    return d;
+}
+__device__ __forceinline__ uint64_t f2_mul(uint64_t a, uint64_t b) {
+    uint64_t d;
+    asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+    return d;
+}
+__device__ __forceinline__ float max3f(float a, float b, float c) {
+    float d;
+    asm("max.f32 %0, %1, %2, %3;" : "=f"(d) : "f"(a), "f"(b), "f"(c));
+    return d;
 }
 
 // One 32-column chunk of this thread's share of a TMEM accumulator block.
@@ -861,12 +897,13 @@ __global__ void __launch_bounds__(kAppend ? kThreadsAppend : kThreads, 1)
             }
             const int ob = k & 1;
             float m_used = -INFINITY;
-            // Partial sums of the scores' exponentials.  TREE: l4[0..1] hold
-            // them (the lse) and l4[2..3] the same values rounded to bf16 as
-            // the PV product sees them (the normalisation, so that o is a
-            // convex combination of V rows: a row that sees few keys, as in a
-            // short tree, is then within rounding of its dominant V row).
-            float l4[4] = {0.f, 0.f, 0.f, 0.f};
+            // Partial sums of the scores' exponentials, two packed pairs.
+            // TREE: lacc[0] holds them (the lse) and lacc[1] the same values
+            // rounded to bf16 as the PV product sees them (the normalisation,
+            // so that o is a convex combination of V rows: a row that sees few
+            // keys, as in a short tree, is then within rounding of its
+            // dominant V row).
+            uint64_t lacc[2] = {f2_pack(0.f, 0.f), f2_pack(0.f, 0.f)};
             for (int j = pc.a; j < pc.e; ++j, ++g) {
                 const long t0 = (long)j * kBN;
                 const int sb = (int)(g & 1);
@@ -924,7 +961,8 @@ __global__ void __launch_bounds__(kAppend ? kThreadsAppend : kThreads, 1)
                 }
                 float mx[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
 #pragma unroll
-                for (int c = 0; c < NC; ++c) mx[c & 3] = fmaxf(mx[c & 3], sv[c]);
+                for (int c = 0; c < NC; c += 2)
+                    mx[(c >> 1) & 3] = max3f(mx[(c >> 1) & 3], sv[c], sv[c + 1]);
                 float mt = fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3]));
                 if constexpr (M == 64) mt = fmaxf(mt, __shfl_xor_sync(0xffffffffu, mt, 16));
                 const float m_new = mt * sl2;
@@ -935,26 +973,32 @@ __global__ void __launch_bounds__(kAppend ? kThreadsAppend : kThreads, 1)
                     m_used = m_new;
                     resc = true;
                 }
-#pragma unroll
-                for (int q = 0; q < 4; ++q) l4[q] *= alpha;
+                {
+                    const uint64_t a2 = f2_pack(alpha, alpha);
+                    lacc[0] = f2_mul(lacc[0], a2);
+                    lacc[1] = f2_mul(lacc[1], a2);
+                }
                 uint32_t pk[NC / 2];
                 if (m_used == -INFINITY) {
 #pragma unroll
                     for (int c = 0; c < NC / 2; ++c) pk[c] = 0u;
                 } else {
                     const float neg_m = -m_used;
+                    const uint64_t sc2 = f2_pack(sl2, sl2), nm2 = f2_pack(neg_m, neg_m);
 #pragma unroll
                     for (int c = 0; c < NC / 2; ++c) {
-                        const float p0 = ex2_approx(fmaf(sv[2 * c], sl2, neg_m));
-                        const float p1 = ex2_approx(fmaf(sv[2 * c + 1], sl2, neg_m));
+                        const float2 xv =
+                            f2_unpack(f2_fma(f2_pack(sv[2 * c], sv[2 * c + 1]), sc2, nm2));
+                        const float p0 = ex2_approx(xv.x);
+                        const float p1 = ex2_approx(xv.y);
                         const uint32_t pr = pack_bf16x2(p0, p1);
                         pk[c] = pr;
                         if constexpr (kTree) {
-                            l4[c & 1] += p0 + p1;
-                            l4[2 + (c & 1)] +=
-                                __uint_as_float(pr << 16) + __uint_as_float(pr & 0xffff0000u);
+                            lacc[0] = f2_add(lacc[0], f2_pack(p0, p1));
+                            lacc[1] = f2_add(lacc[1], f2_pack(__uint_as_float(pr << 16),
+                                                              __uint_as_float(pr & 0xffff0000u)));
                         } else {
-                            l4[c & 3] += p0 + p1;
+                            lacc[c & 1] = f2_add(lacc[c & 1], f2_pack(p0, p1));
                         }
                     }
                 }
@@ -1032,13 +1076,14 @@ __global__ void __launch_bounds__(kAppend ? kThreadsAppend : kThreads, 1)
 
             // ---- end of the piece
             {
+                const float2 la = f2_unpack(lacc[0]), lb = f2_unpack(lacc[1]);
                 float l, lr;
                 if constexpr (kTree) {
-                    l = l4[0] + l4[1];
-                    lr = l4[2] + l4[3];
+                    l = la.x + la.y;
+                    lr = lb.x + lb.y;
                     if constexpr (M == 64) lr += __shfl_xor_sync(0xffffffffu, lr, 16);
                 } else {
-                    l = (l4[0] + l4[1]) + (l4[2] + l4[3]);
+                    l = (la.x + la.y) + (lb.x + lb.y);
                 }
                 if constexpr (M == 64) l += __shfl_xor_sync(0xffffffffu, l, 16);
                 if constexpr (!kTree) lr = l;
