@@ -133,6 +133,7 @@ struct Params {
     int32_t *dev_status;
     uint64_t magic_S;        // floor((2^64 - 1) / grid), see range_start
     int max_pages, num_pages, bs, B, Hq, Hkv, G, rows, page_size, log2_ps, box_rows, mode;
+    int out_v8;              // out is 32-byte aligned: the M = 128 epilogue stores 32 bytes
     float scale_log2;
 };
 
@@ -144,6 +145,15 @@ struct AppendParams {
     uint16_t *k_cache;       // the caches they are written into
     uint16_t *v_cache;
 };
+
+// 32-byte global store (one whole sector per lane).
+__device__ __forceinline__ void st_global_v8(void *p, uint32_t a, uint32_t b, uint32_t c,
+                                             uint32_t d, uint32_t e, uint32_t f, uint32_t g,
+                                             uint32_t h) {
+    asm volatile("st.global.v8.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8};" ::"l"(p), "r"(a),
+                 "r"(b), "r"(c), "r"(d), "r"(e), "r"(f), "r"(g), "r"(h)
+                 : "memory");
+}
 
 __device__ __forceinline__ void st_shared_v4(uint32_t addr, uint32_t a, uint32_t b, uint32_t c,
                                              uint32_t d) {
@@ -829,6 +839,9 @@ __global__ void __launch_bounds__(kAppend ? kThreadsAppend : kThreads, 1)
                 stage_busy = true;
                 stage_k = e.k;
             } else {
+                // M = 128: one thread per row stores its row directly, 32 bytes
+                // a lane per instruction (whole sectors; the partial slots are
+                // 256-byte aligned, out when it is 32-byte aligned).
 #pragma unroll
                 for (int c = 0; c < OC / 32; ++c) {
                     float v32[32];
@@ -836,23 +849,34 @@ __global__ void __launch_bounds__(kAppend ? kThreadsAppend : kThreads, 1)
                     if (!valid_row) continue;
                     const int col0 = half * OC + c * 32;
                     if (e.complete) {
-                        uint4 *dst = reinterpret_cast<uint4 *>(prm.out + e.orow * D + col0);
+                        uint32_t w[16];
 #pragma unroll
-                        for (int v = 0; v < 4; ++v) {
-                            uint4 w;
-                            w.x = pack_bf16x2(v32[8 * v + 0] * sc, v32[8 * v + 1] * sc);
-                            w.y = pack_bf16x2(v32[8 * v + 2] * sc, v32[8 * v + 3] * sc);
-                            w.z = pack_bf16x2(v32[8 * v + 4] * sc, v32[8 * v + 5] * sc);
-                            w.w = pack_bf16x2(v32[8 * v + 6] * sc, v32[8 * v + 7] * sc);
-                            dst[v] = w;
+                        for (int v = 0; v < 16; ++v)
+                            w[v] = pack_bf16x2(v32[2 * v] * sc, v32[2 * v + 1] * sc);
+                        uint16_t *dst = prm.out + e.orow * D + col0;
+                        if (prm.out_v8) {
+                            st_global_v8(dst, w[0], w[1], w[2], w[3], w[4], w[5], w[6], w[7]);
+                            st_global_v8(dst + 16, w[8], w[9], w[10], w[11], w[12], w[13], w[14],
+                                         w[15]);
+                        } else {
+                            uint4 *d4 = reinterpret_cast<uint4 *>(dst);
+#pragma unroll
+                            for (int v = 0; v < 4; ++v)
+                                d4[v] = make_uint4(w[4 * v], w[4 * v + 1], w[4 * v + 2],
+                                                   w[4 * v + 3]);
                         }
                     } else {
-                        float4 *dst = reinterpret_cast<float4 *>(
-                            prm.part_o + ((long)e.slot * prm.rows + row) * D + col0);
+                        float *dst = prm.part_o + ((long)e.slot * prm.rows + row) * D + col0;
 #pragma unroll
-                        for (int v = 0; v < 8; ++v)
-                            dst[v] = make_float4(v32[4 * v] * sc, v32[4 * v + 1] * sc,
-                                                 v32[4 * v + 2] * sc, v32[4 * v + 3] * sc);
+                        for (int v = 0; v < 4; ++v)
+                            st_global_v8(dst + 8 * v, __float_as_uint(v32[8 * v] * sc),
+                                         __float_as_uint(v32[8 * v + 1] * sc),
+                                         __float_as_uint(v32[8 * v + 2] * sc),
+                                         __float_as_uint(v32[8 * v + 3] * sc),
+                                         __float_as_uint(v32[8 * v + 4] * sc),
+                                         __float_as_uint(v32[8 * v + 5] * sc),
+                                         __float_as_uint(v32[8 * v + 6] * sc),
+                                         __float_as_uint(v32[8 * v + 7] * sc));
                     }
                 }
                 tc_fence_before();
@@ -1340,6 +1364,7 @@ int launch_impl(const AttnArgs &a, const AttnPlan &plan, cudaStream_t stream) {
     prm.seq_lens = a.seq_lens;
     prm.part_bad = reinterpret_cast<int32_t *>(ws + plan.off_part_bad);
     prm.out = a.out;
+    prm.out_v8 = (reinterpret_cast<uintptr_t>(a.out) & 31) == 0;
     prm.lse = a.lse;
     prm.tree_mask = a.tree_mask;
     prm.part_o = reinterpret_cast<float *>(ws + plan.off_part_o);

@@ -205,3 +205,28 @@ def test_full_size_sampled(dev, name):
         assert torch.isfinite(out.float()).all()
     del d, inp
     torch.cuda.empty_cache()
+
+
+@pytest.mark.parametrize("sms", [0, FORCE_SPLIT])
+def test_output_16_byte_aligned_only(dev, sms):
+    """An output buffer that is 16- but not 32-byte aligned (the M = 128 tile
+    then stores 16 bytes a lane instead of 32) gives the same bits as an
+    aligned one."""
+    import block_diffusion_speculative_attn_gb300 as bdsa
+    name, Hq, Hkv, D, B, ps, lens = SHAPES[2]  # 128 rows a tile
+    cfg = _cfg(name, len(lens), Hq, Hkv, D, B, ps, lens)
+    inp = wl.make_attn_inputs(cfg, extra_pages=2)
+    d = DevAttn(inp)
+    ref, _ = run_attn(d, VERIFY, sms=sms, lse=False)
+    n = d.q.numel()
+    base = torch.empty(n + 64, dtype=torch.bfloat16, device=dev)
+    off = (-(base.data_ptr() // 2) % 16) + 8  # 32-byte boundary + 16 bytes
+    out = base[off:off + n].view(d.q.shape)
+    assert out.data_ptr() % 32 == 16
+    status = torch.zeros(1, dtype=torch.int32, device=dev)
+    bdsa.block_attn_paged(d.q, d.k, d.v, d.bt, d.sl, B=cfg.B, page_size=cfg.page_size,
+                          scale=inp.scale, mode=VERIFY, max_ctx_len=inp.max_ctx_len,
+                          num_pages=inp.num_pages, out=out, dev_status=status, sms=sms)
+    torch.cuda.synchronize()
+    assert status.item() == 0
+    assert torch.equal(out.view(torch.int16), ref.view(torch.int16))
