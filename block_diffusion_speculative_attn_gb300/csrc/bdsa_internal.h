@@ -17,7 +17,7 @@ namespace bdsa {
 struct AttnPlan {
     int grid;
     int rows;             // packed query rows per unit (G * B)
-    size_t off_part_bad, off_part_o, off_part_lse;
+    size_t off_part_bad, off_part_ready, off_part_o, off_part_lse;
     size_t workspace;     // total bytes
 };
 

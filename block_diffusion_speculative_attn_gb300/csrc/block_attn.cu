@@ -48,6 +48,8 @@
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
 
+#include <atomic>
+#include <chrono>
 #include <mutex>
 #include <utility>
 
@@ -112,7 +114,10 @@ struct Cfg {
     static constexpr int EW = OE + 2;
     static constexpr int ER = EW + 1;
     static constexpr int DR = ER + 1;     // drain
-    static constexpr int kNumBars = DR + 1;
+    // every softmax warp has fenced its stores of a partial piece; one phase
+    // per partial piece, waited by thread 0 alone before it publishes the slot
+    static constexpr int PB = DR + 1;
+    static constexpr int kNumBars = PB + 1;
     static constexpr int kOffMisc = kOffBar + 8 * kNumBars;
     static constexpr int kOffMiscEnd = kOffMisc + 144;  // the schedule state (Sched)
     // + slack to align the base to 1 KB.  With D = 128 this is within a few
@@ -125,6 +130,8 @@ struct Params {
     const int32_t *block_table;
     const int32_t *seq_lens;
     int32_t *part_bad;       // [2 * grid] partial slot saw a page id outside the pool
+    uint64_t *part_ready;    // [2 * grid] the call's ticket once the slot is written
+    uint64_t ticket;         // this call's ticket (unique a call, never 0)
     uint16_t *out;
     float *lse;
     const uint64_t *tree_mask;  // TREE mode: [bs * B] block keys visible to each block row
@@ -145,6 +152,15 @@ struct AppendParams {
     uint16_t *k_cache;       // the caches they are written into
     uint16_t *v_cache;
 };
+
+__device__ __forceinline__ void st_release_gpu_u64(uint64_t *p, uint64_t v) {
+    asm volatile("st.release.gpu.global.u64 [%0], %1;" ::"l"(p), "l"(v) : "memory");
+}
+__device__ __forceinline__ uint64_t ld_acquire_gpu_u64(const uint64_t *p) {
+    uint64_t v;
+    asm volatile("ld.acquire.gpu.global.u64 %0, [%1];" : "=l"(v) : "l"(p) : "memory");
+    return v;
+}
 
 // 32-byte global store (one whole sector per lane).
 __device__ __forceinline__ void st_global_v8(void *p, uint32_t a, uint32_t b, uint32_t c,
@@ -433,8 +449,7 @@ __global__ void __launch_bounds__(kAppend ? kThreadsAppend : kThreads, 1)
     block_attn_kernel(const __grid_constant__ CUtensorMap tm_q,
                       const __grid_constant__ CUtensorMap tm_k,
                       const __grid_constant__ CUtensorMap tm_v,
-                      const __grid_constant__ CUtensorMap tm_out,
-                      const __grid_constant__ CUtensorMap tm_part, const Params prm,
+                      const __grid_constant__ CUtensorMap tm_out, const Params prm,
                       const AppendParams app) {
     using C = Cfg<D, M>;
     extern __shared__ uint8_t smem_raw[];
@@ -481,6 +496,7 @@ __global__ void __launch_bounds__(kAppend ? kThreadsAppend : kThreads, 1)
         mbar_init(bar(C::EW), kSoftmaxWarps);
         mbar_init(bar(C::ER), 1);
         mbar_init(bar(C::DR), 1);
+        mbar_init(bar(C::PB), kSoftmaxWarps);
         *abort_flag = 0;
         sch->appended = 0;
         fence_mbarrier_init();
@@ -746,6 +762,7 @@ __global__ void __launch_bounds__(kAppend ? kThreadsAppend : kThreads, 1)
         // returns; they are released before the next write to them.
         bool stage_busy = false;
         int stage_k = 0;
+        int n_pub = 0;  // partial pieces published so far (phases of PB)
         auto release_stage = [&]() -> bool {
             if (tid == 0) {
                 bulk_wait_group_read0();
@@ -799,15 +816,19 @@ __global__ void __launch_bounds__(kAppend ? kThreadsAppend : kThreads, 1)
                                          pack_bf16x2(v32[8 * v + 4] * sc, v32[8 * v + 5] * sc),
                                          pack_bf16x2(v32[8 * v + 6] * sc, v32[8 * v + 7] * sc));
                     } else {
-                        // 32 fp32 = one 128-byte row of a 32-column box
-                        const uint32_t rbase = stage + (col0 >> 5) * C::kSlab + row * 128;
+                        // a partial goes straight to its slot (generic stores, so
+                        // that the ready word published below orders them)
+                        float *dst = prm.part_o + ((long)e.slot * prm.rows + row) * D + col0;
 #pragma unroll
-                        for (int v = 0; v < 8; ++v)
-                            st_shared_v4(rbase + ((v ^ (row & 7)) << 4),
-                                         __float_as_uint(v32[4 * v + 0] * sc),
-                                         __float_as_uint(v32[4 * v + 1] * sc),
-                                         __float_as_uint(v32[4 * v + 2] * sc),
-                                         __float_as_uint(v32[4 * v + 3] * sc));
+                        for (int v = 0; v < 4; ++v)
+                            st_global_v8(dst + 8 * v, __float_as_uint(v32[8 * v] * sc),
+                                         __float_as_uint(v32[8 * v + 1] * sc),
+                                         __float_as_uint(v32[8 * v + 2] * sc),
+                                         __float_as_uint(v32[8 * v + 3] * sc),
+                                         __float_as_uint(v32[8 * v + 4] * sc),
+                                         __float_as_uint(v32[8 * v + 5] * sc),
+                                         __float_as_uint(v32[8 * v + 6] * sc),
+                                         __float_as_uint(v32[8 * v + 7] * sc));
                     }
                 }
                 // the O buffer may take the next unit but one as soon as it is read
@@ -821,16 +842,10 @@ __global__ void __launch_bounds__(kAppend ? kThreadsAppend : kThreads, 1)
                 if (tid == 0) {
                     const bool okw = mbar_wait(bar(C::EW), (uint32_t)(e.k & 1), abort_flag,
                                                prm.dev_status);
-                    if (okw) {
-                        if (e.complete) {
-                            for (int sl = 0; sl < D / 64; ++sl)
-                                tma_store_4d(&tm_out, stage + sl * C::kSlab, sl * 64, 0, e.h,
-                                             e.r * B);
-                        } else {
-                            for (int bx = 0; bx < D / 32; ++bx)
-                                tma_store_2d(&tm_part, stage + bx * C::kSlab, bx * 32,
-                                             e.slot * prm.rows);
-                        }
+                    if (okw && e.complete) {
+                        for (int sl = 0; sl < D / 64; ++sl)
+                            tma_store_4d(&tm_out, stage + sl * C::kSlab, sl * 64, 0, e.h,
+                                         e.r * B);
                         bulk_commit_group();
                     }
                 }
@@ -892,7 +907,22 @@ __global__ void __launch_bounds__(kAppend ? kThreadsAppend : kThreads, 1)
                     prm.part_lse[(long)e.slot * prm.rows + row] = e.lse2;
                 }
             }
-            if (!e.complete && tid == 0) prm.part_bad[e.slot] = e.bad ? 1 : 0;
+            if (!e.complete) {
+                // Publish the partial: once every softmax warp has arrived
+                // after its stores of it (the arrival releases them at CTA
+                // scope), thread 0 writes this call's ticket into the slot's
+                // ready word with a GPU-scope release, which carries those
+                // stores with it; the merge kernel may read the slot once it
+                // acquires the word.  Only thread 0 waits, and boundedly.
+                if (tid == 0) prm.part_bad[e.slot] = e.bad ? 1 : 0;
+                __syncwarp();
+                if (lane == 0) mbar_arrive(bar(C::PB));
+                if (tid == 0) {
+                    if (mbar_wait(bar(C::PB), (uint32_t)(n_pub & 1), abort_flag, prm.dev_status))
+                        st_release_gpu_u64(prm.part_ready + e.slot, prm.ticket);
+                }
+                ++n_pub;
+            }
             return true;
         };
         long g = 0;
@@ -1156,6 +1186,7 @@ __global__ void __launch_bounds__(kAppend ? kThreadsAppend : kThreads, 1)
 constexpr int kMergeThreads = 256;
 constexpr int kMergeTPR = 4;      // threads per row
 constexpr int kMergeSlots = 16;   // piece slots listed in shared memory
+constexpr uint64_t kMergeWaitNs = 20000000ull;  // 20 ms, then wait for the whole grid
 
 // At most 64 registers a thread (launch bound of 4 CTAs an SM): two merge warps
 // must fit on each SM sub-partition beside two attention warps, so that the
@@ -1169,11 +1200,19 @@ __global__ void __launch_bounds__(kMergeThreads, 4) attn_merge_kernel(const Para
     const int b = blockIdx.x, S = gridDim.x;
     schedule<kMergeThreads>(prm, b, S, &sch);
     const long W = sch.W, Wc = sch.Wc, x0 = sch.x0;
-    if (x0 >= W) return;
+    // Every CTA ends with griddepcontrol.wait, so that this grid completes
+    // after the attention grid and a kernel that waits on it sees every row.
+    if (x0 >= W) {
+        grid_dependency_wait();
+        return;
+    }
     const long u_off = sch.u_off0, cu = sch.cu0;
     // the cut at this CTA's start splits the unit's tiles, and CTA b - 1 holds
     // the unit's first tile (so this is the unit's first cut)
-    if (!(u_off < x0 && range_start(b - 1, Wc, S, prm.magic_S) <= cu + kUnitCost)) return;
+    if (!(u_off < x0 && range_start(b - 1, Wc, S, prm.magic_S) <= cu + kUnitCost)) {
+        grid_dependency_wait();
+        return;
+    }
     const int r = sch.r0, h = sch.h0;
     const int b_first = cta_of(cu + kUnitCost, Wc, S);
     const int b_last = cta_of(cu + kUnitCost + sch.nt0 - 1, Wc, S);
@@ -1190,9 +1229,32 @@ __global__ void __launch_bounds__(kMergeThreads, 4) attn_merge_kernel(const Para
         }
         s_np = n;
     }
+    // Wait until every piece of the unit is published (ready word == this
+    // call's ticket, written after the piece's stores and a GPU-wide fence),
+    // so that the merge overlaps the attention CTAs still streaming.  All the
+    // attention CTAs are resident (this grid starts only once each of them has
+    // passed its launch_dependents), so the words do get written; the wait is
+    // still bounded, and past the limit the merge waits for the whole
+    // attention grid instead, by when every slot is final.
+    if (threadIdx.x == 0) {
+        const uint64_t t0 = global_timer_ns();
+        bool late = false;
+        for (int bb = b_first; bb <= b_last && !late; ++bb) {
+            const long cb = range_start(bb, Wc, S, prm.magic_S);
+            if (!(cb < range_start(bb + 1, Wc, S, prm.magic_S))) continue;
+            const uint64_t *w = prm.part_ready + 2 * bb + (cb >= cu ? 0 : 1);
+            while (ld_acquire_gpu_u64(w) != prm.ticket) {
+                if (global_timer_ns() - t0 > kMergeWaitNs) {
+                    late = true;
+                    break;
+                }
+                __nanosleep(256);
+            }
+        }
+        if (late) grid_dependency_wait();
+    }
     __syncthreads();
     const int np = s_np;
-    grid_dependency_wait();  // the attention grid's partials
     constexpr int C4 = D / 4;
     constexpr int F4 = C4 / kMergeTPR;  // 16-byte columns per thread
     const int items = prm.rows * kMergeTPR;
@@ -1256,6 +1318,7 @@ __global__ void __launch_bounds__(kMergeThreads, 4) attn_merge_kernel(const Para
         }
         if (sub == 0 && prm.lse) prm.lse[orow] = ok ? (mmax + log2f(den)) * kLn2 : -INFINITY;
     }
+    grid_dependency_wait();
 }
 
 // ------------------------------------------------------------------ host side
@@ -1276,6 +1339,26 @@ EncodeTiledFn encode_fn() {
             fn = reinterpret_cast<EncodeTiledFn>(p);
     });
     return fn;
+}
+
+// A ticket unique to each call and never 0: a partial slot's ready word holds
+// the ticket of the call that last wrote it, so it cannot show the current
+// call's ticket before this call publishes the slot.  The counter starts at a
+// value mixed from the clock (the splitmix64 finaliser), so that a workspace
+// left by another process is as unlikely to match.
+uint64_t next_ticket() {
+    static std::atomic<uint64_t> counter{[] {
+        uint64_t x = (uint64_t)std::chrono::steady_clock::now().time_since_epoch().count();
+        x += 0x9E3779B97F4A7C15ull;
+        x = (x ^ (x >> 30)) * 0xBF58476D1CE4E5B9ull;
+        x = (x ^ (x >> 27)) * 0x94D049BB133111EBull;
+        return x ^ (x >> 31);
+    }()};
+    uint64_t t;
+    do {
+        t = counter.fetch_add(1, std::memory_order_relaxed) + 1;
+    } while (t == 0);
+    return t;
 }
 
 // Launch with the programmatic-stream-serialization attribute, so the kernel
@@ -1332,7 +1415,7 @@ int launch_impl(const AttnArgs &a, const AttnPlan &plan, cudaStream_t stream) {
             return BDSA_CUDA_ERROR;
     }
     char *ws = static_cast<char *>(a.workspace);
-    CUtensorMap tout, tpart;
+    CUtensorMap tout;
     {
         // out has q's layout; the epilogue stores a whole unit's rows per box.
         cuuint64_t dims[4] = {(cuuint64_t)D, (cuuint64_t)G, (cuuint64_t)a.Hkv,
@@ -1347,22 +1430,12 @@ int launch_impl(const AttnArgs &a, const AttnPlan &plan, cudaStream_t stream) {
             CUDA_SUCCESS)
             return BDSA_CUDA_ERROR;
     }
-    {
-        // partial slots [2 * grid * rows, D] fp32, stored 32 columns x rows per box.
-        cuuint64_t dims[2] = {(cuuint64_t)D, (cuuint64_t)2 * plan.grid * plan.rows};
-        cuuint64_t strides[1] = {(cuuint64_t)D * 4};
-        cuuint32_t box[2] = {32, (cuuint32_t)plan.rows};
-        cuuint32_t es[2] = {1, 1};
-        if (enc(&tpart, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2, ws + plan.off_part_o, dims, strides,
-                box, es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
-                CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) !=
-            CUDA_SUCCESS)
-            return BDSA_CUDA_ERROR;
-    }
     Params prm;
     prm.block_table = a.block_table;
     prm.seq_lens = a.seq_lens;
     prm.part_bad = reinterpret_cast<int32_t *>(ws + plan.off_part_bad);
+    prm.part_ready = reinterpret_cast<uint64_t *>(ws + plan.off_part_ready);
+    prm.ticket = next_ticket();
     prm.out = a.out;
     prm.out_v8 = (reinterpret_cast<uintptr_t>(a.out) & 31) == 0;
     prm.lse = a.lse;
@@ -1405,8 +1478,7 @@ int launch_impl(const AttnArgs &a, const AttnPlan &plan, cudaStream_t stream) {
         attr_set[inst] = true;
     }
     if (launch_pdl(kernel, dim3(plan.grid), dim3(append ? kThreadsAppend : kThreads), C::kSmem,
-                   stream, tq, tk, tv, tout,
-                   tpart, prm, app) != cudaSuccess)
+                   stream, tq, tk, tv, tout, prm, app) != cudaSuccess)
         return BDSA_CUDA_ERROR;
     if (launch_pdl(attn_merge_kernel<D>, dim3(plan.grid), dim3(kMergeThreads), 0, stream,
                    prm) != cudaSuccess)
@@ -1427,6 +1499,8 @@ AttnPlan attn_plan(int bs, int B, int Hq, int Hkv, int D, int max_ctx_len, int n
     (void)bs;
     p.off_part_bad = off;
     off += align256((size_t)2 * p.grid * sizeof(int32_t));
+    p.off_part_ready = off;
+    off += align256((size_t)2 * p.grid * sizeof(uint64_t));
     p.off_part_lse = off;
     off += align256((size_t)2 * p.grid * p.rows * sizeof(float));
     p.off_part_o = off;

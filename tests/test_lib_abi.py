@@ -107,13 +107,14 @@ def test_prepare_host_checks(L):
 
 
 def test_workspace_plans(L):
-    # persistent schedule: two partial slots per CTA (bad-page flag, log2-sum-exp
-    # per row, output rows)
+    # persistent schedule: two partial slots per CTA (bad-page flag, 64-bit
+    # ready word, log2-sum-exp per row, output rows)
     def al(x):
         return (x + 255) // 256 * 256
     bs, B, Hq, Hkv, D, sms = 32, 16, 32, 8, 128, 152
     rows = Hq // Hkv * B
-    want = al(2 * sms * 4) + al(2 * sms * rows * 4) + al(2 * sms * rows * D * 4)
+    want = (al(2 * sms * 4) + al(2 * sms * 8) + al(2 * sms * rows * 4)
+            + al(2 * sms * rows * D * 4))
     assert L.bdsa_block_attn_workspace_bytes(bs, B, Hq, Hkv, D, 4096, sms) == want
     # independent of the context length bound
     assert L.bdsa_block_attn_workspace_bytes(bs, B, Hq, Hkv, D, 131072, sms) == want
