@@ -23,8 +23,9 @@
 //           references; a unit that references one outside the pool is written
 //           as zeros (lse -inf) and reported;
 //   merge   one CTA per range boundary that is a unit's first cut: merges the
-//           unit's partials in tile order, from a descriptor of the cut that
-//           the attention CTA left.
+//           unit's partials in tile order as soon as each is published (a
+//           ready word per partial slot carrying the call's ticket), while the
+//           attention grid finishes.
 //
 // Inside a CTA (warp roles: 0-3 softmax + epilogue, 4 Q/K producer, 5 MMA
 // issuer + TMEM owner, 6 V producer):
@@ -1178,7 +1179,8 @@ __global__ void __launch_bounds__(kAppend ? kThreadsAppend : kThreads, 1)
 // unit whose first interior cut is the start of attention CTA b's range: it
 // derives that unit and the slots of its pieces from the context lengths (the
 // same schedule as the attention kernel, computed while the attention runs),
-// waits for the attention grid, then merges the pieces in tile order.  Four
+// waits until each piece's ready word carries the call's ticket, then merges
+// the pieces in tile order, and ends with griddepcontrol.wait.  Four
 // threads share a row, their 16-byte columns interleaved so each warp load
 // reads whole 32-byte sectors, and walk the pieces with all of a piece's
 // loads in flight.  A unit any of whose pieces saw a page id outside the pool
