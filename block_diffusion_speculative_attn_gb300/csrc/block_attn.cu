@@ -133,6 +133,7 @@ struct Params {
     int32_t *part_bad;       // [2 * grid] partial slot saw a page id outside the pool
     uint64_t *part_ready;    // [2 * grid] the call's ticket once the slot is written
     uint64_t ticket;         // this call's ticket (unique a call, never 0)
+    int early_merge;         // M = 128: partials are published, the merge starts on them
     uint16_t *out;
     float *lse;
     const uint64_t *tree_mask;  // TREE mode: [bs * B] block keys visible to each block row
@@ -450,7 +451,8 @@ __global__ void __launch_bounds__(kAppend ? kThreadsAppend : kThreads, 1)
     block_attn_kernel(const __grid_constant__ CUtensorMap tm_q,
                       const __grid_constant__ CUtensorMap tm_k,
                       const __grid_constant__ CUtensorMap tm_v,
-                      const __grid_constant__ CUtensorMap tm_out, const Params prm,
+                      const __grid_constant__ CUtensorMap tm_out,
+                      const __grid_constant__ CUtensorMap tm_part, const Params prm,
                       const AppendParams app) {
     using C = Cfg<D, M>;
     extern __shared__ uint8_t smem_raw[];
@@ -817,19 +819,15 @@ __global__ void __launch_bounds__(kAppend ? kThreadsAppend : kThreads, 1)
                                          pack_bf16x2(v32[8 * v + 4] * sc, v32[8 * v + 5] * sc),
                                          pack_bf16x2(v32[8 * v + 6] * sc, v32[8 * v + 7] * sc));
                     } else {
-                        // a partial goes straight to its slot (generic stores, so
-                        // that the ready word published below orders them)
-                        float *dst = prm.part_o + ((long)e.slot * prm.rows + row) * D + col0;
+                        // 32 fp32 = one 128-byte row of a 32-column box
+                        const uint32_t rbase = stage + (col0 >> 5) * C::kSlab + row * 128;
 #pragma unroll
-                        for (int v = 0; v < 4; ++v)
-                            st_global_v8(dst + 8 * v, __float_as_uint(v32[8 * v] * sc),
-                                         __float_as_uint(v32[8 * v + 1] * sc),
-                                         __float_as_uint(v32[8 * v + 2] * sc),
-                                         __float_as_uint(v32[8 * v + 3] * sc),
-                                         __float_as_uint(v32[8 * v + 4] * sc),
-                                         __float_as_uint(v32[8 * v + 5] * sc),
-                                         __float_as_uint(v32[8 * v + 6] * sc),
-                                         __float_as_uint(v32[8 * v + 7] * sc));
+                        for (int v = 0; v < 8; ++v)
+                            st_shared_v4(rbase + ((v ^ (row & 7)) << 4),
+                                         __float_as_uint(v32[4 * v + 0] * sc),
+                                         __float_as_uint(v32[4 * v + 1] * sc),
+                                         __float_as_uint(v32[4 * v + 2] * sc),
+                                         __float_as_uint(v32[4 * v + 3] * sc));
                     }
                 }
                 // the O buffer may take the next unit but one as soon as it is read
@@ -843,10 +841,16 @@ __global__ void __launch_bounds__(kAppend ? kThreadsAppend : kThreads, 1)
                 if (tid == 0) {
                     const bool okw = mbar_wait(bar(C::EW), (uint32_t)(e.k & 1), abort_flag,
                                                prm.dev_status);
-                    if (okw && e.complete) {
-                        for (int sl = 0; sl < D / 64; ++sl)
-                            tma_store_4d(&tm_out, stage + sl * C::kSlab, sl * 64, 0, e.h,
-                                         e.r * B);
+                    if (okw) {
+                        if (e.complete) {
+                            for (int sl = 0; sl < D / 64; ++sl)
+                                tma_store_4d(&tm_out, stage + sl * C::kSlab, sl * 64, 0, e.h,
+                                             e.r * B);
+                        } else {
+                            for (int bx = 0; bx < D / 32; ++bx)
+                                tma_store_2d(&tm_part, stage + bx * C::kSlab, bx * 32,
+                                             e.slot * prm.rows);
+                        }
                         bulk_commit_group();
                     }
                 }
@@ -908,14 +912,16 @@ __global__ void __launch_bounds__(kAppend ? kThreadsAppend : kThreads, 1)
                     prm.part_lse[(long)e.slot * prm.rows + row] = e.lse2;
                 }
             }
-            if (!e.complete) {
-                // Publish the partial: once every softmax warp has arrived
+            if (!e.complete && tid == 0) prm.part_bad[e.slot] = e.bad ? 1 : 0;
+            if (M == 128 && !e.complete) {
+                // M = 128 publishes the partial: once every softmax warp has arrived
                 // after its stores of it (the arrival releases them at CTA
                 // scope), thread 0 writes this call's ticket into the slot's
                 // ready word with a GPU-scope release, which carries those
                 // stores with it; the merge kernel may read the slot once it
-                // acquires the word.  Only thread 0 waits, and boundedly.
-                if (tid == 0) prm.part_bad[e.slot] = e.bad ? 1 : 0;
+                // acquires the word.  Only thread 0 waits, and boundedly.  (M =
+                // 64 stores its partials with TMA tile stores, and its merge
+                // waits for the whole attention grid.)
                 __syncwarp();
                 if (lane == 0) mbar_arrive(bar(C::PB));
                 if (tid == 0) {
@@ -1202,17 +1208,20 @@ __global__ void __launch_bounds__(kMergeThreads, 4) attn_merge_kernel(const Para
     const int b = blockIdx.x, S = gridDim.x;
     schedule<kMergeThreads>(prm, b, S, &sch);
     const long W = sch.W, Wc = sch.Wc, x0 = sch.x0;
-    // Every CTA ends with griddepcontrol.wait, so that this grid completes
-    // after the attention grid and a kernel that waits on it sees every row.
+    // This grid must complete after the attention grid, so that a kernel that
+    // waits on it sees every row: with published partials every CTA ends with
+    // griddepcontrol.wait; otherwise the merging CTAs wait before they start,
+    // and CTA 0 waits even when it has nothing to merge.
+    const bool hold = prm.early_merge || b == 0;
     if (x0 >= W) {
-        grid_dependency_wait();
+        if (hold) grid_dependency_wait();
         return;
     }
     const long u_off = sch.u_off0, cu = sch.cu0;
     // the cut at this CTA's start splits the unit's tiles, and CTA b - 1 holds
     // the unit's first tile (so this is the unit's first cut)
     if (!(u_off < x0 && range_start(b - 1, Wc, S, prm.magic_S) <= cu + kUnitCost)) {
-        grid_dependency_wait();
+        if (hold) grid_dependency_wait();
         return;
     }
     const int r = sch.r0, h = sch.h0;
@@ -1238,7 +1247,9 @@ __global__ void __launch_bounds__(kMergeThreads, 4) attn_merge_kernel(const Para
     // passed its launch_dependents), so the words do get written; the wait is
     // still bounded, and past the limit the merge waits for the whole
     // attention grid instead, by when every slot is final.
-    if (threadIdx.x == 0) {
+    if (!prm.early_merge) {
+        grid_dependency_wait();  // the attention grid's partials
+    } else if (threadIdx.x == 0) {
         const uint64_t t0 = global_timer_ns();
         bool late = false;
         for (int bb = b_first; bb <= b_last && !late; ++bb) {
@@ -1320,7 +1331,7 @@ __global__ void __launch_bounds__(kMergeThreads, 4) attn_merge_kernel(const Para
         }
         if (sub == 0 && prm.lse) prm.lse[orow] = ok ? (mmax + log2f(den)) * kLn2 : -INFINITY;
     }
-    grid_dependency_wait();
+    if (prm.early_merge) grid_dependency_wait();
 }
 
 // ------------------------------------------------------------------ host side
@@ -1417,7 +1428,7 @@ int launch_impl(const AttnArgs &a, const AttnPlan &plan, cudaStream_t stream) {
             return BDSA_CUDA_ERROR;
     }
     char *ws = static_cast<char *>(a.workspace);
-    CUtensorMap tout;
+    CUtensorMap tout, tpart;
     {
         // out has q's layout; the epilogue stores a whole unit's rows per box.
         cuuint64_t dims[4] = {(cuuint64_t)D, (cuuint64_t)G, (cuuint64_t)a.Hkv,
@@ -1432,12 +1443,25 @@ int launch_impl(const AttnArgs &a, const AttnPlan &plan, cudaStream_t stream) {
             CUDA_SUCCESS)
             return BDSA_CUDA_ERROR;
     }
+    {
+        // partial slots [2 * grid * rows, D] fp32, stored 32 columns x rows per box.
+        cuuint64_t dims[2] = {(cuuint64_t)D, (cuuint64_t)2 * plan.grid * plan.rows};
+        cuuint64_t strides[1] = {(cuuint64_t)D * 4};
+        cuuint32_t box[2] = {32, (cuuint32_t)plan.rows};
+        cuuint32_t es[2] = {1, 1};
+        if (enc(&tpart, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2, ws + plan.off_part_o, dims, strides,
+                box, es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) !=
+            CUDA_SUCCESS)
+            return BDSA_CUDA_ERROR;
+    }
     Params prm;
     prm.block_table = a.block_table;
     prm.seq_lens = a.seq_lens;
     prm.part_bad = reinterpret_cast<int32_t *>(ws + plan.off_part_bad);
     prm.part_ready = reinterpret_cast<uint64_t *>(ws + plan.off_part_ready);
     prm.ticket = next_ticket();
+    prm.early_merge = M == 128;
     prm.out = a.out;
     prm.out_v8 = (reinterpret_cast<uintptr_t>(a.out) & 31) == 0;
     prm.lse = a.lse;
@@ -1480,7 +1504,7 @@ int launch_impl(const AttnArgs &a, const AttnPlan &plan, cudaStream_t stream) {
         attr_set[inst] = true;
     }
     if (launch_pdl(kernel, dim3(plan.grid), dim3(append ? kThreadsAppend : kThreads), C::kSmem,
-                   stream, tq, tk, tv, tout, prm, app) != cudaSuccess)
+                   stream, tq, tk, tv, tout, tpart, prm, app) != cudaSuccess)
         return BDSA_CUDA_ERROR;
     if (launch_pdl(attn_merge_kernel<D>, dim3(plan.grid), dim3(kMergeThreads), 0, stream,
                    prm) != cudaSuccess)
