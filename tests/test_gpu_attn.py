@@ -230,3 +230,33 @@ def test_output_16_byte_aligned_only(dev, sms):
     torch.cuda.synchronize()
     assert status.item() == 0
     assert torch.equal(out.view(torch.int16), ref.view(torch.int16))
+
+
+def test_split_partials_reuse_a_dirty_workspace(dev):
+    """The 128-row tile publishes its split-KV partials through ready words in
+    the workspace: calls that reuse one workspace (left by an earlier call, or
+    filled with arbitrary bytes) on different inputs each match the oracle."""
+    import block_diffusion_speculative_attn_gb300 as bdsa
+    name, Hq, Hkv, D, B, ps, lens = SHAPES[2]  # 128 rows a tile
+    ws_bytes = 0
+    cases = []
+    for seed in (5, 6):
+        cfg = _cfg(name, len(lens), Hq, Hkv, D, B, ps, lens, seed=seed)
+        inp = wl.make_attn_inputs(cfg, extra_pages=2)
+        cases.append((cfg, inp, DevAttn(inp)))
+        ws_bytes = max(ws_bytes, bdsa.block_attn_workspace_bytes(
+            cfg.bs, cfg.B, cfg.Hq, cfg.Hkv, cfg.D, inp.max_ctx_len, FORCE_SPLIT))
+    ws = torch.randint(0, 256, (ws_bytes,), dtype=torch.uint8, device=dev)
+    for rep in range(2):
+        for cfg, inp, d in cases:
+            status = torch.zeros(1, dtype=torch.int32, device=dev)
+            lse = torch.empty((d.q.shape[0], cfg.Hq), dtype=torch.float32, device=dev)
+            out = bdsa.block_attn_paged(d.q, d.k, d.v, d.bt, d.sl, B=cfg.B,
+                                        page_size=cfg.page_size, scale=inp.scale, mode=VERIFY,
+                                        max_ctx_len=inp.max_ctx_len, num_pages=inp.num_pages,
+                                        lse=lse, workspace=ws, dev_status=status,
+                                        sms=FORCE_SPLIT)
+            torch.cuda.synchronize()
+            assert status.item() == 0
+            ref, ref_lse = oracle_attn_full(inp, VERIFY)
+            assert_attn_close(out, ref, lse, ref_lse, tag=f"reuse {rep} seed {cfg.seed}")
