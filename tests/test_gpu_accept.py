@@ -214,3 +214,33 @@ def test_bad_draft_id_sets_status():
     torch.cuda.synchronize()
     assert status.item() == 16
     assert got["accept_len"][2].item() <= 2
+
+
+@pytest.mark.parametrize("greedy", [False, True])
+def test_cuda_graph_capture_and_replay(greedy):
+    """The acceptance launch (clusters above the portable 8 CTAs at this shape)
+    can be captured in a CUDA graph; replays give the eager call's outputs."""
+    cfg = wl.config("qwen3_8b_verify")
+    acc = wl.make_accept_inputs(cfg, device="cuda")
+    q = None if greedy else acc.q
+    want = bdsa.spec_accept(acc.block_ids, acc.p, q, acc.u_acc, acc.u_samp, acc.seq_lens)
+    torch.cuda.synchronize()
+    out = {k: torch.full_like(v, -7) for k, v in want.items()}
+    s = torch.cuda.Stream()
+    s.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(s):  # warm-up on the capture stream
+        bdsa.spec_accept(acc.block_ids, acc.p, q, acc.u_acc, acc.u_samp, acc.seq_lens, out=out)
+    torch.cuda.current_stream().wait_stream(s)
+    torch.cuda.synchronize()
+    for v in out.values():
+        v.fill_(-7)
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        bdsa.spec_accept(acc.block_ids, acc.p, q, acc.u_acc, acc.u_samp, acc.seq_lens, out=out)
+    for _ in range(2):
+        for v in out.values():
+            v.fill_(-7)
+        g.replay()
+        torch.cuda.synchronize()
+        for k in want:
+            assert torch.equal(out[k], want[k]), k
