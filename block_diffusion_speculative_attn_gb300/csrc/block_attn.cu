@@ -1461,7 +1461,11 @@ int launch_impl(const AttnArgs &a, const AttnPlan &plan, cudaStream_t stream) {
     prm.part_bad = reinterpret_cast<int32_t *>(ws + plan.off_part_bad);
     prm.part_ready = reinterpret_cast<uint64_t *>(ws + plan.off_part_ready);
     prm.ticket = next_ticket();
-    prm.early_merge = M == 128;
+    // A CUDA graph would replay this call's ticket, so while the stream is
+    // being captured the merge waits for the whole attention grid instead.
+    cudaStreamCaptureStatus cap = cudaStreamCaptureStatusNone;
+    if (cudaStreamIsCapturing(stream, &cap) != cudaSuccess) return BDSA_CUDA_ERROR;
+    prm.early_merge = M == 128 && cap == cudaStreamCaptureStatusNone;
     prm.out = a.out;
     prm.out_v8 = (reinterpret_cast<uintptr_t>(a.out) & 31) == 0;
     prm.lse = a.lse;

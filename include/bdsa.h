@@ -135,8 +135,8 @@ int32_t bdsa_prepare_block(const int32_t *verified_id, const int32_t *seq_lens,
  * memory, 256-byte aligned: two partial slots per CTA (a flag, a 64-bit ready
  * word and G*B*(D+1) fp32 values).  Its contents need no initialisation and
  * are not meaningful after the call (each call stamps the slots it writes with
- * a ticket of its own); calls that share one workspace must be ordered on the
- * same stream.
+ * a ticket of its own; a call captured into a CUDA graph does not rely on
+ * them); calls that share one workspace must be ordered on the same stream.
  */
 size_t bdsa_block_attn_workspace_bytes(int32_t bs, int32_t B, int32_t Hq, int32_t Hkv, int32_t D,
                                        int32_t max_ctx_len, int32_t num_sms);

@@ -260,3 +260,49 @@ def test_split_partials_reuse_a_dirty_workspace(dev):
             assert status.item() == 0
             ref, ref_lse = oracle_attn_full(inp, VERIFY)
             assert_attn_close(out, ref, lse, ref_lse, tag=f"reuse {rep} seed {cfg.seed}")
+
+
+def test_cuda_graph_replays_with_new_inputs(dev):
+    """The attention call captured into a CUDA graph (128-row tile, every unit
+    split, so partials and the merge are exercised) replays correctly when new
+    inputs are copied into the captured buffers between replays."""
+    import block_diffusion_speculative_attn_gb300 as bdsa
+    name, Hq, Hkv, D, B, ps, lens = SHAPES[2]
+    inps = [wl.make_attn_inputs(_cfg(name, len(lens), Hq, Hkv, D, B, ps, lens, seed=s),
+                                extra_pages=2) for s in (11, 12, 13)]
+    cfg = inps[0].cfg
+    d = DevAttn(inps[0])
+    q, k, v = d.q.clone(), d.k.clone(), d.v.clone()
+    out = torch.empty_like(q)
+    lse = torch.empty((q.shape[0], cfg.Hq), dtype=torch.float32, device=dev)
+    ws = torch.empty(bdsa.block_attn_workspace_bytes(cfg.bs, cfg.B, cfg.Hq, cfg.Hkv, cfg.D,
+                                                     inps[0].max_ctx_len, FORCE_SPLIT),
+                     dtype=torch.uint8, device=dev)
+
+    def call():
+        bdsa.block_attn_paged(q, k, v, d.bt, d.sl, B=cfg.B, page_size=cfg.page_size,
+                              scale=inps[0].scale, mode=VERIFY, max_ctx_len=inps[0].max_ctx_len,
+                              num_pages=inps[0].num_pages, out=out, lse=lse, workspace=ws,
+                              sms=FORCE_SPLIT)
+
+    s = torch.cuda.Stream()
+    s.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(s):
+        call()
+    torch.cuda.current_stream().wait_stream(s)
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        call()
+    base = inps[0]
+    for other in inps[1:] + inps[:1]:
+        # the captured seq_lens and block table with another seed's q, k, v
+        inp = wl.AttnInputs(base.cfg, base.seq_lens, base.block_table, base.num_pages,
+                            other.q, other.k_cache, other.v_cache, base.scale)
+        q.copy_(inp.q)
+        k.copy_(inp.k_cache)
+        v.copy_(inp.v_cache)
+        g.replay()
+        torch.cuda.synchronize()
+        ref, ref_lse = oracle_attn_full(inp, VERIFY)
+        assert_attn_close(out, ref, lse, ref_lse, tag=f"graph replay seed {other.cfg.seed}")
