@@ -44,8 +44,8 @@ METRIC = "draft/verify block-attn query tokens/s + % HBM roofline; accept rows/s
 # in profiles/qwen3_8b_verify_step_ncu.md): attention 308.41 + 4.63 MB, merge
 # 8.79 MB (cold under ncu; L2 hits in the timed step).  Valid only for the
 # kernel sources it was taken on: reported as null once they change.
-ATTN_TRAFFIC = {"workload": "qwen3_8b_verify", "bytes_per_call": 321.81e6,
-                "sources_sha256": "13790881168326d4f74ca17cd8df0d238d491026f1ef8f8dcb5a4137eb94a047"}
+ATTN_TRAFFIC = {"workload": "qwen3_8b_verify", "bytes_per_call": 321.79e6,
+                "sources_sha256": "ca382c9131e6d440e6e8801b1f40976f34b4fa141ba4de38e1fb533501486dcc"}
 ATTN_SOURCES = ("block_diffusion_speculative_attn_gb300/csrc/block_attn.cu",
                 "block_diffusion_speculative_attn_gb300/csrc/bdsa_device.cuh")
 L2_FLUSH_BYTES = 512 << 20  # > 129 MB L2
