@@ -215,9 +215,12 @@ int32_t bdsa_block_attn_paged_append(const bdsa_bf16 *q, const bdsa_bf16 *k_new,
  * Greedy mode (q == NULL): a = number of leading i with d_i == argmax p[r,i-1]
  *   (lowest index on ties); token = argmax p[r,a].  u_acc / u_samp are unused.
  * InvCDF(w, u) = smallest k with C_k > u*S, C_k the cumulative weight in index
- *   order, S the total; cumulative sums are accumulated without fp32 rounding
- *   loss and kept in fp64 (within ~1e-13*S of the exact sums), so the draw is
- *   the exact-arithmetic one unless u*S lies within that distance of a boundary.
+ *   order, S the total.  The kernel adds the fp32 weights with error-free
+ *   transformations (TwoSum) and carries the running sums and S as
+ *   float-float pairs (hi + lo, about 48 significant bits, all in fp32
+ *   arithmetic); u*S is formed and compared as a float-float product too.  The
+ *   sums are within ~1e-12*S of the exact ones, so the draw is the
+ *   exact-arithmetic one unless u*S lies within that distance of a boundary.
  * Outputs: accept_len[r] = a, commit_len[r] = a+1,
  *   out_tokens[r] = [d_1..d_a, token, -1...] ([bs, B]), bonus_id[r] = token,
  *   new_seq_lens[r] = seq_lens[r] + a + 1.
@@ -248,22 +251,25 @@ int32_t bdsa_spec_accept(const int32_t *block_ids, const float *p, int64_t p_str
  *
  * The acceptance step of bdsa_spec_accept (same inputs, outputs, rules and
  * results) for callers that cannot give this library device memory for
- * scratch: a serving loop whose memory is planned once at start-up, code that
- * runs while a CUDA graph is being captured (allocation is not allowed there),
- * or a framework that owns the allocator and passes only the step's tensors.
- * Instead of a workspace it uses a fixed 8 MiB array in the library's device
- * image (present on every GPU that loads the library, until the process exits).
+ * scratch: a serving loop whose device memory is planned once at start-up and
+ * may not grow afterwards, or a framework that owns the device allocator and
+ * passes only the step's own tensors.  Instead of a workspace it uses a fixed
+ * 8 MiB array in the library's device image (present on every GPU that loads
+ * the library, and held there until the process exits).
  *   - Nothing is allocated: no cudaMalloc / cudaFree or allocating call.
- *   - The first call on each device looks up the array's device address
- *     (cudaGetSymbolAddress) with that device current; make that first call
- *     before any stream capture.
- *   - All calls on a device share the array.  Calls whose kernels may overlap
- *     on the GPU (unordered streams) race on it; order them on one stream.
- *     Problems with V <= 2^21 need no scratch and do not touch the array.
- *     Above that, each call clears the per-row counters it needs at zero (an
- *     asynchronous memset on `stream`); the rest of the array keeps the last
- *     call's values.
- *   - Returns BDSA_WORKSPACE_TOO_SMALL, launching nothing, when the problem
+ *   - Set-up: the first call on each device looks up the array's device
+ *     address (cudaGetSymbolAddress, with that device current) and keeps it
+ *     for the life of the process; make that first call before any stream
+ *     capture.  A cudaDeviceReset later in the process is not supported.
+ *   - All calls on a device share the array, and it keeps the last call's
+ *     contents.  Calls whose kernels may overlap on the GPU (unordered
+ *     streams) race on it; order them on one stream.  Problems with
+ *     V <= 2^21 need no scratch: their kernels do not read or write the
+ *     array.  Above that, each call clears the per-row counters it needs to
+ *     zero (an asynchronous memset on `stream`) before its kernel runs; every
+ *     other value it reads there is written earlier by the same call.
+ *   - Argument errors are reported exactly as by bdsa_spec_accept.  Then it
+ *     returns BDSA_WORKSPACE_TOO_SMALL, launching nothing, when the problem
  *     needs more than 8 MiB of scratch, i.e. when
  *     bdsa_spec_accept_workspace_bytes(bs, B, V, num_sms) > 8 MiB (for
  *     example 128 rows at V = 2^22).

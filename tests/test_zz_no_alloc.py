@@ -1,19 +1,31 @@
 """bdsa_spec_accept_noalloc: the acceptance step for callers that cannot give
-the library device memory for scratch (a memory plan fixed at start-up, a CUDA
-graph capture in progress, a framework that owns the allocator).  It uses a
-fixed scratch array inside the library and must give exactly the results of
-bdsa_spec_accept.  This file is collected last on purpose: if it fails, a run
-that stops at the first failure has already run every other test."""
-import ctypes
+the library device memory for scratch -- a serving loop whose device memory is
+planned once at start-up and may not grow, or a framework that owns the device
+allocator and hands the library only the step's own tensors.  It keeps its
+scratch in a fixed array inside the library and must give exactly the results
+of bdsa_spec_accept (with a workspace) and of the oracle.
 
+Vocabularies above 2^21 are the ones that use that array: the scratch tests
+run at V = 2^21 + 1000 and make two calls in a row on different inputs and
+batch sizes, so that the second call starts from the first call's leftovers.
+
+This file is collected last on purpose: if it fails, a run that stops at the
+first failure has already run every other test."""
+import ctypes
+import os
+
+import numpy as np
 import pytest
 import torch
 
 import block_diffusion_speculative_attn_gb300 as bdsa
+import oracle
 from block_diffusion_speculative_attn_gb300 import workloads as wl
 
 pytestmark = pytest.mark.gpu
 KEYS = ("accept_len", "commit_len", "out_tokens", "bonus_id", "new_seq_lens")
+SCRATCH_BYTES = 8 << 20  # the fixed array's size, as declared in include/bdsa.h
+V_SCRATCH = (1 << 21) + 1000  # just past the vocabularies that need no scratch
 
 
 def _ptr(t):
@@ -21,7 +33,8 @@ def _ptr(t):
 
 
 def _noalloc(acc: wl.AcceptInputs, greedy: bool):
-    """Call the entry point through the C ABI with outputs allocated here."""
+    """Call the entry point through the C ABI; outputs are pre-filled with -7
+    so that anything left unwritten shows."""
     L = bdsa.lib()
     bs, B = acc.block_ids.shape
     V = acc.p.shape[-1]
@@ -39,10 +52,72 @@ def _noalloc(acc: wl.AcceptInputs, greedy: bool):
     return st, out, status
 
 
+def _with_workspace(acc: wl.AcceptInputs, greedy: bool):
+    bs, B = acc.block_ids.shape
+    ws_bytes = bdsa.spec_accept_workspace_bytes(bs, B, acc.p.shape[-1])
+    ws = torch.empty(max(ws_bytes, 256), dtype=torch.uint8, device="cuda")
+    return bdsa.spec_accept(acc.block_ids, acc.p, None if greedy else acc.q, acc.u_acc,
+                            acc.u_samp, acc.seq_lens, workspace=ws)
+
+
+def _wide_vocab_inputs(bs: int, B: int, V: int, seed: int) -> wl.AcceptInputs:
+    """Peaked p (u^8, normalised), q = p with +-50% noise, drafts drawn from q."""
+    rng = np.random.default_rng(seed)
+    p = rng.random((bs, B, V), dtype=np.float32) ** 8
+    p /= p.sum(-1, keepdims=True)
+    q = p[:, :B - 1] * rng.uniform(0.5, 1.5, (bs, B - 1, V)).astype(np.float32)
+    q /= q.sum(-1, keepdims=True)
+    ids = np.empty((bs, B), np.int32)
+    ids[:, 0] = rng.integers(0, V, bs)
+    for i in range(1, B):
+        c = np.cumsum(q[:, i - 1].astype(np.float64), -1)
+        u = rng.random(bs)[:, None] * c[:, -1:]
+        ids[:, i] = np.minimum((c <= u).sum(-1), V - 1)
+    return wl.AcceptInputs(torch.from_numpy(ids), torch.from_numpy(p), torch.from_numpy(q),
+                           torch.from_numpy(rng.random((bs, B - 1), dtype=np.float32)),
+                           torch.from_numpy(rng.random(bs, dtype=np.float32)),
+                           torch.from_numpy(rng.integers(0, 1000, bs).astype(np.int32)))
+
+
+def _to(acc: wl.AcceptInputs, dev) -> wl.AcceptInputs:
+    return wl.AcceptInputs(*(t.to(dev) for t in (acc.block_ids, acc.p, acc.q, acc.u_acc,
+                                                   acc.u_samp, acc.seq_lens)))
+
+
 @pytest.mark.parametrize("greedy", [False, True])
-def test_matches_workspace_entry_point_on_two_calls(greedy):
+def test_fixed_scratch_two_calls_in_a_row(greedy):
+    """Two calls in a row through the fixed array (bs 3, then bs 4 on other
+    inputs): each equals the workspace entry point and the oracle bit for bit."""
+    B = 4
+    for bs, seed in ((3, 101), (4, 202)):
+        need = bdsa.spec_accept_workspace_bytes(bs, B, V_SCRATCH)
+        assert 0 < need <= SCRATCH_BYTES  # this problem does go through the array
+        host = _wide_vocab_inputs(bs, B, V_SCRATCH, seed)
+        acc = _to(host, "cuda")
+        st, got, status = _noalloc(acc, greedy)
+        assert st == 0, bdsa.STATUS.get(st, st)
+        want = _with_workspace(acc, greedy)
+        torch.cuda.synchronize()
+        assert status.item() == 0
+        for k in KEYS:
+            assert torch.equal(got[k], want[k]), (k, bs)
+        ref = oracle.spec_accept(host.block_ids.numpy(), host.p.numpy(),
+                                 None if greedy else host.q.numpy(), host.u_acc.numpy(),
+                                 host.u_samp.numpy(), host.seq_lens.numpy(),
+                                 nthreads=os.cpu_count() or 1)
+        # no draw within the summation-order band of a boundary (flag bit 2);
+        # greedy ties (bit 16) are settled by the lowest index on both sides
+        assert ((ref["flags"] & 2) == 0).all()
+        for k in KEYS:
+            assert (got[k].cpu().numpy() == ref[k]).all(), (k, bs)
+
+
+@pytest.mark.parametrize("greedy", [False, True])
+def test_no_scratch_needed_two_calls_in_a_row(greedy):
+    """At the Qwen3-8B vocabulary (151936 <= 2^21) nothing uses the array; two
+    calls in a row still equal the workspace entry point."""
     cfg = wl.config("qwen3_8b_verify")
-    for seed in (11, 12):  # two calls in a row, different inputs
+    for seed in (11, 12):
         acc = wl.make_accept_inputs(cfg, device="cuda", seed=seed)
         st, got, status = _noalloc(acc, greedy)
         assert st == 0, bdsa.STATUS.get(st, st)
@@ -67,15 +142,25 @@ def test_small_vocab_and_batch_reuse():
             assert torch.equal(got[k], want[k]), k
 
 
-def test_rejects_problems_larger_than_the_fixed_scratch():
+def _raw(bs, B, V, ptr):
     L = bdsa.lib()
-    # vocabularies above 2^21 keep their segment totals in global scratch:
-    # 128 rows of 2^22 needs ~17 MB, the array holds 8 MiB
+    return L.bdsa_spec_accept_noalloc(ptr, ptr, 0, 0, ptr, 0, 0, ptr, ptr, ptr, bs, B, V, ptr,
+                                      ptr, ptr, ptr, ptr, 0, None, None)
+
+
+def test_rejects_problems_larger_than_the_fixed_scratch():
+    # 128 rows of 2^22 need ~17 MB of scratch; the array holds 8 MiB
     bs, B, V = 128, 16, 1 << 22
-    assert L.bdsa_spec_accept_workspace_bytes(bs, B, V, 0) > (8 << 20)
+    assert bdsa.lib().bdsa_spec_accept_workspace_bytes(bs, B, V, 0) > SCRATCH_BYTES
     dummy = torch.zeros(16, dtype=torch.int32, device="cuda")
-    st = L.bdsa_spec_accept_noalloc(_ptr(dummy), _ptr(dummy), 0, 0, _ptr(dummy), 0, 0,
-                                    _ptr(dummy), _ptr(dummy), _ptr(dummy), bs, B, V, _ptr(dummy),
-                                    _ptr(dummy), _ptr(dummy), _ptr(dummy), _ptr(dummy), 0, None,
-                                    None)
-    assert st == 4  # BDSA_WORKSPACE_TOO_SMALL, nothing launched
+    assert _raw(bs, B, V, _ptr(dummy)) == 4  # BDSA_WORKSPACE_TOO_SMALL, nothing launched
+
+
+def test_argument_errors_match_the_workspace_entry_point():
+    # the argument checks come before the size check: B > 64 is UNSUPPORTED and
+    # a null pointer INVALID_ARG, even for a problem too large for the array
+    dummy = torch.zeros(16, dtype=torch.int32, device="cuda")
+    assert _raw(128, 65, 1 << 22, _ptr(dummy)) == 2
+    assert _raw(128, 16, 1 << 22, None) == 1
+    assert _raw(-1, 4, 1000, _ptr(dummy)) == 1
+    assert _raw(0, 4, 1000, _ptr(dummy)) == 0
