@@ -63,6 +63,8 @@ def parse_args(argv=None):
                     help="target CPU time of the oracle baseline sample")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-workloads", action="store_true",
+                    help="skip the other workloads' attention and acceptance timings")
     return ap.parse_args(argv)
 
 
@@ -85,6 +87,36 @@ def accept_bytes(cfg: wl.StepConfig) -> int:
     """One full row of p and q at the resolved position per request (upper bound
     of the algorithmic bytes: a fully accepted row reads p alone)."""
     return cfg.bs * 2 * cfg.V * 4 if cfg.V else 0
+
+
+def accept_bytes_exact(cfg: wl.StepConfig, accept_len: np.ndarray, greedy: bool = False) -> int:
+    """Algorithmic bytes of one acceptance call from its outcome.  Per row:
+    the block ids, uniforms and length read and the outputs written; the (p, q)
+    pairs it tests (the accepted drafts and the first rejected one); then the
+    full rows the draw reads at the resolved position -- p and q for a residual
+    draw after a rejection, p alone for the bonus.  Greedy reads the B rows of
+    p it compares (up to the first mismatch) and the bonus row."""
+    B, V = cfg.B, cfg.V
+    total = 0
+    for a in np.asarray(accept_len).tolist():
+        total += 4 * (B + (B - 1) + 2) + 4 * (B + 4)
+        if greedy:
+            total += (a + 1) * V * 4
+            continue
+        total += 8 * min(a + 1, B - 1)
+        total += (2 if a < B - 1 else 1) * V * 4
+    return total
+
+
+def config_dict(cfg: wl.StepConfig, world: int) -> dict:
+    """The workload's description, identical on the GPU arm and the reference arm."""
+    return {"workload": cfg.name, "batch": cfg.bs, "B": cfg.B, "Hq": cfg.Hq, "Hkv": cfg.Hkv,
+            "D": cfg.D, "page_size": cfg.page_size,
+            "ctx": list(cfg.ctx[0]) if isinstance(cfg.ctx[0], tuple) else "fixed",
+            "modes": ["draft" if m == 0 else "verify" for m in cfg.modes], "vocab": cfg.V,
+            "l2": "GPU arm: flushed between steps (512 MB write, then 256 MB read); "
+                  "CPU reference arm: not applicable",
+            "parallelism": f"replicas x{world}"}
 
 
 def attn_traffic(workload: str):
@@ -592,6 +624,86 @@ def time_tree(cfg: wl.StepConfig, dev, flush, clean, n_nodes: int = 32, iters: i
             "iters": iters}
 
 
+OTHER_WORKLOADS = ("llada2_block_draft", "uno_1k8k_step", "long_ctx_verify")
+
+
+def time_workload(name: str, dev, flush, clean, iters: int = 10, cpu: bool = False):
+    """Another workload's step: every attention pass (DRAFT and / or VERIFY)
+    and the acceptance, each timed alone with CUDA events (L2 flushed before
+    every step), with its algorithmic bytes against the HBM peak; the step
+    itself is timed again without events between its kernels."""
+    cfg = wl.config(name)
+    st = Step(cfg, dev, seed=cfg.seed)
+    hbm, _, src = peaks()
+    mk = lambda: (torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))  # noqa: E731
+    for _ in range(3):
+        flush.zero_()
+        clean.sum()
+        st.run()
+    torch.cuda.synchronize()
+    assert st.status.item() == 0, st.bdsa.STATUS.get(st.status.item())
+    step_ev = []
+    for _ in range(iters):
+        flush.zero_()
+        clean.sum()
+        e = mk()
+        e[0].record()
+        st.run()
+        e[1].record()
+        step_ev.append(e)
+    stage_ev = []
+    for _ in range(iters):
+        flush.zero_()
+        clean.sum()
+        ev = {"attn": [mk() for _ in cfg.modes], "accept": mk()}
+        st.run(ev)
+        stage_ev.append(ev)
+    torch.cuda.synchronize()
+    step_ms = statistics.mean(a.elapsed_time(b) for a, b in step_ev)
+    abytes = attn_bytes(cfg, st.attn.seq_lens)
+    passes = []
+    for j, m in enumerate(cfg.modes):
+        ms = statistics.mean(e["attn"][j][0].elapsed_time(e["attn"][j][1]) for e in stage_ev)
+        ach = abytes / (ms / 1e3) / 1e9
+        passes.append({"mode": "draft" if m == wl.DRAFT else "verify", "launch_ms": ms,
+                       "query_tokens_per_s": cfg.bs * cfg.B / (ms / 1e3),
+                       "roofline": {"bound": "hbm", "achieved": ach, "peak": hbm, "unit": "GB/s",
+                                    "frac": ach / hbm, "peak_source": src,
+                                    "algorithmic_bytes_per_launch": abytes,
+                                    "flops_per_launch": attn_flops(cfg, st.attn.seq_lens, m)}})
+    acc = None
+    if cfg.V:
+        ms = statistics.mean(e["accept"][0].elapsed_time(e["accept"][1]) for e in stage_ev)
+        nb = accept_bytes_exact(cfg, st.acc_out["accept_len"].cpu().numpy())
+        ach = nb / (ms / 1e3) / 1e9
+        acc = {"launch_ms": ms, "rows_per_s": cfg.bs / (ms / 1e3),
+               "roofline": {"bound": "hbm", "achieved": ach, "peak": hbm, "unit": "GB/s",
+                            "frac": ach / hbm, "peak_source": src,
+                            "algorithmic_bytes_per_launch": nb}}
+    base = None
+    if cpu:
+        # the oracle's whole step on the first request, best of 3
+        cores = len(os.sched_getaffinity(0))
+        smp = oracle_sample(cfg, st.attn, st.acc, [0], cores)
+        times = []
+        for _ in range(3):
+            t0 = time.perf_counter()
+            oracle_step(cfg, smp, st.attn.scale, cores)
+            times.append(time.perf_counter() - t0)
+        best = min(times)
+        base = {"value": cfg.B * len(cfg.modes) / best, "unit": "query tokens/s",
+                "cores": cores, "kind": "oracle",
+                "sample": f"first 1 of {cfg.bs} requests of {cfg.name}, whole step, fp64 C "
+                          f"oracle, {cores} OpenMP threads, best of 3", "seconds": best}
+    out = {"config": config_dict(cfg, 1), "step_ms": step_ms,
+           "query_tokens_per_s": cfg.bs * cfg.B * len(cfg.modes) / (step_ms / 1e3),
+           "attention_passes": passes, "accept": acc, "cpu_baseline": base, "iters": iters,
+           "gpu_launches_per_step": st.launches}
+    del st
+    torch.cuda.empty_cache()
+    return out
+
+
 # ---------------------------------------------------------------------------
 def oracle_sample(cfg: wl.StepConfig, attn: wl.AttnInputs, acc, reqs, nthreads):
     """Host copies of the sampled requests' inputs (compact page pool)."""
@@ -632,7 +744,7 @@ def oracle_step(cfg: wl.StepConfig, s, scale, nthreads):
                            nthreads=nthreads)
 
 
-def cpu_baseline(cfg, attn, acc, target_s: float, reps: int = 1):
+def cpu_baseline(cfg, attn, acc, target_s: float, reps: int = 3):
     """Time the oracle on a bounded sample of the same workload on the host cores."""
     cores = len(os.sched_getaffinity(0))
     # grow the sample of requests until one oracle step takes a measurable time
@@ -718,12 +830,11 @@ def main_reference(args, world, rank):
             "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
             "ms_per_step": dt * 1e3, "higher_is_better": True, "scaling": "weak",
             "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-            "config": {"workload": cfg.name, "requests_per_step": len(reqs), "B": cfg.B,
-                       "Hq": cfg.Hq, "Hkv": cfg.Hkv, "D": cfg.D, "page_size": cfg.page_size,
-                       "vocab": cfg.V, "l2": "n/a (CPU)"},
+            "config": config_dict(cfg, world),
             "cpu_baseline": {"value": value, "unit": "query tokens/s", "cores": cores,
                              "kind": "oracle",
-                             "sample": f"first {len(reqs)} of {cfg.bs} requests per step"},
+                             "sample": f"first {len(reqs)} of {cfg.bs} requests per step",
+                             "requests_per_step": len(reqs)},
             "e2e": {"value": value, "unit": "query tokens/s", "h2d_bytes_per_step": 0,
                     "d2h_bytes_per_step": 0}}
     print(json.dumps(line), flush=True)
@@ -806,6 +917,15 @@ def main(argv=None):
                 "algorithmic_bytes_per_launch": abytes, "peak_source": peak_src,
                 "launch_ms": attn_ms}
 
+    acc_roof = None
+    if acc_ms:
+        nb = accept_bytes_exact(cfg, step.acc_out["accept_len"].cpu().numpy())
+        ach = nb / (acc_ms / 1e3) / 1e9
+        acc_roof = {"bound": "hbm", "achieved": ach, "peak": hbm, "unit": "GB/s",
+                    "frac": ach / hbm, "peak_source": peak_src,
+                    "kernel": "spec_accept (stochastic)", "algorithmic_bytes_per_launch": nb,
+                    "launch_ms": acc_ms}
+
     # the side lines run on single-pass workloads (the default one included)
     single = len(cfg.modes) == 1
     fused_append = None
@@ -817,6 +937,10 @@ def main(argv=None):
     idlm = time_idlm(cfg, dev, flush, clean, cpu=cpu_side) if side else None
     kvmat = time_kvmat(step, flush, clean, cpu=cpu_side) if side else None
     tree = time_tree(cfg, dev, flush, clean, cpu=cpu_side) if side else None
+    # the other workloads' attention passes (draft mode among them) and acceptance
+    others = None
+    if cfg.name == "qwen3_8b_verify" and not args.no_workloads:
+        others = {n: time_workload(n, dev, flush, clean, cpu=cpu_side) for n in OTHER_WORKLOADS}
 
     e2e = None
     if not args.no_e2e:
@@ -832,16 +956,13 @@ def main(argv=None):
     line = {"metric": METRIC, "value": value, "unit": "query tokens/s", "n_gpus": world,
             "steps": K, "warmup": args.warmup, "ms_per_step": ms_max, "higher_is_better": True,
             "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
-            "config": {"workload": cfg.name, "batch": cfg.bs, "B": cfg.B, "Hq": cfg.Hq,
-                       "Hkv": cfg.Hkv, "D": cfg.D, "page_size": cfg.page_size,
-                       "ctx": list(cfg.ctx[0]) if isinstance(cfg.ctx[0], tuple) else "fixed",
-                       "modes": ["draft" if m == 0 else "verify" for m in cfg.modes],
-                       "vocab": cfg.V, "l2": "flushed between steps (512 MB write, then 256 MB read)",
-                       "parallelism": f"replicas x{world}"},
+            "config": config_dict(cfg, world),
             "roofline": roof,
             "attn_query_tokens_per_s": (cfg.bs * cfg.B / (attn_ms / 1e3)) if attn_ms else None,
             "accept_rows_per_s": (cfg.bs / (acc_ms / 1e3)) if acc_ms else None,
             "accept_ms": acc_ms,
+            "accept_roofline": acc_roof,
+            "workloads": others,
             "fused_append": fused_append,
             "idlm_round": idlm,
             "kv_materialize": kvmat,

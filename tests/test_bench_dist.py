@@ -84,3 +84,23 @@ def test_reference_arm_under_torchrun_prints_on_rank0_only():
 
 if __name__ == "__main__":
     sys.exit(pytest.main([__file__, "-q"]))
+    # the same workload description as the GPU arm prints, so the two lines compare
+    sys.path.insert(0, ROOT)
+    import bench
+    from block_diffusion_speculative_attn_gb300 import workloads as wl
+    assert line["config"] == bench.config_dict(wl.config("tiny"), 2)
+
+
+def test_accept_bytes_count_the_rows_each_outcome_reads():
+    sys.path.insert(0, ROOT)
+    import bench
+    from block_diffusion_speculative_attn_gb300 import workloads as wl
+    cfg = wl.config("qwen3_8b_verify")
+    B, V = cfg.B, cfg.V
+    small = 4 * (B + (B - 1) + 2) + 4 * (B + 4)
+    # a rejection at slot 3 reads 4 pairs and the p and q rows there; a fully
+    # accepted row reads B - 1 pairs and the bonus row of p alone
+    assert bench.accept_bytes_exact(cfg, [3]) == small + 8 * 4 + 2 * V * 4
+    assert bench.accept_bytes_exact(cfg, [B - 1]) == small + 8 * (B - 1) + V * 4
+    assert bench.accept_bytes_exact(cfg, [0, B - 1]) == (bench.accept_bytes_exact(cfg, [0]) +
+                                                         bench.accept_bytes_exact(cfg, [B - 1]))

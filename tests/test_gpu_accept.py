@@ -148,7 +148,10 @@ def test_full_size(name):
                               acc.u_samp[r_t].cpu().numpy(), acc.seq_lens[r_t].cpu().numpy(),
                               nthreads=os.cpu_count() or 1)
     sub = {k: v[r_t] for k, v in got.items()}
-    _compare(sub, want, max_flag_frac=0.05)
+    # at these vocabularies no draw falls within 1e-9*S of a boundary: every
+    # sampled row is compared
+    assert ((want["flags"] & 2) != 0).sum() == 0
+    _compare(sub, want, max_flag_frac=0.0)
     c = got["commit_len"].cpu().numpy()
     assert c.min() >= 1 and c.max() <= cfg.B
 
