@@ -10,7 +10,7 @@
 //   set (the node and its ancestors: the tree attention of the Psi-Spec Tree
 //   sampler, "Unlocking Lossless Speedups in LLMs via Discrete Diffusion").
 //
-// One call = two launches chained with programmatic dependent launch:
+// One call = one or two launches chained with programmatic dependent launch:
 //   attend  persistent, one CTA per SM.  Every (request, KV head) unit is a run
 //           of 128-key tiles; the runs are concatenated and each CTA takes an
 //           equal contiguous range (stream-K style), so the work is balanced to
@@ -21,11 +21,16 @@
 //           CTAs leaves an fp32 partial (o / l and log2-sum-exp) in one of each
 //           CTA's two slots.  The softmax warps check every page id a piece
 //           references; a unit that references one outside the pool is written
-//           as zeros (lse -inf) and reported;
-//   merge   one CTA per range boundary that is a unit's first cut: merges the
-//           unit's partials in tile order as soon as each is published (a
-//           ready word per partial slot carrying the call's ticket), while the
-//           attention grid finishes.
+//           as zeros (lse -inf) and reported.  With the 64-row tile (and a
+//           grid no larger than the device), a cut unit's pieces other than
+//           its first are each the first piece of a later CTA and are
+//           published early (a ready word carrying the call's ticket); the
+//           CTA holding the first piece -- its last piece -- merges them into
+//           its own before writing the unit's output, so no second launch;
+//   merge   otherwise (the 128-row tile, or a grid larger than the device):
+//           one CTA per range boundary that is a unit's first cut merges the
+//           unit's partials in tile order, as soon as each is published
+//           (128-row tile) or once the attention grid has finished.
 //
 // Inside a CTA (warp roles: 0-3 softmax + epilogue, 4 Q/K producer, 5 MMA
 // issuer + TMEM owner, 6 V producer):
@@ -118,7 +123,10 @@ struct Cfg {
     // every softmax warp has fenced its stores of a partial piece; one phase
     // per partial piece, waited by thread 0 alone before it publishes the slot
     static constexpr int PB = DR + 1;
-    static constexpr int kNumBars = PB + 1;
+    // owner merge (M = 64): every softmax warp has read the other pieces'
+    // ready words; waited by thread 0 alone before it resets them
+    static constexpr int MR = PB + 1;
+    static constexpr int kNumBars = MR + 1;
     static constexpr int kOffMisc = kOffBar + 8 * kNumBars;
     static constexpr int kOffMiscEnd = kOffMisc + 144;  // the schedule state (Sched)
     // + slack to align the base to 1 KB.  With D = 128 this is within a few
@@ -134,6 +142,7 @@ struct Params {
     uint64_t *part_ready;    // [2 * grid] the call's ticket once the slot is written
     uint64_t ticket;         // this call's ticket (unique a call, never 0)
     int early_merge;         // M = 128: partials are published, the merge starts on them
+    int owner_merge;         // M = 64: the CTA holding a cut unit's first tile merges it
     uint16_t *out;
     float *lse;
     const uint64_t *tree_mask;  // TREE mode: [bs * B] block keys visible to each block row
@@ -500,6 +509,7 @@ __global__ void __launch_bounds__(kAppend ? kThreadsAppend : kThreads, 1)
         mbar_init(bar(C::ER), 1);
         mbar_init(bar(C::DR), 1);
         mbar_init(bar(C::PB), kSoftmaxWarps);
+        mbar_init(bar(C::MR), kSoftmaxWarps);
         *abort_flag = 0;
         sch->appended = 0;
         fence_mbarrier_init();
@@ -754,24 +764,30 @@ __global__ void __launch_bounds__(kAppend ? kThreadsAppend : kThreads, 1)
         const bool valid_row = row < prm.rows;
         const int i_blk = row / G;
         // A piece's output: O from TMEM scaled by 1/l, to `out` (bf16) when the
-        // piece is the whole unit, else to the CTA's partial slot (fp32).
+        // piece is the whole unit (or, M = 64, the owner of a cut unit, which
+        // first merges the unit's other pieces into madd), else to the CTA's
+        // partial slot (fp32).
         struct Epi {
             long lastg, orow;
             float inv_l, lse2;
             int ob, slot, r, h, k;
-            bool complete, bad;
+            bool complete, owner, bad;
         };
+        // Owner merge (M = 64): the other pieces' share of this thread's output
+        // columns, added to O * inv_l by the epilogue (zero for other pieces).
+        float madd[OC];
         // M = 64: a piece's tile store reads the P buffers after the epilogue
         // returns; they are released before the next write to them.
         bool stage_busy = false;
-        int stage_k = 0;
-        int n_pub = 0;  // partial pieces published so far (phases of PB)
+        int n_stage = 0;  // pieces staged in the P buffers so far (phases of EW / ER)
+        int n_pub = 0;    // partial pieces published so far (phases of PB)
         auto release_stage = [&]() -> bool {
             if (tid == 0) {
                 bulk_wait_group_read0();
                 mbar_arrive(bar(C::ER));
             }
-            bool okr = mbar_wait(bar(C::ER), (uint32_t)(stage_k & 1), abort_flag, prm.dev_status);
+            bool okr = mbar_wait(bar(C::ER), (uint32_t)((n_stage - 1) & 1), abort_flag,
+                                 prm.dev_status);
             okr = __all_sync(0xffffffffu, okr);
             stage_busy = false;
             return okr;
@@ -783,7 +799,8 @@ __global__ void __launch_bounds__(kAppend ? kThreadsAppend : kThreads, 1)
             if (!okw) return false;
             tc_fence_after();
             const float sc = e.inv_l;
-            const bool zero = e.complete && e.bad;  // zeros, whatever O holds (it may be NaN)
+            const bool fin = e.complete || e.owner;  // this piece writes the unit's output
+            const bool zero = fin && e.bad;  // zeros, whatever O holds (it may be NaN)
             // This thread's output columns [half * OC, half * OC + OC), read from
             // TMEM 32 at a time.
             auto load_chunk = [&](int c, float (&v32)[32]) {
@@ -794,134 +811,158 @@ __global__ void __launch_bounds__(kAppend ? kThreadsAppend : kThreads, 1)
                     for (int q = 0; q < 32; ++q) v32[q] = 0.f;
                 }
             };
-            if constexpr (M == 64) {
-                // Stage the rows in the two P buffers (free: the piece's last two
-                // PVs are done and the next tile's P is not written before this
-                // returns), 128-byte rows swizzled like the tensor maps, then one
-                // thread stores them with TMA: bf16 to `out` for a whole unit,
-                // fp32 to the partial slot otherwise.
-                const uint32_t stage = sbase + C::kOffP;
+            // fp32 partial rows stored directly, 32 bytes a lane per instruction
+            // (whole sectors; the partial slots are 256-byte aligned).
+            auto store_partial_direct = [&]() {
 #pragma unroll
                 for (int c = 0; c < OC / 32; ++c) {
                     float v32[32];
                     load_chunk(c, v32);
                     if (!valid_row) continue;
                     const int col0 = half * OC + c * 32;
-                    if (e.complete) {
-                        // 32 bf16 = four 16-byte chunks of the 64-column slab
-                        const uint32_t rbase = stage + (col0 >> 6) * C::kSlab + row * 128;
-                        const int u0 = (col0 & 63) >> 3;
+                    float *dst = prm.part_o + ((long)e.slot * prm.rows + row) * D + col0;
 #pragma unroll
-                        for (int v = 0; v < 4; ++v)
-                            st_shared_v4(rbase + (((u0 + v) ^ (row & 7)) << 4),
-                                         pack_bf16x2(v32[8 * v + 0] * sc, v32[8 * v + 1] * sc),
-                                         pack_bf16x2(v32[8 * v + 2] * sc, v32[8 * v + 3] * sc),
-                                         pack_bf16x2(v32[8 * v + 4] * sc, v32[8 * v + 5] * sc),
-                                         pack_bf16x2(v32[8 * v + 6] * sc, v32[8 * v + 7] * sc));
-                    } else {
-                        // 32 fp32 = one 128-byte row of a 32-column box
-                        const uint32_t rbase = stage + (col0 >> 5) * C::kSlab + row * 128;
-#pragma unroll
-                        for (int v = 0; v < 8; ++v)
-                            st_shared_v4(rbase + ((v ^ (row & 7)) << 4),
-                                         __float_as_uint(v32[4 * v + 0] * sc),
-                                         __float_as_uint(v32[4 * v + 1] * sc),
-                                         __float_as_uint(v32[4 * v + 2] * sc),
-                                         __float_as_uint(v32[4 * v + 3] * sc));
-                    }
+                    for (int v = 0; v < 4; ++v)
+                        st_global_v8(dst + 8 * v, __float_as_uint(v32[8 * v] * sc),
+                                     __float_as_uint(v32[8 * v + 1] * sc),
+                                     __float_as_uint(v32[8 * v + 2] * sc),
+                                     __float_as_uint(v32[8 * v + 3] * sc),
+                                     __float_as_uint(v32[8 * v + 4] * sc),
+                                     __float_as_uint(v32[8 * v + 5] * sc),
+                                     __float_as_uint(v32[8 * v + 6] * sc),
+                                     __float_as_uint(v32[8 * v + 7] * sc));
                 }
-                // the O buffer may take the next unit but one as soon as it is read
                 tc_fence_before();
-                fence_proxy_async_smem();
                 __syncwarp();
-                if (lane == 0) {
-                    mbar_arrive(bar(C::OE + e.ob));
-                    mbar_arrive(bar(C::EW));
-                }
-                if (tid == 0) {
-                    const bool okw = mbar_wait(bar(C::EW), (uint32_t)(e.k & 1), abort_flag,
-                                               prm.dev_status);
-                    if (okw) {
-                        if (e.complete) {
-                            for (int sl = 0; sl < D / 64; ++sl)
-                                tma_store_4d(&tm_out, stage + sl * C::kSlab, sl * 64, 0, e.h,
-                                             e.r * B);
-                        } else {
-                            for (int bx = 0; bx < D / 32; ++bx)
-                                tma_store_2d(&tm_part, stage + bx * C::kSlab, bx * 32,
-                                             e.slot * prm.rows);
-                        }
-                        bulk_commit_group();
-                    }
-                }
-                // The staging area is released (ER) before the next P write,
-                // by when the store has long read it.
-                stage_busy = true;
-                stage_k = e.k;
-            } else {
-                // M = 128: one thread per row stores its row directly, 32 bytes
-                // a lane per instruction (whole sectors; the partial slots are
-                // 256-byte aligned, out when it is 32-byte aligned).
+                if (lane == 0) mbar_arrive(bar(C::OE + e.ob));
+            };
+            if constexpr (M == 64) {
+                if (fin || !prm.owner_merge) {
+                    // Stage the rows in the two P buffers (free: the piece's last
+                    // two PVs are done and the next tile's P is not written before
+                    // this returns), 128-byte rows swizzled like the tensor maps,
+                    // then one thread stores them with TMA: bf16 to `out` for a
+                    // unit's output, fp32 to the partial slot otherwise.
+                    const uint32_t stage = sbase + C::kOffP;
 #pragma unroll
-                for (int c = 0; c < OC / 32; ++c) {
-                    float v32[32];
-                    load_chunk(c, v32);
-                    if (!valid_row) continue;
-                    const int col0 = half * OC + c * 32;
-                    if (e.complete) {
-                        uint32_t w[16];
-#pragma unroll
-                        for (int v = 0; v < 16; ++v)
-                            w[v] = pack_bf16x2(v32[2 * v] * sc, v32[2 * v + 1] * sc);
-                        uint16_t *dst = prm.out + e.orow * D + col0;
-                        if (prm.out_v8) {
-                            st_global_v8(dst, w[0], w[1], w[2], w[3], w[4], w[5], w[6], w[7]);
-                            st_global_v8(dst + 16, w[8], w[9], w[10], w[11], w[12], w[13], w[14],
-                                         w[15]);
-                        } else {
-                            uint4 *d4 = reinterpret_cast<uint4 *>(dst);
+                    for (int c = 0; c < OC / 32; ++c) {
+                        float v32[32];
+                        load_chunk(c, v32);
+                        if (!valid_row) continue;
+                        const int col0 = half * OC + c * 32;
+                        if (fin) {
+                            // 32 bf16 = four 16-byte chunks of the 64-column slab
+                            const uint32_t rbase = stage + (col0 >> 6) * C::kSlab + row * 128;
+                            const int u0 = (col0 & 63) >> 3;
+                            const float *ad = madd + c * 32;
 #pragma unroll
                             for (int v = 0; v < 4; ++v)
-                                d4[v] = make_uint4(w[4 * v], w[4 * v + 1], w[4 * v + 2],
-                                                   w[4 * v + 3]);
+                                st_shared_v4(
+                                    rbase + (((u0 + v) ^ (row & 7)) << 4),
+                                    pack_bf16x2(fmaf(v32[8 * v + 0], sc, ad[8 * v + 0]),
+                                                fmaf(v32[8 * v + 1], sc, ad[8 * v + 1])),
+                                    pack_bf16x2(fmaf(v32[8 * v + 2], sc, ad[8 * v + 2]),
+                                                fmaf(v32[8 * v + 3], sc, ad[8 * v + 3])),
+                                    pack_bf16x2(fmaf(v32[8 * v + 4], sc, ad[8 * v + 4]),
+                                                fmaf(v32[8 * v + 5], sc, ad[8 * v + 5])),
+                                    pack_bf16x2(fmaf(v32[8 * v + 6], sc, ad[8 * v + 6]),
+                                                fmaf(v32[8 * v + 7], sc, ad[8 * v + 7])));
+                        } else {
+                            // 32 fp32 = one 128-byte row of a 32-column box
+                            const uint32_t rbase = stage + (col0 >> 5) * C::kSlab + row * 128;
+#pragma unroll
+                            for (int v = 0; v < 8; ++v)
+                                st_shared_v4(rbase + ((v ^ (row & 7)) << 4),
+                                             __float_as_uint(v32[4 * v + 0] * sc),
+                                             __float_as_uint(v32[4 * v + 1] * sc),
+                                             __float_as_uint(v32[4 * v + 2] * sc),
+                                             __float_as_uint(v32[4 * v + 3] * sc));
                         }
+                    }
+                    // the O buffer may take the next unit but one as soon as it is read
+                    tc_fence_before();
+                    fence_proxy_async_smem();
+                    __syncwarp();
+                    if (lane == 0) {
+                        mbar_arrive(bar(C::OE + e.ob));
+                        mbar_arrive(bar(C::EW));
+                    }
+                    if (tid == 0) {
+                        const bool okw2 = mbar_wait(bar(C::EW), (uint32_t)(n_stage & 1),
+                                                    abort_flag, prm.dev_status);
+                        if (okw2) {
+                            if (fin) {
+                                for (int sl = 0; sl < D / 64; ++sl)
+                                    tma_store_4d(&tm_out, stage + sl * C::kSlab, sl * 64, 0, e.h,
+                                                 e.r * B);
+                            } else {
+                                for (int bx = 0; bx < D / 32; ++bx)
+                                    tma_store_2d(&tm_part, stage + bx * C::kSlab, bx * 32,
+                                                 e.slot * prm.rows);
+                            }
+                            bulk_commit_group();
+                        }
+                    }
+                    // The staging area is released (ER) before the next P write,
+                    // by when the store has long read it.
+                    stage_busy = true;
+                    ++n_stage;
+                } else {
+                    // a piece the owner merges: published with direct stores below
+                    store_partial_direct();
+                }
+            } else if (e.complete) {
+                // M = 128: one thread per row stores its row directly, 32 bytes
+                // a lane per instruction (whole sectors; out when it is 32-byte
+                // aligned).
+#pragma unroll
+                for (int c = 0; c < OC / 32; ++c) {
+                    float v32[32];
+                    load_chunk(c, v32);
+                    if (!valid_row) continue;
+                    const int col0 = half * OC + c * 32;
+                    uint32_t w[16];
+#pragma unroll
+                    for (int v = 0; v < 16; ++v)
+                        w[v] = pack_bf16x2(v32[2 * v] * sc, v32[2 * v + 1] * sc);
+                    uint16_t *dst = prm.out + e.orow * D + col0;
+                    if (prm.out_v8) {
+                        st_global_v8(dst, w[0], w[1], w[2], w[3], w[4], w[5], w[6], w[7]);
+                        st_global_v8(dst + 16, w[8], w[9], w[10], w[11], w[12], w[13], w[14],
+                                     w[15]);
                     } else {
-                        float *dst = prm.part_o + ((long)e.slot * prm.rows + row) * D + col0;
+                        uint4 *d4 = reinterpret_cast<uint4 *>(dst);
 #pragma unroll
                         for (int v = 0; v < 4; ++v)
-                            st_global_v8(dst + 8 * v, __float_as_uint(v32[8 * v] * sc),
-                                         __float_as_uint(v32[8 * v + 1] * sc),
-                                         __float_as_uint(v32[8 * v + 2] * sc),
-                                         __float_as_uint(v32[8 * v + 3] * sc),
-                                         __float_as_uint(v32[8 * v + 4] * sc),
-                                         __float_as_uint(v32[8 * v + 5] * sc),
-                                         __float_as_uint(v32[8 * v + 6] * sc),
-                                         __float_as_uint(v32[8 * v + 7] * sc));
+                            d4[v] = make_uint4(w[4 * v], w[4 * v + 1], w[4 * v + 2], w[4 * v + 3]);
                     }
                 }
                 tc_fence_before();
                 __syncwarp();
                 if (lane == 0) mbar_arrive(bar(C::OE + e.ob));
+            } else {
+                store_partial_direct();
             }
             if (valid_row && half == 0) {
-                if (e.complete && e.bad) {
+                if (fin && e.bad) {
                     if (prm.lse) prm.lse[e.orow] = -INFINITY;
-                } else if (e.complete) {
+                } else if (fin) {
                     if (prm.lse) prm.lse[e.orow] = e.lse2 * kLn2;
                 } else {
                     prm.part_lse[(long)e.slot * prm.rows + row] = e.lse2;
                 }
             }
-            if (!e.complete && tid == 0) prm.part_bad[e.slot] = e.bad ? 1 : 0;
-            if (M == 128 && !e.complete) {
-                // M = 128 publishes the partial: once every softmax warp has arrived
-                // after its stores of it (the arrival releases them at CTA
-                // scope), thread 0 writes this call's ticket into the slot's
-                // ready word with a GPU-scope release, which carries those
-                // stores with it; the merge kernel may read the slot once it
-                // acquires the word.  Only thread 0 waits, and boundedly.  (M =
-                // 64 stores its partials with TMA tile stores, and its merge
-                // waits for the whole attention grid.)
+            if (!fin && tid == 0) prm.part_bad[e.slot] = e.bad ? 1 : 0;
+            if (!fin && (M == 128 || prm.owner_merge)) {
+                // Publish the partial: once every softmax warp has arrived after
+                // its stores of it (the arrival releases them at CTA scope),
+                // thread 0 writes this call's ticket into the slot's ready word
+                // with a GPU-scope release, which carries those stores with it;
+                // the merge kernel (M = 128) or the owner CTA (M = 64) may read
+                // the slot once it acquires the word.  Only thread 0 waits, and
+                // boundedly.  (Without the owner merge, M = 64 stores its
+                // partials with TMA tile stores, and its merge kernel waits for
+                // the whole attention grid.)
                 __syncwarp();
                 if (lane == 0) mbar_arrive(bar(C::PB));
                 if (tid == 0) {
@@ -931,6 +972,100 @@ __global__ void __launch_bounds__(kAppend ? kThreadsAppend : kThreads, 1)
                 ++n_pub;
             }
             return true;
+        };
+        // Owner merge (M = 64): before the epilogue of the piece holding a cut
+        // unit's first tile -- always the last piece of this CTA -- fold in
+        // the unit's other pieces.  Each is the first piece of a later CTA
+        // (slot 2 * bb), published with a ready word carrying this call's
+        // ticket; they are read in tile order as each word shows the ticket
+        // (a bounded wait), combined in the log2 domain with this piece's
+        // (m_used, l), and leave madd = the other pieces' share of the output
+        // and e.inv_l, e.lse2, e.bad for the whole unit.  The words read are
+        // then reset to 0, so a CUDA graph replaying this call's ticket never
+        // finds one already set.
+        int n_own = 0;  // units merged by this CTA as owner (phases of MR)
+        auto owner_gather = [&](Epi &e, const Piece &pc, float lr) -> bool {
+            const long long cu =
+                (long long)pc.u_off + (long long)kUnitCost * ((long long)pc.r * prm.Hkv + pc.h);
+            const long long last = cu + kUnitCost + pc.nt - 1;  // cost of the unit's last tile
+            const long long Wc = sch->Wc;
+            float m_run = e.lse2;
+            float s_own = m_run == -INFINITY ? 0.f : 1.f;
+            float den = s_own;
+            bool bad = e.bad, okg = true;
+#pragma unroll
+            for (int c = 0; c < OC; ++c) madd[c] = 0.f;
+            int bb = b + 1;
+            for (; okg && bb < S; ++bb) {
+                const long long cb = range_start(bb, Wc, S, prm.magic_S);
+                if (cb > last) break;
+                if (cb >= range_start(bb + 1, Wc, S, prm.magic_S)) continue;  // empty range
+                const int sl = 2 * bb;
+                if (!valid_row) continue;
+                const uint64_t *w = prm.part_ready + sl;
+                if (ld_acquire_gpu_u64(w) != prm.ticket) {
+                    const uint64_t t0 = global_timer_ns();
+                    while (ld_acquire_gpu_u64(w) != prm.ticket) {
+                        if (*abort_flag) {
+                            okg = false;
+                            break;
+                        }
+                        if (global_timer_ns() - t0 > kWaitLimitNs) {
+                            *abort_flag = 1;
+                            report_status(prm.dev_status, BDSA_DEVICE_TIMEOUT);
+                            okg = false;
+                            break;
+                        }
+                        __nanosleep(64);
+                    }
+                    if (!okg) break;
+                }
+                const float4 *src = reinterpret_cast<const float4 *>(
+                    prm.part_o + ((long)sl * prm.rows + row) * D + half * OC);
+                float4 po[OC / 4];
+#pragma unroll
+                for (int v = 0; v < OC / 4; ++v) po[v] = __ldcg(src + v);
+                const float ls = __ldcg(prm.part_lse + (long)sl * prm.rows + row);
+                bad = bad || __ldcg(prm.part_bad + sl) != 0;
+                if (ls == -INFINITY) continue;  // no key of that piece is visible to the row
+                const float m_new = fmaxf(m_run, ls);
+                const float a = m_run == -INFINITY ? 0.f : exp2f(m_run - m_new);
+                const float wj = exp2f(ls - m_new);
+                s_own *= a;
+                den = den * a + wj;
+#pragma unroll
+                for (int v = 0; v < OC / 4; ++v) {
+                    madd[4 * v + 0] = fmaf(madd[4 * v + 0], a, wj * po[v].x);
+                    madd[4 * v + 1] = fmaf(madd[4 * v + 1], a, wj * po[v].y);
+                    madd[4 * v + 2] = fmaf(madd[4 * v + 2], a, wj * po[v].z);
+                    madd[4 * v + 3] = fmaf(madd[4 * v + 3], a, wj * po[v].w);
+                }
+                m_run = m_new;
+            }
+            // every softmax warp has read the words (a bounded wait on MR, one
+            // phase per owned unit) before thread 0 resets them
+            __syncwarp();
+            if (lane == 0) mbar_arrive(bar(C::MR));
+            if (tid == 0 &&
+                mbar_wait(bar(C::MR), (uint32_t)(n_own & 1), abort_flag, prm.dev_status)) {
+                for (int q = b + 1; q < bb && q < S; ++q) {
+                    const long long cb = range_start(q, Wc, S, prm.magic_S);
+                    if (cb < range_start(q + 1, Wc, S, prm.magic_S))
+                        prm.part_ready[2 * q] = 0ull;
+                }
+            }
+            ++n_own;
+            okg = __all_sync(0xffffffffu, okg);
+            bad = __any_sync(0xffffffffu, bad);
+            const bool good = !bad && den > 0.f;
+            const float inv_den = good ? 1.f / den : 0.f;
+            // (a bad piece's partial may hold anything, NaN included)
+#pragma unroll
+            for (int c = 0; c < OC; ++c) madd[c] = good ? madd[c] * inv_den : 0.f;
+            e.inv_l = (good && lr > 0.f) ? s_own * inv_den / lr : 0.f;
+            e.lse2 = good ? m_run + log2f(den) : -INFINITY;
+            e.bad = bad;
+            return okg;
         };
         long g = 0;
         int k = 0;
@@ -1155,6 +1290,7 @@ __global__ void __launch_bounds__(kAppend ? kThreadsAppend : kThreads, 1)
                 e.inv_l = lr > 0.f ? 1.f / lr : 0.f;
                 e.lse2 = l > 0.f ? m_used + log2f(l) : -INFINITY;
                 e.complete = pc.a == 0 && pc.e == pc.nt;
+                e.owner = M == 64 && prm.owner_merge && pc.a == 0 && pc.e < pc.nt;
                 // every warp checked every page of the piece
                 e.bad = shape_bad || __any_sync(0xffffffffu, page_bad);
                 e.orow = ((long)pc.r * B + i_blk) * prm.Hq + (long)pc.h * G + row % G;
@@ -1163,6 +1299,15 @@ __global__ void __launch_bounds__(kAppend ? kThreadsAppend : kThreads, 1)
                 e.h = pc.h;
                 e.k = k;
                 if (e.bad && tid == 0) report_status(prm.dev_status, BDSA_DEVICE_OUT_OF_RANGE);
+                if constexpr (M == 64) {
+                    if (e.owner) {
+                        ok = owner_gather(e, pc, lr);
+                        if (!ok) break;
+                    } else {
+#pragma unroll
+                        for (int c = 0; c < OC; ++c) madd[c] = 0.f;
+                    }
+                }
                 ok = epilogue(e);
                 if (!ok) break;
             }
@@ -1466,6 +1611,11 @@ int launch_impl(const AttnArgs &a, const AttnPlan &plan, cudaStream_t stream) {
     cudaStreamCaptureStatus cap = cudaStreamCaptureStatusNone;
     if (cudaStreamIsCapturing(stream, &cap) != cudaSuccess) return BDSA_CUDA_ERROR;
     prm.early_merge = M == 128 && cap == cudaStreamCaptureStatusNone;
+    // M = 64: the owner of each cut unit merges it inside the attention launch.
+    // Its wait needs every CTA of the grid resident at once, so only a grid of
+    // at most one CTA per SM takes this path; a larger one (a caller's num_sms
+    // above the device's) keeps the separate merge launch.
+    prm.owner_merge = M == 64 && plan.grid <= device_num_sms(0);
     prm.out = a.out;
     prm.out_v8 = (reinterpret_cast<uintptr_t>(a.out) & 31) == 0;
     prm.lse = a.lse;
@@ -1510,6 +1660,7 @@ int launch_impl(const AttnArgs &a, const AttnPlan &plan, cudaStream_t stream) {
     if (launch_pdl(kernel, dim3(plan.grid), dim3(append ? kThreadsAppend : kThreads), C::kSmem,
                    stream, tq, tk, tv, tout, tpart, prm, app) != cudaSuccess)
         return BDSA_CUDA_ERROR;
+    if (prm.owner_merge) return BDSA_OK;
     if (launch_pdl(attn_merge_kernel<D>, dim3(plan.grid), dim3(kMergeThreads), 0, stream,
                    prm) != cudaSuccess)
         return BDSA_CUDA_ERROR;

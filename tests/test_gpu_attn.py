@@ -18,6 +18,12 @@ from gpu_helpers import (DevAttn, assert_attn_close, oracle_attn_full, oracle_at
 pytestmark = pytest.mark.gpu
 DRAFT, VERIFY = wl.DRAFT, wl.VERIFY
 FORCE_SPLIT = 4096  # an SM count that makes the planner split every unit's KV range
+# A grid of 5 CTAs: units are cut into several pieces, and (being no larger than
+# the device) the 64-row tile merges them in the attention launch, in the CTA
+# holding each cut unit's first tile; FORCE_SPLIT (more CTAs than SMs) keeps
+# the separate merge launch.
+OWNER = 5
+SMS = [0, OWNER, FORCE_SPLIT]
 
 
 def _cfg(name, bs, Hq, Hkv, D, B, ps, seq_lens, seed=77):
@@ -47,7 +53,7 @@ def dev():
 
 
 @pytest.mark.parametrize("mode", [DRAFT, VERIFY])
-@pytest.mark.parametrize("sms", [0, FORCE_SPLIT])
+@pytest.mark.parametrize("sms", SMS)
 def test_tiny_config(dev, mode, sms):
     inp = wl.make_attn_inputs(wl.config("tiny"))
     d = DevAttn(inp)
@@ -60,7 +66,7 @@ def test_tiny_config(dev, mode, sms):
 
 @pytest.mark.parametrize("shape", SHAPES, ids=[s[0] for s in SHAPES])
 @pytest.mark.parametrize("mode", [DRAFT, VERIFY])
-@pytest.mark.parametrize("sms", [0, FORCE_SPLIT])
+@pytest.mark.parametrize("sms", SMS)
 def test_shapes(dev, shape, mode, sms):
     name, Hq, Hkv, D, B, ps, lens = shape
     cfg = _cfg(name, len(lens), Hq, Hkv, D, B, ps, lens)
@@ -89,7 +95,7 @@ def test_unused_slots_hold_nan(dev):
     d_nan = DevAttn(wl.AttnInputs(cfg, inp.seq_lens, inp.block_table, inp.num_pages, inp.q,
                                   k_nan, v_nan, inp.scale))
     for mode in (DRAFT, VERIFY):
-        for sms in (0, FORCE_SPLIT):
+        for sms in SMS:
             a, _ = run_attn(d_clean, mode, sms=sms)
             b, _ = run_attn(d_nan, mode, sms=sms)
             assert torch.equal(a, b)
@@ -110,7 +116,7 @@ def test_page_permutation_is_bit_identical(dev):
     table2 = np.where(a.block_table >= 0, inv[np.maximum(a.block_table, 0)], -1).astype(np.int32)
     b = wl.AttnInputs(cfg, a.seq_lens, table2, a.num_pages, a.q, k2, v2, a.scale)
     for mode in (DRAFT, VERIFY):
-        for sms in (0, FORCE_SPLIT):
+        for sms in SMS:
             oa, la = run_attn(DevAttn(a), mode, sms=sms)
             ob, lb = run_attn(DevAttn(b), mode, sms=sms)
             assert torch.equal(oa, ob) and torch.equal(la, lb)
@@ -140,7 +146,7 @@ def test_bad_page_id_sets_status_and_skips_unit(dev):
     ref, _ = oracle_attn_full(inp, VERIFY)
     # sms = FORCE_SPLIT cuts every unit into one-tile pieces, so only one piece
     # of each of request 1's units sees the bad page and the merge must zero it
-    for sms in (0, FORCE_SPLIT):
+    for sms in SMS:
         status = torch.zeros(1, dtype=torch.int32, device=dev)
         out, lse = run_attn(d, VERIFY, sms=sms, status=status)
         assert status.item() == 16  # BDSA_DEVICE_OUT_OF_RANGE
@@ -165,7 +171,7 @@ def test_context_the_table_cannot_hold_sets_status(dev, L_bad):
     L = -1 if L_bad == -1 else max_pages * cfg.page_size - cfg.B + 1
     d.sl = d.sl.clone()
     d.sl[2] = L
-    for sms in (0, FORCE_SPLIT):
+    for sms in SMS:
         status = torch.zeros(1, dtype=torch.int32, device=dev)
         out, lse = run_attn(d, VERIFY, sms=sms, status=status)
         assert status.item() == 16
@@ -232,12 +238,15 @@ def test_output_16_byte_aligned_only(dev, sms):
     assert torch.equal(out.view(torch.int16), ref.view(torch.int16))
 
 
-def test_split_partials_reuse_a_dirty_workspace(dev):
-    """The 128-row tile publishes its split-KV partials through ready words in
-    the workspace: calls that reuse one workspace (left by an earlier call, or
-    filled with arbitrary bytes) on different inputs each match the oracle."""
+@pytest.mark.parametrize("shape_i,sms", [(2, FORCE_SPLIT), (1, OWNER)],
+                         ids=["rows128_merge_launch", "rows64_owner_merge"])
+def test_split_partials_reuse_a_dirty_workspace(dev, shape_i, sms):
+    """Split-KV partials are published through ready words in the workspace
+    (to the merge launch for the 128-row tile, to the owner CTA for the 64-row
+    one): calls that reuse one workspace (left by an earlier call, or filled
+    with arbitrary bytes) on different inputs each match the oracle."""
     import block_diffusion_speculative_attn_gb300 as bdsa
-    name, Hq, Hkv, D, B, ps, lens = SHAPES[2]  # 128 rows a tile
+    name, Hq, Hkv, D, B, ps, lens = SHAPES[shape_i]
     ws_bytes = 0
     cases = []
     for seed in (5, 6):
@@ -245,7 +254,7 @@ def test_split_partials_reuse_a_dirty_workspace(dev):
         inp = wl.make_attn_inputs(cfg, extra_pages=2)
         cases.append((cfg, inp, DevAttn(inp)))
         ws_bytes = max(ws_bytes, bdsa.block_attn_workspace_bytes(
-            cfg.bs, cfg.B, cfg.Hq, cfg.Hkv, cfg.D, inp.max_ctx_len, FORCE_SPLIT))
+            cfg.bs, cfg.B, cfg.Hq, cfg.Hkv, cfg.D, inp.max_ctx_len, sms))
     ws = torch.randint(0, 256, (ws_bytes,), dtype=torch.uint8, device=dev)
     for rep in range(2):
         for cfg, inp, d in cases:
@@ -255,19 +264,23 @@ def test_split_partials_reuse_a_dirty_workspace(dev):
                                         page_size=cfg.page_size, scale=inp.scale, mode=VERIFY,
                                         max_ctx_len=inp.max_ctx_len, num_pages=inp.num_pages,
                                         lse=lse, workspace=ws, dev_status=status,
-                                        sms=FORCE_SPLIT)
+                                        sms=sms)
             torch.cuda.synchronize()
             assert status.item() == 0
             ref, ref_lse = oracle_attn_full(inp, VERIFY)
             assert_attn_close(out, ref, lse, ref_lse, tag=f"reuse {rep} seed {cfg.seed}")
 
 
-def test_cuda_graph_replays_with_new_inputs(dev):
-    """The attention call captured into a CUDA graph (128-row tile, every unit
-    split, so partials and the merge are exercised) replays correctly when new
-    inputs are copied into the captured buffers between replays."""
+@pytest.mark.parametrize("shape_i,sms", [(2, FORCE_SPLIT), (1, OWNER)],
+                         ids=["rows128_merge_launch", "rows64_owner_merge"])
+def test_cuda_graph_replays_with_new_inputs(dev, shape_i, sms):
+    """The attention call captured into a CUDA graph (units split, so partials
+    and their merge are exercised: by the merge launch for the 128-row tile,
+    by the owner CTA for the 64-row one, whose ready words must not carry over
+    from one replay to the next) replays correctly when new inputs are copied
+    into the captured buffers between replays."""
     import block_diffusion_speculative_attn_gb300 as bdsa
-    name, Hq, Hkv, D, B, ps, lens = SHAPES[2]
+    name, Hq, Hkv, D, B, ps, lens = SHAPES[shape_i]
     inps = [wl.make_attn_inputs(_cfg(name, len(lens), Hq, Hkv, D, B, ps, lens, seed=s),
                                 extra_pages=2) for s in (11, 12, 13)]
     cfg = inps[0].cfg
@@ -276,14 +289,14 @@ def test_cuda_graph_replays_with_new_inputs(dev):
     out = torch.empty_like(q)
     lse = torch.empty((q.shape[0], cfg.Hq), dtype=torch.float32, device=dev)
     ws = torch.empty(bdsa.block_attn_workspace_bytes(cfg.bs, cfg.B, cfg.Hq, cfg.Hkv, cfg.D,
-                                                     inps[0].max_ctx_len, FORCE_SPLIT),
+                                                     inps[0].max_ctx_len, sms),
                      dtype=torch.uint8, device=dev)
 
     def call():
         bdsa.block_attn_paged(q, k, v, d.bt, d.sl, B=cfg.B, page_size=cfg.page_size,
                               scale=inps[0].scale, mode=VERIFY, max_ctx_len=inps[0].max_ctx_len,
                               num_pages=inps[0].num_pages, out=out, lse=lse, workspace=ws,
-                              sms=FORCE_SPLIT)
+                              sms=sms)
 
     s = torch.cuda.Stream()
     s.wait_stream(torch.cuda.current_stream())

@@ -67,7 +67,7 @@ def _run_append(inp, cfg, k_cache, v_cache, k_new, v_new, mode, sms=0, status=No
 
 @pytest.mark.parametrize("shape", SHAPES, ids=[s[0] for s in SHAPES])
 @pytest.mark.parametrize("mode", [DRAFT, VERIFY])
-@pytest.mark.parametrize("sms", [0, FORCE_SPLIT])
+@pytest.mark.parametrize("sms", [0, 5, FORCE_SPLIT])
 def test_append_then_attend(shape, mode, sms):
     name, Hq, Hkv, D, B, ps, lens = shape
     cfg = _cfg(name, len(lens), Hq, Hkv, D, B, ps, lens)
@@ -103,7 +103,7 @@ def test_append_skips_pages_outside_the_pool():
     k_exp, v_exp = oracle.append_block_kv(wl.bf16_bits(inp.k_cache), wl.bf16_bits(inp.v_cache),
                                           wl.bf16_bits(k_new), wl.bf16_bits(v_new), table,
                                           inp.seq_lens, cfg.B, cfg.page_size, inp.num_pages)
-    for sms in (0, FORCE_SPLIT):
+    for sms in (0, 5, FORCE_SPLIT):
         status = torch.zeros(1, dtype=torch.int32, device="cuda")
         out, lse, kc, vc = _run_append(bad_inp, cfg, inp.k_cache, inp.v_cache, k_new, v_new,
                                        VERIFY, sms, status)
