@@ -330,10 +330,47 @@ def random_tree_parents(rng: np.random.Generator, bs: int, n: int, window: int =
     return par
 
 
+def psi_spec_tree_parents(rng: np.random.Generator, bs: int, n_nodes: int, block: int = 16,
+                          prefixes: int = 32) -> np.ndarray:
+    """Token trees shaped like the Psi-Spec Tree sampler's (B, K, V) = (16, 32,
+    32): below the root (the first token, always accepted) up to `prefixes`
+    drafted prefixes of block - 1 tokens, merged into a trie.  Each new prefix
+    leaves an earlier one at a random depth, drawn so that exactly n_nodes
+    nodes (at most 1 + prefixes * (block - 1)) result; nodes are numbered in
+    creation order, which is topological."""
+    depth_max = block - 1
+    if not 1 <= n_nodes <= 1 + prefixes * depth_max:
+        raise ValueError("n_nodes out of range for the sampler's tree")
+    par = np.full((bs, n_nodes), -1, np.int32)
+    for r in range(bs):
+        paths: list = []
+        nodes = 1
+        while nodes < n_nodes:
+            left = prefixes - len(paths)
+            need = -(-(n_nodes - nodes) // left)  # new nodes this prefix must add at least
+            if paths:
+                base = paths[int(rng.integers(len(paths)))]
+                s = int(rng.integers(0, min(len(base), depth_max - need) + 1))
+            else:
+                base, s = [], 0
+            path = list(base[:s])
+            prev = path[-1] if path else 0
+            for _ in range(s, depth_max):
+                if nodes == n_nodes:
+                    break
+                par[r, nodes] = prev
+                path.append(nodes)
+                prev = nodes
+                nodes += 1
+            paths.append(path)
+    return par
+
+
 def make_tree_inputs(cfg: StepConfig, n_nodes: int, device="cpu", seed: int | None = None,
-                     bs: int | None = None) -> TreeInputs:
-    """Trees of n_nodes nodes shaped like a top-K expansion: the children of a
-    node carry the most likely tokens of its verifier distribution in rank
+                     bs: int | None = None, shape: str = "bushy") -> TreeInputs:
+    """Trees of n_nodes nodes shaped like a top-K expansion (shape "bushy":
+    random_tree_parents; "psi_spec": psi_spec_tree_parents): the children of
+    a node carry the most likely tokens of its verifier distribution in rank
     order (a drafter close to the verifier).  p = softmax(2 N(0, 1) logits
     with one random token per node raised by 15), a confident verifier whose
     top token holds about three quarters of the mass at V = 151936."""
@@ -341,7 +378,8 @@ def make_tree_inputs(cfg: StepConfig, n_nodes: int, device="cpu", seed: int | No
     bs = cfg.bs if bs is None else bs
     V = cfg.V
     rng = np.random.default_rng(seed)
-    par = random_tree_parents(rng, bs, n_nodes)
+    par = (psi_spec_tree_parents(rng, bs, n_nodes) if shape == "psi_spec"
+           else random_tree_parents(rng, bs, n_nodes))
     g = _gen(device, seed)
     logits = 2.0 * torch.randn((bs, n_nodes, V), generator=g, device=device)
     hot = torch.randint(0, V, (bs, n_nodes, 1), generator=g, device=device)

@@ -82,7 +82,7 @@ def _load():
         lib.oracle_kv_materialize.argtypes = [P, P, P, P, P, P, P, P, i32, f64, i32, i32, i32,
                                                i32, i32, i32, i64, P, P, P, i32]
         lib.oracle_kv_materialize.restype = i32
-        lib.oracle_tree_prepare.argtypes = [P, P, P, i32, i32, i32, i32, i32, P, P, P, P]
+        lib.oracle_tree_prepare.argtypes = [P, P, P, i32, i32, i32, i32, i32, P, P, P, P, i32]
         lib.oracle_tree_prepare.restype = i32
         lib.oracle_block_attn_tree.argtypes = [P, P, P, P, i32, i32, P, P, i32, i32, i32, i32,
                                                i32, i32, f64, P, P, i32]
@@ -325,16 +325,18 @@ def kv_materialize(hidden_bits, commit_len, positions, cache_loc, w_bits, k_norm
 def tree_prepare(parent, seq_lens, block_table, num_pages, page_size):
     """Token tree of B nodes per request (parent [bs, B], node 0 the root with
     parent -1).  Returns (depth, positions, cache_loc [bs, B] int32, mask
-    [bs, B] uint64 ancestor-or-self bits, n_bad)."""
+    [bs, B, ceil(B / 64)] uint64: bit j % 64 of word j // 64 set iff node j is
+    the node or one of its ancestors, n_bad)."""
     lib = _load()
     parent = _c(parent, np.int32)
     bs, B = parent.shape
     block_table = _c(block_table, np.int32)
     out = [np.empty((bs, B), np.int32) for _ in range(3)]
-    mask = np.empty((bs, B), np.uint64)
+    W = (B + 63) // 64
+    mask = np.empty((bs, B, W), np.uint64)
     bad = lib.oracle_tree_prepare(_ptr(parent), _ptr(_c(seq_lens, np.int32)), _ptr(block_table),
                                   block_table.shape[1], num_pages, bs, B, page_size,
-                                  *[_ptr(o) for o in out], _ptr(mask))
+                                  *[_ptr(o) for o in out], _ptr(mask), W)
     return out[0], out[1], out[2], mask, int(bad)
 
 

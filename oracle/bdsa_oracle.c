@@ -663,26 +663,30 @@ static int tree_is_ancestor(const int32_t *par, int j, int i) {  /* j == i count
 }
 
 /* depth, positions L + depth, cache_loc of block slot i (as prepare_block),
- * mask[i] = bit j set iff node j is node i or one of its ancestors.  Returns
- * the number of invalid parents plus failed page lookups. */
+ * and the ancestor-or-self set of node i as mask_words 64-bit words
+ * (mask[(r * B + i) * mask_words + j / 64] has bit j % 64 set iff node j is
+ * node i or one of its ancestors; mask_words >= ceil(B / 64), words past the
+ * tree are 0).  Returns the number of invalid parents plus failed page
+ * lookups, or -1 when mask_words is too small. */
 int oracle_tree_prepare(const int32_t *parent, const int32_t *seq_lens,
                         const int32_t *block_table, int max_pages_per_req, int num_pages, int bs,
                         int B, int page_size, int32_t *depth, int32_t *positions,
-                        int32_t *cache_loc, uint64_t *mask) {
+                        int32_t *cache_loc, uint64_t *mask, int mask_words) {
+    if (mask_words < (B + 63) / 64) return -1;
     int bad = 0;
     for (int r = 0; r < bs; ++r) {
         const int32_t *par = parent + (long)r * B;
         for (int i = 0; i < B; ++i) {
             const long row = (long)r * B + i;
             if (i == 0 ? par[0] != -1 : tree_parent(par, i) < 0) ++bad;
+            uint64_t *m = mask + row * mask_words;
+            for (int w = 0; w < mask_words; ++w) m[w] = 0;
             int d = -1;
-            uint64_t m = 0;
             for (int k = i; k >= 0; k = tree_parent(par, k)) {
                 ++d;
-                m |= (uint64_t)1 << k;
+                m[k / 64] |= (uint64_t)1 << (k % 64);
             }
             depth[row] = d;
-            mask[row] = m;
             const long L = seq_lens[r];
             positions[row] = (int32_t)(L + d);
             const long t = L + i;

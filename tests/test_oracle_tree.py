@@ -39,7 +39,7 @@ def test_golden_layout():
     assert bad == 0
     assert depth[0].tolist() == t["depth"]
     assert pos[0].tolist() == t["positions"]
-    assert mask[0].tolist() == t["mask"]
+    assert mask.shape == (1, B, 1) and mask[0, :, 0].tolist() == t["mask"]
     assert loc[0].tolist() == [t["seq_len"] + i for i in range(B)]  # identity paging
 
 
@@ -60,7 +60,7 @@ def test_invalid_parent_is_reported_and_made_a_root():
     par = np.array([[5, 0, 3, 1]], np.int32)  # root must be -1; node 2's parent is later
     depth, _, _, mask, bad = oracle.tree_prepare(par, [0], np.zeros((1, 1), np.int32), 1, 8)
     assert bad == 2
-    assert depth[0].tolist() == [0, 1, 0, 2] and mask[0].tolist() == [1, 3, 4, 11]
+    assert depth[0].tolist() == [0, 1, 0, 2] and mask[0, :, 0].tolist() == [1, 3, 4, 11]
 
 
 # --------------------------------------------------------------- attention
@@ -263,3 +263,115 @@ def test_root_acceptance_rate(lossless_walks):
     rate = (r["accept_len"] >= 1).mean()
     assert abs(rate - expect) < 5 * np.sqrt(expect * (1 - expect) / n)
     assert (r["new_seq_lens"] == r["accept_len"] + 1).all()
+
+
+# ------------------------------------------------- trees above 64 nodes
+# The Psi-Spec Tree sampler ((B, K, V) = (16, 32, 32): the top-32 prefixes of
+# 15 drafted tokens under the root) gives trees of up to 481 nodes, so the
+# ancestor sets span several 64-bit words.
+def _mask_words(nodes, W):
+    """Words of a node set, written out bit by bit."""
+    w = [0] * W
+    for n in nodes:
+        w[n // 64] |= 1 << (n % 64)
+    return w
+
+
+def test_chain_masks_across_words():
+    B = 200
+    par = np.arange(-1, B - 1, dtype=np.int32)[None]
+    depth, pos, _, mask, bad = oracle.tree_prepare(par, [10], np.zeros((1, 64), np.int32), 1, 8)
+    W = 4
+    assert mask.shape == (1, B, W)
+    for i in (0, 1, 62, 63, 64, 65, 127, 128, 150, 199):
+        # closed form: node i's set is {0, ..., i}; full words below i's word
+        want = [(2 ** 64 - 1) if 64 * (w + 1) <= i + 1 else
+                (0 if 64 * w > i else (1 << (i + 1 - 64 * w)) - 1) for w in range(W)]
+        assert [int(x) for x in mask[0, i]] == want, i
+    assert depth[0].tolist() == list(range(B)) and pos[0].tolist() == [10 + i for i in range(B)]
+
+
+def test_star_masks_across_words():
+    B = 150
+    par = np.zeros((1, B), np.int32)
+    par[0, 0] = -1
+    _, _, _, mask, _ = oracle.tree_prepare(par, [0], np.zeros((1, 64), np.int32), 1, 8)
+    for i in range(1, B):
+        assert [int(x) for x in mask[0, i]] == _mask_words([0, i], 3), i
+
+
+def test_stride_tree_masks_repeat_a_bit_in_every_word():
+    # parent(i) = i - 64 for i >= 64, 0 below: node i's ancestors share its bit
+    # position in every lower word, so a shifted word index or bit shows
+    B = 200
+    par = np.array([[-1] + [0 if i < 64 else i - 64 for i in range(1, B)]], np.int32)
+    depth, _, _, mask, bad = oracle.tree_prepare(par, [0], np.zeros((1, 64), np.int32), 1, 8)
+    assert bad == 0
+    for i in (1, 63, 64, 65, 100, 128, 191, 192, 199):
+        chain = [0] + [j for j in range(i % 64 or 64, i + 1, 64)]
+        assert [int(x) for x in mask[0, i]] == _mask_words(chain, 4), i
+        assert depth[0, i] == len(chain) - 1
+
+
+@pytest.mark.parametrize("shape", ["random", "psi_spec"])
+def test_large_tree_masks_follow_the_parent_recurrence(shape):
+    from block_diffusion_speculative_attn_gb300 import workloads as wl
+    rng = np.random.default_rng(11)
+    B = 300
+    par = (wl.psi_spec_tree_parents(rng, 2, B) if shape == "psi_spec"
+           else np.stack([_random_tree(rng, B) for _ in range(2)]))
+    depth, _, _, mask, bad = oracle.tree_prepare(par, [3, 4], np.zeros((2, 64), np.int32), 1, 8)
+    assert mask.shape == (2, B, 5)
+    for r in range(2):
+        for i in range(1, B):
+            own = np.array(_mask_words([i], 5), np.uint64)
+            np.testing.assert_array_equal(mask[r, i], mask[r, par[r, i]] | own)
+            assert sum(bin(int(x)).count("1") for x in mask[r, i]) == depth[r, i] + 1
+
+
+def test_large_tree_brute_force_sdpa():
+    """150 nodes: every node's output is torch's fp64 attention over the
+    context and its ancestor chain (the words past the first included)."""
+    rng = np.random.default_rng(12)
+    bs, B, Hq, Hkv, D, ps = 1, 150, 2, 1, 16, 8
+    q, k, v, table, L, total = _attn_inputs(rng, bs, B, Hq, Hkv, D, ps, [37])
+    par = _random_tree(rng, B)[None]
+    scale = 0.3
+    o_t, l_t = oracle.block_attn_tree(q, k, v, table, L, par, B, Hq, Hkv, D, ps, scale,
+                                      num_pages=total)
+    qf, kf, vf = _f64(q), _f64(k), _f64(v)
+    Lr = int(L[0])
+    slot = lambda t: int(table[0, t // ps]) * ps + t % ps  # noqa: E731
+    for i in list(range(0, B, 7)) + [B - 1]:
+        chain, n = [], i
+        while n >= 0:
+            chain.append(n)
+            n = int(par[0, n])
+        keys = [slot(t) for t in range(Lr)] + [slot(Lr + n) for n in sorted(chain)]
+        for j in range(Hq):
+            qq = torch.from_numpy(qf[i, j])[None, None, None]
+            kk = torch.from_numpy(kf[keys, 0])[None, None]
+            vv = torch.from_numpy(vf[keys, 0])[None, None]
+            ref = torch.nn.functional.scaled_dot_product_attention(qq, kk, vv, scale=scale)
+            np.testing.assert_allclose(o_t[i, j], ref[0, 0, 0].numpy(), rtol=1e-10, atol=1e-12)
+
+
+@pytest.mark.parametrize("greedy", [True, False])
+def test_long_chain_walk_accepts_every_node(greedy):
+    """A 100-node chain whose verifier puts all its mass on the next node's
+    token: the walk accepts all 99 nodes below the root and draws the bonus
+    from the last node's distribution."""
+    B, V = 100, 50
+    rng = np.random.default_rng(13)
+    ids = rng.integers(0, V, (1, B)).astype(np.int32)
+    par = np.arange(-1, B - 1, dtype=np.int32)[None]
+    p = np.zeros((1, B, V), np.float32)
+    for n in range(B - 1):
+        p[0, n, ids[0, n + 1]] = 1.0
+    p[0, B - 1, 7] = 1.0
+    u = None if greedy else rng.random((1, B)).astype(np.float32)
+    r = oracle.tree_accept(ids, par, p, u, [9])
+    assert r["accept_len"][0] == B - 1
+    assert r["path"][0].tolist() == list(range(B))
+    assert r["out_tokens"][0].tolist() == ids[0, 1:].tolist() + [7]
+    assert r["bonus_id"][0] == 7 and r["new_seq_lens"][0] == 9 + B
