@@ -524,27 +524,36 @@ def time_kvmat(step: "Step", flush, clean, n_layers: int = 5, H: int = 4096, ite
             "gpu_launches_per_call": 2, "iters": iters}
 
 
-def time_tree(cfg: wl.StepConfig, dev, flush, clean, n_nodes: int = 32, iters: int = 20,
+def tree_attn_flops(c: wl.StepConfig, seq_lens: np.ndarray, depth: np.ndarray) -> int:
+    """Algorithmic FLOPs of tree attention: every query row (request r, node i,
+    query head) against the L_r + depth(i) + 1 keys it sees, QK^T and PV at
+    2 FLOPs a multiply-add each."""
+    keys = seq_lens.astype(np.int64)[:, None] + depth.astype(np.int64) + 1
+    return int(keys.sum()) * c.Hq * c.D * 4
+
+
+def time_tree(cfg: wl.StepConfig, dev, flush, clean, n_nodes: int = 481, iters: int = 10,
               cpu: bool = False):
-    """Tree verify at the workload's shape with token trees of n_nodes nodes:
-    the layout (tree_prepare) plus tree attention over the paged cache, and
-    the tree acceptance walk over the vocabulary; L2 flushed before each call;
-    mean event times in ms."""
+    """Tree verify at the workload's shape with token trees shaped like the
+    Psi-Spec Tree sampler's (B, K, V) = (16, 32, 32): 32 prefixes of 15 drafted
+    tokens under the root, n_nodes = 481 nodes.  Times the layout
+    (tree_prepare) plus tree attention over the paged cache (row tiles of
+    128 / G nodes), and the tree acceptance walk over the vocabulary; L2
+    flushed before each call; mean event times in ms.  The attention is bound
+    by the tensor cores at this size (each key serves G * 481 query rows)."""
     import dataclasses
 
     import block_diffusion_speculative_attn_gb300 as bdsa
-    # the tree attention keeps a request's G x nodes query rows in one
-    # 128-row tile: 32 nodes at G = 4, 16 at G = 8
-    n_nodes = min(n_nodes, 128 // (cfg.Hq // cfg.Hkv))
     c = dataclasses.replace(cfg, B=n_nodes)
     attn = wl.make_attn_inputs(c, device=dev, seed=c.seed + 77)
     bt = torch.from_numpy(attn.block_table).to(dev)
     sl = torch.from_numpy(attn.seq_lens).to(dev)
-    x = wl.make_tree_inputs(cfg, n_nodes, device=dev)
+    x = wl.make_tree_inputs(cfg, n_nodes, device=dev, shape="psi_spec")
     par = torch.from_numpy(x.parent).to(dev)
     status = torch.zeros(1, dtype=torch.int32, device=dev)
     prep = tuple(torch.empty((c.bs, n_nodes), dtype=torch.int32, device=dev) for _ in range(3)) \
-        + (torch.empty((c.bs, n_nodes), dtype=torch.int64, device=dev),)
+        + (torch.empty((c.bs, n_nodes, bdsa.tree_mask_words(n_nodes)), dtype=torch.int64,
+                       device=dev),)
     out = torch.empty_like(attn.q)
     ws = torch.empty(max(bdsa.block_attn_workspace_bytes(c.bs, c.B, c.Hq, c.Hkv, c.D,
                                                          attn.max_ctx_len), 256),
@@ -577,13 +586,15 @@ def time_tree(cfg: wl.StepConfig, dev, flush, clean, n_nodes: int = 32, iters: i
     assert status.item() == 0, bdsa.STATUS.get(status.item())
     attn_ms = statistics.mean(a.elapsed_time(b) for a, b in t_attn)
     acc_ms = statistics.mean(a.elapsed_time(b) for a, b in t_acc)
-    hbm, _, src = peaks()
+    hbm, tf, src = peaks()
     abytes = attn_bytes(c, attn.seq_lens)
+    aflops = tree_attn_flops(c, attn.seq_lens, prep[0].cpu().numpy())
     depth = acc["accept_len"].cpu().numpy()
     accbytes = int((depth + 1).sum()) * cfg.V * 4
     base = None
     if cpu:
-        # the oracle: tree attention of the first request, acceptance of all rows
+        # the oracle: tree attention of the first request, acceptance of the
+        # first four rows
         import oracle
         cores = len(os.sched_getaffinity(0))
         ps = c.page_size
@@ -598,21 +609,25 @@ def time_tree(cfg: wl.StepConfig, dev, flush, clean, n_nodes: int = 32, iters: i
                                attn.seq_lens[:1], x.parent[:1], c.B, c.Hq, c.Hkv, c.D, ps,
                                attn.scale, num_pages=need, nthreads=cores)
         dt_attn = time.perf_counter() - t0
-        host = [x.block_ids.cpu().numpy(), x.parent, x.p.cpu().numpy(), x.u.cpu().numpy(),
-                x.seq_lens.cpu().numpy()]
+        na = min(4, c.bs)
+        host = [x.block_ids[:na].cpu().numpy(), x.parent[:na], x.p[:na].cpu().numpy(),
+                x.u[:na].cpu().numpy(), x.seq_lens[:na].cpu().numpy()]
         t0 = time.perf_counter()
         oracle.tree_accept(*host, nthreads=cores)
         dt_acc = time.perf_counter() - t0
         base = {"value": n_nodes / dt_attn, "unit": "query tokens/s (tree attention)",
-                "accept_rows_per_s": c.bs / dt_acc, "cores": cores, "kind": "oracle",
-                "sample": f"tree attention of 1 of {c.bs} requests, acceptance of all "
-                          f"{c.bs} rows, fp64 C oracle, {cores} threads",
+                "accept_rows_per_s": na / dt_acc, "cores": cores, "kind": "oracle",
+                "sample": f"tree attention of 1 of {c.bs} requests, acceptance of {na} "
+                          f"rows, fp64 C oracle, {cores} threads",
                 "seconds": dt_attn + dt_acc}
-    return {"nodes": n_nodes, "batch": c.bs, "vocab": cfg.V, "cpu_baseline": base,
+    tach = aflops / (attn_ms / 1e3) / 1e12
+    return {"nodes": n_nodes, "tree": "Psi-Spec (16, 32, 32): 32 prefixes of 15 tokens",
+            "batch": c.bs, "vocab": cfg.V, "cpu_baseline": base,
             "attn_ms": attn_ms, "attn_query_tokens_per_s": c.bs * n_nodes / (attn_ms / 1e3),
-            "attn_roofline": {"bound": "hbm", "achieved": abytes / (attn_ms / 1e3) / 1e9,
-                              "peak": hbm, "unit": "GB/s",
-                              "frac": abytes / (attn_ms / 1e3) / 1e9 / hbm, "peak_source": src,
+            "attn_roofline": {"bound": "tensor", "achieved": tach, "peak": tf,
+                              "unit": "TFLOP/s", "frac": tach / tf, "peak_source": src,
+                              "algorithmic_flops_per_launch": aflops,
+                              "hbm_achieved_gbs": abytes / (attn_ms / 1e3) / 1e9,
                               "algorithmic_bytes_per_launch": abytes,
                               "kernels": "tree_prepare + block attention (TREE) + merge"},
             "accept_ms": acc_ms, "accept_rows_per_s": c.bs / (acc_ms / 1e3),

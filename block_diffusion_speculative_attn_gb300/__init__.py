@@ -194,6 +194,8 @@ def block_attn_paged(q, k_cache, v_cache, block_table, seq_lens, *, B: int, page
     ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
     if tree_mask is not None:
         _dev(tree_mask, "tree_mask", torch.int64)
+        if tree_mask.numel() < bs * B * tree_mask_words(B):
+            raise ValueError("tree_mask holds fewer than bs * B * ceil(B / 64) words")
         if k_new is not None:
             raise ValueError("the tree call has no fused append")
         st = lib().bdsa_block_attn_paged_tree(
@@ -395,11 +397,16 @@ def kv_materialize(hidden, commit_len, positions, cache_loc, w_kv, k_norm_w, rop
 TREE_KEYS = ("accept_len", "bonus_id", "new_seq_lens")
 
 
+def tree_mask_words(B: int) -> int:
+    """64-bit words of one node's ancestor-or-self set in a tree of B nodes."""
+    return (B + 63) // 64
+
+
 def tree_prepare(parent, seq_lens, block_table, num_pages: int, page_size: int, out=None,
                  dev_status=None):
     """bdsa_tree_prepare.  parent [bs, B] int32 (node 0 the root, parent -1).
     Returns (depth, positions, cache_loc) int32 [bs, B] and tree_mask int64
-    [bs, B] (uint64 ancestor-or-self bits)."""
+    [bs, B, ceil(B / 64)] (uint64 words of ancestor-or-self bits)."""
     _dev(parent, "parent", torch.int32)
     _dev(seq_lens, "seq_lens", torch.int32)
     _dev(block_table, "block_table", torch.int32)
@@ -407,7 +414,9 @@ def tree_prepare(parent, seq_lens, block_table, num_pages: int, page_size: int, 
     dev = parent.device
     if out is None:
         out = tuple(torch.empty((bs, B), dtype=torch.int32, device=dev) for _ in range(3)) + \
-            (torch.empty((bs, B), dtype=torch.int64, device=dev),)
+            (torch.empty((bs, B, tree_mask_words(B)), dtype=torch.int64, device=dev),)
+    if out[3].numel() < bs * B * tree_mask_words(B):
+        raise ValueError("tree_mask holds fewer than bs * B * ceil(B / 64) words")
     st = lib().bdsa_tree_prepare(_ptr(parent), _ptr(seq_lens), _ptr(block_table),
                                  block_table.shape[1], num_pages, bs, B, page_size, _ptr(out[0]),
                                  _ptr(out[1]), _ptr(out[2]), _ptr(out[3]), _ptr(dev_status),

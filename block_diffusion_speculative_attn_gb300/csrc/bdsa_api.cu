@@ -99,7 +99,11 @@ int32_t attn_call(const bdsa_bf16 *q, const bdsa_bf16 *k_new, const bdsa_bf16 *v
     if ((k_new == nullptr) != (v_new == nullptr)) return BDSA_INVALID_ARG;
     if (Hq % Hkv != 0) return BDSA_INVALID_ARG;
     if (D != 64 && D != 128) return BDSA_UNSUPPORTED;
-    if (B > 64 || (Hq / Hkv) * B > 128) return BDSA_UNSUPPORTED;
+    // DRAFT / VERIFY: one tile of G * B <= 128 query rows a (request, KV head);
+    // TREE: trees of up to BDSA_TREE_MAX_NODES nodes in 128-row tiles
+    if (tree_mask == nullptr ? (B > 64 || (Hq / Hkv) * B > 128)
+                             : (B > BDSA_TREE_MAX_NODES || Hq / Hkv > 128))
+        return BDSA_UNSUPPORTED;
     if (!pow2(page_size) || page_size < 8) return BDSA_UNSUPPORTED;
     if ((int64_t)num_pages * page_size > INT32_MAX) return BDSA_UNSUPPORTED;
     if ((int64_t)bs * B > INT32_MAX) return BDSA_UNSUPPORTED;
@@ -365,7 +369,7 @@ int32_t bdsa_tree_prepare(const int32_t *parent, const int32_t *seq_lens,
                           uint64_t *tree_mask, int32_t *dev_status, void *stream) {
     if (bs < 0 || B < 1 || page_size < 1 || max_pages_per_req < 1 || num_pages < 1)
         return BDSA_INVALID_ARG;
-    if (B > 64) return BDSA_UNSUPPORTED;
+    if (B > BDSA_TREE_MAX_NODES) return BDSA_UNSUPPORTED;
     if (bs == 0) return BDSA_OK;
     if (!parent || !seq_lens || !block_table || !depth || !positions || !cache_loc || !tree_mask)
         return BDSA_INVALID_ARG;
@@ -383,7 +387,7 @@ int32_t bdsa_tree_accept(const int32_t *block_ids, const int32_t *parent, const 
                          int32_t *bonus_id, int32_t *new_seq_lens, int32_t num_sms,
                          int32_t *dev_status, void *stream) {
     if (bs < 0 || B < 1 || V < 1 || p_stride_r < 0 || p_stride_n < 0) return BDSA_INVALID_ARG;
-    if (B > 64 || V > (1 << 21)) return BDSA_UNSUPPORTED;
+    if (B > BDSA_TREE_MAX_NODES || V > (1 << 21)) return BDSA_UNSUPPORTED;
     if (bs == 0) return BDSA_OK;
     if (!block_ids || !parent || !p || !seq_lens || !accept_len || !path || !out_tokens ||
         !bonus_id || !new_seq_lens)

@@ -176,6 +176,13 @@ __device__ __forceinline__ uint64_t l2_policy_evict_first() {
     return p;
 }
 
+// L2 evict-normal policy (data another CTA or a later unit reads again).
+__device__ __forceinline__ uint64_t l2_policy_evict_normal() {
+    uint64_t p;
+    asm volatile("createpolicy.fractional.L2::evict_normal.b64 %0, 1.0;" : "=l"(p));
+    return p;
+}
+
 // Programmatic dependent launch: wait for the preceding grid's results /
 // allow the next grid to start its prologue.
 __device__ __forceinline__ void grid_dependency_wait() {

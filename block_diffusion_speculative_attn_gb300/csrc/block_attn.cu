@@ -145,12 +145,20 @@ struct Params {
     int owner_merge;         // M = 64: the CTA holding a cut unit's first tile merges it
     uint16_t *out;
     float *lse;
-    const uint64_t *tree_mask;  // TREE mode: [bs * B] block keys visible to each block row
+    const uint64_t *tree_mask;  // TREE mode: [bs * B, mask_words] block keys visible to each row
     float *part_o;           // [2 * grid, rows, D]
     float *part_lse;         // [2 * grid, rows]
     int32_t *dev_status;
     uint64_t magic_S;        // floor((2^64 - 1) / grid), see range_start
     int max_pages, num_pages, bs, B, Hq, Hkv, G, rows, page_size, log2_ps, box_rows, mode;
+    // Row tiles: a block of more rows than one tile (TREE with G * B > 128)
+    // is cut into n_rt tiles of npt nodes, and the KV heads are folded into
+    // the virtual requests: rv = (r * Hkv + h) * n_rt + t is request r's KV
+    // head h, row tile t, one unit each (hu = 1), so that the row tiles that
+    // read the same keys and values run back to back.  Otherwise n_rt = 1,
+    // npt = B, rv = r and a virtual request has hu = Hkv units, one a head.
+    int bs_v, n_rt, npt, hu;
+    int mask_words;          // TREE: 64-bit words of a node's ancestor-or-self set
     int out_v8;              // out is 32-byte aligned: the M = 128 epilogue stores 32 bytes
     float scale_log2;
 };
@@ -241,11 +249,32 @@ __device__ __forceinline__ void tmem_store_chunk(uint32_t taddr, const float (&v
     else tmem_st32(taddr, v);
 }
 
-// Tiles of a request with context length L (at least one, so that every
-// unit has an epilogue).
-__device__ __forceinline__ int tiles_of(long L, int B) {
-    const long nk = L + B;
+
+// 128-key tiles of a unit with nk keys (at least one, so that every unit has
+// an epilogue).
+__device__ __forceinline__ int tiles_of_keys(long nk) {
     return nk > 0 ? (int)min((nk + kBN - 1) / kBN, 1L << 24) : 1;
+}
+
+// Virtual request rv: its request, its first KV head (the head of unit u of
+// rv is vreq_h0 + u), its first node (the row tile's), the context length
+// and its key count -- the context and the block's first min(B, (t + 1) *
+// npt) slots: a node sees only itself and its ancestors, all at lower block
+// slots, so a row tile's keys end at its last node.
+__device__ __forceinline__ int vreq_r(const Params &prm, int rv) {
+    return prm.n_rt == 1 ? rv : rv / (prm.Hkv * prm.n_rt);
+}
+__device__ __forceinline__ int vreq_h0(const Params &prm, int rv) {
+    return prm.n_rt == 1 ? 0 : (rv / prm.n_rt) % prm.Hkv;
+}
+__device__ __forceinline__ int vreq_node0(const Params &prm, int rv) {
+    return prm.n_rt == 1 ? 0 : (rv % prm.n_rt) * prm.npt;
+}
+__device__ __forceinline__ int vreq_L(const Params &prm, int rv) {
+    return __ldg(prm.seq_lens + vreq_r(prm, rv));
+}
+__device__ __forceinline__ long vreq_keys(const Params &prm, int rv, long L) {
+    return L + min(prm.B, vreq_node0(prm, rv) + prm.npt);
 }
 
 // Schedule.  Units (request, KV head) are concatenated in order; each unit is
@@ -263,7 +292,7 @@ constexpr int kUnitCost = 2;
 struct Sched {
     uint32_t tmem;           // attention: TMEM base address (written by tcgen05.alloc)
     int abort;               // attention: a bounded wait gave up
-    int r0, h0, nt0, L0;     // the unit holding the CTA's cost start (if below Wc)
+    int r0, u0, nt0, L0;     // the unit holding the CTA's cost start (if below Wc)
     long long u_off0;        // its first real tile
     long long cu0;           // its cost offset
     long long x0, x1, W, Wc;
@@ -272,22 +301,25 @@ struct Sched {
 };
 static_assert(sizeof(Sched) <= 144, "the attention kernel keeps Sched in 144 bytes");
 
-// The unit a role is working through, walked in (request, KV head) order.
+// The unit a role is working through, walked in (virtual request, unit)
+// order; u is the unit's index within its virtual request.
 struct Cursor {
-    int r, h, nt, L;
+    int r, u, nt, L;
     long u_off;  // global index of the unit's first tile
 };
 
-// A maximal run of one unit's tiles inside a CTA's range.
+// A maximal run of one unit's tiles inside a CTA's range: r the virtual
+// request, u the unit within it, h its KV head.
 struct Piece {
-    int r, h, a, e, nt, L;
+    int r, u, h, a, e, nt, L;
     long u_off;
 };
 
-__device__ __forceinline__ Piece piece_at(const Cursor &c, long x, long x1) {
+__device__ __forceinline__ Piece piece_at(const Params &prm, const Cursor &c, long x, long x1) {
     Piece pc;
     pc.r = c.r;
-    pc.h = c.h;
+    pc.u = c.u;
+    pc.h = vreq_h0(prm, c.r) + c.u;
     pc.nt = c.nt;
     pc.L = c.L;
     pc.u_off = c.u_off;
@@ -316,11 +348,11 @@ template <int NT>
 __device__ void schedule(const Params &prm, int b, int S, Sched *sch) {
     static_assert(NT % 32 == 0 && NT <= 256, "scan partials hold 8 warps");
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-    const int bs = prm.bs;
+    const int bs = prm.bs_v;  // virtual requests (row tiles)
     const int per = (bs + NT - 1) / NT;
     const int i0 = min(bs, tid * per), i1 = min(bs, i0 + per);
     long long sum = 0;
-    for (int i = i0; i < i1; ++i) sum += tiles_of(__ldg(prm.seq_lens + i), prm.B);
+    for (int i = i0; i < i1; ++i) sum += tiles_of_keys(vreq_keys(prm, i, vreq_L(prm, i)));
     long long inc = sum;
 #pragma unroll
     for (int o = 1; o < 32; o <<= 1) {
@@ -336,7 +368,7 @@ __device__ void schedule(const Params &prm, int b, int S, Sched *sch) {
         if (w < warp) wex += v;
         T += v;
     }
-    const long long Hkv = prm.Hkv;
+    const long long Hkv = prm.hu;  // units a virtual request
     const long long W = Hkv * T, Wc = Hkv * (T + (long long)kUnitCost * bs);
     const long long c0 = range_start(b, Wc, S, prm.magic_S);
     const long long c1 = range_start(b + 1, Wc, S, prm.magic_S);
@@ -349,8 +381,8 @@ __device__ void schedule(const Params &prm, int b, int S, Sched *sch) {
         if (!(c < Wc && clo <= c && c < chi)) continue;
         long long tp = pre;  // tiles before request i
         for (int i = i0; i < i1; ++i) {
-            const int L = __ldg(prm.seq_lens + i);
-            const int nt = tiles_of(L, prm.B);
+            const int L = vreq_L(prm, i);
+            const int nt = tiles_of_keys(vreq_keys(prm, i, L));
             const long long ci = Hkv * (tp + (long long)kUnitCost * i);
             const long long span = nt + kUnitCost;  // cost of one unit of request i
             if (c < ci + Hkv * span) {
@@ -360,7 +392,7 @@ __device__ void schedule(const Params &prm, int b, int S, Sched *sch) {
                 const long long x = u_off + max(0LL, pos - kUnitCost);
                 if (which == 0) {
                     sch->r0 = i;
-                    sch->h0 = h;
+                    sch->u0 = h;
                     sch->nt0 = nt;
                     sch->L0 = L;
                     sch->u_off0 = u_off;
@@ -386,11 +418,11 @@ __device__ void schedule(const Params &prm, int b, int S, Sched *sch) {
 // Move the cursor past a finished unit.
 __device__ __forceinline__ void next_unit(Cursor &c, const Params &prm) {
     c.u_off += c.nt;
-    if (++c.h == prm.Hkv) {
-        c.h = 0;
-        if (++c.r < prm.bs) {
-            c.L = __ldg(prm.seq_lens + c.r);
-            c.nt = tiles_of(c.L, prm.B);
+    if (++c.u == prm.hu) {
+        c.u = 0;
+        if (++c.r < prm.bs_v) {
+            c.L = vreq_L(prm, c.r);
+            c.nt = tiles_of_keys(vreq_keys(prm, c.r, c.L));
         }
     }
 }
@@ -556,7 +588,7 @@ __global__ void __launch_bounds__(kAppend ? kThreadsAppend : kThreads, 1)
     Cursor cur0;
     if (x0 < x1) {
         cur0.r = sch->r0;
-        cur0.h = sch->h0;
+        cur0.u = sch->u0;
         cur0.nt = sch->nt0;
         cur0.L = sch->L0;
         cur0.u_off = sch->u_off0;
@@ -566,7 +598,10 @@ __global__ void __launch_bounds__(kAppend ? kThreadsAppend : kThreads, 1)
         // ------------------------------------------------ TMA producers
         const bool is_k = warp == kKProducerWarp;
         if (lane == 0) {
-            const uint64_t policy = l2_policy_evict_first();
+            // Every K / V byte is read once, except by the row tiles of a large
+            // tree, which read their (request, KV head)'s keys one after another.
+            const uint64_t policy =
+                prm.n_rt == 1 ? l2_policy_evict_first() : l2_policy_evict_normal();
             const int rows_box = prm.box_rows;
             const int NR = is_k ? C::NK : C::NV;
             const int FULL = is_k ? C::KF : C::VF;
@@ -578,7 +613,7 @@ __global__ void __launch_bounds__(kAppend ? kThreadsAppend : kThreads, 1)
             bool ok = true;
             Cursor cur = cur0;
             for (long x = x0; ok && x < x1; ++k) {
-                const Piece pc = piece_at(cur, x, x1);
+                const Piece pc = piece_at(prm, cur, x, x1);
                 if (is_k) {
                     const int qb = k % C::NQ;
                     if (k >= C::NQ) {
@@ -587,13 +622,14 @@ __global__ void __launch_bounds__(kAppend ? kThreadsAppend : kThreads, 1)
                         if (!ok) break;
                     }
                     mbar_arrive_expect_tx(bar(C::QF + qb), (uint32_t)(prm.rows * D * 2));
+                    const int qtok = vreq_r(prm, pc.r) * B + vreq_node0(prm, pc.r);
                     for (int c = 0; c < C::DH; ++c)
                         tma_load_4d(sbase + C::kOffQ + qb * C::kQBuf + c * C::kSlab, &tm_q,
-                                    c * 64, 0, pc.h, pc.r * B, bar(C::QF + qb));
+                                    c * 64, 0, pc.h, qtok, bar(C::QF + qb));
                     q_issued = k + 1;
                 }
-                const long n_keys = (long)pc.L + B;
-                const int32_t *bt = prm.block_table + (long)pc.r * prm.max_pages;
+                const long n_keys = vreq_keys(prm, pc.r, pc.L);
+                const int32_t *bt = prm.block_table + (long)vreq_r(prm, pc.r) * prm.max_pages;
                 // With the fused append, the first tile holding the block's
                 // own rows waits until the append warp has written this piece.
                 const int j_app = (kAppend && pc.L >= 0) ? max(pc.a, pc.L / kBN) : pc.e;
@@ -688,7 +724,7 @@ __global__ void __launch_bounds__(kAppend ? kThreadsAppend : kThreads, 1)
             bool ok = true;
             Cursor cur = cur0;
             for (long x = x0; ok && x < x1; ++k) {
-                const Piece pc = piece_at(cur, x, x1);
+                const Piece pc = piece_at(prm, cur, x, x1);
                 if (have) {
                     ok = issue_pv(pend);
                     have = false;
@@ -742,7 +778,7 @@ __global__ void __launch_bounds__(kAppend ? kThreadsAppend : kThreads, 1)
         // (a release per lane) for the producers' TMA loads.
         Cursor cur = cur0;
         for (long x = x0; x < x1;) {
-            const Piece pc = piece_at(cur, x, x1);
+            const Piece pc = piece_at(prm, cur, x, x1);
             append_piece_rows<D>(prm, app, prm.block_table + (long)pc.r * prm.max_pages, pc.r,
                                  pc.h, pc.L, (long)pc.a * kBN, (long)pc.e * kBN, lane);
             fence_proxy_async_global();
@@ -761,8 +797,10 @@ __global__ void __launch_bounds__(kAppend ? kThreadsAppend : kThreads, 1)
         const int row = (M == 64) ? warp * 16 + (lane & 15) : tid;
         const uint32_t lane_base = (uint32_t)(warp * 32) << 16;
         const float sl2 = prm.scale_log2;
-        const bool valid_row = row < prm.rows;
-        const int i_blk = row / G;
+        // (set per piece: a row tile's rows past the request's last node are
+        // not real rows)
+        bool valid_row = row < prm.rows;
+        const int i_blk = row / G;  // node within the row tile
         // A piece's output: O from TMEM scaled by 1/l, to `out` (bf16) when the
         // piece is the whole unit (or, M = 64, the owner of a cut unit, which
         // first merges the unit's other pieces into madd), else to the CTA's
@@ -986,7 +1024,7 @@ __global__ void __launch_bounds__(kAppend ? kThreadsAppend : kThreads, 1)
         int n_own = 0;  // units merged by this CTA as owner (phases of MR)
         auto owner_gather = [&](Epi &e, const Piece &pc, float lr) -> bool {
             const long long cu =
-                (long long)pc.u_off + (long long)kUnitCost * ((long long)pc.r * prm.Hkv + pc.h);
+                (long long)pc.u_off + (long long)kUnitCost * ((long long)pc.r * prm.hu + pc.u);
             const long long last = cu + kUnitCost + pc.nt - 1;  // cost of the unit's last tile
             const long long Wc = sch->Wc;
             float m_run = e.lse2;
@@ -1072,24 +1110,29 @@ __global__ void __launch_bounds__(kAppend ? kThreadsAppend : kThreads, 1)
         bool ok = true;
         Cursor cur = cur0;
         for (long x = x0; ok && x < x1; ++k) {
-            const Piece pc = piece_at(cur, x, x1);
-            const long n_keys = (long)pc.L + B;
+            const Piece pc = piece_at(prm, cur, x, x1);
+            const long n_keys = vreq_keys(prm, pc.r, pc.L);
+            const int rr = vreq_r(prm, pc.r);              // the request
+            const int node = vreq_node0(prm, pc.r) + i_blk;  // this row's block slot
+            valid_row = row < prm.rows && node < B;
             // Page ids this piece references: a context that needs more pages
-            // than the block-table row holds, or an id outside the pool, makes
-            // the unit's output zeros.  Each tile's ids are loaded during the
-            // tile and checked during the next one (or the epilogue).
+            // than the block-table row holds (for the whole block, so every row
+            // tile of a request agrees), or an id outside the pool, makes the
+            // unit's output zeros.  Each tile's ids are loaded during the tile
+            // and checked during the next one (or the epilogue).
             const bool shape_bad =
-                pc.L < 0 || (n_keys + ps - 1) / ps > (long)prm.max_pages;
-            const int32_t *bt_row = prm.block_table + (long)pc.r * prm.max_pages;
+                pc.L < 0 || ((long)pc.L + B + ps - 1) / ps > (long)prm.max_pages;
+            const int32_t *bt_row = prm.block_table + (long)rr * prm.max_pages;
             bool page_bad = false, pend = false;
             int32_t pend_pg = 0;
             const long limit = (kTree || prm.mode == BDSA_MODE_DRAFT)
                                    ? n_keys
                                    : min(n_keys, (long)pc.L + i_blk + 1);
-            // TREE: the block keys this row's node sees (itself and its ancestors)
-            uint64_t amask = ~0ull;
+            // TREE: the block keys this row's node sees (itself and its
+            // ancestors), mask_words words from mrow
+            const uint64_t *mrow = nullptr;
             if constexpr (kTree) {
-                if (valid_row) amask = __ldg(prm.tree_mask + (long)pc.r * B + i_blk);
+                if (valid_row) mrow = prm.tree_mask + ((long)rr * B + node) * prm.mask_words;
             }
             const int ob = k & 1;
             float m_used = -INFINITY;
@@ -1103,6 +1146,21 @@ __global__ void __launch_bounds__(kAppend ? kThreadsAppend : kThreads, 1)
             for (int j = pc.a; j < pc.e; ++j, ++g) {
                 const long t0 = (long)j * kBN;
                 const int sb = (int)(g & 1);
+                // TREE: the mask words this tile's block keys need (at most
+                // three from word wb), loaded before the wait for S
+                long moff = 0;
+                int wb = 0;
+                uint64_t mw0 = 0ull, mw1 = 0ull, mw2 = 0ull;
+                if constexpr (kTree) {
+                    moff = t0 + half * NC - pc.L;  // block slot of this thread's column 0
+                    if (moff + NC > 0 && mrow != nullptr) {
+                        wb = (int)(max(moff, 0L) >> 6);
+                        const int W = prm.mask_words;
+                        if (wb < W) mw0 = __ldg(mrow + wb);
+                        if (wb + 1 < W) mw1 = __ldg(mrow + wb + 1);
+                        if (wb + 2 < W) mw2 = __ldg(mrow + wb + 2);
+                    }
+                }
                 if (pend) page_bad |= pend_pg < 0 || pend_pg >= prm.num_pages;
                 {
                     const long kend = min(t0 + kBN, n_keys);
@@ -1133,19 +1191,23 @@ __global__ void __launch_bounds__(kAppend ? kThreadsAppend : kThreads, 1)
                         if (c >= nvalid) sv[c] = -INFINITY;
                 }
                 if constexpr (kTree) {
-                    const long off = t0 + half * NC - pc.L;  // block slot of column 0
-                    if (off + NC > 0) {
+                    if (moff + NC > 0) {
                         // visibility of this thread's columns, 64 to a word: context
-                        // keys (slot < 0) visible, block keys by the row's mask,
-                        // keys past the block already masked by the limit
+                        // keys (slot < 0) visible, block keys by the row's mask
+                        // (bits past the tree are 0; keys past the row tile's
+                        // last node are already masked by the limit)
 #pragma unroll
                         for (int wd = 0; wd < NC / 64; ++wd) {
-                            const long o = off + 64 * wd;
+                            const long o = moff + 64 * wd;
                             uint64_t vis = ~0ull;
-                            if (o >= 0 && o < 64)
-                                vis = (amask >> o) | (o > 0 ? ~0ull << (64 - o) : 0ull);
-                            else if (o < 0 && o > -64)
-                                vis = (amask << (-o)) | ((1ull << (-o)) - 1ull);
+                            if (o < 0) {
+                                if (o > -64) vis = (mw0 << (-o)) | ((1ull << (-o)) - 1ull);
+                            } else {
+                                const int w = (int)(o >> 6) - wb, sh = (int)(o & 63);
+                                const uint64_t lo = w == 0 ? mw0 : (w == 1 ? mw1 : mw2);
+                                const uint64_t hi = w == 0 ? mw1 : (w == 1 ? mw2 : 0ull);
+                                vis = sh ? (lo >> sh) | (hi << (64 - sh)) : lo;
+                            }
                             const uint32_t vlo = (uint32_t)vis, vhi = (uint32_t)(vis >> 32);
 #pragma unroll
                             for (int c = 0; c < 32; ++c) {
@@ -1293,9 +1355,9 @@ __global__ void __launch_bounds__(kAppend ? kThreadsAppend : kThreads, 1)
                 e.owner = M == 64 && prm.owner_merge && pc.a == 0 && pc.e < pc.nt;
                 // every warp checked every page of the piece
                 e.bad = shape_bad || __any_sync(0xffffffffu, page_bad);
-                e.orow = ((long)pc.r * B + i_blk) * prm.Hq + (long)pc.h * G + row % G;
+                e.orow = ((long)rr * B + node) * prm.Hq + (long)pc.h * G + row % G;
                 e.slot = 2 * b + (k == 0 ? 0 : 1);
-                e.r = pc.r;
+                e.r = rr;  // (the 64-row tile has one row tile: rr * B is its first token)
                 e.h = pc.h;
                 e.k = k;
                 if (e.bad && tid == 0) report_status(prm.dev_status, BDSA_DEVICE_OUT_OF_RANGE);
@@ -1369,7 +1431,8 @@ __global__ void __launch_bounds__(kMergeThreads, 4) attn_merge_kernel(const Para
         if (hold) grid_dependency_wait();
         return;
     }
-    const int r = sch.r0, h = sch.h0;
+    const int rv = sch.r0, h = vreq_h0(prm, rv) + sch.u0;
+    const int r = vreq_r(prm, rv), node0 = vreq_node0(prm, rv);
     const int b_first = cta_of(cu + kUnitCost, Wc, S);
     const int b_last = cta_of(cu + kUnitCost + sch.nt0 - 1, Wc, S);
     // Partial slots of the unit's pieces, in tile order.  Every CTA from
@@ -1463,7 +1526,9 @@ __global__ void __launch_bounds__(kMergeThreads, 4) attn_merge_kernel(const Para
         }
         const bool ok = den > 0.f && !bad;
         const float inv = ok ? 1.f / den : 0.f;
-        const long orow = ((long)r * prm.B + row / prm.G) * prm.Hq + (long)h * prm.G + row % prm.G;
+        const int node = node0 + row / prm.G;
+        if (node >= prm.B) continue;  // a row tile's rows past the last node
+        const long orow = ((long)r * prm.B + node) * prm.Hq + (long)h * prm.G + row % prm.G;
         uint2 *dst = reinterpret_cast<uint2 *>(prm.out + orow * D);
 #pragma unroll
         for (int v = 0; v < F4; ++v) {
@@ -1543,14 +1608,19 @@ int launch_impl(const AttnArgs &a, const AttnPlan &plan, cudaStream_t stream) {
     EncodeTiledFn enc = encode_fn();
     if (enc == nullptr) return BDSA_CUDA_ERROR;
     const int G = a.Hq / a.Hkv;
+    // Row tiles (TREE with more than M rows): npt nodes a tile
+    const int npt = G * a.B <= M ? a.B : M / G;
+    const int n_rt = (a.B + npt - 1) / npt;
+    if (n_rt > 1 && (long)a.bs * a.Hkv * n_rt > INT32_MAX) return BDSA_UNSUPPORTED;
     CUtensorMap tq, tk, tv;
     {
-        // q[(token*Hq + h*G + g)*D + d] as a 4-D tensor (d, g, h, token).
+        // q[(token*Hq + h*G + g)*D + d] as a 4-D tensor (d, g, h, token); a box
+        // is one row tile of one KV head
         cuuint64_t dims[4] = {(cuuint64_t)D, (cuuint64_t)G, (cuuint64_t)a.Hkv,
                               (cuuint64_t)a.bs * a.B};
         cuuint64_t strides[3] = {(cuuint64_t)D * 2, (cuuint64_t)G * D * 2,
                                  (cuuint64_t)a.Hq * D * 2};
-        cuuint32_t box[4] = {64, (cuuint32_t)G, 1, (cuuint32_t)a.B};
+        cuuint32_t box[4] = {64, (cuuint32_t)G, 1, (cuuint32_t)npt};
         cuuint32_t es[4] = {1, 1, 1, 1};
         if (enc(&tq, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<uint16_t *>(a.q), dims,
                 strides, box, es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
@@ -1575,12 +1645,13 @@ int launch_impl(const AttnArgs &a, const AttnPlan &plan, cudaStream_t stream) {
     char *ws = static_cast<char *>(a.workspace);
     CUtensorMap tout, tpart;
     {
-        // out has q's layout; the epilogue stores a whole unit's rows per box.
+        // out has q's layout; the epilogue stores a whole unit's rows per box
+        // (the 64-row tile, whose unit is one row tile: npt = B).
         cuuint64_t dims[4] = {(cuuint64_t)D, (cuuint64_t)G, (cuuint64_t)a.Hkv,
                               (cuuint64_t)a.bs * a.B};
         cuuint64_t strides[3] = {(cuuint64_t)D * 2, (cuuint64_t)G * D * 2,
                                  (cuuint64_t)a.Hq * D * 2};
-        cuuint32_t box[4] = {64, (cuuint32_t)G, 1, (cuuint32_t)a.B};
+        cuuint32_t box[4] = {64, (cuuint32_t)G, 1, (cuuint32_t)npt};
         cuuint32_t es[4] = {1, 1, 1, 1};
         if (enc(&tout, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, a.out, dims, strides, box, es,
                 CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
@@ -1630,7 +1701,12 @@ int launch_impl(const AttnArgs &a, const AttnPlan &plan, cudaStream_t stream) {
     prm.Hq = a.Hq;
     prm.Hkv = a.Hkv;
     prm.G = G;
-    prm.rows = G * a.B;
+    prm.rows = G * npt;
+    prm.npt = npt;
+    prm.n_rt = n_rt;
+    prm.bs_v = n_rt == 1 ? a.bs : a.bs * a.Hkv * n_rt;
+    prm.hu = n_rt == 1 ? a.Hkv : 1;
+    prm.mask_words = (a.B + 63) / 64;
     prm.page_size = a.page_size;
     int lg = 0;
     while ((1 << lg) < a.page_size) ++lg;
@@ -1675,7 +1751,9 @@ AttnPlan attn_plan(int bs, int B, int Hq, int Hkv, int D, int max_ctx_len, int n
     (void)max_ctx_len;
     AttnPlan p;
     p.grid = num_sms > 0 ? num_sms : 1;
-    p.rows = (Hq / Hkv) * B;
+    // rows a unit: G * B, or one 128-row tile of whole nodes when more (TREE)
+    const int G = Hq / Hkv;
+    p.rows = G * B <= 128 ? G * B : G * (128 / G);
     size_t off = 0;
     (void)bs;
     p.off_part_bad = off;

@@ -70,9 +70,10 @@ __global__ void __launch_bounds__(256)
 // Tree verify layout ("Unlocking Lossless Speedups in LLMs via Discrete
 // Diffusion", Psi-Spec Tree sampler): node i of request r sits at block slot i
 // (cache location of position L + i) and at sequence position L + depth(i);
-// tree_mask bit j is set iff node j is node i or one of its ancestors.  A
-// parent outside [0, i) (or node 0's parent other than -1) makes the node a
-// root and is reported.
+// node i's ancestor-or-self set is W = ceil(B / 64) words at
+// tree_mask[(r * B + i) * W], bit j % 64 of word j / 64 set iff node j is node
+// i or one of its ancestors.  A parent outside [0, i) (or node 0's parent
+// other than -1) makes the node a root and is reported.
 __global__ void __launch_bounds__(256)
     tree_prepare_kernel(const int32_t *__restrict__ parent, const int32_t *__restrict__ seq_lens,
                         const int32_t *__restrict__ block_table, int max_pages, int num_pages,
@@ -85,17 +86,30 @@ __global__ void __launch_bounds__(256)
     const int32_t *par = parent + (long)r * B;
     const int p_i = __ldg(par + i);
     if (i == 0 ? p_i != -1 : (p_i < 0 || p_i >= i)) report_status(dev_status, BDSA_DEVICE_OUT_OF_RANGE);
-    int d = -1;
-    uint64_t m = 0;
+    // The walk visits decreasing node indices, so the word it sets never
+    // moves up: one word is built in a register and written (with the empty
+    // words the walk skips) each time the walk leaves it.
+    const int W = (B + 63) >> 6;
+    uint64_t *mrow = tree_mask + idx * W;
+    int d = -1, cw = W - 1;
+    uint64_t cur = 0;
     for (int k = i; k >= 0;) {
         ++d;
-        m |= 1ull << k;
+        const int w = k >> 6;
+        for (; cw > w; --cw) {
+            mrow[cw] = cur;
+            cur = 0;
+        }
+        cur |= 1ull << (k & 63);
         const int pk = k > 0 ? __ldg(par + k) : -1;
         k = (pk >= 0 && pk < k) ? pk : -1;
     }
+    for (; cw >= 0; --cw) {
+        mrow[cw] = cur;
+        cur = 0;
+    }
     const int L = __ldg(seq_lens + r);
     depth[idx] = d;
-    tree_mask[idx] = m;
     positions[idx] = L + d;
     const long t = (long)L + i;
     int32_t loc = -1;

@@ -831,6 +831,7 @@ struct TreeParams {
 // so that every request's cluster is resident at once.
 constexpr int kTreeMaxCluster = kMaxCluster;
 constexpr int kTreeUnroll = 4;
+constexpr int kTreeMaxNodes = BDSA_TREE_MAX_NODES;
 
 // One thread-block cluster per request, its CTAs the vocabulary chunks.  Each
 // step of the walk sweeps p[n] (segment totals, or chunk maxima when greedy,
@@ -844,12 +845,13 @@ __global__ void __launch_bounds__(kThreads, 2) tree_accept_kernel(const TreePara
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int B = P.B;
     extern __shared__ float2 s_tot[];  // [nseg], used in chunk 0
-    __shared__ int s_ids[kMaxB], s_par[kMaxB], s_path[kMaxB], s_tok[kMaxB];
+    __shared__ int s_ids[kTreeMaxNodes], s_par[kTreeMaxNodes], s_path[kTreeMaxNodes],
+        s_tok[kTreeMaxNodes];
     __shared__ float s_cv[kTreeMaxCluster];
     __shared__ int s_ci[kTreeMaxCluster];
     __shared__ float s_wv[kWarps];
     __shared__ int s_wi[kWarps];
-    __shared__ int s_next, s_x;
+    __shared__ int s_next, s_x, s_child;
     if (chunk == 0) {
         for (int i = tid; i < B; i += kThreads) {
             s_ids[i] = __ldg(P.block_ids + (long)r * B + i);
@@ -926,13 +928,14 @@ __global__ void __launch_bounds__(kThreads, 2) tree_accept_kernel(const TreePara
                 __syncthreads();
                 x = s_x;
             }
+            // the lowest-index child of n carrying x, searched by the whole CTA
+            if (tid == 0) s_child = INT_MAX;
+            __syncthreads();
+            for (int c = n + 1 + tid; c < B; c += kThreads)
+                if (s_par[c] == n && s_ids[c] == x) atomicMin(&s_child, c);
+            __syncthreads();
             if (tid == 0) {
-                int child = -1;
-                for (int c = n + 1; c < B; ++c)
-                    if (s_par[c] == n && s_ids[c] == x) {
-                        child = c;
-                        break;
-                    }
+                const int child = s_child == INT_MAX ? -1 : s_child;
                 s_tok[depth] = x;
                 if (child >= 0) s_path[depth + 1] = child;
                 for (int rk = 0; rk < P.nchunk; ++rk) *map_to_rank(&s_next, (uint32_t)rk) = child;

@@ -60,6 +60,11 @@ typedef struct bdsa_bf16 { uint16_t bits; } bdsa_bf16; /* IEEE bfloat16 storage 
 
 enum { BDSA_MODE_DRAFT = 0, BDSA_MODE_VERIFY = 1, BDSA_MODE_TREE = 2 /* bdsa_block_attn_paged_tree */ };
 
+/* Largest token tree (nodes per request) of the tree-verify calls: the
+ * Psi-Spec Tree sampler's (B, K, V) = (16, 32, 32) keeps at most 32 prefixes
+ * of 15 drafted tokens below the root, 481 nodes. */
+enum { BDSA_TREE_MAX_NODES = 512 };
+
 /* Human-readable name of a status code (static string, never NULL). */
 const char *bdsa_status_string(int32_t status);
 
@@ -423,21 +428,29 @@ int32_t bdsa_kv_materialize(const bdsa_bf16 *hidden, const int32_t *commit_len,
  * 2.0", section "Attention Mask": the block's queries see the whole context,
  * the intra-block mask follows the verify structure.
  *
- * A request's block holds a token tree of B <= 64 nodes in topological order:
- * parent [bs, B] int32, node 0 the root (the last verified token, parent -1),
- * node i > 0 with a parent in [0, i).  A parent outside that range makes the
- * node a root of its own and sets *dev_status = BDSA_DEVICE_OUT_OF_RANGE.
+ * A request's block holds a token tree of B <= BDSA_TREE_MAX_NODES nodes in
+ * topological order: parent [bs, B] int32, node 0 the root (the last verified
+ * token, parent -1), node i > 0 with a parent in [0, i).  A parent outside
+ * that range makes the node a root of its own and sets
+ * *dev_status = BDSA_DEVICE_OUT_OF_RANGE.
  *
  * bdsa_tree_prepare: node i sits at block slot i (cache_loc of position
  *   L_r + i, as bdsa_prepare_block computes it, -1 and OUT_OF_RANGE when the
  *   lookup fails) and at sequence position L_r + depth(i) (positions, for
- *   RoPE); tree_mask[r, i] (uint64, 8-byte aligned) has bit j set iff node j
- *   is node i or one of its ancestors.  Outputs [bs, B].  One launch.
+ *   RoPE).  tree_mask [bs, B, W] uint64 (W = ceil(B / 64), 8-byte aligned)
+ *   holds node i's ancestor-or-self set: bit j % 64 of word j / 64 of
+ *   tree_mask[r, i] is set iff node j is node i or one of its ancestors (bits
+ *   j >= B are 0).  Other outputs [bs, B].  One launch.
  *
  * bdsa_block_attn_paged_tree: bdsa_block_attn_paged with the intra-block mask
  *   "block key j is visible to block row i iff bit j of tree_mask[r, i] is
- *   set" (mode BDSA_MODE_TREE); everything else (layouts, workspace, schedule,
- *   limits, errors) as bdsa_block_attn_paged.
+ *   set" (mode BDSA_MODE_TREE, tree_mask as bdsa_tree_prepare writes it);
+ *   layouts, workspace, errors as bdsa_block_attn_paged.  Limits: B <=
+ *   BDSA_TREE_MAX_NODES and G = Hq / Hkv <= 128.  A request's G * B query rows
+ *   of one KV head are processed in 128-row tiles of floor(128 / G) whole
+ *   nodes (one tile of G * B rows when G * B <= 128), each over the context
+ *   and the block keys up to its last node; the workspace holds partials of
+ *   those tiles.
  *
  * bdsa_tree_accept: p [bs, B, V] fp32 (p + r*p_stride_r + n*p_stride_n) is
  *   the verifier's distribution after node n, i.e. for n's children; u [bs, B]
@@ -454,7 +467,7 @@ int32_t bdsa_kv_materialize(const bdsa_bf16 *hidden, const int32_t *commit_len,
  *   out_tokens [bs, B] (the accepted nodes' tokens, then x; -1 padding),
  *   bonus_id [bs] = x, new_seq_lens [bs] = seq_lens + accept_len + 1.  The KV
  *   rows of the path's nodes are the ones to keep.
- *   Limits: B <= 64, V <= 2^21.  No workspace.  Launch: one thread-block
+ *   Limits: B <= BDSA_TREE_MAX_NODES, V <= 2^21.  No workspace.  Launch: one thread-block
  *   cluster per request (its CTAs the vocabulary chunks; num_sms sizes them,
  *   0 = the current device's SM count); two cluster barriers per step of the
  *   walk, at most B steps.

@@ -29,7 +29,7 @@ def _t(x, dtype):
 
 
 # ------------------------------------------------------------------ prepare
-@pytest.mark.parametrize("B", [1, 2, 7, 32, 64])
+@pytest.mark.parametrize("B", [1, 2, 7, 32, 64, 65, 200, 481, 512])
 def test_prepare_matches_oracle(B):
     rng = np.random.default_rng(B)
     bs, ps = 97, 16
@@ -49,12 +49,16 @@ def test_prepare_matches_oracle(B):
 
 
 # ---------------------------------------------------------------- attention
-def _tree_attn_case(cfg, n_nodes, seed, chain=False):
+def _tree_attn_case(cfg, n_nodes, seed, chain=False, shape="bushy", device="cpu"):
     c = dataclasses.replace(cfg, B=n_nodes)
-    inp = wl.make_attn_inputs(c, device="cpu", seed=seed)
+    inp = wl.make_attn_inputs(c, device=device, seed=seed)
     rng = np.random.default_rng(seed)
-    par = (np.tile(np.arange(-1, n_nodes - 1, dtype=np.int32), (c.bs, 1)) if chain
-           else wl.random_tree_parents(rng, c.bs, n_nodes))
+    if chain:
+        par = np.tile(np.arange(-1, n_nodes - 1, dtype=np.int32), (c.bs, 1))
+    elif shape == "psi_spec":
+        par = wl.psi_spec_tree_parents(rng, c.bs, n_nodes)
+    else:
+        par = wl.random_tree_parents(rng, c.bs, n_nodes)
     return c, inp, par
 
 
@@ -71,17 +75,55 @@ def _run_tree_attn(c, inp, par, sms=0):
     return out, lse, (q, k, v, bt, sl)
 
 
-@pytest.mark.parametrize("n_nodes", [1, 5, 16, 32])
+def _oracle_tree(c, inp, par):
+    return oracle.block_attn_tree(wl.bf16_bits(inp.q), wl.bf16_bits(inp.k_cache),
+                                  wl.bf16_bits(inp.v_cache), inp.block_table, inp.seq_lens, par,
+                                  c.B, c.Hq, c.Hkv, c.D, c.page_size, inp.scale,
+                                  num_pages=inp.num_pages, nthreads=oracle.max_threads())
+
+
+@pytest.mark.parametrize("n_nodes", [1, 5, 16, 32, 33, 100, 481])
 def test_tree_attention_matches_oracle(n_nodes):
+    """G = 4: one tile of 4 * nodes rows up to 32 nodes, then row tiles of 32
+    nodes (two at 33 nodes, sixteen at 481, the last holding one node)."""
     cfg = dataclasses.replace(wl.config("tiny"), bs=3, Hq=8, Hkv=2, D=128, page_size=16,
                               ctx=((0, 300),))
     c, inp, par = _tree_attn_case(cfg, n_nodes, 11 + n_nodes)
     out, lse, _ = _run_tree_attn(c, inp, par)
-    ref, ref_lse = oracle.block_attn_tree(wl.bf16_bits(inp.q), wl.bf16_bits(inp.k_cache),
-                                          wl.bf16_bits(inp.v_cache), inp.block_table,
-                                          inp.seq_lens, par, c.B, c.Hq, c.Hkv, c.D, c.page_size,
-                                          inp.scale, num_pages=inp.num_pages, nthreads=8)
+    ref, ref_lse = _oracle_tree(c, inp, par)
     assert_attn_close(out, ref, lse, ref_lse, tag=f"tree {n_nodes}")
+
+
+@pytest.mark.parametrize("sms", [0, 7])
+@pytest.mark.parametrize("D,Hq,Hkv,n_nodes", [(64, 2, 2, 200), (128, 16, 2, 100),
+                                              (128, 6, 2, 150), (128, 8, 2, 512),
+                                              (64, 256, 2, 3)])
+def test_row_tiles_match_oracle(D, Hq, Hkv, n_nodes, sms):
+    """Trees of more than 128 / G nodes in row tiles of floor(128 / G) nodes:
+    G = 1 (two tiles of 128 nodes), G = 8 (seven of 16), G = 3 (four of 42,
+    126-row tiles), G = 4 at the largest tree (sixteen of 32), G = 128 (one
+    node a tile); contexts up to 1500 keys, and with sms = 7 every row tile
+    cut between CTAs (merged partials)."""
+    cfg = dataclasses.replace(wl.config("tiny"), bs=3, Hq=Hq, Hkv=Hkv, D=D, page_size=32,
+                              ctx=((0, 1500),))
+    c, inp, par = _tree_attn_case(cfg, n_nodes, 3 * n_nodes + Hq)
+    out, lse, _ = _run_tree_attn(c, inp, par, sms=sms)
+    ref, ref_lse = _oracle_tree(c, inp, par)
+    assert_attn_close(out, ref, lse, ref_lse, tag=f"row tiles G={Hq // Hkv} nodes={n_nodes}")
+
+
+def test_long_chain_tree_is_the_verify_mask():
+    """A 200-node chain (seven row tiles of 32 nodes at G = 4) masks exactly as
+    VERIFY with B = 200: it matches the fp64 VERIFY oracle."""
+    cfg = dataclasses.replace(wl.config("tiny"), bs=2, Hq=8, Hkv=2, D=128, page_size=16,
+                              ctx=((100, 900),))
+    c, inp, par = _tree_attn_case(cfg, 200, 21, chain=True)
+    out, lse, _ = _run_tree_attn(c, inp, par)
+    ref, ref_lse = oracle.block_attn(wl.bf16_bits(inp.q), wl.bf16_bits(inp.k_cache),
+                                     wl.bf16_bits(inp.v_cache), inp.block_table, inp.seq_lens,
+                                     c.B, c.Hq, c.Hkv, c.D, c.page_size, inp.scale, bdsa.VERIFY,
+                                     num_pages=inp.num_pages, nthreads=oracle.max_threads())
+    assert_attn_close(out, ref, lse, ref_lse, tag="200-node chain vs verify oracle")
 
 
 @pytest.mark.parametrize("D,G", [(64, 1), (128, 4), (128, 8)])
@@ -106,11 +148,14 @@ def test_chain_tree_is_the_verify_mask(D, G):
                       lse_v.cpu().numpy().reshape(ref_lse.shape), tag="chain tree vs verify")
 
 
-def test_qwen3_8b_shaped_tree_attention():
-    """Batch 32, 32/8 heads, 32-node trees (G * nodes = 128: the M = 128 tile),
-    contexts U[1024, 4096]; the oracle checks four requests."""
+@pytest.mark.parametrize("n_nodes,shape", [(32, "bushy"), (481, "psi_spec"), (256, "psi_spec")])
+def test_qwen3_8b_shaped_tree_attention(n_nodes, shape):
+    """Batch 32, 32/8 heads, contexts U[1024, 4096]: 32-node trees (G * nodes =
+    128: one M = 128 tile), and trees shaped like the Psi-Spec Tree sampler's
+    (B, K, V) = (16, 32, 32) -- 32 prefixes of 15 tokens under the root, 481
+    nodes (sixteen row tiles), or 256; the oracle checks four requests."""
     cfg = wl.config("qwen3_8b_verify")
-    c, inp, par = _tree_attn_case(cfg, 32, 5)
+    c, inp, par = _tree_attn_case(cfg, n_nodes, 5, shape=shape)
     out, lse, (q, k, v, bt, sl) = _run_tree_attn(c, inp, par)
     reqs = [0, 10, 21, 31]
     # compact copy of the sampled requests' pages for the oracle
@@ -159,7 +204,7 @@ def test_golden_accept(case):
 
 @pytest.mark.parametrize("greedy", [False, True])
 @pytest.mark.parametrize("V", [1, 7, 257, 4099])
-@pytest.mark.parametrize("n_nodes", [1, 2, 9, 64])
+@pytest.mark.parametrize("n_nodes", [1, 2, 9, 64, 65, 300])
 def test_random_trees(n_nodes, V, greedy):
     cfg = dataclasses.replace(wl.config("tiny"), V=V)
     x = wl.make_tree_inputs(cfg, n_nodes, bs=64, seed=n_nodes * 31 + V)
@@ -208,3 +253,20 @@ def test_qwen3_8b_shaped_tree_acceptance():
                               nthreads=oracle.max_threads())
     _compare(got, want, max_flag_frac=2 / 32)
     assert got["accept_len"].float().mean().item() >= 1.0
+
+
+@pytest.mark.parametrize("greedy", [False, True])
+def test_psi_spec_sized_tree_acceptance(greedy):
+    """Eight requests with 481-node trees shaped like the Psi-Spec Tree
+    sampler's (B, K, V) = (16, 32, 32) at vocabulary 151936: every row against
+    the oracle (the walk is at most 16 nodes deep)."""
+    cfg = wl.config("qwen3_8b_verify")
+    x = wl.make_tree_inputs(cfg, 481, device=DEV, bs=8, shape="psi_spec")
+    u = None if greedy else x.u
+    got = bdsa.tree_accept(x.block_ids, _t(x.parent, torch.int32), x.p, u, x.seq_lens)
+    torch.cuda.synchronize()
+    want = oracle.tree_accept(x.block_ids.cpu().numpy(), x.parent, x.p.cpu().numpy(),
+                              None if u is None else u.cpu().numpy(), x.seq_lens.cpu().numpy(),
+                              nthreads=oracle.max_threads())
+    _compare(got, want, max_flag_frac=1 / 8)
+    assert got["accept_len"].max().item() <= 15

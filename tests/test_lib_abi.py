@@ -187,3 +187,47 @@ def test_kv_materialize_host_checks(L):
     # gathered rows: a count, (slot, position) per row, a dense copy of each row
     need = L.bdsa_kv_materialize_workspace_bytes(32, 16, 4096)
     assert need == 256 + 32 * 16 * 8 + 32 * 16 * 4096 * 2
+
+
+def _tree_attn(L, **kw):
+    a = dict(q=FAKE, k=FAKE, v=FAKE, bt=FAKE, max_pages=40, num_pages=80, sl=FAKE, max_ctx=100,
+             bs=2, B=481, Hq=32, Hkv=8, D=128, ps=16, scale=0.1, mask=FAKE, out=FAKE, lse=None,
+             ws=None, ws_bytes=0, sms=152)
+    a.update(kw)
+    return L.bdsa_block_attn_paged_tree(a["q"], a["k"], a["v"], a["bt"], a["max_pages"],
+                                        a["num_pages"], a["sl"], a["max_ctx"], a["bs"], a["B"],
+                                        a["Hq"], a["Hkv"], a["D"], a["ps"], a["scale"],
+                                        a["mask"], a["out"], a["lse"], a["ws"], a["ws_bytes"],
+                                        a["sms"], None, None)
+
+
+def test_tree_host_checks(L):
+    # trees of up to BDSA_TREE_MAX_NODES = 512 nodes (the Psi-Spec Tree
+    # sampler's 481), G <= 128: a valid shape gets past the limits to the
+    # workspace check
+    assert _tree_attn(L) == 4                          # WORKSPACE_TOO_SMALL
+    assert _tree_attn(L, B=512) == 4
+    assert _tree_attn(L, Hq=256, Hkv=2, B=3) == 4      # G = 128: one node a row tile
+    assert _tree_attn(L, B=513) == 2                   # UNSUPPORTED
+    assert _tree_attn(L, Hq=258, Hkv=1, B=2) == 2      # G > 128
+    assert _tree_attn(L, mask=None) == 1               # INVALID_ARG
+    assert _tree_attn(L, mask=ctypes.c_void_p(0x100004)) == 3   # MISALIGNED (8 bytes)
+    # the workspace holds partials of 128-row tiles of whole nodes
+    def al(x):
+        return (x + 255) // 256 * 256
+    sms, rows, D = 152, 128, 128
+    want = al(2 * sms * 4) + al(2 * sms * 8) + al(2 * sms * rows * 4) + al(2 * sms * rows * D * 4)
+    assert L.bdsa_block_attn_workspace_bytes(32, 481, 32, 8, D, 4096, sms) == want
+    rows = 42 * 3                                      # G = 3: 42 nodes a tile
+    want = al(2 * sms * 4) + al(2 * sms * 8) + al(2 * sms * rows * 4) + al(2 * sms * rows * D * 4)
+    assert L.bdsa_block_attn_workspace_bytes(32, 150, 6, 2, D, 4096, sms) == want
+    tp = L.bdsa_tree_prepare
+    # (empty batches: the size limits are checked before the batch is)
+    assert tp(FAKE, FAKE, FAKE, 4, 8, 0, 512, 16, FAKE, FAKE, FAKE, FAKE, None, None) == 0
+    assert tp(FAKE, FAKE, FAKE, 4, 8, 0, 513, 16, FAKE, FAKE, FAKE, FAKE, None, None) == 2
+    ta = L.bdsa_tree_accept
+    o = FAKE
+    assert ta(FAKE, FAKE, FAKE, 0, 0, FAKE, FAKE, 0, 512, 1000, o, o, o, o, o, 152, None,
+              None) == 0
+    assert ta(FAKE, FAKE, FAKE, 0, 0, FAKE, FAKE, 0, 513, 1000, o, o, o, o, o, 152, None,
+              None) == 2
