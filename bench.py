@@ -228,9 +228,11 @@ class Step:
             self.acc_out["out_tokens"] = torch.empty((bs, B), dtype=torch.int32, device=device)
             aws = bdsa.spec_accept_workspace_bytes(bs, B, cfg.V)
             self.acc_ws = torch.empty(max(aws, 256), dtype=torch.uint8, device=device)
-        plan_splits = ws > 0
-        # kernels of ours per step: prepare, per pass (attention + combine when split), accept
-        self.launches = 1 + len(cfg.modes) * (2 if plan_splits else 1) + (1 if cfg.V else 0)
+        # kernels of ours per step: prepare, per pass the attention (plus the
+        # merge launch for the 128-row tile; the 64-row tile merges cut units
+        # inside the attention launch), accept
+        attn_launches = 1 if (cfg.Hq // cfg.Hkv) * B <= 64 else 2
+        self.launches = 1 + len(cfg.modes) * attn_launches + (1 if cfg.V else 0)
 
     def prepare(self):
         c = self.cfg

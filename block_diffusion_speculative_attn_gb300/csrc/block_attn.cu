@@ -260,22 +260,34 @@ __device__ __forceinline__ int tiles_of_keys(long nk) {
 // rv is vreq_h0 + u), its first node (the row tile's), the context length
 // and its key count -- the context and the block's first min(B, (t + 1) *
 // npt) slots: a node sees only itself and its ancestors, all at lower block
-// slots, so a row tile's keys end at its last node.
+// slots, so a row tile's keys end at its last node.  kRT: row tiles are
+// possible (the TREE instantiations); otherwise a virtual request is a
+// request, compiled as such.
+template <bool kRT>
 __device__ __forceinline__ int vreq_r(const Params &prm, int rv) {
-    return prm.n_rt == 1 ? rv : rv / (prm.Hkv * prm.n_rt);
+    return (!kRT || prm.n_rt == 1) ? rv : rv / (prm.Hkv * prm.n_rt);
 }
+template <bool kRT>
 __device__ __forceinline__ int vreq_h0(const Params &prm, int rv) {
-    return prm.n_rt == 1 ? 0 : (rv / prm.n_rt) % prm.Hkv;
+    return (!kRT || prm.n_rt == 1) ? 0 : (rv / prm.n_rt) % prm.Hkv;
 }
+template <bool kRT>
 __device__ __forceinline__ int vreq_node0(const Params &prm, int rv) {
-    return prm.n_rt == 1 ? 0 : (rv % prm.n_rt) * prm.npt;
+    return (!kRT || prm.n_rt == 1) ? 0 : (rv % prm.n_rt) * prm.npt;
 }
+template <bool kRT>
 __device__ __forceinline__ int vreq_L(const Params &prm, int rv) {
-    return __ldg(prm.seq_lens + vreq_r(prm, rv));
+    return __ldg(prm.seq_lens + vreq_r<kRT>(prm, rv));
 }
+template <bool kRT>
 __device__ __forceinline__ long vreq_keys(const Params &prm, int rv, long L) {
-    return L + min(prm.B, vreq_node0(prm, rv) + prm.npt);
+    if constexpr (!kRT) return L + prm.B;
+    return L + min(prm.B, vreq_node0<kRT>(prm, rv) + prm.npt);
 }
+template <bool kRT>
+__device__ __forceinline__ int vreq_count(const Params &prm) { return kRT ? prm.bs_v : prm.bs; }
+template <bool kRT>
+__device__ __forceinline__ int vreq_units(const Params &prm) { return kRT ? prm.hu : prm.Hkv; }
 
 // Schedule.  Units (request, KV head) are concatenated in order; each unit is
 // kUnitCost "virtual" tiles followed by its real tiles, and CTA b takes the
@@ -315,11 +327,12 @@ struct Piece {
     long u_off;
 };
 
+template <bool kRT>
 __device__ __forceinline__ Piece piece_at(const Params &prm, const Cursor &c, long x, long x1) {
     Piece pc;
     pc.r = c.r;
     pc.u = c.u;
-    pc.h = vreq_h0(prm, c.r) + c.u;
+    pc.h = vreq_h0<kRT>(prm, c.r) + c.u;
     pc.nt = c.nt;
     pc.L = c.L;
     pc.u_off = c.u_off;
@@ -344,15 +357,16 @@ __device__ __forceinline__ long range_start(int b, long W, int S, uint64_t magic
 // counts of a contiguous block of requests, a scan gives each block's first
 // tile, and the threads whose blocks hold the CTA's cost bounds map them to
 // real tiles.  Two __syncthreads; results in *sch.
-template <int NT>
+template <int NT, bool kRT>
 __device__ void schedule(const Params &prm, int b, int S, Sched *sch) {
     static_assert(NT % 32 == 0 && NT <= 256, "scan partials hold 8 warps");
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-    const int bs = prm.bs_v;  // virtual requests (row tiles)
+    const int bs = vreq_count<kRT>(prm);  // virtual requests
     const int per = (bs + NT - 1) / NT;
     const int i0 = min(bs, tid * per), i1 = min(bs, i0 + per);
     long long sum = 0;
-    for (int i = i0; i < i1; ++i) sum += tiles_of_keys(vreq_keys(prm, i, vreq_L(prm, i)));
+    for (int i = i0; i < i1; ++i)
+        sum += tiles_of_keys(vreq_keys<kRT>(prm, i, vreq_L<kRT>(prm, i)));
     long long inc = sum;
 #pragma unroll
     for (int o = 1; o < 32; o <<= 1) {
@@ -368,7 +382,7 @@ __device__ void schedule(const Params &prm, int b, int S, Sched *sch) {
         if (w < warp) wex += v;
         T += v;
     }
-    const long long Hkv = prm.hu;  // units a virtual request
+    const long long Hkv = vreq_units<kRT>(prm);  // units a virtual request
     const long long W = Hkv * T, Wc = Hkv * (T + (long long)kUnitCost * bs);
     const long long c0 = range_start(b, Wc, S, prm.magic_S);
     const long long c1 = range_start(b + 1, Wc, S, prm.magic_S);
@@ -381,8 +395,8 @@ __device__ void schedule(const Params &prm, int b, int S, Sched *sch) {
         if (!(c < Wc && clo <= c && c < chi)) continue;
         long long tp = pre;  // tiles before request i
         for (int i = i0; i < i1; ++i) {
-            const int L = vreq_L(prm, i);
-            const int nt = tiles_of_keys(vreq_keys(prm, i, L));
+            const int L = vreq_L<kRT>(prm, i);
+            const int nt = tiles_of_keys(vreq_keys<kRT>(prm, i, L));
             const long long ci = Hkv * (tp + (long long)kUnitCost * i);
             const long long span = nt + kUnitCost;  // cost of one unit of request i
             if (c < ci + Hkv * span) {
@@ -416,13 +430,14 @@ __device__ void schedule(const Params &prm, int b, int S, Sched *sch) {
 }
 
 // Move the cursor past a finished unit.
+template <bool kRT>
 __device__ __forceinline__ void next_unit(Cursor &c, const Params &prm) {
     c.u_off += c.nt;
-    if (++c.u == prm.hu) {
+    if (++c.u == vreq_units<kRT>(prm)) {
         c.u = 0;
-        if (++c.r < prm.bs_v) {
-            c.L = vreq_L(prm, c.r);
-            c.nt = tiles_of_keys(vreq_keys(prm, c.r, c.L));
+        if (++c.r < vreq_count<kRT>(prm)) {
+            c.L = vreq_L<kRT>(prm, c.r);
+            c.nt = tiles_of_keys(vreq_keys<kRT>(prm, c.r, c.L));
         }
     }
 }
@@ -569,8 +584,12 @@ __global__ void __launch_bounds__(kAppend ? kThreadsAppend : kThreads, 1)
 
     // ---- inputs written by earlier kernels on the stream are read from here on
     grid_dependency_wait();
-    // The merge kernel may start now: its schedule reads only this call's inputs.
-    grid_launch_dependents();
+    // The merge kernel may start now: its schedule reads only this call's
+    // inputs.  With the owner merge there is no merge kernel, and the next
+    // kernel on the stream is left to start when this grid ends: launched
+    // early, it made a Qwen3-8B-shaped step (prepare, attention, acceptance)
+    // 8.5 us slower (89.4 against 80.9 us, A/B medians).
+    if (!prm.owner_merge) grid_launch_dependents();
     const int S = gridDim.x;
     const int b = blockIdx.x;
     if (warp == kKProducerWarp) {
@@ -583,7 +602,7 @@ __global__ void __launch_bounds__(kAppend ? kThreadsAppend : kThreads, 1)
         if (lane < 24 && r >= 0 && r < prm.bs && e < prm.max_pages)
             asm volatile("prefetch.global.L2 [%0];" ::"l"(prm.block_table + r * prm.max_pages + e));
     }
-    schedule<NT>(prm, b, S, sch);
+    schedule<NT, kTree>(prm, b, S, sch);
     const long x0 = sch->x0, x1 = sch->x1;
     Cursor cur0;
     if (x0 < x1) {
@@ -613,7 +632,7 @@ __global__ void __launch_bounds__(kAppend ? kThreadsAppend : kThreads, 1)
             bool ok = true;
             Cursor cur = cur0;
             for (long x = x0; ok && x < x1; ++k) {
-                const Piece pc = piece_at(prm, cur, x, x1);
+                const Piece pc = piece_at<kTree>(prm, cur, x, x1);
                 if (is_k) {
                     const int qb = k % C::NQ;
                     if (k >= C::NQ) {
@@ -622,14 +641,15 @@ __global__ void __launch_bounds__(kAppend ? kThreadsAppend : kThreads, 1)
                         if (!ok) break;
                     }
                     mbar_arrive_expect_tx(bar(C::QF + qb), (uint32_t)(prm.rows * D * 2));
-                    const int qtok = vreq_r(prm, pc.r) * B + vreq_node0(prm, pc.r);
+                    const int qtok = vreq_r<kTree>(prm, pc.r) * B + vreq_node0<kTree>(prm, pc.r);
                     for (int c = 0; c < C::DH; ++c)
                         tma_load_4d(sbase + C::kOffQ + qb * C::kQBuf + c * C::kSlab, &tm_q,
                                     c * 64, 0, pc.h, qtok, bar(C::QF + qb));
                     q_issued = k + 1;
                 }
-                const long n_keys = vreq_keys(prm, pc.r, pc.L);
-                const int32_t *bt = prm.block_table + (long)vreq_r(prm, pc.r) * prm.max_pages;
+                const long n_keys = vreq_keys<kTree>(prm, pc.r, pc.L);
+                const int32_t *bt =
+                    prm.block_table + (long)vreq_r<kTree>(prm, pc.r) * prm.max_pages;
                 // With the fused append, the first tile holding the block's
                 // own rows waits until the append warp has written this piece.
                 const int j_app = (kAppend && pc.L >= 0) ? max(pc.a, pc.L / kBN) : pc.e;
@@ -668,7 +688,7 @@ __global__ void __launch_bounds__(kAppend ? kThreadsAppend : kThreads, 1)
                     issued = g + 1;
                 }
                 x += pc.e - pc.a;
-                if (pc.e == pc.nt) next_unit(cur, prm);
+                if (pc.e == pc.nt) next_unit<kTree>(cur, prm);
             }
             // Drain: the last load issued into each buffer must have landed before exit.
             for (long i = max(0L, q_issued - C::NQ); i < q_issued; ++i)
@@ -724,7 +744,7 @@ __global__ void __launch_bounds__(kAppend ? kThreadsAppend : kThreads, 1)
             bool ok = true;
             Cursor cur = cur0;
             for (long x = x0; ok && x < x1; ++k) {
-                const Piece pc = piece_at(prm, cur, x, x1);
+                const Piece pc = piece_at<kTree>(prm, cur, x, x1);
                 if (have) {
                     ok = issue_pv(pend);
                     have = false;
@@ -764,7 +784,7 @@ __global__ void __launch_bounds__(kAppend ? kThreadsAppend : kThreads, 1)
                     have = true;
                 }
                 x += n;
-                if (pc.e == pc.nt) next_unit(cur, prm);
+                if (pc.e == pc.nt) next_unit<kTree>(cur, prm);
             }
             if (ok && have) ok = issue_pv(pend);
             // Drain: every MMA issued above has completed before TMEM is released.
@@ -778,13 +798,13 @@ __global__ void __launch_bounds__(kAppend ? kThreadsAppend : kThreads, 1)
         // (a release per lane) for the producers' TMA loads.
         Cursor cur = cur0;
         for (long x = x0; x < x1;) {
-            const Piece pc = piece_at(prm, cur, x, x1);
+            const Piece pc = piece_at<kTree>(prm, cur, x, x1);
             append_piece_rows<D>(prm, app, prm.block_table + (long)pc.r * prm.max_pages, pc.r,
                                  pc.h, pc.L, (long)pc.a * kBN, (long)pc.e * kBN, lane);
             fence_proxy_async_global();
             red_release_add_shared(&sch->appended, 1);
             x += pc.e - pc.a;
-            if (pc.e == pc.nt) next_unit(cur, prm);
+            if (pc.e == pc.nt) next_unit<kTree>(cur, prm);
         }
     } else if (warp < kSoftmaxWarps) {
         // ------------------------------------------------ softmax + epilogue
@@ -1024,7 +1044,8 @@ __global__ void __launch_bounds__(kAppend ? kThreadsAppend : kThreads, 1)
         int n_own = 0;  // units merged by this CTA as owner (phases of MR)
         auto owner_gather = [&](Epi &e, const Piece &pc, float lr) -> bool {
             const long long cu =
-                (long long)pc.u_off + (long long)kUnitCost * ((long long)pc.r * prm.hu + pc.u);
+                (long long)pc.u_off +
+                (long long)kUnitCost * ((long long)pc.r * vreq_units<kTree>(prm) + pc.u);
             const long long last = cu + kUnitCost + pc.nt - 1;  // cost of the unit's last tile
             const long long Wc = sch->Wc;
             float m_run = e.lse2;
@@ -1110,10 +1131,10 @@ __global__ void __launch_bounds__(kAppend ? kThreadsAppend : kThreads, 1)
         bool ok = true;
         Cursor cur = cur0;
         for (long x = x0; ok && x < x1; ++k) {
-            const Piece pc = piece_at(prm, cur, x, x1);
-            const long n_keys = vreq_keys(prm, pc.r, pc.L);
-            const int rr = vreq_r(prm, pc.r);              // the request
-            const int node = vreq_node0(prm, pc.r) + i_blk;  // this row's block slot
+            const Piece pc = piece_at<kTree>(prm, cur, x, x1);
+            const long n_keys = vreq_keys<kTree>(prm, pc.r, pc.L);
+            const int rr = vreq_r<kTree>(prm, pc.r);              // the request
+            const int node = vreq_node0<kTree>(prm, pc.r) + i_blk;  // this row's block slot
             valid_row = row < prm.rows && node < B;
             // Page ids this piece references: a context that needs more pages
             // than the block-table row holds (for the whole block, so every row
@@ -1374,7 +1395,7 @@ __global__ void __launch_bounds__(kAppend ? kThreadsAppend : kThreads, 1)
                 if (!ok) break;
             }
             x += pc.e - pc.a;
-            if (pc.e == pc.nt) next_unit(cur, prm);
+            if (pc.e == pc.nt) next_unit<kTree>(cur, prm);
         }
     }
 
@@ -1407,13 +1428,13 @@ constexpr uint64_t kMergeWaitNs = 20000000ull;  // 20 ms, then wait for the whol
 // must fit on each SM sub-partition beside two attention warps, so that the
 // merge CTAs become resident, and compute the schedule, while the attention
 // grid still runs.
-template <int D>
+template <int D, bool kRT>
 __global__ void __launch_bounds__(kMergeThreads, 4) attn_merge_kernel(const Params prm) {
     __shared__ Sched sch;
     __shared__ int s_slot[kMergeSlots];
     __shared__ int s_np;
     const int b = blockIdx.x, S = gridDim.x;
-    schedule<kMergeThreads>(prm, b, S, &sch);
+    schedule<kMergeThreads, kRT>(prm, b, S, &sch);
     const long W = sch.W, Wc = sch.Wc, x0 = sch.x0;
     // This grid must complete after the attention grid, so that a kernel that
     // waits on it sees every row: with published partials every CTA ends with
@@ -1431,8 +1452,8 @@ __global__ void __launch_bounds__(kMergeThreads, 4) attn_merge_kernel(const Para
         if (hold) grid_dependency_wait();
         return;
     }
-    const int rv = sch.r0, h = vreq_h0(prm, rv) + sch.u0;
-    const int r = vreq_r(prm, rv), node0 = vreq_node0(prm, rv);
+    const int rv = sch.r0, h = vreq_h0<kRT>(prm, rv) + sch.u0;
+    const int r = vreq_r<kRT>(prm, rv), node0 = vreq_node0<kRT>(prm, rv);
     const int b_first = cta_of(cu + kUnitCost, Wc, S);
     const int b_last = cta_of(cu + kUnitCost + sch.nt0 - 1, Wc, S);
     // Partial slots of the unit's pieces, in tile order.  Every CTA from
@@ -1737,7 +1758,8 @@ int launch_impl(const AttnArgs &a, const AttnPlan &plan, cudaStream_t stream) {
                    stream, tq, tk, tv, tout, tpart, prm, app) != cudaSuccess)
         return BDSA_CUDA_ERROR;
     if (prm.owner_merge) return BDSA_OK;
-    if (launch_pdl(attn_merge_kernel<D>, dim3(plan.grid), dim3(kMergeThreads), 0, stream,
+    if (launch_pdl(tree ? attn_merge_kernel<D, true> : attn_merge_kernel<D, false>,
+                   dim3(plan.grid), dim3(kMergeThreads), 0, stream,
                    prm) != cudaSuccess)
         return BDSA_CUDA_ERROR;
     return BDSA_OK;
