@@ -55,6 +55,7 @@
 #include <cuda_runtime.h>
 
 #include <atomic>
+#include <cstdlib>
 #include <chrono>
 #include <mutex>
 #include <utility>
@@ -141,6 +142,8 @@ struct Params {
     int32_t *part_bad;       // [2 * grid] partial slot saw a page id outside the pool
     uint64_t *part_ready;    // [2 * grid] the call's ticket once the slot is written
     uint64_t ticket;         // this call's ticket (unique a call, never 0)
+    uint64_t owner_ticket;   // the ticket the owner merge waits for (= ticket; see
+                             // expire_owner_waits)
     int early_merge;         // M = 128: partials are published, the merge starts on them
     int owner_merge;         // M = 64: the CTA holding a cut unit's first tile merges it
     uint16_t *out;
@@ -1062,9 +1065,9 @@ __global__ void __launch_bounds__(kAppend ? kThreadsAppend : kThreads, 1)
                 const int sl = 2 * bb;
                 if (!valid_row) continue;
                 const uint64_t *w = prm.part_ready + sl;
-                if (ld_acquire_gpu_u64(w) != prm.ticket) {
+                if (ld_acquire_gpu_u64(w) != prm.owner_ticket) {
                     const uint64_t t0 = global_timer_ns();
-                    while (ld_acquire_gpu_u64(w) != prm.ticket) {
+                    while (ld_acquire_gpu_u64(w) != prm.owner_ticket) {
                         if (*abort_flag) {
                             okg = false;
                             break;
@@ -1605,6 +1608,17 @@ uint64_t next_ticket() {
     return t;
 }
 
+// Test hook for the bounded waits: with BDSA_TEST_EXPIRE_OWNER_WAITS=1 in the
+// environment, the owner merge (64-row tile) waits for a ticket no CTA
+// publishes, so each owner CTA gives up after the wait limit (1 s), records
+// BDSA_DEVICE_TIMEOUT in dev_status and exits cleanly (no copy or MMA in
+// flight: its other pieces are done); the units it owns are left unwritten.
+// Read at every call; never set outside tests.
+bool expire_owner_waits() {
+    const char *v = getenv("BDSA_TEST_EXPIRE_OWNER_WAITS");
+    return v != nullptr && v[0] == '1' && v[1] == '\0';
+}
+
 // Launch with the programmatic-stream-serialization attribute, so the kernel
 // may start its prologue while the previous kernel on the stream finishes.
 template <typename... KArgs, typename... Args>
@@ -1698,6 +1712,7 @@ int launch_impl(const AttnArgs &a, const AttnPlan &plan, cudaStream_t stream) {
     prm.part_bad = reinterpret_cast<int32_t *>(ws + plan.off_part_bad);
     prm.part_ready = reinterpret_cast<uint64_t *>(ws + plan.off_part_ready);
     prm.ticket = next_ticket();
+    prm.owner_ticket = expire_owner_waits() ? (~prm.ticket | 1ull) : prm.ticket;
     // A CUDA graph would replay this call's ticket, so while the stream is
     // being captured the merge waits for the whole attention grid instead.
     cudaStreamCaptureStatus cap = cudaStreamCaptureStatusNone;
