@@ -67,30 +67,36 @@ namespace bdsa {
 namespace {
 
 constexpr int kBN = 128;                  // keys per tile
-constexpr int kThreads = 224;
-constexpr int kThreadsAppend = 256;       // + the append warp
-constexpr int kKProducerWarp = 4;
-constexpr int kMmaWarp = 5;
-constexpr int kVProducerWarp = 6;
-constexpr int kSoftmaxWarps = 4;
-constexpr int kAppendWarp = 7;
 constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kTmemO = 256;          // S at columns 0 / 128, O at 256 / 384
 constexpr float kRescaleLog2 = 8.0f;      // rescale O only when the max grows by > 2^8
 constexpr float kLn2 = 0.6931471805599453f;
 
-template <int D, int M>
+// W8: the 128-row tile with eight softmax warps, two threads a row (the TREE
+// kernels: a large tree's row tiles read keys mostly from L2 and are bound by
+// the softmax's instruction issue, which one warp per SM sub-partition cannot
+// keep up with); otherwise four softmax warps.
+template <int D, int M, bool W8 = false>
 struct Cfg {
+    static_assert(!W8 || M == 128, "eight softmax warps only with the 128-row tile");
     static constexpr int DH = D / 64;               // 64-element (128-byte) slabs per row
     static constexpr int kSlab = M * 128;           // one M-row slab of 128-byte rows
     static constexpr int kKVSlab = kBN * 128;       // one 128-key slab
     static constexpr int NQ = (M == 64) ? 2 : 1;    // Q buffers
     static constexpr int NP = (M == 64) ? 2 : 1;    // P buffers
     // V is held from its load until PV, K only until S: the deeper V ring lets
-    // each V load start about three tiles before its PV.
+    // each V load start about three tiles before its PV (two with eight
+    // softmax warps, whose keys come mostly from L2, to make room for the
+    // row-statistics exchange).
     static constexpr int NK = (D == 128) ? 2 : 4;
-    static constexpr int NV = (D == 128) ? 3 : 4;
-    static constexpr int TPR = (M == 64) ? 2 : 1;   // softmax threads per row
+    static constexpr int NV = (D == 128) ? (W8 ? 2 : 3) : 4;
+    static constexpr int TPR = (M == 64 || W8) ? 2 : 1;  // softmax threads per row
+    // warp roles: softmax warps first, then the Q/K producer, the MMA issuer,
+    // the V producer and (with the fused append) the append warp
+    static constexpr int SW = W8 ? 8 : 4;
+    static constexpr int KPW = SW, MMAW = SW + 1, VPW = SW + 2, APW = SW + 3;
+    static constexpr int kThreads = (SW + 3) * 32;
+    static constexpr int kThreadsAppend = kThreads + 32;
     static constexpr int NC = kBN / TPR;            // score columns per thread
     static constexpr int OC = D / TPR;              // output columns per thread
     static constexpr int kQBuf = DH * kSlab;
@@ -127,9 +133,17 @@ struct Cfg {
     // owner merge (M = 64): every softmax warp has read the other pieces'
     // ready words; waited by thread 0 alone before it resets them
     static constexpr int MR = PB + 1;
-    static constexpr int kNumBars = MR + 1;
-    static constexpr int kOffMisc = kOffBar + 8 * kNumBars;
-    static constexpr int kOffMiscEnd = kOffMisc + 144;  // the schedule state (Sched)
+    // W8: the two warps sharing a TMEM lane quadrant have written their halves
+    // of an exchange (one barrier per pair of warps, a phase per exchange)
+    static constexpr int XB = MR + 1;
+    static constexpr int kNumBars = XB + (W8 ? 4 : 0);
+    // W8: the two threads of a row exchange their row maxima (per tile) and
+    // row sums (per piece) through shared memory, two buffers by exchange
+    // parity
+    static constexpr int kOffXch = kOffBar + 8 * kNumBars;
+    static constexpr int kXchBytes = W8 ? 2 * 2 * 128 * 4 : 0;
+    static constexpr int kOffMisc = kOffXch + kXchBytes;
+    static constexpr int kOffMiscEnd = kOffMisc + 176;  // the schedule state (Sched)
     // + slack to align the base to 1 KB.  With D = 128 this is within a few
     // hundred bytes of the SM's shared memory less one merge CTA's, so that a
     // merge CTA can wait beside each attention CTA: keep both small.
@@ -311,10 +325,10 @@ struct Sched {
     long long u_off0;        // its first real tile
     long long cu0;           // its cost offset
     long long x0, x1, W, Wc;
-    long long wsum[8];       // per-warp partial sums of the scan (<= 256 threads)
+    long long wsum[12];      // per-warp partial sums of the scan (<= 384 threads)
     int appended;            // attention with the fused append: 32 x pieces whose rows are written
 };
-static_assert(sizeof(Sched) <= 144, "the attention kernel keeps Sched in 144 bytes");
+static_assert(sizeof(Sched) <= 176, "the attention kernel keeps Sched in 176 bytes");
 
 // The unit a role is working through, walked in (virtual request, unit)
 // order; u is the unit's index within its virtual request.
@@ -362,7 +376,7 @@ __device__ __forceinline__ long range_start(int b, long W, int S, uint64_t magic
 // real tiles.  Two __syncthreads; results in *sch.
 template <int NT, bool kRT>
 __device__ void schedule(const Params &prm, int b, int S, Sched *sch) {
-    static_assert(NT % 32 == 0 && NT <= 256, "scan partials hold 8 warps");
+    static_assert(NT % 32 == 0 && NT <= 384, "scan partials hold 12 warps");
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const int bs = vreq_count<kRT>(prm);  // virtual requests
     const int per = (bs + NT - 1) / NT;
@@ -506,14 +520,17 @@ __device__ void append_piece_rows(const Params &prm, const AppendParams &app, co
 // kTree: the TREE mask (block keys by tree_mask bits), in an instantiation of
 // its own so that the DRAFT / VERIFY tile loop carries none of its code.
 template <int D, int M, bool kAppend, bool kTree>
-__global__ void __launch_bounds__(kAppend ? kThreadsAppend : kThreads, 1)
+__global__ void __launch_bounds__(kAppend ? Cfg<D, M, kTree && M == 128>::kThreadsAppend
+                                          : Cfg<D, M, kTree && M == 128>::kThreads,
+                                  1)
     block_attn_kernel(const __grid_constant__ CUtensorMap tm_q,
                       const __grid_constant__ CUtensorMap tm_k,
                       const __grid_constant__ CUtensorMap tm_v,
                       const __grid_constant__ CUtensorMap tm_out,
                       const __grid_constant__ CUtensorMap tm_part, const Params prm,
                       const AppendParams app) {
-    using C = Cfg<D, M>;
+    constexpr bool W8 = kTree && M == 128;
+    using C = Cfg<D, M, W8>;
     extern __shared__ uint8_t smem_raw[];
     const uint32_t raw = smem_u32(smem_raw);
     const uint32_t sbase = (raw + 1023u) & ~1023u;
@@ -521,7 +538,9 @@ __global__ void __launch_bounds__(kAppend ? kThreadsAppend : kThreads, 1)
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int B = prm.B, G = prm.G;
     const long ps = prm.page_size;
-    constexpr int NT = kAppend ? kThreadsAppend : kThreads;
+    constexpr int NT = kAppend ? C::kThreadsAppend : C::kThreads;
+    constexpr int kKProducerWarp = C::KPW, kMmaWarp = C::MMAW, kVProducerWarp = C::VPW;
+    constexpr int kAppendWarp = C::APW, kSoftmaxWarps = C::SW;
 
     auto bar = [&](int i) -> uint32_t { return sbase + C::kOffBar + 8u * (uint32_t)i; };
     Sched *sch = reinterpret_cast<Sched *>(smem + C::kOffMisc);
@@ -560,6 +579,9 @@ __global__ void __launch_bounds__(kAppend ? kThreadsAppend : kThreads, 1)
         mbar_init(bar(C::DR), 1);
         mbar_init(bar(C::PB), kSoftmaxWarps);
         mbar_init(bar(C::MR), kSoftmaxWarps);
+        if constexpr (W8) {
+            for (int k = 0; k < 4; ++k) mbar_init(bar(C::XB + k), 2);
+        }
         *abort_flag = 0;
         sch->appended = 0;
         fence_mbarrier_init();
@@ -816,9 +838,33 @@ __global__ void __launch_bounds__(kAppend ? kThreadsAppend : kThreads, 1)
         // [64 * half, 64 * half + 64) of every 128-column block.
         constexpr int NC = C::NC;
         constexpr int OC = C::OC;
-        const int half = (M == 64) ? (lane >> 4) : 0;
-        const int row = (M == 64) ? warp * 16 + (lane & 15) : tid;
-        const uint32_t lane_base = (uint32_t)(warp * 32) << 16;
+        // W8: warps w and w + 4 share TMEM lane quadrant w % 4 (rows
+        // 32 (w % 4) + lane), warp w / 4 = half taking columns [64 half, 64
+        // half + 64) of S and [half * OC, half * OC + OC) of O; the row's two
+        // threads exchange row maxima and sums through xch (named barrier
+        // 1 + w % 4 for the pair of warps).
+        const int half = (M == 64) ? (lane >> 4) : (W8 ? (warp >> 2) : 0);
+        const int row = (M == 64) ? warp * 16 + (lane & 15) : (W8 ? (warp & 3) * 32 + lane : tid);
+        const uint32_t lane_base = (uint32_t)((W8 ? (warp & 3) : warp) * 32) << 16;
+        const uint32_t s_col = W8 ? (uint32_t)(half * NC) : 0u;  // this thread's S columns
+        const uint32_t o_col = W8 ? (uint32_t)(half * OC) : 0u;  // and O columns
+        float *xch = reinterpret_cast<float *>(smem + C::kOffXch);
+        // W8: exchange v with the row's other thread (exchange n of the pair
+        // of warps uses buffer n % 2 and phase n of barrier XB + w % 4; a
+        // bounded wait, so a pair whose other warp gave up ends too)
+        int n_xch = 0;
+        auto pair_exchange = [&](float v, float &other) -> bool {
+            const int bufi = n_xch & 1;
+            xch[(bufi * 2 + half) * 128 + row] = v;
+            __syncwarp();
+            if (lane == 0) mbar_arrive(bar(C::XB + (warp & 3)));
+            bool okx = mbar_wait(bar(C::XB + (warp & 3)), (uint32_t)(n_xch & 1), abort_flag,
+                                 prm.dev_status);
+            okx = __all_sync(0xffffffffu, okx);
+            other = xch[(bufi * 2 + (half ^ 1)) * 128 + row];
+            ++n_xch;
+            return okx;
+        };
         const float sl2 = prm.scale_log2;
         // (set per piece: a row tile's rows past the request's last node are
         // not real rows)
@@ -865,7 +911,8 @@ __global__ void __launch_bounds__(kAppend ? kThreadsAppend : kThreads, 1)
             // This thread's output columns [half * OC, half * OC + OC), read from
             // TMEM 32 at a time.
             auto load_chunk = [&](int c, float (&v32)[32]) {
-                tmem_load_chunk<M, D / 2>(tmem + lane_base + kTmemO + e.ob * 128 + c * 32, v32);
+                tmem_load_chunk<M, D / 2>(tmem + lane_base + kTmemO + e.ob * 128 + o_col + c * 32,
+                                          v32);
                 tmem_wait_ld();
                 if (zero) {
 #pragma unroll
@@ -1200,7 +1247,7 @@ __global__ void __launch_bounds__(kAppend ? kThreadsAppend : kThreads, 1)
                 float sv[NC];
 #pragma unroll
                 for (int c = 0; c < NC / 32; ++c)
-                    tmem_load_chunk<M, NC>(tmem + lane_base + sb * 128 + c * 32,
+                    tmem_load_chunk<M, NC>(tmem + lane_base + sb * 128 + s_col + c * 32,
                                            *reinterpret_cast<float(*)[32]>(&sv[c * 32]));
                 tmem_wait_ld();
                 tc_fence_before();
@@ -1247,6 +1294,12 @@ __global__ void __launch_bounds__(kAppend ? kThreadsAppend : kThreads, 1)
                     mx[(c >> 1) & 3] = max3f(mx[(c >> 1) & 3], sv[c], sv[c + 1]);
                 float mt = fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3]));
                 if constexpr (M == 64) mt = fmaxf(mt, __shfl_xor_sync(0xffffffffu, mt, 16));
+                if constexpr (W8) {
+                    float mo;
+                    ok = pair_exchange(mt, mo);
+                    if (!ok) break;
+                    mt = fmaxf(mt, mo);
+                }
                 const float m_new = mt * sl2;
                 float alpha = 1.f;
                 bool resc = false;
@@ -1304,7 +1357,7 @@ __global__ void __launch_bounds__(kAppend ? kThreadsAppend : kThreads, 1)
 #pragma unroll
                     for (int c = 0; c < OC / 32; ++c) {
                         float ov[32];
-                        const uint32_t ta = tmem + lane_base + kTmemO + ob * 128 + c * 32;
+                        const uint32_t ta = tmem + lane_base + kTmemO + ob * 128 + o_col + c * 32;
                         tmem_load_chunk<M, D / 2>(ta, ov);
                         tmem_wait_ld();
 #pragma unroll
@@ -1322,7 +1375,7 @@ __global__ void __launch_bounds__(kAppend ? kThreadsAppend : kThreads, 1)
                     const uint32_t pbase = sbase + C::kOffP + pb * C::kPBuf;
 #pragma unroll
                     for (int u = 0; u < NC / 8; ++u) {
-                        const int slab = (M == 64) ? half : (u >> 3);
+                        const int slab = (C::TPR == 2) ? half : (u >> 3);
                         const int cu = u & 7;
                         const uint32_t addr = pbase + slab * C::kSlab + row * 128 +
                                               ((uint32_t)(cu ^ (row & 7)) << 4);
@@ -1339,7 +1392,7 @@ __global__ void __launch_bounds__(kAppend ? kThreadsAppend : kThreads, 1)
                                    prm.dev_status);
                     ok = __all_sync(0xffffffffu, ok);
                     if (!ok) break;
-                    if (tid >= tile_keys) {
+                    if (tid < kBN && tid >= tile_keys) {
 #pragma unroll
                         for (int c = 0; c < C::DH; ++c)
 #pragma unroll
@@ -1364,6 +1417,14 @@ __global__ void __launch_bounds__(kAppend ? kThreadsAppend : kThreads, 1)
                     l = la.x + la.y;
                     lr = lb.x + lb.y;
                     if constexpr (M == 64) lr += __shfl_xor_sync(0xffffffffu, lr, 16);
+                    if constexpr (W8) {
+                        float o1, o2;
+                        ok = pair_exchange(lr, o1);
+                        ok = ok && pair_exchange(l, o2);
+                        if (!ok) break;
+                        lr += o1;
+                        l += o2;
+                    }
                 } else {
                     l = (la.x + la.y) + (lb.x + lb.y);
                 }
@@ -1640,6 +1701,7 @@ cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t s
 template <int D, int M>
 int launch_impl(const AttnArgs &a, const AttnPlan &plan, cudaStream_t stream) {
     using C = Cfg<D, M>;
+    using CT = Cfg<D, M, M == 128>;  // the TREE kernels' configuration
     EncodeTiledFn enc = encode_fn();
     if (enc == nullptr) return BDSA_CUDA_ERROR;
     const int G = a.Hq / a.Hkv;
@@ -1762,15 +1824,17 @@ int launch_impl(const AttnArgs &a, const AttnPlan &plan, cudaStream_t stream) {
                        : (append ? block_attn_kernel<D, M, true, false>
                                  : block_attn_kernel<D, M, false, false>);
     const int inst = tree ? 2 : (append ? 1 : 0);
+    const int smem = tree ? CT::kSmem : C::kSmem;
+    const int threads = tree ? CT::kThreads : (append ? C::kThreadsAppend : C::kThreads);
     static bool attr_set[3] = {false, false, false};  // per instantiation
     if (!attr_set[inst]) {
-        if (cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                 C::kSmem) != cudaSuccess)
+        if (cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) !=
+            cudaSuccess)
             return BDSA_CUDA_ERROR;
         attr_set[inst] = true;
     }
-    if (launch_pdl(kernel, dim3(plan.grid), dim3(append ? kThreadsAppend : kThreads), C::kSmem,
-                   stream, tq, tk, tv, tout, tpart, prm, app) != cudaSuccess)
+    if (launch_pdl(kernel, dim3(plan.grid), dim3(threads), (size_t)smem, stream, tq, tk, tv, tout,
+                   tpart, prm, app) != cudaSuccess)
         return BDSA_CUDA_ERROR;
     if (prm.owner_merge) return BDSA_OK;
     if (launch_pdl(tree ? attn_merge_kernel<D, true> : attn_merge_kernel<D, false>,
