@@ -40,12 +40,13 @@ from block_diffusion_speculative_attn_gb300 import workloads as wl  # noqa: E402
 
 METRIC = "draft/verify block-attn query tokens/s + % HBM roofline; accept rows/s"
 # DRAM bytes (read + write) of one attention call on the Qwen3-8B-shaped verify
-# batch, from one ncu capture of each of its two kernels (summary and commands
-# in profiles/qwen3_8b_verify_step_ncu.md): attention 308.41 + 4.63 MB, merge
-# 8.79 MB (cold under ncu; L2 hits in the timed step).  Valid only for the
-# kernel sources it was taken on: reported as null once they change.
-ATTN_TRAFFIC = {"workload": "qwen3_8b_verify", "bytes_per_call": 321.79e6,
-                "sources_sha256": "ca382c9131e6d440e6e8801b1f40976f34b4fa141ba4de38e1fb533501486dcc"}
+# batch, from one ncu capture (summary and commands in
+# profiles/qwen3_8b_verify_step_ncu.md): attention 308.42 MB read + 4.84 MB
+# written (the 64-row tile merges its cut units inside the launch: no merge
+# kernel).  Valid only for the kernel sources it was taken on: reported as
+# null once they change.
+ATTN_TRAFFIC = {"workload": "qwen3_8b_verify", "bytes_per_call": 313.26e6,
+                "sources_sha256": "c660bd6784307dc414bf9531f1117bbfbf834f4f34f42da50dc1d88c42db834b"}
 ATTN_SOURCES = ("block_diffusion_speculative_attn_gb300/csrc/block_attn.cu",
                 "block_diffusion_speculative_attn_gb300/csrc/bdsa_device.cuh")
 L2_FLUSH_BYTES = 512 << 20  # > 129 MB L2
@@ -65,6 +66,12 @@ def parse_args(argv=None):
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-workloads", action="store_true",
                     help="skip the other workloads' attention and acceptance timings")
+    ap.add_argument("--tree-only", type=int, default=0, metavar="BATCH",
+                    help="time only the tree-verify attention (481-node trees) at this "
+                         "batch and print its line (for profiling)")
+    ap.add_argument("--only-step", action="store_true",
+                    help="time the step alone: no side lines (fused append, I-DLM, KV "
+                         "materialisation, tree verify), no other workloads")
     return ap.parse_args(argv)
 
 
@@ -535,7 +542,7 @@ def tree_attn_flops(c: wl.StepConfig, seq_lens: np.ndarray, depth: np.ndarray) -
 
 
 def time_tree(cfg: wl.StepConfig, dev, flush, clean, n_nodes: int = 481, iters: int = 10,
-              cpu: bool = False):
+              cpu: bool = False, accept: bool = True):
     """Tree verify at the workload's shape with token trees shaped like the
     Psi-Spec Tree sampler's (B, K, V) = (16, 32, 32): 32 prefixes of 15 drafted
     tokens under the root, n_nodes = 481 nodes.  Times the layout
@@ -550,8 +557,13 @@ def time_tree(cfg: wl.StepConfig, dev, flush, clean, n_nodes: int = 481, iters: 
     attn = wl.make_attn_inputs(c, device=dev, seed=c.seed + 77)
     bt = torch.from_numpy(attn.block_table).to(dev)
     sl = torch.from_numpy(attn.seq_lens).to(dev)
-    x = wl.make_tree_inputs(cfg, n_nodes, device=dev, shape="psi_spec")
-    par = torch.from_numpy(x.parent).to(dev)
+    if accept:
+        x = wl.make_tree_inputs(cfg, n_nodes, device=dev, shape="psi_spec")
+        parents = x.parent
+    else:
+        parents = wl.psi_spec_tree_parents(np.random.default_rng(c.seed + 32452843), c.bs,
+                                           n_nodes)
+    par = torch.from_numpy(parents).to(dev)
     status = torch.zeros(1, dtype=torch.int32, device=dev)
     prep = tuple(torch.empty((c.bs, n_nodes), dtype=torch.int32, device=dev) for _ in range(3)) \
         + (torch.empty((c.bs, n_nodes, bdsa.tree_mask_words(n_nodes)), dtype=torch.int64,
@@ -579,7 +591,8 @@ def time_tree(cfg: wl.StepConfig, dev, flush, clean, n_nodes: int = 481, iters: 
         clean.sum()
         ev2 = [torch.cuda.Event(enable_timing=True) for _ in range(2)]
         ev2[0].record()
-        bdsa.tree_accept(x.block_ids, par, x.p, x.u, x.seq_lens, out=acc, dev_status=status)
+        if accept:
+            bdsa.tree_accept(x.block_ids, par, x.p, x.u, x.seq_lens, out=acc, dev_status=status)
         ev2[1].record()
         if i >= 3:
             t_attn.append(ev[:2])
@@ -591,10 +604,10 @@ def time_tree(cfg: wl.StepConfig, dev, flush, clean, n_nodes: int = 481, iters: 
     hbm, tf, src = peaks()
     abytes = attn_bytes(c, attn.seq_lens)
     aflops = tree_attn_flops(c, attn.seq_lens, prep[0].cpu().numpy())
-    depth = acc["accept_len"].cpu().numpy()
+    depth = acc["accept_len"].cpu().numpy() if accept else np.zeros(c.bs, np.int64)
     accbytes = int((depth + 1).sum()) * cfg.V * 4
     base = None
-    if cpu:
+    if cpu and accept:
         # the oracle: tree attention of the first request, acceptance of the
         # first four rows
         import oracle
@@ -623,6 +636,8 @@ def time_tree(cfg: wl.StepConfig, dev, flush, clean, n_nodes: int = 481, iters: 
                           f"rows, fp64 C oracle, {cores} threads",
                 "seconds": dt_attn + dt_acc}
     tach = aflops / (attn_ms / 1e3) / 1e12
+    if not accept:
+        acc_ms = None
     return {"nodes": n_nodes, "tree": "Psi-Spec (16, 32, 32): 32 prefixes of 15 tokens",
             "batch": c.bs, "vocab": cfg.V, "cpu_baseline": base,
             "attn_ms": attn_ms, "attn_query_tokens_per_s": c.bs * n_nodes / (attn_ms / 1e3),
@@ -632,12 +647,13 @@ def time_tree(cfg: wl.StepConfig, dev, flush, clean, n_nodes: int = 481, iters: 
                               "hbm_achieved_gbs": abytes / (attn_ms / 1e3) / 1e9,
                               "algorithmic_bytes_per_launch": abytes,
                               "kernels": "tree_prepare + block attention (TREE) + merge"},
-            "accept_ms": acc_ms, "accept_rows_per_s": c.bs / (acc_ms / 1e3),
-            "mean_accept_len": float(depth.mean()),
-            "accept_roofline": {"bound": "hbm", "achieved": accbytes / (acc_ms / 1e3) / 1e9,
-                                "peak": hbm, "unit": "GB/s",
-                                "frac": accbytes / (acc_ms / 1e3) / 1e9 / hbm,
-                                "peak_source": src, "algorithmic_bytes_per_launch": accbytes},
+            "accept_ms": acc_ms,
+            "accept_rows_per_s": c.bs / (acc_ms / 1e3) if acc_ms else None,
+            "mean_accept_len": float(depth.mean()) if accept else None,
+            "accept_roofline": None if not accept else {
+                "bound": "hbm", "achieved": accbytes / (acc_ms / 1e3) / 1e9, "peak": hbm,
+                "unit": "GB/s", "frac": accbytes / (acc_ms / 1e3) / 1e9 / hbm,
+                "peak_source": src, "algorithmic_bytes_per_launch": accbytes},
             "iters": iters}
 
 
@@ -870,9 +886,15 @@ def main(argv=None):
     import block_diffusion_speculative_attn_gb300 as bdsa
     bdsa.lib()
     cfg = wl.config(args.workload)
-    step = Step(cfg, dev, seed=cfg.seed + 1000 * rank)
     flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
     clean = torch.ones(L2_CLEAN_BYTES // 4, dtype=torch.float32, device=dev)
+    if args.tree_only:
+        import dataclasses
+        tc = dataclasses.replace(cfg, bs=args.tree_only)
+        print(json.dumps({"tree_verify": time_tree(tc, dev, flush, clean, iters=args.steps,
+                                                   accept=False)}), flush=True)
+        return
+    step = Step(cfg, dev, seed=cfg.seed + 1000 * rank)
     K = args.steps
     ev = [{"step": (torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)),
            "attn": [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
@@ -946,17 +968,17 @@ def main(argv=None):
     # the side lines run on single-pass workloads (the default one included)
     single = len(cfg.modes) == 1
     fused_append = None
-    if single:
+    if single and not args.only_step:
         fused_append = time_fused_append(step, flush, clean)
         assert step.status.item() == 0, bdsa.STATUS.get(step.status.item())
-    side = cfg.V and single
+    side = cfg.V and single and not args.only_step
     cpu_side = rank == 0 and world == 1 and not args.no_cpu_baseline
     idlm = time_idlm(cfg, dev, flush, clean, cpu=cpu_side) if side else None
     kvmat = time_kvmat(step, flush, clean, cpu=cpu_side) if side else None
     tree = time_tree(cfg, dev, flush, clean, cpu=cpu_side) if side else None
     # the other workloads' attention passes (draft mode among them) and acceptance
     others = None
-    if cfg.name == "qwen3_8b_verify" and not args.no_workloads:
+    if cfg.name == "qwen3_8b_verify" and not (args.no_workloads or args.only_step):
         others = {n: time_workload(n, dev, flush, clean, cpu=cpu_side) for n in OTHER_WORKLOADS}
 
     e2e = None
