@@ -198,6 +198,15 @@ __device__ __forceinline__ uint64_t ld_acquire_gpu_u64(const uint64_t *p) {
     return v;
 }
 
+// 32-byte global load bypassing L1 (one whole sector per lane); p 32-byte aligned.
+__device__ __forceinline__ void ld_cg_v8(const float *p, float *v) {
+    asm volatile("ld.global.cg.v8.f32 {%0, %1, %2, %3, %4, %5, %6, %7}, [%8];"
+                 : "=f"(v[0]), "=f"(v[1]), "=f"(v[2]), "=f"(v[3]), "=f"(v[4]), "=f"(v[5]),
+                   "=f"(v[6]), "=f"(v[7])
+                 : "l"(p)
+                 : "memory");
+}
+
 // 32-byte global store (one whole sector per lane).
 __device__ __forceinline__ void st_global_v8(void *p, uint32_t a, uint32_t b, uint32_t c,
                                              uint32_t d, uint32_t e, uint32_t f, uint32_t g,
@@ -618,14 +627,22 @@ __global__ void __launch_bounds__(kAppend ? Cfg<D, M, kTree && M == 128>::kThrea
     const int S = gridDim.x;
     const int b = blockIdx.x;
     if (warp == kKProducerWarp) {
-        // Warm L2 with the block-table rows this CTA most likely starts in
-        // (exact when the requests are of similar length), so the first page
-        // lookups overlap the schedule's context-length reads.
-        const long guess = (long)b * prm.bs / S;
-        const long r = guess - 1 + lane / 8;
-        const long e = (long)(lane % 8) * 32;  // 32 entries = one 128-byte line
-        if (lane < 24 && r >= 0 && r < prm.bs && e < prm.max_pages)
-            asm volatile("prefetch.global.L2 [%0];" ::"l"(prm.block_table + r * prm.max_pages + e));
+        // Warm L2 with the block table, so that the first page lookups overlap
+        // the schedule's context-length reads: all of it when it is small
+        // (every CTA asks; DRAM serves it once), else the rows this CTA most
+        // likely starts in (exact when the requests are of similar length).
+        const long entries = (long)prm.bs * prm.max_pages;
+        if (entries <= 16384) {
+            for (long e = (long)lane * 32; e < entries; e += 32 * 32)
+                asm volatile("prefetch.global.L2 [%0];" ::"l"(prm.block_table + e));
+        } else {
+            const long guess = (long)b * prm.bs / S;
+            const long r = guess - 1 + lane / 8;
+            const long e = (long)(lane % 8) * 32;  // 32 entries = one 128-byte line
+            if (lane < 24 && r >= 0 && r < prm.bs && e < prm.max_pages)
+                asm volatile("prefetch.global.L2 [%0];" ::"l"(prm.block_table + r * prm.max_pages +
+                                                              e));
+        }
     }
     schedule<NT, kTree>(prm, b, S, sch);
     const long x0 = sch->x0, x1 = sch->x1;
@@ -1129,11 +1146,12 @@ __global__ void __launch_bounds__(kAppend ? Cfg<D, M, kTree && M == 128>::kThrea
                     }
                     if (!okg) break;
                 }
-                const float4 *src = reinterpret_cast<const float4 *>(
-                    prm.part_o + ((long)sl * prm.rows + row) * D + half * OC);
-                float4 po[OC / 4];
+                // this thread's OC columns of the row: 32-byte loads (whole
+                // sectors), all in flight before the first is used
+                const float *src = prm.part_o + ((long)sl * prm.rows + row) * D + half * OC;
+                float po[OC];
 #pragma unroll
-                for (int v = 0; v < OC / 4; ++v) po[v] = __ldcg(src + v);
+                for (int v = 0; v < OC / 8; ++v) ld_cg_v8(src + 8 * v, &po[8 * v]);
                 const float ls = __ldcg(prm.part_lse + (long)sl * prm.rows + row);
                 bad = bad || __ldcg(prm.part_bad + sl) != 0;
                 if (ls == -INFINITY) continue;  // no key of that piece is visible to the row
@@ -1143,12 +1161,7 @@ __global__ void __launch_bounds__(kAppend ? Cfg<D, M, kTree && M == 128>::kThrea
                 s_own *= a;
                 den = den * a + wj;
 #pragma unroll
-                for (int v = 0; v < OC / 4; ++v) {
-                    madd[4 * v + 0] = fmaf(madd[4 * v + 0], a, wj * po[v].x);
-                    madd[4 * v + 1] = fmaf(madd[4 * v + 1], a, wj * po[v].y);
-                    madd[4 * v + 2] = fmaf(madd[4 * v + 2], a, wj * po[v].z);
-                    madd[4 * v + 3] = fmaf(madd[4 * v + 3], a, wj * po[v].w);
-                }
+                for (int c = 0; c < OC; ++c) madd[c] = fmaf(madd[c], a, wj * po[c]);
                 m_run = m_new;
             }
             // every softmax warp has read the words (a bounded wait on MR, one
