@@ -13,18 +13,22 @@
 // Two launches, chained with programmatic dependent launch:
 //   gather  four CTAs per request: copy the committed hidden rows into a
 //           dense buffer in the workspace and list (slot, position) per row;
-//   project one CTA pair (a thread-block cluster of 2) per (layer, K or V,
-//           head): the two CTAs take the two halves of the hidden dimension.
-//           Each streams its 128 x H/2 weight block once by TMA (128-byte
-//           swizzle) while the rows stream from L2, runs D^T = W X^T on the
-//           tensor cores (tcgen05, M = 128 head dims, N = up to 128 rows,
-//           fp32 accumulator in TMEM), then the pair adds its halves through
-//           distributed shared memory: each CTA sends the partner the row
-//           chunks the partner finishes and finishes the others (K norm,
-//           RoPE from the tables, bf16 store at the row's slot).
-// The weights do not depend on the gather, so the projection CTAs start
-// their weight stream before waiting for it.  More than 128 committed rows
-// run as several passes over the weights.
+//   project one thread-block cluster of three CTAs per (layer, K or V, head):
+//           the CTAs take three ranges of the hidden dimension's 64-element
+//           slabs.  Each streams its 128-row slice of the weight block once
+//           by TMA (128-byte swizzle) while the rows stream from L2, runs
+//           D^T = W X^T on the tensor cores (tcgen05, M = 128 head dims, N =
+//           up to 128 rows, fp32 accumulator in TMEM), then the three add
+//           their partial sums through distributed shared memory: each CTA
+//           sends its partners the row chunks they finish and finishes the
+//           others (the sum in a fixed order, K norm, RoPE from the tables,
+//           bf16 store at the row's slot).
+// The stream is bound by the latency of its TMA loads (about 1 us for a
+// 16 KB box under load), so its time follows the slabs a CTA streams: three
+// CTAs a head stream 21 or 22 slabs each where two streamed 32, and 240 CTAs
+// still fit two an SM.  The weights do not depend on the gather, so the
+// projection CTAs start their weight stream before waiting for it.  More than
+// 256 committed rows run as several passes over the weights.
 #include <cuda.h>
 #include <cuda_runtime.h>
 
@@ -37,6 +41,7 @@ namespace bdsa {
 namespace {
 
 constexpr int kD = 128;              // head dim (the accumulator's 128 lanes)
+constexpr int kSplit = 3;            // CTAs (hidden-dimension ranges) a head: a cluster
 constexpr int kBox = 128;            // gathered rows per X box (TMA box, MMA N <= 128)
 constexpr int kMaxBoxes = 2;         // boxes per weight stream: 256 rows, 256 TMEM columns
 constexpr int kStreamRows = kBox * kMaxBoxes;
@@ -62,17 +67,21 @@ constexpr int kXF = kWE + kWStages;     // row box full
 constexpr int kXE = kXF + kXStages;     // row box free
 constexpr int kAF = kXE + kXStages;     // accumulators of the stream complete
 constexpr int kTF = kAF + 1;            // epilogue done with TMEM and T
-constexpr int kPR = kTF + 1;            // the partner's T may be written (remote arrive)
-constexpr int kRX = kPR + 1;            // the partner's chunks have landed here
+constexpr int kPR = kTF + 1;            // both partners may take this CTA's chunks (remote arrivals)
+constexpr int kRX = kPR + 1;            // both partners' chunks have landed here
 constexpr int kEB = kRX + 1;            // the four epilogue warps meet
 constexpr int kDR = kEB + 1;            // drain of the MMA warp
 constexpr int kNumBars = kDR + 1;
 constexpr int kOffMisc = kOffBar + 8 * kNumBars;
 constexpr int kSmem = kOffMisc + 64 + 1024;  // + slack to align the base to 1 KB
-// The epilogue's T tile, [64 rows][128 dims] fp32 (32 KB), aliases the row
-// ring: it is used only between a stream's last MMA and the next stream's
-// first row load.  Two CTAs fit one SM (shared memory, 256 TMEM columns each).
-static_assert(kXStages * kXSlab >= 64 * kD * 4, "T fits the row ring");
+// The epilogue's receive buffers R[p][i] (partner slot p, chunk i: four
+// [32 rows][128 dims] fp32 tiles, 64 KB) alias the weight and row rings: they
+// are used only between a stream's last MMA and the next stream's first
+// loads.  R[0] doubles as the tile of summed rows.  Two CTAs fit one SM
+// (shared memory, 256 TMEM columns each).
+constexpr int kRTile = 32 * kD * 4;  // one received chunk
+static_assert(kWStages * kWSlab + kXStages * kXSlab >= 4 * kRTile && kOffX == kOffW + kWStages * kWSlab,
+              "the receive buffers fit the rings");
 static_assert(2 * (kSmem + 1024) <= 228 * 1024, "two CTAs an SM");
 
 struct Params {
@@ -216,12 +225,12 @@ __global__ void __launch_bounds__(kGatherThreads)
 
 // ------------------------------------------------------------------ project
 // CTA (cluster rank `rank`) of head `head` = (l * 2 + kv) * Hkv + h handles
-// hidden elements [rank * H/2, (rank + 1) * H/2).  Weight stream g covers
-// gathered rows [g * 256, g * 256 + 256) as up to two 128-row boxes, box b
-// accumulating into TMEM columns [128 b, 128 b + 128).  Its 32-row chunk c is
-// finished by the CTA of rank c % 2; the epilogue works in rounds of four
-// chunks (two a CTA), chunk 4 rho + 2 i + rank landing in T rows
-// [32 i, 32 i + 32).
+// the hidden dimension's 64-element slabs [rank * n / 3, (rank + 1) * n / 3),
+// n = H / 64.  Weight stream g covers gathered rows [g * 256, g * 256 + 256)
+// as up to two 128-row boxes, box b accumulating into TMEM columns [128 b,
+// 128 b + 128).  Its 32-row chunk c is finished by the CTA of rank c % 3; the
+// epilogue works in rounds of six chunks (two a CTA), chunk 6 rho + 3 i +
+// rank summed into R[0][i].
 __global__ void __launch_bounds__(kThreads, 2)
     kvmat_project_kernel(const __grid_constant__ CUtensorMap tm_w,
                          const __grid_constant__ CUtensorMap tm_x, const Params P) {
@@ -235,13 +244,13 @@ __global__ void __launch_bounds__(kThreads, 2)
     volatile int *abort_flag = reinterpret_cast<volatile int *>(smem + kOffMisc + 4);
 
     const uint32_t rank = cluster_rank();
-    const uint32_t peer = rank ^ 1u;
-    const int head = (int)(blockIdx.x >> 1);
+    const int head = (int)(blockIdx.x / kSplit);
     const int Hkv = P.Hkv;
     const int l = head / (2 * Hkv), kv = (head / Hkv) & 1, h = head % Hkv;
-    const int half_k = P.H / 2;
-    const int nslab = half_k / 64;
-    const int k0 = (int)rank * half_k;
+    const int nslab_all = P.H / 64;
+    const int s_begin = (int)rank * nslab_all / kSplit;
+    const int nslab = ((int)rank + 1) * nslab_all / kSplit - s_begin;
+    const int k0 = s_begin * 64;
     const int w_row = head * kD;
 
     if (warp == kMmaWarp) {
@@ -259,8 +268,8 @@ __global__ void __launch_bounds__(kThreads, 2)
         }
         mbar_init(bar(kAF), 1);
         mbar_init(bar(kTF), kEpiThreads / 32);
-        mbar_init(bar(kPR), 1);
-        mbar_init(bar(kRX), kEpiThreads);
+        mbar_init(bar(kPR), kSplit - 1);
+        mbar_init(bar(kRX), (kSplit - 1) * kEpiThreads);
         mbar_init(bar(kEB), kEpiThreads / 32);
         mbar_init(bar(kDR), 1);
         *abort_flag = 0;
@@ -271,7 +280,7 @@ __global__ void __launch_bounds__(kThreads, 2)
         tma_prefetch_desc(&tm_x);
     }
     tc_fence_before();
-    // both CTAs' barriers exist before either arrives on the other's
+    // every CTA's barriers exist before any arrives on another's
     cluster_sync_all();
     tc_fence_after();
     const uint32_t tmem = *tmem_slot;
@@ -295,6 +304,12 @@ __global__ void __launch_bounds__(kThreads, 2)
                 const int nbox = (nrows + kBox - 1) / kBox;
                 for (int s = 0; ok && s < nslab; ++s) {
                     const long gs = (long)g * nslab + s;
+                    if (g > 0 && s == 0) {
+                        // the rings double as the epilogue's receive buffers
+                        ok = mbar_wait(bar(kTF), (uint32_t)((g - 1) & 1), abort_flag,
+                                       P.dev_status);
+                        if (!ok) break;
+                    }
                     if (gs >= issued_w) {
                         const int st = (int)(gs % kWStages);
                         ok = mbar_wait(bar(kWE + st), (uint32_t)(((gs / kWStages) & 1) ^ 1),
@@ -304,12 +319,6 @@ __global__ void __launch_bounds__(kThreads, 2)
                         tma_load_2d(sbase + kOffW + st * kWSlab, &tm_w, k0 + s * 64, w_row,
                                     bar(kWF + st));
                         issued_w = gs + 1;
-                    }
-                    if (g > 0 && s == 0) {
-                        // the row ring doubles as the epilogue's T tile
-                        ok = mbar_wait(bar(kTF), (uint32_t)((g - 1) & 1), abort_flag,
-                                       P.dev_status);
-                        if (!ok) break;
                     }
                     for (int b = 0; b < nbox; ++b, ++xb) {
                         const int xs = (int)(xb % kXStages);
@@ -385,10 +394,18 @@ __global__ void __launch_bounds__(kThreads, 2)
         const int nstream = (M + kStreamRows - 1) / kStreamRows;
         const int d = tid;
         const uint32_t lane_base = (uint32_t)(warp * 32) << 16;
-        float *T = reinterpret_cast<float *>(smem + kOffX);  // [64][kD]
-        const uint32_t t_peer = map_shared_rank(sbase + kOffX, peer);
-        const uint32_t pr_peer = map_shared_rank(bar(kPR), peer);
-        const uint32_t rx_peer = map_shared_rank(bar(kRX), peer);
+        // R[p][i] at kOffW + (2 p + i) * kRTile; R[0] ([64 rows][kD]) takes the sums
+        float *R = reinterpret_cast<float *>(smem + kOffW);
+        float *T = R;
+        // partner slot j (0, 1) is the CTA of rank (rank + 1 + j) % 3; in that
+        // CTA this one is partner slot 1 - j
+        uint32_t r_peer[2], pr_peer[2], rx_peer[2];
+        for (int j = 0; j < 2; ++j) {
+            const uint32_t y = (rank + 1u + (uint32_t)j) % (uint32_t)kSplit;
+            r_peer[j] = map_shared_rank(sbase + kOffW + (uint32_t)((1 - j) * 2 * kRTile), y);
+            pr_peer[j] = map_shared_rank(bar(kPR), y);
+            rx_peer[j] = map_shared_rank(bar(kRX), y);
+        }
         const int q = tid & 3;  // dims [16q, 16q + 16) and [64 + 16q, 64 + 16q + 16)
         uint16_t *cache = kv == 0 ? P.k_cache : P.v_cache;
         float gain[32];
@@ -419,49 +436,69 @@ __global__ void __launch_bounds__(kThreads, 2)
                             mbar_wait(bar(kAF), (uint32_t)(g & 1), abort_flag, P.dev_status));
             if (!ok) break;
             tc_fence_after();
-            for (int c0 = 0; ok && c0 < nchunk; c0 += 4, ++round) {
-                // This CTA's T may take the partner's chunks: its MMAs are done
-                // and (after the first round) its warps have finished reading T.
+            for (int c0 = 0; ok && c0 < nchunk; c0 += 2 * kSplit, ++round) {
+                // This CTA's receive buffers may take the partners' chunks: its
+                // MMAs are done and (after the first round) its warps have
+                // finished reading them.
                 if (c0 > 0) {
                     ok = epi_sync();
                     if (!ok) break;
                 }
-                if (tid == 0) mbar_arrive_remote_release(pr_peer);
+                if (tid == 0) {
+                    mbar_arrive_remote_release(pr_peer[0]);
+                    mbar_arrive_remote_release(pr_peer[1]);
+                }
                 ok = __all_sync(0xffffffffu, mbar_wait_cluster(bar(kPR), (uint32_t)(round & 1),
                                                                abort_flag, P.dev_status));
                 if (!ok) break;
-                for (int i = 0; i < 2; ++i) {
-                    const int c = c0 + 2 * i + (int)peer;
-                    if (c >= nchunk) break;
-                    float v[32];
-                    tmem_ld32(tmem + lane_base + (uint32_t)(c * 32), v);
-                    tmem_wait_ld();
-                    const uint32_t base = t_peer + (uint32_t)((i * 32 * kD + d) * 4);
+                // each partner's chunks of the round, this thread's dim d of 32 rows
+                for (int jp = 0; jp < 2; ++jp) {
+                    const int y = (int)((rank + 1u + (uint32_t)jp) % (uint32_t)kSplit);
+                    for (int i = 0; i < 2; ++i) {
+                        const int c = c0 + kSplit * i + y;
+                        if (c >= nchunk) break;
+                        float v[32];
+                        tmem_ld32(tmem + lane_base + (uint32_t)(c * 32), v);
+                        tmem_wait_ld();
+                        if (nslab == 0) {  // no slab of the hidden dimension here (H = 128)
 #pragma unroll
-                    for (int j = 0; j < 32; ++j)
-                        st_cluster_f32(base + (uint32_t)(j * kD * 4), v[j]);
+                            for (int jj = 0; jj < 32; ++jj) v[jj] = 0.f;
+                        }
+                        const uint32_t base = r_peer[jp] + (uint32_t)((i * 32 * kD + d) * 4);
+#pragma unroll
+                        for (int jj = 0; jj < 32; ++jj)
+                            st_cluster_f32(base + (uint32_t)(jj * kD * 4), v[jj]);
+                    }
                 }
-                mbar_arrive_remote_release(rx_peer);
+                mbar_arrive_remote_release(rx_peer[0]);
+                mbar_arrive_remote_release(rx_peer[1]);
                 ok = __all_sync(0xffffffffu, mbar_wait_cluster(bar(kRX), (uint32_t)(round & 1),
                                                                abort_flag, P.dev_status));
                 if (!ok) break;
+                // this CTA's chunks: own partial + slot 0's + slot 1's, into R[0]
                 for (int i = 0; i < 2; ++i) {
-                    const int c = c0 + 2 * i + (int)rank;
+                    const int c = c0 + kSplit * i + (int)rank;
                     if (c >= nchunk) break;
                     float v[32];
                     tmem_ld32(tmem + lane_base + (uint32_t)(c * 32), v);
                     tmem_wait_ld();
-                    float *col = T + i * 32 * kD + d;
+                    if (nslab == 0) {
 #pragma unroll
-                    for (int j = 0; j < 32; ++j) col[j * kD] += v[j];
+                        for (int jj = 0; jj < 32; ++jj) v[jj] = 0.f;
+                    }
+                    float *col0 = R + i * 32 * kD + d;
+                    const float *col1 = R + (2 + i) * 32 * kD + d;
+#pragma unroll
+                    for (int jj = 0; jj < 32; ++jj)
+                        col0[jj * kD] = (v[jj] + col0[jj * kD]) + col1[jj * kD];
                 }
                 tc_fence_before();
-                ok = epi_sync();  // T complete: every epilogue warp has added its dims
+                ok = epi_sync();  // the sums are complete: every epilogue warp has added its dims
                 if (!ok) break;
                 // finish this CTA's rows of the round, four threads a row
                 for (int i = 0; i < 2; ++i) {
                     const int tl = i * 32 + (tid >> 2);             // row of T
-                    const int c = c0 + 2 * i + (int)rank;           // its chunk
+                    const int c = c0 + kSplit * i + (int)rank;      // its chunk
                     const int t = c * 32 + (tl & 31);               // its row in the stream
                     const bool live = t < nrows;
                     float v[32];
@@ -518,8 +555,8 @@ __global__ void __launch_bounds__(kThreads, 2)
         }
     }
 
-    // Every thread of both CTAs gets here (all waits are bounded): after this
-    // barrier neither CTA touches the other's shared memory again.
+    // Every thread of the cluster's CTAs gets here (all waits are bounded):
+    // after this barrier no CTA touches another's shared memory again.
     __syncwarp();
     tc_fence_before();
     cluster_sync_all();
@@ -627,13 +664,13 @@ int launch_kv_materialize(const KvMatArgs &a, cudaStream_t stream) {
         attr_set = true;
     }
     cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3((unsigned)(heads * 2));
+    cfg.gridDim = dim3((unsigned)(heads * kSplit));
     cfg.blockDim = dim3(kThreads);
     cfg.dynamicSmemBytes = kSmem;
     cfg.stream = stream;
     cudaLaunchAttribute attr[2];
     attr[0].id = cudaLaunchAttributeClusterDimension;
-    attr[0].val.clusterDim.x = 2;
+    attr[0].val.clusterDim.x = kSplit;
     attr[0].val.clusterDim.y = 1;
     attr[0].val.clusterDim.z = 1;
     attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
