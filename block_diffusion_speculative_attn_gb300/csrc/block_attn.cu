@@ -32,13 +32,17 @@
 //           unit's partials in tile order, as soon as each is published
 //           (128-row tile) or once the attention grid has finished.
 //
-// Inside a CTA (warp roles: 0-3 softmax + epilogue, 4 Q/K producer, 5 MMA
-// issuer + TMEM owner, 6 V producer):
+// Inside a CTA (warp roles: the softmax + epilogue warps -- four with the
+// 64-row tile, eight with the 128-row tile -- then the Q/K producer, the MMA
+// issuer + TMEM owner, the V producer and, with the fused append, the append
+// warp):
 //   * the G*B query rows (row m = i*G + g) form the A operand of a tcgen05 MMA
 //     tile: M = 64 when G*B <= 64, else M = 128 (zero rows pad it).  An M = 64
 //     accumulator spreads its rows over lanes 0-15 of all four TMEM lane
 //     quadrants, so all four SM sub-partitions run the softmax with two
-//     threads per row (16x32bx2 TMEM accesses); M = 128 has one thread per row;
+//     threads per row (16x32bx2 TMEM accesses); with M = 128 warps w and w + 4
+//     share lane quadrant w % 4 and take the two 64-column halves of a row,
+//     exchanging row maxima and sums through shared memory;
 //   * K and V tiles arrive by TMA, one box per page (or per 128 keys of a
 //     larger page), into 128-byte-swizzled shared memory, through a K ring and
 //     a deeper V ring fed by separate producer warps, with an L2 evict-first
@@ -72,10 +76,10 @@ constexpr uint32_t kTmemO = 256;          // S at columns 0 / 128, O at 256 / 38
 constexpr float kRescaleLog2 = 8.0f;      // rescale O only when the max grows by > 2^8
 constexpr float kLn2 = 0.6931471805599453f;
 
-// W8: the 128-row tile with eight softmax warps, two threads a row (the TREE
-// kernels: a large tree's row tiles read keys mostly from L2 and are bound by
-// the softmax's instruction issue, which one warp per SM sub-partition cannot
-// keep up with); otherwise four softmax warps.
+// W8: the 128-row tile with eight softmax warps, two threads a row: its
+// 128-column softmax is bound by instruction latency, which one warp per SM
+// sub-partition cannot hide (a large tree's row tiles, which read keys mostly
+// from L2, most of all); the 64-row tile keeps four softmax warps.
 template <int D, int M, bool W8 = false>
 struct Cfg {
     static_assert(!W8 || M == 128, "eight softmax warps only with the 128-row tile");
@@ -529,8 +533,8 @@ __device__ void append_piece_rows(const Params &prm, const AppendParams &app, co
 // kTree: the TREE mask (block keys by tree_mask bits), in an instantiation of
 // its own so that the DRAFT / VERIFY tile loop carries none of its code.
 template <int D, int M, bool kAppend, bool kTree>
-__global__ void __launch_bounds__(kAppend ? Cfg<D, M, kTree && M == 128>::kThreadsAppend
-                                          : Cfg<D, M, kTree && M == 128>::kThreads,
+__global__ void __launch_bounds__(kAppend ? Cfg<D, M, M == 128>::kThreadsAppend
+                                          : Cfg<D, M, M == 128>::kThreads,
                                   1)
     block_attn_kernel(const __grid_constant__ CUtensorMap tm_q,
                       const __grid_constant__ CUtensorMap tm_k,
@@ -538,7 +542,7 @@ __global__ void __launch_bounds__(kAppend ? Cfg<D, M, kTree && M == 128>::kThrea
                       const __grid_constant__ CUtensorMap tm_out,
                       const __grid_constant__ CUtensorMap tm_part, const Params prm,
                       const AppendParams app) {
-    constexpr bool W8 = kTree && M == 128;
+    constexpr bool W8 = M == 128;
     using C = Cfg<D, M, W8>;
     extern __shared__ uint8_t smem_raw[];
     const uint32_t raw = smem_u32(smem_raw);
@@ -1440,6 +1444,12 @@ __global__ void __launch_bounds__(kAppend ? Cfg<D, M, kTree && M == 128>::kThrea
                     }
                 } else {
                     l = (la.x + la.y) + (lb.x + lb.y);
+                    if constexpr (W8) {
+                        float o2;
+                        ok = pair_exchange(l, o2);
+                        if (!ok) break;
+                        l += o2;
+                    }
                 }
                 if constexpr (M == 64) l += __shfl_xor_sync(0xffffffffu, l, 16);
                 if constexpr (!kTree) lr = l;
@@ -1713,8 +1723,7 @@ cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t s
 
 template <int D, int M>
 int launch_impl(const AttnArgs &a, const AttnPlan &plan, cudaStream_t stream) {
-    using C = Cfg<D, M>;
-    using CT = Cfg<D, M, M == 128>;  // the TREE kernels' configuration
+    using C = Cfg<D, M, M == 128>;
     EncodeTiledFn enc = encode_fn();
     if (enc == nullptr) return BDSA_CUDA_ERROR;
     const int G = a.Hq / a.Hkv;
@@ -1837,8 +1846,8 @@ int launch_impl(const AttnArgs &a, const AttnPlan &plan, cudaStream_t stream) {
                        : (append ? block_attn_kernel<D, M, true, false>
                                  : block_attn_kernel<D, M, false, false>);
     const int inst = tree ? 2 : (append ? 1 : 0);
-    const int smem = tree ? CT::kSmem : C::kSmem;
-    const int threads = tree ? CT::kThreads : (append ? C::kThreadsAppend : C::kThreads);
+    const int smem = C::kSmem;
+    const int threads = append ? C::kThreadsAppend : C::kThreads;
     static bool attr_set[3] = {false, false, false};  // per instantiation
     if (!attr_set[inst]) {
         if (cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) !=
