@@ -41,12 +41,12 @@ from block_diffusion_speculative_attn_gb300 import workloads as wl  # noqa: E402
 METRIC = "draft/verify block-attn query tokens/s + % HBM roofline; accept rows/s"
 # DRAM bytes (read + write) of one attention call on the Qwen3-8B-shaped verify
 # batch, from one ncu capture (summary and commands in
-# profiles/qwen3_8b_verify_step_ncu.md): attention 308.43 MB read + 4.25 MB
+# profiles/qwen3_8b_verify_step_ncu.md): attention 308.42 MB read + 4.68 MB
 # written (the 64-row tile merges its cut units inside the launch: no merge
 # kernel).  Valid only for the kernel sources it was taken on: reported as
 # null once they change.
-ATTN_TRAFFIC = {"workload": "qwen3_8b_verify", "bytes_per_call": 312.68e6,
-                "sources_sha256": "2d783f2c4eda1d4c99fb7c9bbdf74c5144d1c848162679616a9dce4aefc51873"}
+ATTN_TRAFFIC = {"workload": "qwen3_8b_verify", "bytes_per_call": 313.10e6,
+                "sources_sha256": "81c362c40d38074c16e8d670cda0c2aac4f6ed022c7a874a0fe499d8e213814c"}
 ATTN_SOURCES = ("block_diffusion_speculative_attn_gb300/csrc/block_attn.cu",
                 "block_diffusion_speculative_attn_gb300/csrc/bdsa_device.cuh")
 L2_FLUSH_BYTES = 512 << 20  # > 129 MB L2
