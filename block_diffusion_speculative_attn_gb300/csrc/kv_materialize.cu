@@ -632,6 +632,22 @@ int launch_kv_materialize(const KvMatArgs &a, cudaStream_t stream) {
     if (!encode_rows(enc, &tm_w, a.w_kv, (uint64_t)heads * kD, (uint64_t)a.H, kD) ||
         !encode_rows(enc, &tm_x, xc, (uint64_t)a.bs * a.B, (uint64_t)a.H, kBox))
         return BDSA_CUDA_ERROR;
+    static bool attr_set = false;
+    if (!attr_set) {
+        // two CTAs an SM need the largest shared-memory carve-out
+        if (cudaFuncSetAttribute(kvmat_project_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 kSmem) != cudaSuccess ||
+            // the gather runs with the same carve-out, so that projection
+            // CTAs can start on SMs still running gather CTAs
+            cudaFuncSetAttribute(kvmat_gather_kernel,
+                                 cudaFuncAttributePreferredSharedMemoryCarveout,
+                                 cudaSharedmemCarveoutMaxShared) != cudaSuccess ||
+            cudaFuncSetAttribute(kvmat_project_kernel,
+                                 cudaFuncAttributePreferredSharedMemoryCarveout,
+                                 cudaSharedmemCarveoutMaxShared) != cudaSuccess)
+            return BDSA_CUDA_ERROR;
+        attr_set = true;
+    }
     kvmat_gather_kernel<<<dim3((unsigned)a.bs, kGatherParts), kGatherThreads, 0, stream>>>(
         reinterpret_cast<const uint4 *>(a.hidden), a.commit_len, a.positions, a.cache_loc, a.bs,
         a.B, a.H, a.max_pos, a.num_slots, count, meta, reinterpret_cast<uint4 *>(xc),
@@ -652,17 +668,6 @@ int launch_kv_materialize(const KvMatArgs &a, cudaStream_t stream) {
     P.max_pos = a.max_pos;
     P.eps = a.eps;
     P.dev_status = a.dev_status;
-    static bool attr_set = false;
-    if (!attr_set) {
-        // two CTAs an SM need the largest shared-memory carve-out
-        if (cudaFuncSetAttribute(kvmat_project_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                 kSmem) != cudaSuccess ||
-            cudaFuncSetAttribute(kvmat_project_kernel,
-                                 cudaFuncAttributePreferredSharedMemoryCarveout,
-                                 cudaSharedmemCarveoutMaxShared) != cudaSuccess)
-            return BDSA_CUDA_ERROR;
-        attr_set = true;
-    }
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3((unsigned)(heads * kSplit));
     cfg.blockDim = dim3(kThreads);

@@ -4,6 +4,12 @@
 // block starts with the last verified token, every other slot holds the mask
 // token, and positions / cache locations are prepared in the same kernel
 // instead of a chain of small eager ops.  One thread per (request, slot).
+//
+// Each kernel lets the next kernel on the stream launch at once (it is the
+// attention, launched with programmatic dependent launch, which waits for
+// this grid's writes before it reads its inputs), and asks for the shared
+// memory carve-out the attention runs with, so that the attention's CTAs can
+// start their prologue on SMs still running this grid.
 #include <cuda_runtime.h>
 
 #include "bdsa_device.cuh"
@@ -12,6 +18,12 @@
 namespace bdsa {
 namespace {
 
+template <typename K>
+bool prefer_max_shared(K *kernel) {
+    return cudaFuncSetAttribute(kernel, cudaFuncAttributePreferredSharedMemoryCarveout,
+                                cudaSharedmemCarveoutMaxShared) == cudaSuccess;
+}
+
 __global__ void __launch_bounds__(256)
     prepare_block_kernel(const int32_t *__restrict__ verified_id,
                          const int32_t *__restrict__ seq_lens,
@@ -19,6 +31,7 @@ __global__ void __launch_bounds__(256)
                          int bs, int B, int page_size, int mask_token_id,
                          int32_t *__restrict__ block_ids, int32_t *__restrict__ positions,
                          int32_t *__restrict__ cache_loc, int32_t *dev_status) {
+    grid_launch_dependents();
     const long idx = (long)blockIdx.x * blockDim.x + threadIdx.x;
     if (idx >= (long)bs * B) return;
     const int r = (int)(idx / B), i = (int)(idx % B);
@@ -46,6 +59,7 @@ __global__ void __launch_bounds__(256)
                         int bs, int N, int page_size, int mask_token_id,
                         int32_t *__restrict__ block_ids, int32_t *__restrict__ positions,
                         int32_t *__restrict__ cache_loc, int32_t *dev_status) {
+    grid_launch_dependents();
     const int blk = 2 * N - 1;
     const long idx = (long)blockIdx.x * blockDim.x + threadIdx.x;
     if (idx >= (long)bs * blk) return;
@@ -80,6 +94,7 @@ __global__ void __launch_bounds__(256)
                         int bs, int B, int page_size, int32_t *__restrict__ depth,
                         int32_t *__restrict__ positions, int32_t *__restrict__ cache_loc,
                         uint64_t *__restrict__ tree_mask, int32_t *dev_status) {
+    grid_launch_dependents();
     const long idx = (long)blockIdx.x * blockDim.x + threadIdx.x;
     if (idx >= (long)bs * B) return;
     const int r = (int)(idx / B), i = (int)(idx % B);
@@ -130,6 +145,8 @@ int launch_idlm_prepare(const int32_t *pending, const int32_t *specs, const int3
                         int32_t *dev_status, cudaStream_t stream) {
     const long n = (long)bs * (2 * N - 1);
     if (n == 0) return BDSA_OK;
+    static const bool carve = prefer_max_shared(idlm_prepare_kernel);
+    if (!carve) return BDSA_CUDA_ERROR;
     const unsigned grid = (unsigned)((n + 255) / 256);
     idlm_prepare_kernel<<<grid, 256, 0, stream>>>(pending, specs, mode, seq_lens, block_table,
                                                   max_pages, num_pages, bs, N, page_size,
@@ -144,6 +161,8 @@ int launch_tree_prepare(const int32_t *parent, const int32_t *seq_lens, const in
                         uint64_t *tree_mask, int32_t *dev_status, cudaStream_t stream) {
     const long n = (long)bs * B;
     if (n == 0) return BDSA_OK;
+    static const bool carve = prefer_max_shared(tree_prepare_kernel);
+    if (!carve) return BDSA_CUDA_ERROR;
     tree_prepare_kernel<<<(unsigned)((n + 255) / 256), 256, 0, stream>>>(
         parent, seq_lens, block_table, max_pages, num_pages, bs, B, page_size, depth, positions,
         cache_loc, tree_mask, dev_status);
@@ -157,6 +176,8 @@ int launch_prepare_block(const int32_t *verified_id, const int32_t *seq_lens,
                          cudaStream_t stream) {
     const long n = (long)bs * B;
     if (n == 0) return BDSA_OK;
+    static const bool carve = prefer_max_shared(prepare_block_kernel);
+    if (!carve) return BDSA_CUDA_ERROR;
     const unsigned grid = (unsigned)((n + 255) / 256);
     prepare_block_kernel<<<grid, 256, 0, stream>>>(verified_id, seq_lens, block_table, max_pages,
                                                    num_pages, bs, B, page_size, mask_token_id,
