@@ -45,8 +45,8 @@ METRIC = "draft/verify block-attn query tokens/s + % HBM roofline; accept rows/s
 # written (the 64-row tile merges its cut units inside the launch: no merge
 # kernel).  Valid only for the kernel sources it was taken on: reported as
 # null once they change.
-ATTN_TRAFFIC = {"workload": "qwen3_8b_verify", "bytes_per_call": 313.10e6,
-                "sources_sha256": "81c362c40d38074c16e8d670cda0c2aac4f6ed022c7a874a0fe499d8e213814c"}
+ATTN_TRAFFIC = {"workload": "qwen3_8b_verify", "bytes_per_call": 313.17e6,
+                "sources_sha256": "3e84ac207984b46a09f45584800706c83a3231a998533581fc2b76589f0eea70"}
 ATTN_SOURCES = ("block_diffusion_speculative_attn_gb300/csrc/block_attn.cu",
                 "block_diffusion_speculative_attn_gb300/csrc/bdsa_device.cuh")
 L2_FLUSH_BYTES = 512 << 20  # > 129 MB L2
@@ -952,7 +952,9 @@ def main(argv=None):
         achieved = abytes / (attn_ms / 1e3) / 1e9
         roof = {"bound": "hbm", "achieved": achieved, "peak": hbm, "unit": "GB/s",
                 "frac": achieved / hbm, "traffic": attn_traffic(cfg.name),
-                "kernel": "block_attn_paged (attention + split-KV combine launch)",
+                "kernel": ("block_attn_paged (one launch: the owner CTA of each cut unit "
+                           "merges it)" if (cfg.Hq // cfg.Hkv) * cfg.B <= 64 else
+                           "block_attn_paged (attention + split-KV merge launch)"),
                 "algorithmic_bytes_per_launch": abytes, "peak_source": peak_src,
                 "launch_ms": attn_ms}
 
