@@ -365,12 +365,18 @@ __device__ int resolve_draw(const PT &P, const float *prow, const float *qrow, f
         s_last_pos = -1;
     }
     __syncthreads();
-    float2 wexcl = make_float2(0.f, 0.f), S = make_float2(0.f, 0.f);
+    // the warps' offsets and the grand total: every warp scans the eight
+    // warp totals in its lanes 0-7 (three dependent float-float additions
+    // where a loop over the warps took sixteen)
+    float2 wt = lane < kWarps ? s_wtot[lane] : make_float2(0.f, 0.f);
 #pragma unroll
-    for (int w = 0; w < kWarps; ++w) {
-        if (w < warp) wexcl = ff_add(wexcl, s_wtot[w]);
-        S = ff_add(S, s_wtot[w]);
+    for (int o = 1; o < kWarps; o <<= 1) {
+        const float2 t = shfl_up_ff(wt, o);
+        if (lane >= o) wt = ff_add(wt, t);
     }
+    const float2 S = shfl_ff(wt, kWarps - 1);
+    float2 wexcl = shfl_ff(wt, warp > 0 ? warp - 1 : 0);
+    if (warp == 0) wexcl = make_float2(0.f, 0.f);
     float2 excl = shfl_up_ff(inc, 1);
     if (lane == 0) excl = make_float2(0.f, 0.f);
     excl = ff_add(excl, wexcl);
