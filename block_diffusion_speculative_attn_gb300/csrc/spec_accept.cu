@@ -1008,7 +1008,8 @@ int launch_idlm_accept(const IdlmArgs &a, cudaStream_t stream) {
     if (a.bs == 0) return BDSA_OK;
     // Many (row, draw) clusters of a round find nothing to draw and exit: the
     // chunks are sized for about eight CTAs an SM over all of them (against
-    // four: 36.8 -> 30.7 us at 32 requests, N = 8, V = 151936).
+    // four: 36.8 -> 30.7 us at 32 requests, N = 8, V = 151936, five chunks a
+    // row; eight, ten and sixteen chunks a row measured slower).
     const AcceptPlan plan = accept_plan(a.bs * a.N, 2 * a.N - 1, a.V, 4 * a.num_sms);
     if (!plan.cluster) return BDSA_UNSUPPORTED;
     IdlmParams P;
