@@ -46,7 +46,7 @@ METRIC = "draft/verify block-attn query tokens/s + % HBM roofline; accept rows/s
 # kernel).  Valid only for the kernel sources it was taken on: reported as
 # null once they change.
 ATTN_TRAFFIC = {"workload": "qwen3_8b_verify", "bytes_per_call": 313.17e6,
-                "sources_sha256": "3e84ac207984b46a09f45584800706c83a3231a998533581fc2b76589f0eea70"}
+                "sources_sha256": "c6395c7cd9846a4ab5a3a704640ce68a53e8467674b45c6ec1b8c718bc5099a0"}
 ATTN_SOURCES = ("block_diffusion_speculative_attn_gb300/csrc/block_attn.cu",
                 "block_diffusion_speculative_attn_gb300/csrc/bdsa_device.cuh")
 L2_FLUSH_BYTES = 512 << 20  # > 129 MB L2
@@ -235,11 +235,9 @@ class Step:
             self.acc_out["out_tokens"] = torch.empty((bs, B), dtype=torch.int32, device=device)
             aws = bdsa.spec_accept_workspace_bytes(bs, B, cfg.V)
             self.acc_ws = torch.empty(max(aws, 256), dtype=torch.uint8, device=device)
-        # kernels of ours per step: prepare, per pass the attention (plus the
-        # merge launch for the 128-row tile; the 64-row tile merges cut units
-        # inside the attention launch), accept
-        attn_launches = 1 if (cfg.Hq // cfg.Hkv) * B <= 64 else 2
-        self.launches = 1 + len(cfg.modes) * attn_launches + (1 if cfg.V else 0)
+        # kernels of ours per step: prepare, per pass the attention (cut units
+        # are merged by their owner CTA inside the attention launch), accept
+        self.launches = 1 + len(cfg.modes) + (1 if cfg.V else 0)
 
     def prepare(self):
         c = self.cfg
@@ -952,9 +950,8 @@ def main(argv=None):
         achieved = abytes / (attn_ms / 1e3) / 1e9
         roof = {"bound": "hbm", "achieved": achieved, "peak": hbm, "unit": "GB/s",
                 "frac": achieved / hbm, "traffic": attn_traffic(cfg.name),
-                "kernel": ("block_attn_paged (one launch: the owner CTA of each cut unit "
-                           "merges it)" if (cfg.Hq // cfg.Hkv) * cfg.B <= 64 else
-                           "block_attn_paged (attention + split-KV merge launch)"),
+                "kernel": "block_attn_paged (one launch: the owner CTA of each cut unit "
+                          "merges it)",
                 "algorithmic_bytes_per_launch": abytes, "peak_source": peak_src,
                 "launch_ms": attn_ms}
 

@@ -21,16 +21,17 @@
 //           CTAs leaves an fp32 partial (o / l and log2-sum-exp) in one of each
 //           CTA's two slots.  The softmax warps check every page id a piece
 //           references; a unit that references one outside the pool is written
-//           as zeros (lse -inf) and reported.  With the 64-row tile (and a
-//           grid no larger than the device), a cut unit's pieces other than
-//           its first are each the first piece of a later CTA and are
-//           published early (a ready word carrying the call's ticket); the
-//           CTA holding the first piece -- its last piece -- merges them into
-//           its own before writing the unit's output, so no second launch;
-//   merge   otherwise (the 128-row tile, or a grid larger than the device):
-//           one CTA per range boundary that is a unit's first cut merges the
-//           unit's partials in tile order, as soon as each is published
-//           (128-row tile) or once the attention grid has finished.
+//           as zeros (lse -inf) and reported.  With a grid no larger than the
+//           device (and not a TREE call with the 128-row tile), a cut unit's
+//           pieces other than its first are each the first piece of a later
+//           CTA and are published early (a ready word carrying the call's
+//           ticket); the CTA holding the first piece -- its last piece --
+//           merges them into its own before writing the unit's output, so no
+//           second launch;
+//   merge   otherwise (TREE calls with the 128-row tile, or a grid larger than
+//           the device): one CTA per range boundary that is a unit's first cut
+//           merges the unit's partials in tile order, as soon as each is
+//           published (128-row tile) or once the attention grid has finished.
 //
 // Inside a CTA (warp roles: the softmax + epilogue warps -- four with the
 // 64-row tile, eight with the 128-row tile -- then the Q/K producer, the MMA
@@ -134,7 +135,7 @@ struct Cfg {
     // every softmax warp has fenced its stores of a partial piece; one phase
     // per partial piece, waited by thread 0 alone before it publishes the slot
     static constexpr int PB = DR + 1;
-    // owner merge (M = 64): every softmax warp has read the other pieces'
+    // owner merge: every softmax warp has read the other pieces'
     // ready words; waited by thread 0 alone before it resets them
     static constexpr int MR = PB + 1;
     // W8: the two warps sharing a TMEM lane quadrant have written their halves
@@ -163,7 +164,7 @@ struct Params {
     uint64_t owner_ticket;   // the ticket the owner merge waits for (= ticket; see
                              // expire_owner_waits)
     int early_merge;         // M = 128: partials are published, the merge starts on them
-    int owner_merge;         // M = 64: the CTA holding a cut unit's first tile merges it
+    int owner_merge;         // the CTA holding a cut unit's first tile merges it
     uint16_t *out;
     float *lse;
     const uint64_t *tree_mask;  // TREE mode: [bs * B, mask_words] block keys visible to each row
@@ -544,6 +545,9 @@ __global__ void __launch_bounds__(kAppend ? Cfg<D, M, M == 128>::kThreadsAppend
                       const AppendParams app) {
     constexpr bool W8 = M == 128;
     using C = Cfg<D, M, W8>;
+    // the owner merge is compiled into every instantiation but the 128-row
+    // TREE one, whose latency-bound softmax measured 5 % slower with it in
+    constexpr bool kOwner = M == 64 || !kTree;
     extern __shared__ uint8_t smem_raw[];
     const uint32_t raw = smem_u32(smem_raw);
     const uint32_t sbase = (raw + 1023u) & ~1023u;
@@ -888,8 +892,8 @@ __global__ void __launch_bounds__(kAppend ? Cfg<D, M, M == 128>::kThreadsAppend
         bool valid_row = row < prm.rows;
         const int i_blk = row / G;  // node within the row tile
         // A piece's output: O from TMEM scaled by 1/l, to `out` (bf16) when the
-        // piece is the whole unit (or, M = 64, the owner of a cut unit, which
-        // first merges the unit's other pieces into madd), else to the CTA's
+        // piece is the whole unit (or the owner of a cut unit, which first
+        // merges the unit's other pieces into madd), else to the CTA's
         // partial slot (fp32).
         struct Epi {
             long lastg, orow;
@@ -897,7 +901,7 @@ __global__ void __launch_bounds__(kAppend ? Cfg<D, M, M == 128>::kThreadsAppend
             int ob, slot, r, h, k;
             bool complete, owner, bad;
         };
-        // Owner merge (M = 64): the other pieces' share of this thread's output
+        // Owner merge: the other pieces' share of this thread's output
         // columns, added to O * inv_l by the epilogue (zero for other pieces).
         float madd[OC];
         // M = 64: a piece's tile store reads the P buffers after the epilogue
@@ -1036,10 +1040,10 @@ __global__ void __launch_bounds__(kAppend ? Cfg<D, M, M == 128>::kThreadsAppend
                     // a piece the owner merges: published with direct stores below
                     store_partial_direct();
                 }
-            } else if (e.complete) {
-                // M = 128: one thread per row stores its row directly, 32 bytes
-                // a lane per instruction (whole sectors; out when it is 32-byte
-                // aligned).
+            } else if (fin) {
+                // M = 128: each thread stores its share of its row directly, 32
+                // bytes a lane per instruction (whole sectors; out when it is
+                // 32-byte aligned), the owner's the whole cut unit's
 #pragma unroll
                 for (int c = 0; c < OC / 32; ++c) {
                     float v32[32];
@@ -1047,9 +1051,17 @@ __global__ void __launch_bounds__(kAppend ? Cfg<D, M, M == 128>::kThreadsAppend
                     if (!valid_row) continue;
                     const int col0 = half * OC + c * 32;
                     uint32_t w[16];
+                    if constexpr (kOwner) {
+                        const float *ad = madd + c * 32;
 #pragma unroll
-                    for (int v = 0; v < 16; ++v)
-                        w[v] = pack_bf16x2(v32[2 * v] * sc, v32[2 * v + 1] * sc);
+                        for (int v = 0; v < 16; ++v)
+                            w[v] = pack_bf16x2(fmaf(v32[2 * v], sc, ad[2 * v]),
+                                               fmaf(v32[2 * v + 1], sc, ad[2 * v + 1]));
+                    } else {
+#pragma unroll
+                        for (int v = 0; v < 16; ++v)
+                            w[v] = pack_bf16x2(v32[2 * v] * sc, v32[2 * v + 1] * sc);
+                    }
                     uint16_t *dst = prm.out + e.orow * D + col0;
                     if (prm.out_v8) {
                         st_global_v8(dst, w[0], w[1], w[2], w[3], w[4], w[5], w[6], w[7]);
@@ -1083,11 +1095,11 @@ __global__ void __launch_bounds__(kAppend ? Cfg<D, M, M == 128>::kThreadsAppend
                 // its stores of it (the arrival releases them at CTA scope),
                 // thread 0 writes this call's ticket into the slot's ready word
                 // with a GPU-scope release, which carries those stores with it;
-                // the merge kernel (M = 128) or the owner CTA (M = 64) may read
-                // the slot once it acquires the word.  Only thread 0 waits, and
-                // boundedly.  (Without the owner merge, M = 64 stores its
-                // partials with TMA tile stores, and its merge kernel waits for
-                // the whole attention grid.)
+                // the owner CTA, or the merge kernel (M = 128 without the owner
+                // merge), may read the slot once it acquires the word.  Only
+                // thread 0 waits, and boundedly.  (Without the owner merge,
+                // M = 64 stores its partials with TMA tile stores, and its
+                // merge kernel waits for the whole attention grid.)
                 __syncwarp();
                 if (lane == 0) mbar_arrive(bar(C::PB));
                 if (tid == 0) {
@@ -1098,7 +1110,7 @@ __global__ void __launch_bounds__(kAppend ? Cfg<D, M, M == 128>::kThreadsAppend
             }
             return true;
         };
-        // Owner merge (M = 64): before the epilogue of the piece holding a cut
+        // Owner merge: before the epilogue of the piece holding a cut
         // unit's first tile -- always the last piece of this CTA -- fold in
         // the unit's other pieces.  Each is the first piece of a later CTA
         // (slot 2 * bb), published with a ready word carrying this call's
@@ -1456,7 +1468,7 @@ __global__ void __launch_bounds__(kAppend ? Cfg<D, M, M == 128>::kThreadsAppend
                 e.inv_l = lr > 0.f ? 1.f / lr : 0.f;
                 e.lse2 = l > 0.f ? m_used + log2f(l) : -INFINITY;
                 e.complete = pc.a == 0 && pc.e == pc.nt;
-                e.owner = M == 64 && prm.owner_merge && pc.a == 0 && pc.e < pc.nt;
+                e.owner = kOwner && prm.owner_merge && pc.a == 0 && pc.e < pc.nt;
                 // every warp checked every page of the piece
                 e.bad = shape_bad || __any_sync(0xffffffffu, page_bad);
                 e.orow = ((long)rr * B + node) * prm.Hq + (long)pc.h * G + row % G;
@@ -1465,7 +1477,7 @@ __global__ void __launch_bounds__(kAppend ? Cfg<D, M, M == 128>::kThreadsAppend
                 e.h = pc.h;
                 e.k = k;
                 if (e.bad && tid == 0) report_status(prm.dev_status, BDSA_DEVICE_OUT_OF_RANGE);
-                if constexpr (M == 64) {
+                if constexpr (kOwner) {
                     if (e.owner) {
                         ok = owner_gather(e, pc, lr);
                         if (!ok) break;
@@ -1798,11 +1810,15 @@ int launch_impl(const AttnArgs &a, const AttnPlan &plan, cudaStream_t stream) {
     cudaStreamCaptureStatus cap = cudaStreamCaptureStatusNone;
     if (cudaStreamIsCapturing(stream, &cap) != cudaSuccess) return BDSA_CUDA_ERROR;
     prm.early_merge = M == 128 && cap == cudaStreamCaptureStatusNone;
-    // M = 64: the owner of each cut unit merges it inside the attention launch.
-    // Its wait needs every CTA of the grid resident at once, so only a grid of
-    // at most one CTA per SM takes this path; a larger one (a caller's num_sms
-    // above the device's) keeps the separate merge launch.
-    prm.owner_merge = M == 64 && plan.grid <= device_num_sms(0);
+    // The owner of each cut unit merges it inside the attention launch.  Its
+    // wait needs every CTA of the grid resident at once, so only a grid of at
+    // most one CTA per SM takes this path; a larger one (a caller's num_sms
+    // above the device's) keeps the separate merge launch, and so do TREE
+    // calls with the 128-row tile: against the merge launch the owner merge
+    // took the Qwen3-8B-shaped verify call 66.2 -> 63.6 us (64-row tile), the
+    // LLaDA2.0-style draft 121.4 -> 109.1 us and long-context verify 338.6 ->
+    // 330.8 us (128-row tile), but 481-node trees 1052 -> 1110 us.
+    prm.owner_merge = plan.grid <= device_num_sms(0) && (M == 64 || a.mode != BDSA_MODE_TREE);
     prm.out = a.out;
     prm.out_v8 = (reinterpret_cast<uintptr_t>(a.out) & 31) == 0;
     prm.lse = a.lse;
