@@ -238,13 +238,15 @@ def test_output_16_byte_aligned_only(dev, sms):
     assert torch.equal(out.view(torch.int16), ref.view(torch.int16))
 
 
-@pytest.mark.parametrize("shape_i,sms", [(2, FORCE_SPLIT), (1, OWNER)],
-                         ids=["rows128_merge_launch", "rows64_owner_merge"])
+@pytest.mark.parametrize("shape_i,sms", [(2, FORCE_SPLIT), (1, OWNER), (2, OWNER)],
+                         ids=["rows128_merge_launch", "rows64_owner_merge",
+                              "rows128_owner_merge"])
 def test_split_partials_reuse_a_dirty_workspace(dev, shape_i, sms):
     """Split-KV partials are published through ready words in the workspace
-    (to the merge launch for the 128-row tile, to the owner CTA for the 64-row
-    one): calls that reuse one workspace (left by an earlier call, or filled
-    with arbitrary bytes) on different inputs each match the oracle."""
+    (to the merge launch when the grid is larger than the device, else to the
+    owner CTA, for both tiles): calls that reuse one workspace (left by an
+    earlier call, or filled with arbitrary bytes) on different inputs each
+    match the oracle."""
     import block_diffusion_speculative_attn_gb300 as bdsa
     name, Hq, Hkv, D, B, ps, lens = SHAPES[shape_i]
     ws_bytes = 0
@@ -271,14 +273,15 @@ def test_split_partials_reuse_a_dirty_workspace(dev, shape_i, sms):
             assert_attn_close(out, ref, lse, ref_lse, tag=f"reuse {rep} seed {cfg.seed}")
 
 
-@pytest.mark.parametrize("shape_i,sms", [(2, FORCE_SPLIT), (1, OWNER)],
-                         ids=["rows128_merge_launch", "rows64_owner_merge"])
+@pytest.mark.parametrize("shape_i,sms", [(2, FORCE_SPLIT), (1, OWNER), (2, OWNER)],
+                         ids=["rows128_merge_launch", "rows64_owner_merge",
+                              "rows128_owner_merge"])
 def test_cuda_graph_replays_with_new_inputs(dev, shape_i, sms):
     """The attention call captured into a CUDA graph (units split, so partials
-    and their merge are exercised: by the merge launch for the 128-row tile,
-    by the owner CTA for the 64-row one, whose ready words must not carry over
-    from one replay to the next) replays correctly when new inputs are copied
-    into the captured buffers between replays."""
+    and their merge are exercised: by the merge launch for a grid larger than
+    the device, by the owner CTA otherwise, whose ready words must not carry
+    over from one replay to the next) replays correctly when new inputs are
+    copied into the captured buffers between replays."""
     import block_diffusion_speculative_attn_gb300 as bdsa
     name, Hq, Hkv, D, B, ps, lens = SHAPES[shape_i]
     inps = [wl.make_attn_inputs(_cfg(name, len(lens), Hq, Hkv, D, B, ps, lens, seed=s),
