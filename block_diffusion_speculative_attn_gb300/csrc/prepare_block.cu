@@ -33,6 +33,14 @@ __global__ void __launch_bounds__(256)
                          int32_t *__restrict__ cache_loc, int32_t *dev_status) {
     grid_launch_dependents();
     const long idx = (long)blockIdx.x * blockDim.x + threadIdx.x;
+    // Pull the block table into L2 (one 128-byte line a thread, up to 2^16
+    // entries), so that the attention that follows finds its first page ids
+    // there: they are on its critical path, right after its schedule (the
+    // Qwen3-8B-shaped verify call measured 64.2 -> 64.0 us, A/B means).  Here
+    // the prefetches compete with nothing on that path.
+    const long lines = ((long)bs * max_pages + 31) / 32;
+    if (idx < lines && idx < 2048)
+        asm volatile("prefetch.global.L2 [%0];" ::"l"(block_table + idx * 32));
     if (idx >= (long)bs * B) return;
     const int r = (int)(idx / B), i = (int)(idx % B);
     const int L = seq_lens[r];
