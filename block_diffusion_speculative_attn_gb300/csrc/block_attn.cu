@@ -182,6 +182,7 @@ struct Params {
     int bs_v, n_rt, npt, hu;
     int mask_words;          // TREE: 64-bit words of a node's ancestor-or-self set
     int out_v8;              // out is 32-byte aligned: the M = 128 epilogue stores 32 bytes
+    int unit_cost;           // virtual tiles a unit switch is charged in the schedule
     float scale_log2;
 };
 
@@ -321,15 +322,13 @@ template <bool kRT>
 __device__ __forceinline__ int vreq_units(const Params &prm) { return kRT ? prm.hu : prm.Hkv; }
 
 // Schedule.  Units (request, KV head) are concatenated in order; each unit is
-// kUnitCost "virtual" tiles followed by its real tiles, and CTA b takes the
-// cost range [b * Wc / S, (b + 1) * Wc / S).  The virtual tiles carry no work:
-// they charge every unit switch (a Q load, an epilogue, a ragged last tile)
-// about the time of kUnitCost tiles, so a CTA that touches more units gets
-// fewer tiles.  Two tiles per switch: per-CTA end times regressed on the
-// schedule (traced) put a switch at one to two tiles, and two measured best.
-// The real tiles inside a CTA's cost range form its range [x0, x1) of global
-// tile indices.
-constexpr int kUnitCost = 2;
+// prm.unit_cost "virtual" tiles followed by its real tiles, and CTA b takes
+// the cost range [b * Wc / S, (b + 1) * Wc / S).  The virtual tiles carry no
+// work: they charge every unit switch (a Q load, an epilogue, a ragged last
+// tile) about the time of unit_cost tiles, so a CTA that touches more units
+// gets fewer tiles.  The real tiles inside a CTA's cost range form its range
+// [x0, x1) of global tile indices.  The host picks the cost per call (see
+// unit_cost_for).
 
 // Schedule state (shared memory).
 struct Sched {
@@ -414,13 +413,14 @@ __device__ void schedule(const Params &prm, int b, int S, Sched *sch) {
         T += v;
     }
     const long long Hkv = vreq_units<kRT>(prm);  // units a virtual request
-    const long long W = Hkv * T, Wc = Hkv * (T + (long long)kUnitCost * bs);
+    const long long uc = prm.unit_cost;
+    const long long W = Hkv * T, Wc = Hkv * (T + uc * bs);
     const long long c0 = range_start(b, Wc, S, prm.magic_S);
     const long long c1 = range_start(b + 1, Wc, S, prm.magic_S);
     const long long pre = wex + inc - sum;  // tiles before request i0
-    // cost offset of request i: Hkv * (tiles before it + kUnitCost * i)
-    const long long clo = Hkv * (pre + (long long)kUnitCost * i0);
-    const long long chi = Hkv * (pre + sum + (long long)kUnitCost * i1);
+    // cost offset of request i: Hkv * (tiles before it + unit_cost * i)
+    const long long clo = Hkv * (pre + uc * i0);
+    const long long chi = Hkv * (pre + sum + uc * i1);
     for (int which = 0; which < 2; ++which) {
         const long long c = which == 0 ? c0 : c1;
         if (!(c < Wc && clo <= c && c < chi)) continue;
@@ -428,13 +428,13 @@ __device__ void schedule(const Params &prm, int b, int S, Sched *sch) {
         for (int i = i0; i < i1; ++i) {
             const int L = vreq_L<kRT>(prm, i);
             const int nt = tiles_of_keys(vreq_keys<kRT>(prm, i, L));
-            const long long ci = Hkv * (tp + (long long)kUnitCost * i);
-            const long long span = nt + kUnitCost;  // cost of one unit of request i
+            const long long ci = Hkv * (tp + uc * i);
+            const long long span = nt + uc;  // cost of one unit of request i
             if (c < ci + Hkv * span) {
                 const int h = (int)((c - ci) / span);
                 const long long pos = (c - ci) - h * span;
                 const long long u_off = Hkv * tp + (long long)h * nt;
-                const long long x = u_off + max(0LL, pos - kUnitCost);
+                const long long x = u_off + max(0LL, pos - uc);
                 if (which == 0) {
                     sch->r0 = i;
                     sch->u0 = h;
@@ -1124,8 +1124,8 @@ __global__ void __launch_bounds__(kAppend ? Cfg<D, M, M == 128>::kThreadsAppend
         auto owner_gather = [&](Epi &e, const Piece &pc, float lr) -> bool {
             const long long cu =
                 (long long)pc.u_off +
-                (long long)kUnitCost * ((long long)pc.r * vreq_units<kTree>(prm) + pc.u);
-            const long long last = cu + kUnitCost + pc.nt - 1;  // cost of the unit's last tile
+                (long long)prm.unit_cost * ((long long)pc.r * vreq_units<kTree>(prm) + pc.u);
+            const long long last = cu + prm.unit_cost + pc.nt - 1;  // cost of the unit's last tile
             const long long Wc = sch->Wc;
             float m_run = e.lse2;
             float s_own = m_run == -INFINITY ? 0.f : 1.f;
@@ -1543,14 +1543,14 @@ __global__ void __launch_bounds__(kMergeThreads, 4) attn_merge_kernel(const Para
     const long u_off = sch.u_off0, cu = sch.cu0;
     // the cut at this CTA's start splits the unit's tiles, and CTA b - 1 holds
     // the unit's first tile (so this is the unit's first cut)
-    if (!(u_off < x0 && range_start(b - 1, Wc, S, prm.magic_S) <= cu + kUnitCost)) {
+    if (!(u_off < x0 && range_start(b - 1, Wc, S, prm.magic_S) <= cu + prm.unit_cost)) {
         if (hold) grid_dependency_wait();
         return;
     }
     const int rv = sch.r0, h = vreq_h0<kRT>(prm, rv) + sch.u0;
     const int r = vreq_r<kRT>(prm, rv), node0 = vreq_node0<kRT>(prm, rv);
-    const int b_first = cta_of(cu + kUnitCost, Wc, S);
-    const int b_last = cta_of(cu + kUnitCost + sch.nt0 - 1, Wc, S);
+    const int b_first = cta_of(cu + prm.unit_cost, Wc, S);
+    const int b_last = cta_of(cu + prm.unit_cost + sch.nt0 - 1, Wc, S);
     // Partial slots of the unit's pieces, in tile order.  Every CTA from
     // b_first to b_last with a non-empty cost range holds one; it is that
     // CTA's first piece (slot 2bb) unless tiles of an earlier unit precede it
@@ -1729,6 +1729,17 @@ cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t s
     return cudaLaunchKernelEx(&cfg, kernel, std::forward<Args>(args)...);
 }
 
+// Virtual tiles a unit switch costs in the schedule (A/B over the bench's
+// workloads against the cost two, which every tile size had before): three
+// for the DRAFT / VERIFY tiles (Qwen3-8B-shaped verify call 64.5 -> 63.7 us,
+// long-context verify 331.2 -> 330.0 us, LLaDA2.0-style draft and Uno within
+// noise) and four for TREE calls, whose units are short row tiles (481-node
+// trees 1053 -> 994 us; three: 1009, five: 998).
+int unit_cost_for(int M, bool tree) {
+    (void)M;
+    return tree ? 4 : 3;
+}
+
 template <int D, int M>
 int launch_impl(const AttnArgs &a, const AttnPlan &plan, cudaStream_t stream) {
     using C = Cfg<D, M, M == 128>;
@@ -1847,6 +1858,7 @@ int launch_impl(const AttnArgs &a, const AttnPlan &plan, cudaStream_t stream) {
     prm.mode = a.mode;
     prm.scale_log2 = a.scale * 1.4426950408889634f;
     prm.magic_S = UINT64_MAX / (uint64_t)plan.grid;
+    prm.unit_cost = unit_cost_for(M, n_rt > 1 || a.mode == BDSA_MODE_TREE);
     AppendParams app;
     app.k_new = a.k_new;
     app.v_new = a.v_new;
