@@ -45,8 +45,8 @@ METRIC = "draft/verify block-attn query tokens/s + % HBM roofline; accept rows/s
 # written (the 64-row tile merges its cut units inside the launch: no merge
 # kernel).  Valid only for the kernel sources it was taken on: reported as
 # null once they change.
-ATTN_TRAFFIC = {"workload": "qwen3_8b_verify", "bytes_per_call": 313.17e6,
-                "sources_sha256": "c6395c7cd9846a4ab5a3a704640ce68a53e8467674b45c6ec1b8c718bc5099a0"}
+ATTN_TRAFFIC = {"workload": "qwen3_8b_verify", "bytes_per_call": 313.04e6,
+                "sources_sha256": "52d7a751db9005cea75463ba2c2cf87513cdeffcd4728d33e99fa757d08b8217"}
 ATTN_SOURCES = ("block_diffusion_speculative_attn_gb300/csrc/block_attn.cu",
                 "block_diffusion_speculative_attn_gb300/csrc/bdsa_device.cuh")
 L2_FLUSH_BYTES = 512 << 20  # > 129 MB L2
