@@ -124,9 +124,12 @@ int32_t bdsa_prepare_block(const int32_t *verified_id, const int32_t *seq_lens,
  * num_sms  number of persistent CTAs (0: the current device's SM count).
  * Schedule: one persistent CTA per SM takes an equal share of the concatenated
  * (request, KV head, 128-key tile) sequence, which each CTA derives from
- * seq_lens itself; a (request, KV head) unit cut between CTAs leaves partials
- * that a second kernel merges.  Two launches per call, chained with
- * programmatic dependent launch (no CTA waits for another).
+ * seq_lens itself; a (request, KV head) unit cut between CTAs leaves partials.
+ * With num_sms at most the device's SM count (every CTA resident at once) the
+ * CTA holding a cut unit's first tile waits, boundedly, for the unit's other
+ * partials and merges them: one launch per call.  With more CTAs than SMs a
+ * second kernel merges them: two launches, chained with programmatic
+ * dependent launch (no CTA of the first waits for another).
  * Pages: a request with L_r < 0, with L_r + B needing more pages than
  * max_pages_per_req, or with a page id it references (pages 0 ..
  * ceil((L_r+B)/ps) - 1 of its row) outside [0, num_pages) gets out = 0 and
@@ -405,7 +408,7 @@ int32_t bdsa_idlm_accept(const int32_t *block_ids, const int32_t *mode, const fl
  * aligned (the gathered rows: a count, (slot, position) per row and a dense
  * copy of each committed hidden row); no initialisation needed.
  * Launches: a gather kernel (four CTAs per request) and a projection kernel of
- * n_layers * 2 * Hkv CTA pairs (thread-block clusters of 2 that split the
+ * n_layers * 2 * Hkv thread-block clusters of 3 CTAs (the three split the
  * hidden dimension), chained with programmatic dependent launch.
  */
 size_t bdsa_kv_materialize_workspace_bytes(int32_t bs, int32_t B, int32_t H);
@@ -450,7 +453,9 @@ int32_t bdsa_kv_materialize(const bdsa_bf16 *hidden, const int32_t *commit_len,
  *   of one KV head are processed in 128-row tiles of floor(128 / G) whole
  *   nodes (one tile of G * B rows when G * B <= 128), each over the context
  *   and the block keys up to its last node; the workspace holds partials of
- *   those tiles.
+ *   those tiles.  With 128-row tiles the cut units are merged by a second
+ *   launch (two launches per call); with a 64-row tile (G * B <= 64) as in
+ *   bdsa_block_attn_paged.
  *
  * bdsa_tree_accept: p [bs, B, V] fp32 (p + r*p_stride_r + n*p_stride_n) is
  *   the verifier's distribution after node n, i.e. for n's children; u [bs, B]
